@@ -1,0 +1,200 @@
+/*
+ * smla.h -- sparse multi-head latent attention (MLA) decode over packed
+ * fp8_ds_mla KV records, for NVIDIA GB300 (sm_103a).  C ABI of libsmla.so.
+ *
+ * What is computed follows these pages:
+ *   [P1] "vllm.models.kimi_k3.amd.ops.flydsl_sparse_mla_gfx950" (FlyDSL sparse
+ *        MLA forward over fp8_ds_mla records, gfx950): module docstring
+ *        (record layout, CSR tiles and masking, preconditions, writer rule)
+ *        and the epilogue of build_sparse_mla_fp8ds_module (output and LSE).
+ *   [P2] "vllm.models.deepseek_v41.amd.mono.attention.back" (K2 back):
+ *        stage_split (per-chunk partial, max, sum) and stage_combine (chunk
+ *        merge with the per-head sink).
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers on the current CUDA device.  The
+ *     library never allocates, frees, or synchronises; every call is
+ *     asynchronous on `stream` (a cudaStream_t passed as void*, NULL = the
+ *     legacy default stream).  The caller owns every buffer.
+ *   - Return value: SMLA_OK (0) or a negative smla_status.  Argument errors are
+ *     detected on the host before anything is enqueued.  A non-zero status
+ *     from a launch is SMLA_ERR_LAUNCH.  smla_strerror() names each code.
+ *   - Integers are little-endian; strides are in elements of the tensor's type.
+ */
+#ifndef SMLA_H
+#define SMLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Record layout, [P1] module docstring "Record (656 B)": bytes [0, 512) hold
+ * 512 E4M3 latent values, [512, 528) four little-endian f32 power-of-two
+ * scales (scale b covers latent dims [128 b, 128 b + 128)), [528, 656) the
+ * 64 bf16 RoPE dims.  656 = 41 * 16, so every record is 16-byte aligned when
+ * the cache base is. */
+#define SMLA_RECORD_BYTES 656
+#define SMLA_LATENT_DIM 512
+#define SMLA_ROPE_DIM 64
+#define SMLA_QK_DIM 576
+#define SMLA_SCALE_BLOCK 128
+#define SMLA_MAX_HEADS 64
+
+typedef enum smla_status {
+  SMLA_OK = 0,
+  SMLA_ERR_NULL = -1,       /* a required pointer is NULL */
+  SMLA_ERR_SHAPE = -2,      /* a size is out of range (n_q < 0, heads not in [1, 64], ...) */
+  SMLA_ERR_STRIDE = -3,     /* a stride overlaps rows/heads or is negative */
+  SMLA_ERR_ALIGN = -4,      /* a pointer or stride breaks the alignment rules below */
+  SMLA_ERR_WORKSPACE = -5,  /* workspace missing or smaller than smla_decode_workspace_size */
+  SMLA_ERR_SPLITS = -6,     /* num_splits outside [0, SMLA_MAX_SPLITS] */
+  SMLA_ERR_DEVICE = -7,     /* no CUDA device, or the current device is not sm_103 */
+  SMLA_ERR_LAUNCH = -8      /* a kernel launch failed (see cudaGetLastError) */
+} smla_status;
+
+/* Bits a decode call ORs into *status (when status != NULL). */
+#define SMLA_STATUS_INDEX_OOB 0x1   /* an index >= n_kv_rows was met and masked */
+#define SMLA_STATUS_TIMEOUT 0x2     /* an in-kernel pipeline wait gave up: results invalid */
+
+#define SMLA_MAX_SPLITS 64
+
+/* Arguments of one decode call.
+ *
+ * Row r's keys are the CSR slice indices[indptr[r] : indptr[r + 1]] ([P1]
+ * module docstring, "Tiles").  Its length is max(indptr[r+1] - indptr[r], 0),
+ * further capped at max(lens[r], 0) when lens != NULL.  Position p of the
+ * slice contributes iff its offset indptr[r] + p lies in [0, n_indices) and
+ * 0 <= indices[offset] < n_kv_rows.  Entries < 0 are masked with or without
+ * has_invalid ([P1] "Tiles": masked positions contribute nothing); an entry
+ * >= n_kv_rows, which [P1] lists as a precondition the host cannot check, is
+ * masked the same way here, never dereferenced, and flagged in *status.
+ * Duplicate entries count once per position.
+ *
+ * For each row r and head h, over the contributing keys t:
+ *   k_t[d] = e4m3(rec_t[d]) * scale_t[d / 128]   (d < 512), bf16 rope (512 <= d < 576)
+ *   s_t    = sm_scale * sum_{d < 576} q[r, h, d] * k_t[d]
+ *   m = max_t s_t,  l = sum_t exp(s_t - m)
+ *   lse[r, h] = m + ln(l)                          ([P1] epilogue; the sink is
+ *                                                  not part of the LSE)
+ *   out[r, h, d] = sum_t exp(s_t - m) k_t[d] / (l + exp(sink[h] - m))   (d < 512)
+ * with the sink term absent when sink == NULL (it enters the denominator once,
+ * as [P2] stage_combine folds it).  A row with no contributing key gives
+ * out = 0 and lse = -inf, sink or not ([P1] epilogue).
+ *
+ * Layouts and alignment:
+ *   q        bf16, element [r][h][d] at q + r*q_stride_row + h*q_stride_head + d;
+ *            16-byte aligned base, strides multiples of 8 elements.
+ *   kv_cache uint8 [n_kv_rows][656], 16-byte aligned.  Row ids are 64-bit
+ *            byte offsets, so caches beyond 4 GiB work; n_kv_rows <= 2^31.
+ *   indices  int32 [n_indices]; indptr int32 [n_q + 1]; lens int32 [n_q] or NULL.
+ *   sink     f32 [num_heads] or NULL, in the natural-log units of s_t.
+ *   out      bf16, element [r][h][d] at out + r*out_stride_row + h*out_stride_head + d;
+ *            16-byte aligned base, strides multiples of 8 elements.
+ *   lse      f32 [n_q][num_heads] contiguous, or NULL.
+ *   n_valid  int32 [n_q] or NULL: number of contributing keys of each row.
+ *   status   int32 [1] or NULL: SMLA_STATUS_* bits are ORed in (never cleared).
+ */
+typedef struct smla_decode_params {
+  int32_t n_q;
+  int32_t num_heads;
+  const void* q;
+  int64_t q_stride_row;
+  int64_t q_stride_head;
+  const void* kv_cache;
+  int64_t n_kv_rows;
+  const int32_t* indices;
+  int64_t n_indices;
+  const int32_t* indptr;
+  const int32_t* lens;
+  /* Planning hints; results never depend on them.  max_row_len: an upper
+   * bound of the rows' slice lengths known on the host (e.g. top-k); <= 0 means
+   * unknown (n_indices / n_q is used).  has_invalid: rows may end in -1
+   * padding; each row is then trimmed after its last entry >= 0 ([P1]
+   * "Tiles", has_invalid). */
+  int32_t max_row_len;
+  int32_t has_invalid;
+  float sm_scale;
+  const float* sink;
+  void* out;
+  int64_t out_stride_row;
+  int64_t out_stride_head;
+  float* lse;
+  int32_t* n_valid;
+  int32_t* status;
+  /* Chunks per row for split-KV ([P2] stage_split / stage_combine): 0 lets the
+   * planner choose from the row length, the batch and the SM count; k >= 1
+   * forces k chunks. */
+  int32_t num_splits;
+} smla_decode_params;
+
+/* The split plan a decode call with these sizes would use on the current
+ * device (or on a device with num_sms SMs when num_sms > 0).
+ *   num_splits   chunks per row (1 = no split, no combine)
+ *   chunk_len    slice positions per chunk (a multiple of tile_len); the last
+ *                chunk of a row also takes every position past num_splits*chunk_len
+ *   tile_len     keys per pipeline tile
+ *   grid         CTAs of the decode launch
+ *   workspace_bytes  bytes of workspace the call needs (0 when num_splits == 1)
+ * Pure host arithmetic when num_sms > 0 (no CUDA call). */
+typedef struct smla_plan_info {
+  int32_t num_splits;
+  int32_t chunk_len;
+  int32_t tile_len;
+  int32_t grid;
+  int64_t workspace_bytes;
+} smla_plan_info;
+
+int smla_plan(int32_t n_q, int32_t num_heads, int32_t max_row_len, int64_t n_indices,
+              int32_t num_splits, int32_t num_sms, smla_plan_info* plan);
+
+/* Workspace bytes smla_decode needs for these sizes on the current device
+ * (same arguments as the params fields of the same names).  Returns 0 when
+ * the call does not split, or when the sizes are invalid.
+ *
+ * Workspace layout (all offsets 256-byte aligned), for C = plan.num_splits:
+ *   ticket  int32 [n_q]                  per-row arrival counters
+ *   o_part  f32 [n_q][C][H][512]         unnormalised chunk partial sum_t 2^(x_t - m) k_t
+ *   ml_part f32 [n_q][C][H][2]           (m, l): m = chunk max of x_t = s_t * log2(e),
+ *                                        l = sum_t 2^(x_t - m); m = -inf, l = 0 if empty
+ *   nv_part int32 [n_q][C]               contributing keys of each chunk
+ * The ticket counters must be zero before the first call that uses this
+ * workspace (e.g. allocate it zeroed); every call returns them to zero.
+ * Calls that share a workspace must be ordered (same stream). */
+size_t smla_decode_workspace_size(int32_t n_q, int32_t num_heads, int32_t max_row_len,
+                                  int64_t n_indices, int32_t num_splits);
+
+/* Sparse MLA decode (the definition above) as one kernel launch: every
+ * (row, chunk) unit gathers its records, runs QK over 576 dims, the online
+ * softmax and PV over 512 dims on tcgen05 tensor cores; when a row is split,
+ * the last chunk of the row to finish merges the partials ([P2]
+ * stage_combine) and writes out / lse.  `workspace` may be NULL only when
+ * smla_decode_workspace_size() returns 0. */
+int smla_decode(const smla_decode_params* params, void* workspace, size_t workspace_bytes,
+                void* stream);
+
+/* The record writer ([P1] module docstring, "Preconditions": vLLM's
+ * concat_and_cache_ds_mla rule).  For each of n records:
+ *   scale_b = pow2ceil(max(amax_b, 1e-4) / 448), amax_b = max |latent[128 b .. 128 b + 127]|
+ *   bytes [0, 512)   = E4M3(latent_d / scale_{d/128}), round to nearest even, saturating
+ *   bytes [512, 528) = the four scales as f32
+ *   bytes [528, 656) = the 64 rope bf16 values, bit for bit
+ * latent: bf16 [n][latent_stride] (first 512 used), rope: bf16 [n][rope_stride]
+ * (first 64 used), kv_out: uint8 [n][656].  Pointers 16-byte aligned, strides
+ * multiples of 8 elements.  scale <= 2^7 holds iff |latent| <= 57344. */
+int smla_pack_records(const void* latent, int64_t latent_stride, const void* rope,
+                      int64_t rope_stride, int64_t n, void* kv_out, void* stream);
+
+/* Name of a status code. */
+const char* smla_strerror(int status);
+
+/* SMLA_OK when the current CUDA device can run the kernels (sm_103). */
+int smla_device_check(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SMLA_H */

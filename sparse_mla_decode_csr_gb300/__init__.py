@@ -1,0 +1,210 @@
+"""Python binding of libsmla.so: sparse MLA decode over fp8_ds_mla records.
+
+Argument marshalling only.  Every step of the computation runs in the CUDA
+kernels of libsmla.so; there is no CPU or PyTorch fallback, and importing
+fails loudly when the library has not been built (``python -c "import
+__graft_entry__ as g; g.build()"``).  PyTorch supplies device memory and
+streams.  The entry points keep the names of the C ABI in include/smla.h.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libsmla.so")
+
+RECORD_BYTES = 656
+LATENT_DIM = 512
+ROPE_DIM = 64
+QK_DIM = 576
+MAX_HEADS = 64
+MAX_SPLITS = 64
+STATUS_INDEX_OOB = 0x1
+STATUS_TIMEOUT = 0x2
+
+
+class SmlaError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {strerror(code)} (status {code})")
+        self.code = code
+
+
+class DecodeParams(ctypes.Structure):
+    _fields_ = [
+        ("n_q", ctypes.c_int32),
+        ("num_heads", ctypes.c_int32),
+        ("q", ctypes.c_void_p),
+        ("q_stride_row", ctypes.c_int64),
+        ("q_stride_head", ctypes.c_int64),
+        ("kv_cache", ctypes.c_void_p),
+        ("n_kv_rows", ctypes.c_int64),
+        ("indices", ctypes.c_void_p),
+        ("n_indices", ctypes.c_int64),
+        ("indptr", ctypes.c_void_p),
+        ("lens", ctypes.c_void_p),
+        ("max_row_len", ctypes.c_int32),
+        ("has_invalid", ctypes.c_int32),
+        ("sm_scale", ctypes.c_float),
+        ("sink", ctypes.c_void_p),
+        ("out", ctypes.c_void_p),
+        ("out_stride_row", ctypes.c_int64),
+        ("out_stride_head", ctypes.c_int64),
+        ("lse", ctypes.c_void_p),
+        ("n_valid", ctypes.c_void_p),
+        ("status", ctypes.c_void_p),
+        ("num_splits", ctypes.c_int32),
+    ]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [
+        ("num_splits", ctypes.c_int32),
+        ("chunk_len", ctypes.c_int32),
+        ("tile_len", ctypes.c_int32),
+        ("grid", ctypes.c_int32),
+        ("workspace_bytes", ctypes.c_int64),
+    ]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is not built: run `python -c \"import __graft_entry__ as g; g.build()\"`")
+    lib = ctypes.CDLL(LIB_PATH)
+    lib.smla_plan.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
+                              ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(PlanInfo)]
+    lib.smla_plan.restype = ctypes.c_int
+    lib.smla_decode_workspace_size.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                               ctypes.c_int64, ctypes.c_int32]
+    lib.smla_decode_workspace_size.restype = ctypes.c_size_t
+    lib.smla_decode.argtypes = [ctypes.POINTER(DecodeParams), ctypes.c_void_p, ctypes.c_size_t,
+                                ctypes.c_void_p]
+    lib.smla_decode.restype = ctypes.c_int
+    lib.smla_pack_records.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
+                                      ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                                      ctypes.c_void_p]
+    lib.smla_pack_records.restype = ctypes.c_int
+    lib.smla_strerror.argtypes = [ctypes.c_int]
+    lib.smla_strerror.restype = ctypes.c_char_p
+    lib.smla_device_check.argtypes = []
+    lib.smla_device_check.restype = ctypes.c_int
+    return lib
+
+
+lib = _load()
+
+EXPORTED_SYMBOLS = ("smla_plan", "smla_decode_workspace_size", "smla_decode",
+                    "smla_pack_records", "smla_strerror", "smla_device_check")
+
+
+def strerror(code: int) -> str:
+    return lib.smla_strerror(int(code)).decode()
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def smla_plan(n_q: int, num_heads: int, max_row_len: int = 0, n_indices: int = 0,
+              num_splits: int = 0, num_sms: int = 0) -> PlanInfo:
+    """The split plan of a decode call (pure host arithmetic when num_sms > 0)."""
+    info = PlanInfo()
+    rc = lib.smla_plan(n_q, num_heads, max_row_len, n_indices, num_splits, num_sms, ctypes.byref(info))
+    if rc != 0:
+        raise SmlaError(rc, "smla_plan")
+    return info
+
+
+def smla_decode_workspace_size(n_q: int, num_heads: int, max_row_len: int = 0,
+                               n_indices: int = 0, num_splits: int = 0) -> int:
+    return int(lib.smla_decode_workspace_size(n_q, num_heads, max_row_len, n_indices, num_splits))
+
+
+_WS: dict = {}
+
+
+def workspace(nbytes: int, device) -> Optional[torch.Tensor]:
+    """A zero-initialised, cached workspace of at least nbytes on device.
+
+    smla_decode leaves the workspace's ticket counters at zero after every
+    call, so a cached workspace stays valid for later calls on the same stream.
+    """
+    if nbytes == 0:
+        return None
+    dev = torch.device(device)
+    key = (dev.type, dev.index)
+    ws = _WS.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=dev)
+        _WS[key] = ws
+    return ws
+
+
+def smla_decode(q: torch.Tensor, kv_cache: torch.Tensor, n_kv_rows: int, indices: torch.Tensor,
+                indptr: torch.Tensor, lens: Optional[torch.Tensor], sm_scale: float,
+                sink: Optional[torch.Tensor], out: torch.Tensor, lse: Optional[torch.Tensor],
+                stream=None, *, max_row_len: int = 0, has_invalid: bool = False,
+                n_valid: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                num_splits: int = 0, workspace_tensor: Optional[torch.Tensor] = None) -> None:
+    """Sparse MLA decode into ``out`` (bf16 [n_q, H, 512]) and ``lse`` (f32 [n_q, H]).
+
+    q: bf16 [n_q, H, 576]; kv_cache: uint8 [n_kv_rows, 656]; indices/indptr/lens:
+    int32; sink: f32 [H] or None; n_valid: int32 [n_q] or None; status: int32 [1]
+    or None.  All tensors on the current CUDA device.  See include/smla.h.
+    """
+    assert q.dtype == torch.bfloat16 and q.dim() == 3 and q.stride(2) == 1
+    assert out.dtype == torch.bfloat16 and out.dim() == 3 and out.stride(2) == 1
+    assert kv_cache.dtype == torch.uint8
+    for t in (indices, indptr, lens, n_valid, status):
+        assert t is None or t.dtype == torch.int32
+    assert sink is None or sink.dtype == torch.float32
+    assert lse is None or (lse.dtype == torch.float32 and lse.is_contiguous())
+    n_q, heads = int(q.shape[0]), int(q.shape[1])
+    p = DecodeParams()
+    p.n_q, p.num_heads = n_q, heads
+    p.q, p.q_stride_row, p.q_stride_head = q.data_ptr(), q.stride(0), q.stride(1)
+    p.kv_cache, p.n_kv_rows = kv_cache.data_ptr(), int(n_kv_rows)
+    p.indices, p.n_indices = _ptr(indices), int(indices.numel())
+    p.indptr, p.lens = _ptr(indptr), _ptr(lens)
+    p.max_row_len, p.has_invalid = int(max_row_len), int(bool(has_invalid))
+    p.sm_scale = float(sm_scale)
+    p.sink = _ptr(sink)
+    p.out, p.out_stride_row, p.out_stride_head = out.data_ptr(), out.stride(0), out.stride(1)
+    p.lse, p.n_valid, p.status = _ptr(lse), _ptr(n_valid), _ptr(status)
+    p.num_splits = int(num_splits)
+    nbytes = smla_decode_workspace_size(n_q, heads, p.max_row_len, p.n_indices, p.num_splits)
+    ws = workspace_tensor if workspace_tensor is not None else workspace(nbytes, q.device)
+    rc = lib.smla_decode(ctypes.byref(p), _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream))
+    if rc != 0:
+        raise SmlaError(rc, "smla_decode")
+
+
+def smla_pack_records(latent: torch.Tensor, rope: torch.Tensor, kv_out: torch.Tensor,
+                      stream=None) -> None:
+    """Record writer: bf16 latent [n, 512] + bf16 rope [n, 64] -> uint8 kv_out [n, 656]."""
+    assert latent.dtype == torch.bfloat16 and rope.dtype == torch.bfloat16
+    assert kv_out.dtype == torch.uint8 and kv_out.is_contiguous()
+    assert latent.stride(1) == 1 and rope.stride(1) == 1
+    n = int(latent.shape[0])
+    assert rope.shape[0] == n and kv_out.numel() >= n * RECORD_BYTES
+    rc = lib.smla_pack_records(latent.data_ptr(), latent.stride(0), rope.data_ptr(), rope.stride(0),
+                               n, kv_out.data_ptr(), _stream(stream))
+    if rc != 0:
+        raise SmlaError(rc, "smla_pack_records")
+
+
+def smla_device_check() -> int:
+    return int(lib.smla_device_check())

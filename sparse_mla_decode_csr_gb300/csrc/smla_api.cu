@@ -1,0 +1,199 @@
+// C-ABI entry points of libsmla.so: argument checks, the split planner, the
+// workspace layout, and the kernel launches.  Everything here is host code;
+// the arithmetic of the method lives in the kernels.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+
+#include "smla.h"
+#include "smla_internal.h"
+
+namespace smla {
+
+namespace {
+
+constexpr int kTile = 64;  // keys per pipeline tile (planning granule)
+
+int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int current_sm_count(int* num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SMLA_ERR_DEVICE;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return SMLA_ERR_DEVICE;
+  *num_sms = n;
+  return SMLA_OK;
+}
+
+// Cost of a split count in "tile times" of the slowest CTA: waves of CTAs
+// times tiles per CTA, plus the partial write/read of split rows expressed in
+// tiles of gathered bytes (partials are mostly L2 traffic, hence the 1/4).
+double split_cost(int64_t n_q, int heads, int64_t tiles, int s, int num_sms) {
+  int64_t units = n_q * s;
+  int64_t waves = (units + num_sms - 1) / num_sms;
+  int64_t per_cta = (tiles + s - 1) / s;
+  double partial = 0.0;
+  if (s > 1) partial = 0.25 * (2.0 * heads * kLatent * 4.0) / (double(kTile) * kRecordBytes);
+  return double(waves) * (double(per_cta) + partial);
+}
+
+}  // namespace
+
+WorkspaceLayout workspace_layout(int32_t n_q, int32_t heads, int32_t splits) {
+  WorkspaceLayout w{};
+  if (splits <= 1) return w;
+  int64_t off = 0;
+  w.ticket_off = off;
+  off = align256(off + int64_t(n_q) * 4);
+  w.o_off = off;
+  off = align256(off + int64_t(n_q) * splits * heads * kLatent * 4);
+  w.ml_off = off;
+  off = align256(off + int64_t(n_q) * splits * heads * 2 * 4);
+  w.nv_off = off;
+  off = align256(off + int64_t(n_q) * splits * 4);
+  w.total = off;
+  return w;
+}
+
+}  // namespace smla
+
+using namespace smla;
+
+extern "C" {
+
+const char* smla_strerror(int status) {
+  switch (status) {
+    case SMLA_OK: return "ok";
+    case SMLA_ERR_NULL: return "a required pointer is NULL";
+    case SMLA_ERR_SHAPE: return "a size is out of range";
+    case SMLA_ERR_STRIDE: return "a stride is negative or overlaps rows/heads";
+    case SMLA_ERR_ALIGN: return "a pointer or stride breaks the 16-byte alignment rules";
+    case SMLA_ERR_WORKSPACE: return "workspace missing or too small";
+    case SMLA_ERR_SPLITS: return "num_splits out of range";
+    case SMLA_ERR_DEVICE: return "no usable sm_103 CUDA device";
+    case SMLA_ERR_LAUNCH: return "kernel launch failed";
+    default: return "unknown status";
+  }
+}
+
+int smla_device_check(void) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SMLA_ERR_DEVICE;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return SMLA_ERR_DEVICE;
+  return (major == 10 && minor == 3) ? SMLA_OK : SMLA_ERR_DEVICE;
+}
+
+int smla_plan(int32_t n_q, int32_t num_heads, int32_t max_row_len, int64_t n_indices,
+              int32_t num_splits, int32_t num_sms, smla_plan_info* plan) {
+  if (plan == nullptr) return SMLA_ERR_NULL;
+  if (n_q < 0 || num_heads < 1 || num_heads > SMLA_MAX_HEADS || n_indices < 0) return SMLA_ERR_SHAPE;
+  if (num_splits < 0 || num_splits > SMLA_MAX_SPLITS) return SMLA_ERR_SPLITS;
+  if (num_sms <= 0) {
+    int rc = current_sm_count(&num_sms);
+    if (rc != SMLA_OK) return rc;
+  }
+  int64_t row_len = max_row_len;
+  if (row_len <= 0) row_len = n_q > 0 ? (n_indices + n_q - 1) / n_q : 0;
+  int64_t tiles = std::max<int64_t>(1, (row_len + kTile - 1) / kTile);
+  int s = 1;
+  if (num_splits > 0) {
+    s = num_splits;
+  } else if (n_q > 0) {
+    int s_max = int(std::min<int64_t>(tiles, SMLA_MAX_SPLITS));
+    double best = split_cost(n_q, num_heads, tiles, 1, num_sms);
+    for (int c = 2; c <= s_max; ++c) {
+      double cost = split_cost(n_q, num_heads, tiles, c, num_sms);
+      if (cost < best * 0.98) {  // more splits only for a clear gain
+        best = cost;
+        s = c;
+      }
+    }
+  }
+  int64_t per_chunk_tiles = (tiles + s - 1) / s;
+  plan->num_splits = s;
+  plan->tile_len = kTile;
+  plan->chunk_len = int32_t(std::min<int64_t>(per_chunk_tiles * kTile, INT32_MAX / 2));
+  plan->grid = int32_t(int64_t(n_q) * s);
+  plan->workspace_bytes = workspace_layout(n_q, num_heads, s).total;
+  return SMLA_OK;
+}
+
+size_t smla_decode_workspace_size(int32_t n_q, int32_t num_heads, int32_t max_row_len,
+                                  int64_t n_indices, int32_t num_splits) {
+  smla_plan_info plan{};
+  if (smla_plan(n_q, num_heads, max_row_len, n_indices, num_splits, 0, &plan) != SMLA_OK) return 0;
+  return size_t(plan.workspace_bytes);
+}
+
+static int check_params(const smla_decode_params* p) {
+  if (p == nullptr) return SMLA_ERR_NULL;
+  if (p->n_q < 0 || p->num_heads < 1 || p->num_heads > SMLA_MAX_HEADS) return SMLA_ERR_SHAPE;
+  if (p->n_kv_rows < 0 || p->n_kv_rows > (int64_t(1) << 31) || p->n_indices < 0) return SMLA_ERR_SHAPE;
+  if (p->num_splits < 0 || p->num_splits > SMLA_MAX_SPLITS) return SMLA_ERR_SPLITS;
+  if (p->n_q == 0) return SMLA_OK;
+  if (!p->q || !p->indptr || !p->out) return SMLA_ERR_NULL;
+  if (p->n_kv_rows > 0 && !p->kv_cache) return SMLA_ERR_NULL;
+  if (p->n_indices > 0 && !p->indices) return SMLA_ERR_NULL;
+  if (p->q_stride_head < SMLA_QK_DIM && p->num_heads > 1) return SMLA_ERR_STRIDE;
+  if (p->q_stride_row < int64_t(p->num_heads - 1) * p->q_stride_head + SMLA_QK_DIM && p->n_q > 1)
+    return SMLA_ERR_STRIDE;
+  if (p->out_stride_head < SMLA_LATENT_DIM && p->num_heads > 1) return SMLA_ERR_STRIDE;
+  if (p->out_stride_row < int64_t(p->num_heads - 1) * p->out_stride_head + SMLA_LATENT_DIM && p->n_q > 1)
+    return SMLA_ERR_STRIDE;
+  if (p->q_stride_row < 0 || p->q_stride_head < 0 || p->out_stride_row < 0 || p->out_stride_head < 0)
+    return SMLA_ERR_STRIDE;
+  if (!aligned16(p->q) || !aligned16(p->out) || (p->kv_cache && !aligned16(p->kv_cache)))
+    return SMLA_ERR_ALIGN;
+  if ((p->q_stride_row | p->q_stride_head | p->out_stride_row | p->out_stride_head) & 7)
+    return SMLA_ERR_ALIGN;
+  if (!std::isfinite(p->sm_scale)) return SMLA_ERR_SHAPE;
+  return SMLA_OK;
+}
+
+int smla_decode(const smla_decode_params* params, void* workspace, size_t workspace_bytes,
+                void* stream) {
+  int rc = check_params(params);
+  if (rc != SMLA_OK) return rc;
+  if (params->n_q == 0) return SMLA_OK;
+  rc = smla_device_check();
+  if (rc != SMLA_OK) return rc;
+  DecodeLaunch L{};
+  L.p = *params;
+  rc = smla_plan(params->n_q, params->num_heads, params->max_row_len, params->n_indices,
+                 params->num_splits, 0, &L.plan);
+  if (rc != SMLA_OK) return rc;
+  L.ws = workspace_layout(params->n_q, params->num_heads, L.plan.num_splits);
+  if (L.ws.total > 0 && (workspace == nullptr || int64_t(workspace_bytes) < L.ws.total))
+    return SMLA_ERR_WORKSPACE;
+  if (L.ws.total > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return SMLA_ERR_ALIGN;
+  L.workspace = workspace;
+  L.stream = static_cast<cudaStream_t>(stream);
+  cudaError_t err = launch_decode_simt(L);
+  return err == cudaSuccess ? SMLA_OK : SMLA_ERR_LAUNCH;
+}
+
+int smla_pack_records(const void* latent, int64_t latent_stride, const void* rope,
+                      int64_t rope_stride, int64_t n, void* kv_out, void* stream) {
+  if (n < 0) return SMLA_ERR_SHAPE;
+  if (n == 0) return SMLA_OK;
+  if (!latent || !rope || !kv_out) return SMLA_ERR_NULL;
+  if (latent_stride < SMLA_LATENT_DIM || rope_stride < SMLA_ROPE_DIM) return SMLA_ERR_STRIDE;
+  if (!aligned16(latent) || !aligned16(rope) || !aligned16(kv_out) || (latent_stride & 7) ||
+      (rope_stride & 7))
+    return SMLA_ERR_ALIGN;
+  int rc = smla_device_check();
+  if (rc != SMLA_OK) return rc;
+  cudaError_t err = launch_pack(latent, latent_stride, rope, rope_stride, n, kv_out,
+                                static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? SMLA_OK : SMLA_ERR_LAUNCH;
+}
+
+}  // extern "C"

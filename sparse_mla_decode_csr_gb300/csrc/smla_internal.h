@@ -1,0 +1,41 @@
+// Internal declarations shared by the translation units of libsmla.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "smla.h"
+
+namespace smla {
+
+constexpr int kRecordBytes = SMLA_RECORD_BYTES;
+constexpr int kLatent = SMLA_LATENT_DIM;
+constexpr int kRope = SMLA_ROPE_DIM;
+constexpr int kQK = SMLA_QK_DIM;
+constexpr int kScaleOffset = 512;
+constexpr int kRopeOffset = 528;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Workspace offsets of one plan (see smla_decode_workspace_size in smla.h).
+struct WorkspaceLayout {
+  int64_t ticket_off, o_off, ml_off, nv_off, total;
+};
+
+WorkspaceLayout workspace_layout(int32_t n_q, int32_t heads, int32_t splits);
+
+// Everything a decode kernel needs, resolved on the host.
+struct DecodeLaunch {
+  smla_decode_params p;
+  smla_plan_info plan;
+  WorkspaceLayout ws;
+  void* workspace;
+  cudaStream_t stream;
+};
+
+// Kernel launchers (one per translation unit).  Return a cudaError_t.
+cudaError_t launch_decode_simt(const DecodeLaunch& L);
+cudaError_t launch_pack(const void* latent, int64_t latent_stride, const void* rope,
+                        int64_t rope_stride, int64_t n, void* kv_out, cudaStream_t stream);
+
+}  // namespace smla

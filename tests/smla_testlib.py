@@ -1,0 +1,102 @@
+"""Shared helpers of the GPU parity tests: build a case on both sides, run the
+CUDA path through the C ABI, run the oracle on the same inputs, compare."""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import smla_workloads as W
+import sparse_mla_decode_csr_gb300 as smla
+
+ATOL = 2e-2
+RTOL = 1e-2
+NORM_RTOL = 1e-2
+
+
+def bits(x: torch.Tensor) -> np.ndarray:
+    return x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def pack_gpu(lat: torch.Tensor, rope: torch.Tensor, dev) -> torch.Tensor:
+    kv = torch.empty(lat.shape[0], 656, dtype=torch.uint8, device=dev)
+    smla.smla_pack_records(lat.to(dev), rope.to(dev), kv)
+    return kv
+
+
+def build_cache(w: W.Workload, dev, gen_device="cuda") -> torch.Tensor:
+    kv = torch.empty(w.n_kv_rows, 656, dtype=torch.uint8, device=dev)
+    for s in range(W.n_slabs(w)):
+        lat, rope = W.latent_slab(w, s, gen_device)
+        start = s * W.SLAB_ROWS
+        smla.smla_pack_records(lat.to(dev), rope.to(dev), kv[start:start + lat.shape[0]])
+        del lat, rope
+    return kv
+
+
+def run_gpu(q, kv, n_kv_rows, indices, indptr, lens, sm_scale, sink, *, max_row_len=0,
+            has_invalid=False, num_splits=0, out=None, q_view=None):
+    dev = kv.device
+    n_q, heads = q.shape[0], q.shape[1]
+    if out is None:
+        out = torch.full((n_q, heads, 512), float("nan"), dtype=torch.bfloat16, device=dev)
+    lse = torch.full((n_q, heads), float("nan"), dtype=torch.float32, device=dev)
+    n_valid = torch.full((n_q,), -7, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    smla.smla_decode(q if q_view is None else q_view, kv, n_kv_rows, indices, indptr, lens, sm_scale,
+                     sink, out, lse, max_row_len=max_row_len, has_invalid=has_invalid,
+                     n_valid=n_valid, status=status, num_splits=num_splits)
+    torch.cuda.synchronize()
+    return out, lse, n_valid, int(status.item())
+
+
+def compare(out_gpu, lse_gpu, ref_out, ref_lse, what=""):
+    """Element-wise |gpu - ref| <= 2e-2 + 1e-2 |ref| for out and finite lse, the
+    norm-relative error of each (row, head) output <= 1e-2, and -inf lse exactly
+    where the oracle has it."""
+    g = out_gpu.float().cpu().double().numpy()
+    assert np.isfinite(g).all(), f"{what}: non-finite output"
+    excess = np.abs(g - ref_out) - (ATOL + RTOL * np.abs(ref_out))
+    worst = np.unravel_index(np.argmax(excess), excess.shape)
+    assert excess.max() <= 0, (f"{what}: out off by {np.abs(g - ref_out)[worst]:.4g} at {worst} "
+                               f"(ref {ref_out[worst]:.4g}, gpu {g[worst]:.4g})")
+    num = np.linalg.norm(g - ref_out, axis=-1)
+    den = np.linalg.norm(ref_out, axis=-1)
+    rel = np.where(den > 0, num / np.maximum(den, 1e-300), num)
+    assert rel.max() <= NORM_RTOL, f"{what}: norm-relative out error {rel.max():.3g}"
+    lg = lse_gpu.cpu().double().numpy()
+    assert np.array_equal(np.isneginf(lg), np.isneginf(ref_lse)), f"{what}: -inf lse pattern differs"
+    fin = np.isfinite(ref_lse)
+    assert np.isfinite(lg[fin]).all()
+    lex = np.abs(lg[fin] - ref_lse[fin]) - (ATOL + RTOL * np.abs(ref_lse[fin]))
+    assert lex.size == 0 or lex.max() <= 0, f"{what}: lse off by {lex.max():.3g} over tolerance"
+    return float(rel.max())
+
+
+def oracle_subproblem(w: W.Workload, indices: torch.Tensor, indptr: torch.Tensor, rows,
+                      kv_gpu: torch.Tensor, gen_device="cuda", lens=None):
+    """Records and remapped CSR of a sample of rows, for the oracle.
+
+    The oracle packs the sampled rows' records itself from the generator's
+    bf16 values; the bytes are compared with the GPU writer's (bit-exact).
+    Returns (rec, idx_sub, indptr_sub, lens_sub) where indices point into rec
+    (masked entries keep a masked value).
+    """
+    ind = indices.cpu().numpy()
+    ptr = indptr.cpu().numpy()
+    slices = [ind[max(ptr[r], 0):max(ptr[r + 1], ptr[r], 0)] for r in rows]
+    cat = np.concatenate(slices) if slices else np.zeros(0, np.int32)
+    valid = (cat >= 0) & (cat < w.n_kv_rows)
+    ids = np.unique(cat[valid])
+    lat, rope = W.latent_rows(w, torch.from_numpy(ids), gen_device)
+    rec = oracle.pack_records(bits(lat), bits(rope))
+    gpu_rec = kv_gpu[torch.from_numpy(ids).to(kv_gpu.device).long()].cpu().numpy()
+    assert np.array_equal(gpu_rec, rec), "GPU record writer differs from the oracle's"
+    remap = np.searchsorted(ids, np.where(valid, cat, 0))
+    sub = np.where(valid, remap, np.where(cat < 0, -1, len(ids))).astype(np.int32)
+    lens_sub = None
+    if lens is not None:
+        lens_sub = lens.cpu().numpy()[list(rows)]
+    ptr_sub = np.concatenate([[0], np.cumsum([len(s) for s in slices])]).astype(np.int32)
+    return rec, sub, ptr_sub, lens_sub

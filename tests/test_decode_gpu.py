@@ -1,0 +1,208 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Index handling and masking are compared bit-exactly (per-row contributing
+key counts, status bits, the record writer's bytes); out and lse within
+|gpu - ref| <= 2e-2 + 1e-2 |ref| element-wise and a norm-relative 1e-2 per
+(row, head).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import smla_workloads as W
+import sparse_mla_decode_csr_gb300 as smla
+from smla_testlib import bits, build_cache, compare, oracle_subproblem, pack_gpu, run_gpu
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def small_case(n_q, heads, n_kv, lens_list, *, seed=0, invalid=0.0, oob=0.0, sink=False,
+               scale_std=1.0):
+    """Random small problem: rows of the given slice lengths (with optional -1
+    and >= n_kv entries), latent ~ N(0, scale_std^2), packed on both sides."""
+    g = torch.Generator().manual_seed(seed)
+    lat = (torch.randn(n_kv, 512, generator=g) * scale_std).to(torch.bfloat16)
+    rope = torch.randn(n_kv, 64, generator=g).to(torch.bfloat16)
+    q = torch.randn(n_q, heads, 576, generator=g).to(torch.bfloat16)
+    parts, ptr = [torch.zeros(0, dtype=torch.int32)], [0]
+    for L in lens_list:
+        ids = torch.randint(0, n_kv, (L,), generator=g).to(torch.int32)
+        u = torch.rand(L, generator=g)
+        ids = torch.where(u < invalid, torch.full_like(ids, -1), ids)
+        ids = torch.where((u >= invalid) & (u < invalid + oob), torch.full_like(ids, n_kv + 5), ids)
+        parts.append(ids)
+        ptr.append(ptr[-1] + L)
+    indices = torch.cat(parts)
+    indptr = torch.tensor(ptr, dtype=torch.int32)
+    sk = torch.randn(heads, generator=g) if sink else None
+    rec = oracle.pack_records(bits(lat), bits(rope))
+    kv = pack_gpu(lat, rope, DEV)
+    assert np.array_equal(kv.cpu().numpy(), rec), "record writer differs from the oracle"
+    return dict(q=q, rec=rec, kv=kv, indices=indices, indptr=indptr, sink=sk, n_kv=n_kv)
+
+
+def run_small(c, *, lens=None, sm_scale=0.0625, num_splits=0, max_row_len=0, has_invalid=False,
+              what=""):
+    lens_d = None if lens is None else lens.to(DEV)
+    sink_d = None if c["sink"] is None else c["sink"].float().to(DEV)
+    out, lse, nv, st = run_gpu(c["q"].to(DEV), c["kv"], c["n_kv"], c["indices"].to(DEV),
+                               c["indptr"].to(DEV), lens_d, sm_scale, sink_d,
+                               max_row_len=max_row_len, has_invalid=has_invalid,
+                               num_splits=num_splits)
+    ref_out, ref_lse, ref_nv = oracle.sparse_mla_decode(
+        c["q"].double().numpy(), c["rec"], c["indices"].numpy(), c["indptr"].numpy(),
+        None if lens is None else lens.numpy(), sm_scale,
+        None if c["sink"] is None else c["sink"].double().numpy(), n_kv_rows=c["n_kv"])
+    assert np.array_equal(nv.cpu().numpy(), ref_nv), f"{what}: contributing-key counts differ"
+    compare(out, lse, ref_out, ref_lse, what)
+    return out, lse, st
+
+
+def test_writer_matches_oracle_bit_exact():
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn(3000, 512, generator=g) * torch.exp2(torch.randint(-30, 16, (3000, 4), generator=g)
+                                                         .float()).repeat_interleave(128, 1)
+    x[7, :128] = 0
+    x[8, 128:256] = 1e-6
+    x[9, 256] = 57344.0
+    x[10, 300] = -3.0e38
+    lat = x.to(torch.bfloat16)
+    rope = torch.randn(3000, 64, generator=g).to(torch.bfloat16)
+    kv = pack_gpu(lat, rope, DEV)
+    rec = oracle.pack_records(bits(lat), bits(rope))
+    assert np.array_equal(kv.cpu().numpy(), rec)
+
+
+@pytest.mark.parametrize("heads", [1, 7, 16, 17, 32, 33, 64])
+def test_head_counts(heads):
+    c = small_case(3, heads, 700, [130, 64, 300], seed=heads, sink=True)
+    run_small(c, max_row_len=300, what=f"H={heads}")
+
+
+def test_row_lengths_around_tiles():
+    lens = [0, 1, 31, 32, 33, 63, 64, 65, 127, 128, 129, 200]
+    c = small_case(len(lens), 16, 900, lens, seed=3)
+    run_small(c, max_row_len=200, what="lengths")
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 5, 17, 64])
+def test_forced_splits(splits):
+    c = small_case(5, 16, 2000, [1000, 10, 999, 0, 640], seed=11, sink=True, invalid=0.05)
+    run_small(c, num_splits=splits, max_row_len=1000, what=f"splits={splits}")
+
+
+def test_masking_and_status():
+    c = small_case(4, 16, 500, [200, 150, 90, 60], seed=21, invalid=0.3, oob=0.1, sink=True)
+    _, _, st = run_small(c, max_row_len=200, has_invalid=True, what="mask")
+    assert st & smla.STATUS_INDEX_OOB
+    c2 = small_case(3, 16, 500, [120, 80, 40], seed=22)
+    _, _, st2 = run_small(c2, max_row_len=120, what="clean")
+    assert st2 == 0
+
+
+def test_all_invalid_and_empty_rows():
+    c = small_case(4, 16, 300, [50, 0, 70, 20], seed=31, sink=True)
+    c["indices"][:50] = -1  # row 0 all -1
+    c["indices"][50:120] = 300  # row 2 all >= n_kv
+    out, lse, _ = run_small(c, max_row_len=70, what="empty")
+    assert torch.all(out[:3].float() == 0) and torch.isneginf(lse[:3]).all()
+
+
+def test_lens_and_bad_indptr():
+    c = small_case(4, 16, 400, [100, 100, 100, 100], seed=41)
+    lens = torch.tensor([100, 37, -5, 1000], dtype=torch.int32)
+    run_small(c, lens=lens, max_row_len=100, what="lens")
+    # rows running past the index buffer, and a decreasing indptr
+    c["indptr"] = torch.tensor([0, 150, 120, 390, 460], dtype=torch.int32)
+    run_small(c, max_row_len=300, what="indptr tail")
+
+
+def test_duplicates_count_per_position():
+    c = small_case(2, 16, 50, [300, 64], seed=51)
+    run_small(c, max_row_len=300, what="duplicates")
+
+
+def test_strided_q_and_out():
+    c = small_case(3, 8, 600, [200, 100, 33], seed=61, sink=True)
+    dev = DEV
+    big_q = torch.zeros(3, 10, 600, dtype=torch.bfloat16, device=dev)
+    big_q[:, 1:9, 8:584] = c["q"].to(dev)
+    qv = big_q[:, 1:9, 8:584]
+    big_o = torch.full((3, 9, 520), 7.0, dtype=torch.bfloat16, device=dev)
+    ov = big_o[:, :8, 8:]
+    out, lse, _, _ = run_gpu(c["q"].to(dev), c["kv"], 600, c["indices"].to(dev), c["indptr"].to(dev),
+                             None, 0.0625, c["sink"].to(dev), max_row_len=200, out=ov, q_view=qv)
+    ref_out, ref_lse, _ = oracle.sparse_mla_decode(c["q"].double().numpy(), c["rec"],
+                                                   c["indices"].numpy(), c["indptr"].numpy(), None,
+                                                   0.0625, c["sink"].double().numpy())
+    compare(ov, lse, ref_out, ref_lse, "strided")
+    assert torch.all(big_o[:, 8:, :] == 7.0) and torch.all(big_o[:, :, :8] == 7.0)
+
+
+def test_repeated_split_calls_reuse_workspace():
+    c = small_case(3, 16, 1000, [900, 800, 700], seed=71, sink=True)
+    o1, l1, _ = run_small(c, num_splits=7, max_row_len=900, what="first")
+    o2, l2, _ = run_small(c, num_splits=7, max_row_len=900, what="second")
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_split_partials_match_oracle():
+    c = small_case(3, 16, 1500, [700, 640, 129], seed=81, invalid=0.1)
+    splits = 4
+    plan = smla.smla_plan(3, 16, 700, int(c["indices"].numel()), splits)
+    ws = torch.zeros(plan.workspace_bytes + 4096, dtype=torch.uint8, device=DEV)
+    out = torch.empty(3, 16, 512, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(3, 16, dtype=torch.float32, device=DEV)
+    smla.smla_decode(c["q"].to(DEV), c["kv"], 1500, c["indices"].to(DEV), c["indptr"].to(DEV), None,
+                     0.0625, None, out, lse, max_row_len=700, num_splits=splits, workspace_tensor=ws)
+    torch.cuda.synchronize()
+    o_ref, m_ref, l_ref, nv_ref = oracle.split_partials(
+        c["q"].double().numpy(), c["rec"], c["indices"].numpy(), c["indptr"].numpy(), None, 0.0625,
+        chunk_len=plan.chunk_len, n_chunks=splits)
+    H, C = 16, splits
+    base = 0
+    off_o = (3 * 4 + 255) // 256 * 256
+    n_o = 3 * C * H * 512
+    off_ml = (off_o + n_o * 4 + 255) // 256 * 256
+    off_nv = (off_ml + 3 * C * H * 2 * 4 + 255) // 256 * 256
+    raw = ws.cpu()
+    ticket = raw[base:base + 12].view(torch.int32).numpy()
+    o = raw[off_o:off_o + n_o * 4].view(torch.float32).numpy().reshape(3, C, H, 512)
+    ml = raw[off_ml:off_ml + 3 * C * H * 8].view(torch.float32).numpy().reshape(3, C, H, 2)
+    nv = raw[off_nv:off_nv + 3 * C * 4].view(torch.int32).numpy().reshape(3, C)
+    assert np.all(ticket == 0), "ticket counters must return to zero"
+    assert np.array_equal(nv, nv_ref)
+    live = l_ref > 0
+    np.testing.assert_array_equal(ml[..., 1] > 0, live)
+    # m is kept in log2 units of the scaled score
+    np.testing.assert_allclose(ml[..., 0][live] * np.log(2.0), m_ref[live], rtol=1e-5, atol=1e-5)
+    np.testing.assert_allclose(ml[..., 1][live], l_ref[live], rtol=1e-2)
+    scale = np.maximum(np.abs(o_ref).max(axis=-1, keepdims=True), 1e-30)
+    assert np.all(np.abs(o - o_ref) <= 2e-2 * scale + 1e-6)
+
+
+@pytest.mark.parametrize("name,rows", [("tiny", None), ("decode", [0, 1, 31, 62, 63]),
+                                       ("ragged", [0, 1, 2, 100, 200, 254, 255]),
+                                       ("wide", [0, 64, 127]), ("long", None)])
+def test_workload_parity(name, rows):
+    w = W.WORKLOADS[name]
+    kv = build_cache(w, DEV)
+    q = W.queries(w, DEV)
+    indices, indptr = W.index_stream(w, DEV)
+    sink = W.sinks(w, DEV)
+    out, lse, nv, st = run_gpu(q, kv, w.n_kv_rows, indices, indptr, None, w.sm_scale, sink,
+                               max_row_len=w.max_row_len, has_invalid=w.has_invalid)
+    assert st == 0
+    rows = list(range(w.n_q)) if rows is None else rows
+    rec, sub, ptr_sub, _ = oracle_subproblem(w, indices, indptr, rows, kv)
+    ref_out, ref_lse, ref_nv = oracle.sparse_mla_decode(
+        q[rows].double().cpu().numpy(), rec, sub, ptr_sub, None, w.sm_scale,
+        None if sink is None else sink.double().cpu().numpy(), n_kv_rows=len(rec))
+    assert np.array_equal(nv.cpu().numpy()[rows], ref_nv)
+    rel = compare(out[rows], lse[rows], ref_out, ref_lse, name)
+    print(f"{name}: max norm-relative error {rel:.3g}")
+    del kv
+    torch.cuda.empty_cache()

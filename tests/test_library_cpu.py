@@ -1,0 +1,105 @@
+"""libsmla.so on the host: it loads, exports every symbol include/smla.h
+declares, plans splits sanely, and rejects bad arguments before any CUDA call."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparse_mla_decode_csr_gb300 as smla
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "smla.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(smla_[a-z0-9_]+)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_symbol():
+    names = header_functions()
+    assert len(names) >= 6, names
+    lib = ctypes.CDLL(smla.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in smla.h but not exported"
+    assert set(smla.EXPORTED_SYMBOLS) <= set(names)
+
+
+def test_strerror_names_every_code():
+    for code in range(0, -9, -1):
+        assert smla.strerror(code) != "unknown status"
+    assert smla.strerror(-99) == "unknown status"
+
+
+@pytest.mark.parametrize("n_q,heads,row_len", [
+    (4, 16, 128), (64, 16, 2048), (256, 16, 2048), (128, 64, 2048), (4, 64, 16384),
+    (1, 1, 1), (1000, 64, 100), (7, 33, 5000), (3, 16, 0)])
+def test_plan_properties(n_q, heads, row_len):
+    p = smla.smla_plan(n_q, heads, row_len, n_q * row_len, 0, 152)
+    assert 1 <= p.num_splits <= smla.MAX_SPLITS
+    assert p.tile_len == 64 and p.chunk_len % p.tile_len == 0 and p.chunk_len > 0
+    assert p.num_splits * p.chunk_len >= row_len
+    assert (p.num_splits - 1) * p.chunk_len < max(row_len, 1)  # no chunk wholly past the row
+    assert p.grid == n_q * p.num_splits
+    assert (p.workspace_bytes == 0) == (p.num_splits == 1)
+    if p.num_splits > 1:
+        need = n_q * 4 + n_q * p.num_splits * heads * (512 + 2) * 4 + n_q * p.num_splits * 4
+        assert p.workspace_bytes >= need
+
+
+def test_plan_splits_short_batches_and_respects_forcing():
+    assert smla.smla_plan(4, 64, 16384, 4 * 16384, 0, 152).num_splits > 16  # long rows split
+    assert smla.smla_plan(2048, 16, 2048, 2048 * 2048, 0, 152).num_splits == 1  # big batch does not
+    for k in (1, 2, 5, 64):
+        assert smla.smla_plan(3, 16, 700, 2100, k, 152).num_splits == k
+    with pytest.raises(smla.SmlaError):
+        smla.smla_plan(3, 16, 700, 2100, 65, 152)
+    with pytest.raises(smla.SmlaError):
+        smla.smla_plan(3, 65, 700, 2100, 0, 152)
+    with pytest.raises(smla.SmlaError):
+        smla.smla_plan(-1, 16, 700, 2100, 0, 152)
+
+
+def _params(**kw):
+    p = smla.DecodeParams()
+    p.n_q, p.num_heads = 2, 16
+    p.q, p.q_stride_row, p.q_stride_head = 0x1000, 16 * 576, 576
+    p.kv_cache, p.n_kv_rows = 0x2000, 100
+    p.indices, p.n_indices, p.indptr = 0x3000, 10, 0x4000
+    p.out, p.out_stride_row, p.out_stride_head = 0x5000, 16 * 512, 512
+    p.sm_scale = 0.05
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), -1), (dict(out=None), -1), (dict(indptr=None), -1), (dict(kv_cache=None), -1),
+    (dict(num_heads=0), -2), (dict(num_heads=65), -2), (dict(n_q=-1), -2),
+    (dict(n_kv_rows=(1 << 31) + 1), -2), (dict(sm_scale=float("nan")), -2),
+    (dict(q_stride_head=100), -3), (dict(out_stride_row=512), -3),
+    (dict(q=0x1008), -4), (dict(out_stride_head=516, out_stride_row=16 * 516), -4), (dict(kv_cache=0x2004), -4),
+    (dict(num_splits=65), -6), (dict(num_splits=-1), -6),
+])
+def test_decode_rejects_bad_arguments_on_host(kw, code):
+    p = _params(**kw)
+    rc = smla.lib.smla_decode(ctypes.byref(p), None, 0, None)
+    assert rc == code, (kw, rc, smla.strerror(rc))
+
+
+def test_decode_with_empty_batch_is_a_noop():
+    p = _params(n_q=0, q=None, out=None, indptr=None)
+    assert smla.lib.smla_decode(ctypes.byref(p), None, 0, None) == 0
+
+
+def test_pack_rejects_bad_arguments_on_host():
+    f = smla.lib.smla_pack_records
+    assert f(None, 512, 0x1000, 64, 4, 0x2000, None) == -1
+    assert f(0x1000, 500, 0x1000, 64, 4, 0x2000, None) == -3
+    assert f(0x1004, 512, 0x1000, 64, 4, 0x2000, None) == -4
+    assert f(0x1000, 512, 0x1000, 64, -1, 0x2000, None) == -2
+    assert f(0x1000, 512, 0x1000, 64, 0, 0x2000, None) == 0
