@@ -48,6 +48,8 @@ def parse_args():
     ap.add_argument("--also", default="wide", help="comma list of extra workloads to time ('' for none)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle CPU-baseline budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", default="tc", choices=["tc", "simt"],
+                    help="tc: the tcgen05 kernel; simt: the CUDA-core cross-check kernel")
     return ap.parse_args()
 
 
@@ -146,12 +148,13 @@ class ClockSampler:
 class Problem:
     """A workload resident on one device: records, queries, index stream, outputs."""
 
-    def __init__(self, w: W.Workload, dev):
+    def __init__(self, w: W.Workload, dev, kernel: str = "tc"):
         import sparse_mla_decode_csr_gb300 as smla
 
         self.smla = smla
         self.w = w
         self.dev = dev
+        self.kernel = smla.KERNEL_TENSOR_CORE if kernel == "tc" else smla.KERNEL_CUDA_CORE
         self.kv = torch.empty(w.n_kv_rows, 656, dtype=torch.uint8, device=dev)
         for s in range(W.n_slabs(w)):
             lat, rope = W.latent_slab(w, s, dev)
@@ -181,7 +184,7 @@ class Problem:
                               self.indptr if indptr is None else indptr, None, w.sm_scale, self.sink,
                               self.out if out is None else out, self.lse if lse is None else lse,
                               stream, max_row_len=w.max_row_len, has_invalid=w.has_invalid,
-                              workspace_tensor=self.ws)
+                              workspace_tensor=self.ws, kernel=self.kernel)
 
 
 def l2_flusher(dev):
@@ -343,7 +346,7 @@ def main():
     if dist_ok:
         torch.distributed.init_process_group("nccl", device_id=dev)
     w = W.WORKLOADS[args.workload]
-    prob = Problem(w, dev)
+    prob = Problem(w, dev, args.kernel)
     flush = l2_flusher(dev)
     with ClockSampler(local_rank) as clk:
         times = time_device(prob, args.steps, args.warmup, flush, dist_ok)
@@ -361,7 +364,7 @@ def main():
     extra = {}
     for name in [x for x in args.also.split(",") if x and x != args.workload]:
         wx = W.WORKLOADS[name]
-        px = Problem(wx, dev)
+        px = Problem(wx, dev, args.kernel)
         tx = time_device(px, max(10, args.steps // 2), args.warmup, flush, False)
         mean_ms = statistics.mean(tx)
         peak, _ = measured_peaks()
@@ -396,7 +399,8 @@ def main():
         "gathered_kv_gbs": achieved * world,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": ncu_traffic(w.name),
-                     "peak_source": peak_src, "kernel": "smla decode (one launch per step)",
+                     "peak_source": peak_src,
+                     "kernel": f"smla decode, {args.kernel} kernel (one launch per step)",
                      "algorithmic_bytes_per_launch": bytes_step},
         "e2e": {"value": world * w.n_q * steps / (e2e_ms * 1e-3), "unit": "rows/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

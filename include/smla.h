@@ -128,7 +128,14 @@ typedef struct smla_decode_params {
    * planner choose from the row length, the batch and the SM count; k >= 1
    * forces k chunks. */
   int32_t num_splits;
+  /* Which kernel runs the call: SMLA_KERNEL_TENSOR_CORE (0, default) or
+   * SMLA_KERNEL_CUDA_CORE (1, an fp32 CUDA-core kernel kept as a cross-check).
+   * Both compute the same definition. */
+  int32_t kernel;
 } smla_decode_params;
+
+#define SMLA_KERNEL_TENSOR_CORE 0
+#define SMLA_KERNEL_CUDA_CORE 1
 
 /* The split plan a decode call with these sizes would use on the current
  * device (or on a device with num_sms SMs when num_sms > 0).
@@ -157,8 +164,10 @@ int smla_plan(int32_t n_q, int32_t num_heads, int32_t max_row_len, int64_t n_ind
  * Workspace layout (all offsets 256-byte aligned), for C = plan.num_splits:
  *   ticket  int32 [n_q]                  per-row arrival counters
  *   o_part  f32 [n_q][C][H][512]         unnormalised chunk partial sum_t 2^(x_t - m) k_t
- *   ml_part f32 [n_q][C][H][2]           (m, l): m = chunk max of x_t = s_t * log2(e),
- *                                        l = sum_t 2^(x_t - m); m = -inf, l = 0 if empty
+ *   ml_part f32 [n_q][C][H][2]           (m, l) of x_t = s_t * log2(e): m is the chunk's
+ *                                        reference maximum (its max, or at most 8 below it),
+ *                                        l = sum_t 2^(x_t - m), and o_part is taken against
+ *                                        the same m; m = -inf, l = 0 if the chunk is empty
  *   nv_part int32 [n_q][C]               contributing keys of each chunk
  * The ticket counters must be zero before the first call that uses this
  * workspace (e.g. allocate it zeroed); every call returns them to zero.
@@ -167,11 +176,13 @@ size_t smla_decode_workspace_size(int32_t n_q, int32_t num_heads, int32_t max_ro
                                   int64_t n_indices, int32_t num_splits);
 
 /* Sparse MLA decode (the definition above) as one kernel launch: every
- * (row, chunk) unit gathers its records, runs QK over 576 dims, the online
- * softmax and PV over 512 dims on tcgen05 tensor cores; when a row is split,
- * the last chunk of the row to finish merges the partials ([P2]
- * stage_combine) and writes out / lse.  `workspace` may be NULL only when
- * smla_decode_workspace_size() returns 0. */
+ * (row, chunk) unit gathers its records, dequantises them to bf16 (exact),
+ * runs QK over 576 dims and PV over 512 dims on the tcgen05 tensor cores with
+ * an online softmax in between; when a row is split, the last chunk of the row
+ * to finish merges the partials ([P2] stage_combine) and writes out / lse.
+ * `workspace` may be NULL only when smla_decode_workspace_size() returns 0.
+ * Accuracy: q, k and v enter the products exactly; p is rounded to bf16, sums
+ * are f32, out is rounded to bf16 (round to nearest even). */
 int smla_decode(const smla_decode_params* params, void* workspace, size_t workspace_bytes,
                 void* stream);
 

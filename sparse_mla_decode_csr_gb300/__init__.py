@@ -26,6 +26,8 @@ MAX_HEADS = 64
 MAX_SPLITS = 64
 STATUS_INDEX_OOB = 0x1
 STATUS_TIMEOUT = 0x2
+KERNEL_TENSOR_CORE = 0
+KERNEL_CUDA_CORE = 1
 
 
 class SmlaError(RuntimeError):
@@ -58,6 +60,7 @@ class DecodeParams(ctypes.Structure):
         ("n_valid", ctypes.c_void_p),
         ("status", ctypes.c_void_p),
         ("num_splits", ctypes.c_int32),
+        ("kernel", ctypes.c_int32),
     ]
 
 
@@ -158,7 +161,8 @@ def smla_decode(q: torch.Tensor, kv_cache: torch.Tensor, n_kv_rows: int, indices
                 sink: Optional[torch.Tensor], out: torch.Tensor, lse: Optional[torch.Tensor],
                 stream=None, *, max_row_len: int = 0, has_invalid: bool = False,
                 n_valid: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
-                num_splits: int = 0, workspace_tensor: Optional[torch.Tensor] = None) -> None:
+                num_splits: int = 0, workspace_tensor: Optional[torch.Tensor] = None,
+                kernel: int = KERNEL_TENSOR_CORE) -> None:
     """Sparse MLA decode into ``out`` (bf16 [n_q, H, 512]) and ``lse`` (f32 [n_q, H]).
 
     q: bf16 [n_q, H, 576]; kv_cache: uint8 [n_kv_rows, 656]; indices/indptr/lens:
@@ -185,6 +189,7 @@ def smla_decode(q: torch.Tensor, kv_cache: torch.Tensor, n_kv_rows: int, indices
     p.out, p.out_stride_row, p.out_stride_head = out.data_ptr(), out.stride(0), out.stride(1)
     p.lse, p.n_valid, p.status = _ptr(lse), _ptr(n_valid), _ptr(status)
     p.num_splits = int(num_splits)
+    p.kernel = int(kernel)
     nbytes = smla_decode_workspace_size(n_q, heads, p.max_row_len, p.n_indices, p.num_splits)
     ws = workspace_tensor if workspace_tensor is not None else workspace(nbytes, q.device)
     rc = lib.smla_decode(ctypes.byref(p), _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream))

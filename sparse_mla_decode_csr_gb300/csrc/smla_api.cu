@@ -155,6 +155,7 @@ static int check_params(const smla_decode_params* p) {
   if ((p->q_stride_row | p->q_stride_head | p->out_stride_row | p->out_stride_head) & 7)
     return SMLA_ERR_ALIGN;
   if (!std::isfinite(p->sm_scale)) return SMLA_ERR_SHAPE;
+  if (p->kernel != SMLA_KERNEL_TENSOR_CORE && p->kernel != SMLA_KERNEL_CUDA_CORE) return SMLA_ERR_SHAPE;
   return SMLA_OK;
 }
 
@@ -176,7 +177,7 @@ int smla_decode(const smla_decode_params* params, void* workspace, size_t worksp
   if (L.ws.total > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return SMLA_ERR_ALIGN;
   L.workspace = workspace;
   L.stream = static_cast<cudaStream_t>(stream);
-  cudaError_t err = launch_decode_simt(L);
+  cudaError_t err = params->kernel == SMLA_KERNEL_CUDA_CORE ? launch_decode_simt(L) : launch_decode_tc(L);
   return err == cudaSuccess ? SMLA_OK : SMLA_ERR_LAUNCH;
 }
 

@@ -165,10 +165,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_simt_kernel(DecodeArgs a) 
         const float al = alpha_s[h];
         float o0 = acc[h][0] * al, o1 = acc[h][1] * al;
         for (int t = 0; t < kT; ++t) {
+          // rows are kKP (odd) floats apart: scalar reads, no 8-byte vector
           const float pv = p_s[h * kT + t];
-          const float2 kv = *reinterpret_cast<const float2*>(k_s + t * kKP + d);
-          o0 = fmaf(pv, kv.x, o0);
-          o1 = fmaf(pv, kv.y, o1);
+          o0 = fmaf(pv, k_s[t * kKP + d], o0);
+          o1 = fmaf(pv, k_s[t * kKP + d + 1], o1);
         }
         acc[h][0] = o0;
         acc[h][1] = o1;

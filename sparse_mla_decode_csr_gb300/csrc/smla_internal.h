@@ -35,6 +35,7 @@ struct DecodeLaunch {
 
 // Kernel launchers (one per translation unit).  Return a cudaError_t.
 cudaError_t launch_decode_simt(const DecodeLaunch& L);
+cudaError_t launch_decode_tc(const DecodeLaunch& L);
 cudaError_t launch_pack(const void* latent, int64_t latent_stride, const void* rope,
                         int64_t rope_stride, int64_t n, void* kv_out, cudaStream_t stream);
 

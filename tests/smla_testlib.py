@@ -35,8 +35,11 @@ def build_cache(w: W.Workload, dev, gen_device="cuda") -> torch.Tensor:
     return kv
 
 
+KERNELS = {"tc": smla.KERNEL_TENSOR_CORE, "simt": smla.KERNEL_CUDA_CORE}
+
+
 def run_gpu(q, kv, n_kv_rows, indices, indptr, lens, sm_scale, sink, *, max_row_len=0,
-            has_invalid=False, num_splits=0, out=None, q_view=None):
+            has_invalid=False, num_splits=0, out=None, q_view=None, kernel="tc"):
     dev = kv.device
     n_q, heads = q.shape[0], q.shape[1]
     if out is None:
@@ -46,7 +49,7 @@ def run_gpu(q, kv, n_kv_rows, indices, indptr, lens, sm_scale, sink, *, max_row_
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     smla.smla_decode(q if q_view is None else q_view, kv, n_kv_rows, indices, indptr, lens, sm_scale,
                      sink, out, lse, max_row_len=max_row_len, has_invalid=has_invalid,
-                     n_valid=n_valid, status=status, num_splits=num_splits)
+                     n_valid=n_valid, status=status, num_splits=num_splits, kernel=KERNELS[kernel])
     torch.cuda.synchronize()
     return out, lse, n_valid, int(status.item())
 
