@@ -187,6 +187,22 @@ class Problem:
                               workspace_tensor=self.ws, kernel=self.kernel)
 
 
+def reduce_max(x: float, dev) -> float:
+    """Max of a per-rank number over all ranks (identity on one process)."""
+    dist = torch.distributed
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_rows_per_s(world: int, rows_per_rank: int, steps: int, max_total_ms: float) -> float:
+    """Whole-job rows/s: every rank decodes its own batch of rows each step;
+    the job takes as long as its slowest rank."""
+    return world * rows_per_rank * steps / (max_total_ms * 1e-3)
+
+
 def l2_flusher(dev):
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     buf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
@@ -350,16 +366,9 @@ def main():
     flush = l2_flusher(dev)
     with ClockSampler(local_rank) as clk:
         times = time_device(prob, args.steps, args.warmup, flush, dist_ok)
-    total_ms = sum(times)
-    if dist_ok:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = reduce_max(sum(times), dev)
     e2e_ms, h2d, d2h = time_e2e(prob, args.steps, flush)
-    if dist_ok:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = reduce_max(e2e_ms, dev)
 
     extra = {}
     for name in [x for x in args.also.split(",") if x and x != args.workload]:
@@ -381,7 +390,7 @@ def main():
         return
     steps = args.steps
     sec = total_ms * 1e-3
-    value = world * w.n_q * steps / sec
+    value = weak_scaling_rows_per_s(world, w.n_q, steps, total_ms)
     mean_ms = total_ms / steps
     bytes_step = prob.bytes_per_step()
     achieved = bytes_step / (mean_ms * 1e-3) / 1e9
@@ -402,7 +411,7 @@ def main():
                      "peak_source": peak_src,
                      "kernel": f"smla decode, {args.kernel} kernel (one launch per step)",
                      "algorithmic_bytes_per_launch": bytes_step},
-        "e2e": {"value": world * w.n_q * steps / (e2e_ms * 1e-3), "unit": "rows/s",
+        "e2e": {"value": weak_scaling_rows_per_s(world, w.n_q, steps, e2e_ms), "unit": "rows/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": steps,
         "clocks": clk.summary(),

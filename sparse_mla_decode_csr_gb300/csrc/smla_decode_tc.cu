@@ -66,8 +66,7 @@ struct Misc {
   uint8_t valid[kStages][kTileK];
   float m_fin[64];
   float alpha[2][32];
-  float red[2][4][32];
-  float lsum[2][4][32];
+  float red[2][4][32];           // tile maxima, then (after the last tile) key sums
   float fac[64];
 };
 
@@ -77,11 +76,16 @@ struct TcLayout {
   static constexpr int q_bytes = kDChunks * HP * 128;
   static constexpr int p_row = 2 * HP;            // bytes of one key's P^T row
   static constexpr int p_bytes = kTileK * p_row;
+  // 64 heads: q takes 72 KB, so P^T is single-buffered to stay within 227 KB
+  static constexpr int p_stages = HP == 64 ? 1 : 2;
   static constexpr int off_q = kStages * kTileBytes;
   static constexpr int off_p = off_q + q_bytes;
-  static constexpr int off_bar = off_p + kStages * p_bytes;
+  static constexpr int off_bar = off_p + p_stages * p_bytes;
   static constexpr int off_misc = off_bar + 16 * 8;
-  static constexpr int total = off_misc + int(sizeof(Misc)) + 1024;  // + alignment slack
+  static constexpr int used = off_misc + int(sizeof(Misc));
+  // slack to align the dynamic shared memory base to 1024 bytes, when it fits
+  static constexpr int slack = used + 1024 <= 232448 ? 1024 : 0;
+  static constexpr int total = used + slack;
   static constexpr int tmem_cols = (6 * HP <= 128) ? 128 : (6 * HP <= 256 ? 256 : 512);
   static constexpr Swizzle p_swz = HP == 64 ? kSw128 : (HP == 32 ? kSw64 : kSw32);
   static constexpr uint32_t p_swmask = HP == 64 ? 7 : (HP == 32 ? 3 : 1);
@@ -157,6 +161,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
   Misc* ms = reinterpret_cast<Misc*>(smem + Lay::off_misc);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (Lay::slack == 0 && (smem_u32(smem_raw) & 1023u) != 0) {
+    // no room to realign: refuse (uniformly, before any barrier or TMEM use)
+    if (tid == 0 && a.status) atomicOr(a.status, SMLA_STATUS_TIMEOUT);
+    return;
+  }
   const Unit u = unit_of(a, blockIdx.x);
   const int H = a.heads;
 
@@ -313,9 +322,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
         lpart[h + 1] += p1v;
         pk[h / 2] = pack_bf16x2(p0, p1v);
       }
-      wait_bar_warp(pv_done + s, ph ^ 1, ms, a);  // PV(j-2) has read this P stage
+      // the P stage is free once the PV that last read it has completed
+      if (Lay::p_stages == 2)
+        wait_bar_warp(pv_done + s, ph ^ 1, ms, a);  // PV(j-2)
+      else if (j > 0)
+        wait_bar_warp(pv_done + ((j - 1) & 1), ((j - 1) >> 1) & 1, ms, a);  // PV(j-1)
+      const int ps = Lay::p_stages == 2 ? s : 0;
       if (active) {
-        uint8_t* prow = p_s + s * Lay::p_bytes;
+        uint8_t* prow = p_s + ps * Lay::p_bytes;
 #pragma unroll
         for (int c = 0; c < HH / 8; ++c) {
           uint32_t off = uint32_t(r) * Lay::p_row + uint32_t(wg * (HH / 8) + c) * 16u;
@@ -334,7 +348,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
       float t = active ? lpart[h] : 0.f;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-      if (lane == 0) ms->lsum[wg][qd][h] = t;
+      if (lane == 0) ms->red[wg][qd][h] = t;
       if (tid == wg * 128) ms->m_fin[wg * HH + h] = mr[h];
     }
   } else if (warp == kMmaWarp) {
@@ -346,7 +360,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
         if (!wait_bar(p_full + s, (j >> 1) & 1, ms, a)) return false;
         tc_fence_after();
         const uint32_t tile = tiles_u32 + s * kTileBytes;
-        const uint32_t pst = p_u32 + s * Lay::p_bytes;
+        const uint32_t pst = p_u32 + (Lay::p_stages == 2 ? s : 0) * Lay::p_bytes;
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt) {
           const uint32_t d = tmem + uint32_t(2 * HP + mt * HP);
@@ -462,9 +476,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
   __syncthreads();
   tc_fence_after();
   const bool aborted = ms->abort != 0;
+  static_assert(TcLayout<HP>::total <= 232448, "shared memory over the per-block limit");
   if (tid < H) {
     const int g = tid / HH, hh = tid % HH;
-    const float l = ms->lsum[g][0][hh] + ms->lsum[g][1][hh] + ms->lsum[g][2][hh] + ms->lsum[g][3][hh];
+    const float l = ms->red[g][0][hh] + ms->red[g][1][hh] + ms->red[g][2][hh] + ms->red[g][3][hh];
     const float m = ms->m_fin[tid];
     if (a.splits == 1) {
       float fac, lse;

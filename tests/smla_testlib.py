@@ -54,25 +54,70 @@ def run_gpu(q, kv, n_kv_rows, indices, indptr, lens, sm_scale, sink, *, max_row_
     return out, lse, n_valid, int(status.item())
 
 
-def compare(out_gpu, lse_gpu, ref_out, ref_lse, what=""):
-    """Element-wise |gpu - ref| <= 2e-2 + 1e-2 |ref| for out and finite lse, the
-    norm-relative error of each (row, head) output <= 1e-2, and -inf lse exactly
-    where the oracle has it."""
+U32 = 2.0 ** -24  # unit roundoff of f32
+
+
+def allowance(q, rec, indices, indptr, lens, sm_scale, sink, n_kv_rows=None):
+    """Rounding allowance of an f32 evaluation of the method, per output element.
+
+    Scores: an f32 dot product of 576 terms is within ds_t = 576 u sum_d |q_d k_td|
+    of the exact one (standard forward bound; doubled here for slack).  To
+    first order a score error moves out_d by sum_t w_t ds_t |v_td - out_d| and
+    the LSE by max_t ds_t (w_t the softmax weights incl. the sink).  Weights
+    rounded to bf16 add 2^-8 sum_t w_t |v_td|.  For N(0,1) data this is ~1e-3;
+    it only matters where the problem is ill-conditioned (heavy-tailed keys,
+    near-tied scores).  Uses the oracle's own row slicing and record reader.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    n_q, heads, _ = q.shape
+    if n_kv_rows is None:
+        n_kv_rows = rec.shape[0]
+    out_allow = np.zeros((n_q, heads, 512))
+    lse_allow = np.zeros((n_q, heads))
+    for r in range(n_q):
+        _, ids = oracle.row_positions(r, indices, indptr, lens, n_kv_rows)
+        if len(ids) == 0:
+            continue
+        keys, values = oracle.row_keys(rec, ids)
+        s = oracle.row_scores(q[r], keys, sm_scale)
+        ds = 2.0 * 576 * U32 * abs(sm_scale) * (np.abs(q[r]) @ np.abs(keys).T)
+        m = s.max(axis=1, keepdims=True)
+        e = np.exp(s - m)
+        den = e.sum(axis=1, keepdims=True)
+        if sink is not None:
+            den = den + np.exp(np.asarray(sink, dtype=np.float64)[:, None] - m)
+        w = e / den
+        av = np.abs(values)
+        out = w @ values
+        wd = w * ds
+        out_allow[r] = wd @ av + wd.sum(axis=1, keepdims=True) * np.abs(out) + 2.0 ** -8 * (w @ av)
+        lse_allow[r] = ds.max(axis=1)
+    return out_allow, lse_allow
+
+
+def compare(out_gpu, lse_gpu, ref_out, ref_lse, what="", allow=None):
+    """Element-wise |gpu - ref| <= 2e-2 + 1e-2 |ref| (+ the f32 rounding
+    allowance of ill-conditioned elements) for out and finite lse; the
+    norm-relative error of each (row, head) output <= 1e-2 (+ the norm of the
+    allowance); -inf lse exactly where the oracle has it."""
+    a_out, a_lse = (0.0, 0.0) if allow is None else allow
     g = out_gpu.float().cpu().double().numpy()
     assert np.isfinite(g).all(), f"{what}: non-finite output"
-    excess = np.abs(g - ref_out) - (ATOL + RTOL * np.abs(ref_out))
+    excess = np.abs(g - ref_out) - (ATOL + RTOL * np.abs(ref_out) + a_out)
     worst = np.unravel_index(np.argmax(excess), excess.shape)
     assert excess.max() <= 0, (f"{what}: out off by {np.abs(g - ref_out)[worst]:.4g} at {worst} "
                                f"(ref {ref_out[worst]:.4g}, gpu {g[worst]:.4g})")
     num = np.linalg.norm(g - ref_out, axis=-1)
     den = np.linalg.norm(ref_out, axis=-1)
-    rel = np.where(den > 0, num / np.maximum(den, 1e-300), num)
+    slack = np.linalg.norm(np.broadcast_to(a_out, ref_out.shape), axis=-1)
+    rel = np.where(den > 0, np.maximum(num - slack, 0) / np.maximum(den, 1e-300), num)
     assert rel.max() <= NORM_RTOL, f"{what}: norm-relative out error {rel.max():.3g}"
     lg = lse_gpu.cpu().double().numpy()
     assert np.array_equal(np.isneginf(lg), np.isneginf(ref_lse)), f"{what}: -inf lse pattern differs"
     fin = np.isfinite(ref_lse)
     assert np.isfinite(lg[fin]).all()
-    lex = np.abs(lg[fin] - ref_lse[fin]) - (ATOL + RTOL * np.abs(ref_lse[fin]))
+    al = np.broadcast_to(a_lse, ref_lse.shape)[fin]
+    lex = np.abs(lg[fin] - ref_lse[fin]) - (ATOL + RTOL * np.abs(ref_lse[fin]) + al)
     assert lex.size == 0 or lex.max() <= 0, f"{what}: lse off by {lex.max():.3g} over tolerance"
     return float(rel.max())
 

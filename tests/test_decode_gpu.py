@@ -13,7 +13,8 @@ import torch
 import oracle
 import smla_workloads as W
 import sparse_mla_decode_csr_gb300 as smla
-from smla_testlib import KERNELS, bits, build_cache, compare, oracle_subproblem, pack_gpu, run_gpu
+from smla_testlib import (KERNELS, allowance, bits, build_cache, compare, oracle_subproblem, pack_gpu,
+                          run_gpu)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -57,12 +58,12 @@ def run_small(c, *, lens=None, sm_scale=0.0625, num_splits=0, max_row_len=0, has
                                c["indptr"].to(DEV), lens_d, sm_scale, sink_d,
                                max_row_len=max_row_len, has_invalid=has_invalid,
                                num_splits=num_splits, kernel=kernel)
-    ref_out, ref_lse, ref_nv = oracle.sparse_mla_decode(
-        c["q"].double().numpy(), c["rec"], c["indices"].numpy(), c["indptr"].numpy(),
-        None if lens is None else lens.numpy(), sm_scale,
-        None if c["sink"] is None else c["sink"].double().numpy(), n_kv_rows=c["n_kv"])
+    args = (c["q"].double().numpy(), c["rec"], c["indices"].numpy(), c["indptr"].numpy(),
+            None if lens is None else lens.numpy(), sm_scale,
+            None if c["sink"] is None else c["sink"].double().numpy())
+    ref_out, ref_lse, ref_nv = oracle.sparse_mla_decode(*args, n_kv_rows=c["n_kv"])
     assert np.array_equal(nv.cpu().numpy(), ref_nv), f"{what}: contributing-key counts differ"
-    compare(out, lse, ref_out, ref_lse, what)
+    compare(out, lse, ref_out, ref_lse, what, allow=allowance(*args, n_kv_rows=c["n_kv"]))
     return out, lse, st
 
 
@@ -185,7 +186,8 @@ def test_split_partials_match_oracle(kernel):
     np.testing.assert_array_equal(ml[..., 1] > 0, live)
     # (m, l, O) of a chunk are taken against a reference maximum m (log2 units):
     # l 2^m and O 2^m are what the oracle's chunk max and sums fix.
-    shift = np.where(live, ml[..., 0] - m_ref / np.log(2.0), 0.0)
+    with np.errstate(invalid="ignore"):
+        shift = np.where(live, ml[..., 0] - m_ref / np.log(2.0), 0.0)
     np.testing.assert_array_less(shift[live], 1e-3)
     np.testing.assert_array_less(-shift[live], 8.0 + 1e-3)
     np.testing.assert_allclose((ml[..., 1] * np.exp2(shift))[live], l_ref[live], rtol=1e-2)
@@ -208,11 +210,11 @@ def test_workload_parity(name, rows, kernel):
     assert st == 0
     rows = list(range(w.n_q)) if rows is None else rows
     rec, sub, ptr_sub, _ = oracle_subproblem(w, indices, indptr, rows, kv)
-    ref_out, ref_lse, ref_nv = oracle.sparse_mla_decode(
-        q[rows].double().cpu().numpy(), rec, sub, ptr_sub, None, w.sm_scale,
-        None if sink is None else sink.double().cpu().numpy(), n_kv_rows=len(rec))
+    args = (q[rows].double().cpu().numpy(), rec, sub, ptr_sub, None, w.sm_scale,
+            None if sink is None else sink.double().cpu().numpy())
+    ref_out, ref_lse, ref_nv = oracle.sparse_mla_decode(*args, n_kv_rows=len(rec))
     assert np.array_equal(nv.cpu().numpy()[rows], ref_nv)
-    rel = compare(out[rows], lse[rows], ref_out, ref_lse, name)
+    rel = compare(out[rows], lse[rows], ref_out, ref_lse, name, allow=allowance(*args, n_kv_rows=len(rec)))
     print(f"{name}: max norm-relative error {rel:.3g}")
     del kv
     torch.cuda.empty_cache()
