@@ -166,9 +166,10 @@ class Problem:
         self.sink = W.sinks(w, dev)
         self.out = torch.empty(w.n_q, w.heads, 512, dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty(w.n_q, w.heads, dtype=torch.float32, device=dev)
-        nbytes = smla.smla_decode_workspace_size(w.n_q, w.heads, w.max_row_len, self.indices.numel(), 0)
-        self.ws = smla.workspace(nbytes, dev)
         self.plan = smla.smla_plan(w.n_q, w.heads, w.max_row_len, self.indices.numel(), 0)
+        # a workspace of this problem's own (zeroed): its ticket counters stay valid
+        nbytes = int(self.plan.workspace_bytes)
+        self.ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev) if nbytes else None
         ind = self.indices
         self.valid_keys = int(((ind >= 0) & (ind < w.n_kv_rows)).sum().item())
         torch.cuda.synchronize(dev)
@@ -218,12 +219,14 @@ def time_device(prob: Problem, steps: int, warmup: int, flush, dist_ok: bool):
     if dist_ok:
         torch.distributed.barrier()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.nvtx.range_push("timed")
     for a, b in evs:
         flush()
         a.record(stream)
         prob.step(stream=stream)
         b.record(stream)
     torch.cuda.synchronize(prob.dev)
+    torch.cuda.nvtx.range_pop()
     if dist_ok:
         torch.distributed.barrier()
     return [a.elapsed_time(b) for a, b in evs]

@@ -169,9 +169,12 @@ int smla_plan(int32_t n_q, int32_t num_heads, int32_t max_row_len, int64_t n_ind
  *                                        l = sum_t 2^(x_t - m), and o_part is taken against
  *                                        the same m; m = -inf, l = 0 if the chunk is empty
  *   nv_part int32 [n_q][C]               contributing keys of each chunk
- * The ticket counters must be zero before the first call that uses this
- * workspace (e.g. allocate it zeroed); every call returns them to zero.
- * Calls that share a workspace must be ordered (same stream). */
+ * The ticket counters must be zero when a call starts (e.g. allocate the
+ * workspace zeroed); every completed call returns them to zero.  A call with
+ * other sizes may have written partials over that region, so re-zero bytes
+ * [0, 4 n_q) before reusing a workspace across calls of different n_q,
+ * num_heads or plan.  Calls that share a workspace must be ordered (same
+ * stream); a call that reports SMLA_STATUS_TIMEOUT leaves it undefined. */
 size_t smla_decode_workspace_size(int32_t n_q, int32_t num_heads, int32_t max_row_len,
                                   int64_t n_indices, int32_t num_splits);
 

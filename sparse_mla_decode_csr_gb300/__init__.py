@@ -139,20 +139,26 @@ def smla_decode_workspace_size(n_q: int, num_heads: int, max_row_len: int = 0,
 _WS: dict = {}
 
 
-def workspace(nbytes: int, device) -> Optional[torch.Tensor]:
-    """A zero-initialised, cached workspace of at least nbytes on device.
+def workspace(nbytes: int, device, layout=None) -> Optional[torch.Tensor]:
+    """A cached workspace of at least nbytes on device, ready for a call with
+    the given layout key (n_q, heads, plan).
 
-    smla_decode leaves the workspace's ticket counters at zero after every
-    call, so a cached workspace stays valid for later calls on the same stream.
+    smla_decode needs the per-row ticket counters at the start of the
+    workspace to be zero, and leaves them zero; a call with another layout may
+    have written partials over that region, so the counters are re-zeroed
+    (on the current stream) whenever the layout changes.
     """
     if nbytes == 0:
         return None
     dev = torch.device(device)
     key = (dev.type, dev.index)
-    ws = _WS.get(key)
+    ws, last = _WS.get(key, (None, None))
     if ws is None or ws.numel() < nbytes:
         ws = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=dev)
-        _WS[key] = ws
+    elif layout != last:
+        n_q = layout[0] if layout else ws.numel() // 4
+        ws[: min(ws.numel(), 4 * n_q + 256)].zero_()
+    _WS[key] = (ws, layout)
     return ws
 
 
@@ -190,8 +196,10 @@ def smla_decode(q: torch.Tensor, kv_cache: torch.Tensor, n_kv_rows: int, indices
     p.lse, p.n_valid, p.status = _ptr(lse), _ptr(n_valid), _ptr(status)
     p.num_splits = int(num_splits)
     p.kernel = int(kernel)
-    nbytes = smla_decode_workspace_size(n_q, heads, p.max_row_len, p.n_indices, p.num_splits)
-    ws = workspace_tensor if workspace_tensor is not None else workspace(nbytes, q.device)
+    ws = workspace_tensor
+    if ws is None:
+        plan = smla_plan(n_q, heads, p.max_row_len, p.n_indices, p.num_splits)
+        ws = workspace(int(plan.workspace_bytes), q.device, (n_q, heads, plan.num_splits, plan.chunk_len))
     rc = lib.smla_decode(ctypes.byref(p), _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream))
     if rc != 0:
         raise SmlaError(rc, "smla_decode")

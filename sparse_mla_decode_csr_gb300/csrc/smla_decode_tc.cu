@@ -51,6 +51,7 @@ constexpr int kConvWarps = 7;
 constexpr int kMmaWarp = 12;
 constexpr int kSoftmaxWarps = 8;
 constexpr int kBatch = 5;                        // records in flight per converter warp
+constexpr int kPerConv = (kTileK + kConvWarps - 1) / kConvWarps;  // records per converter warp and tile
 constexpr float kRescaleMargin = 8.f;            // p <= 2^8 before a max update
 constexpr float kInitMax = -1.0e30f;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
@@ -406,33 +407,47 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
     __syncwarp();
   } else {
     // ---------------- converters ----------------
+    // Warp cw takes records cw, cw + 7, ... of each tile (kPerConv at most).
+    // Lane k holds the record row of the warp's k-th record; the records of
+    // tile i + 2 are prefetched into L2 while tile i is converted.
     const int cw = warp < kMmaWarp ? warp - kSoftmaxWarps : warp - kSoftmaxWarps - 1;  // 0..6
     int nvalid = 0;
     const int ck = lane >> 2;                 // 64-dim column block of this lane's 16 dims
     const int b0 = (lane & 3) * 32;           // byte offset of those dims within the 128-byte row
+    const bool hi_first = (lane >> 2) & 1;    // alternate store order: conflict-free phases
+    auto tile_keys = [&](int i) -> int32_t {  // this lane's record row in tile i, or -1
+      const int r = cw + kConvWarps * lane;
+      const int p = u.p0 + i * kTileK + r;
+      return (i < nt && lane < kPerConv && r < kTileK && p < p1) ? key_of(a, u.beg, p) : -1;
+    };
+    auto prefetch = [&](int32_t id) {
+      if (id >= 0) prefetch_l2(a.kv + int64_t(id) * kRecordBytes, kRecordBytes);
+    };
+    int32_t key_cur = tile_keys(0);
+    int32_t key_nxt = tile_keys(1);
+    prefetch(key_cur);
+    prefetch(key_nxt);
     for (int i = 0; i < nt; ++i) {
       const int s = i & 1;
       const uint32_t ph = (i >> 1) & 1;
-      const int tp0 = u.p0 + i * kTileK;
       uint8_t* tile = tiles + s * kTileBytes;
+      const int32_t key_nn = tile_keys(i + 2);
+      prefetch(key_nn);
       bool waited = false;
       bool ok = true;
-      for (int r0 = cw; r0 < kTileK; r0 += kConvWarps * kBatch) {
+      for (int k0 = 0; k0 < kPerConv; k0 += kBatch) {
         int32_t idx[kBatch];
         uint4 lat[kBatch], rp[kBatch];
         float sc[kBatch];
 #pragma unroll
         for (int b = 0; b < kBatch; ++b) {
-          const int r = r0 + kConvWarps * b;
-          int32_t id = -1;
-          if (lane == 0 && r < kTileK && tp0 + r < p1) id = key_of(a, u.beg, tp0 + r);
-          id = __shfl_sync(0xffffffffu, id, 0);
-          idx[b] = id;
+          const int32_t id = __shfl_sync(0xffffffffu, key_cur, (k0 + b) & 31);
+          idx[b] = (k0 + b < kPerConv) ? id : -1;
           lat[b] = make_uint4(0, 0, 0, 0);
           rp[b] = make_uint4(0, 0, 0, 0);
           sc[b] = 0.f;
-          if (id >= 0) {
-            const uint8_t* rec = a.kv + int64_t(id) * kRecordBytes;
+          if (idx[b] >= 0) {
+            const uint8_t* rec = a.kv + int64_t(idx[b]) * kRecordBytes;
             lat[b] = __ldg(reinterpret_cast<const uint4*>(rec) + lane);
             sc[b] = __ldg(reinterpret_cast<const float*>(rec + kScaleOffset) + (lane >> 3));
             if (lane < 8) rp[b] = __ldg(reinterpret_cast<const uint4*>(rec + kRopeOffset) + lane);
@@ -447,13 +462,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
         }
 #pragma unroll
         for (int b = 0; b < kBatch; ++b) {
-          const int r = r0 + kConvWarps * b;
-          if (r >= kTileK) break;
+          const int r = cw + kConvWarps * (k0 + b);
+          if (k0 + b >= kPerConv || r >= kTileK) break;
           uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
           if (idx[b] >= 0) dequant16_bf16(lat[b], sc[b], lo, hi);
           uint8_t* rowbase = tile + ck * kChunkBytes + (r >> 3) * 1024;
-          *reinterpret_cast<uint4*>(rowbase + sw128_off(r & 7, b0)) = lo;
-          *reinterpret_cast<uint4*>(rowbase + sw128_off(r & 7, b0 + 16)) = hi;
+          const uint4 first = hi_first ? hi : lo, second = hi_first ? lo : hi;
+          *reinterpret_cast<uint4*>(rowbase + sw128_off(r & 7, b0 + (hi_first ? 16 : 0))) = first;
+          *reinterpret_cast<uint4*>(rowbase + sw128_off(r & 7, b0 + (hi_first ? 0 : 16))) = second;
           if (lane < 8)
             *reinterpret_cast<uint4*>(tile + 8 * kChunkBytes + (r >> 3) * 1024 + sw128_off(r & 7, lane * 16)) = rp[b];
           if (lane == 0) {
@@ -467,6 +483,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(kv_full + s);
+      key_cur = key_nxt;
+      key_nxt = key_nn;
     }
     if (lane == 0 && nvalid) atomicAdd(&ms->nvalid, nvalid);
   }
