@@ -1,10 +1,11 @@
 // Sparse MLA decode on the 5th-generation tensor cores (tcgen05, TMEM).
 //
 // One CTA per (row, chunk) unit; 64-key tiles, double-buffered.  Warp roles:
-//   warps 0-7   softmax: warpgroup g (0/1) owns head columns [g*HP/2, (g+1)*HP/2);
+//   warps 0-3 (and 4-7 at 64 heads)  softmax: warpgroup g owns head columns
+//               [g*HH, (g+1)*HH), HH = all heads up to 32, 32 at 64 heads;
 //               they also stage q, rescale O when a running max moves, and run
 //               the epilogue with everyone else
-//   warps 8-11, 13-15  converters: gather the tile's 656-byte records (64-bit
+//   every other warp but 12  converters: gather the tile's 656-byte records (64-bit
 //               addressing), dequantise E4M3 * pow2 scale -> bf16 exactly, and
 //               write the 64 x 576 bf16 key tile in the 128-byte-swizzled
 //               K-major layout
@@ -47,11 +48,7 @@ constexpr int kDChunks = 9;                      // 576 dims = 9 x 64 (128-byte 
 constexpr int kChunkBytes = kTileK * 128;        // one 64-dim column block of a tile
 constexpr int kTileBytes = kDChunks * kChunkBytes;
 constexpr int kStages = 2;
-constexpr int kConvWarps = 7;
 constexpr int kMmaWarp = 12;
-constexpr int kSoftmaxWarps = 8;
-constexpr int kBatch = 5;                        // records in flight per converter warp
-constexpr int kPerConv = (kTileK + kConvWarps - 1) / kConvWarps;  // records per converter warp and tile
 constexpr float kRescaleMargin = 8.f;            // p <= 2^8 before a max update
 constexpr float kInitMax = -1.0e30f;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
@@ -65,7 +62,7 @@ struct Misc {
   int32_t pad[3];
   int32_t flag[2][2][4];         // [warpgroup][stage][quarter] rescale votes
   uint8_t valid[kStages][kTileK];
-  float m_fin[64];
+  float mref[64];                // per-head reference maxima (log2 units)
   float alpha[2][32];
   float red[2][4][32];           // tile maxima, then (after the last tile) key sums
   float fac[64];
@@ -73,7 +70,14 @@ struct Misc {
 
 template <int HP>
 struct TcLayout {
-  static constexpr int HH = HP / 2;               // head columns per softmax warpgroup
+  // softmax warpgroups: one holds all head columns up to 32 heads, two at 64;
+  // every other warp but the MMA issuer converts records
+  static constexpr int SWG = HP == 64 ? 2 : 1;
+  static constexpr int kSoftmaxWarps = 4 * SWG;
+  static constexpr int kConvWarps = 15 - kSoftmaxWarps;
+  static constexpr int kPerConv = (kTileK + kConvWarps - 1) / kConvWarps;  // records per converter warp and tile
+  static constexpr int kBatch = kPerConv <= 6 ? kPerConv : (kPerConv + 1) / 2;  // records in flight
+  static constexpr int HH = HP / SWG;             // head columns per softmax warpgroup
   static constexpr int q_bytes = kDChunks * HP * 128;
   static constexpr int p_row = 2 * HP;            // bytes of one key's P^T row
   static constexpr int p_bytes = kTileK * p_row;
@@ -145,6 +149,10 @@ template <int HP>
 __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) {
   using Lay = TcLayout<HP>;
   constexpr int HH = Lay::HH;
+  constexpr int kSoftmaxWarps = Lay::kSoftmaxWarps;
+  constexpr int kConvWarps = Lay::kConvWarps;
+  constexpr int kPerConv = Lay::kPerConv;
+  constexpr int kBatch = Lay::kBatch;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* tiles = smem;
@@ -182,6 +190,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
     mbar_init(q_full, kSoftmaxWarps);
     mbar_init(mma_drain, 1);
     ms->abort = 0;
+    for (int h = 0; h < 64; ++h) ms->mref[h] = kInitMax;
     ms->last_valid = u.p0 - 1;
     ms->nvalid = 0;
     ms->is_last = 0;
@@ -213,18 +222,13 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
   const uint32_t p_u32 = smem_u32(p_s);
 
   float lpart[HH];
-  float mr[HH];
 #pragma unroll
-  for (int h = 0; h < HH; ++h) {
-    lpart[h] = 0.f;
-    mr[h] = kInitMax;
-  }
+  for (int h = 0; h < HH; ++h) lpart[h] = 0.f;
 
   if (warp < kSoftmaxWarps) {
     // ---------------- softmax warpgroups ----------------
     const int wg = warp >> 2, qd = warp & 3;
-    const int t256 = tid;  // 0..255
-    for (int i = t256; i < HP * (kQK / 8); i += 256) {
+    for (int i = tid; i < HP * (kQK / 8); i += 32 * kSoftmaxWarps) {
       const int h = i / (kQK / 8), c16 = i % (kQK / 8);
       uint4 v = make_uint4(0, 0, 0, 0);
       if (h < H)
@@ -238,6 +242,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
 
     const bool active = s_lane_active(lane);
     const int r = 16 * qd + lane;  // key of this thread within the tile (active lanes)
+    const float* mr = ms->mref + wg * HH;  // this warpgroup's reference maxima (uniform)
     for (int j = 0; j < nt; ++j) {
       const int s = j & 1;
       const uint32_t ph = (j >> 1) & 1;
@@ -284,13 +289,19 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
         for (int h = 0; h < HH; ++h) {
           const float tm = fmaxf(fmaxf(ms->red[wg][0][h], ms->red[wg][1][h]),
                                  fmaxf(ms->red[wg][2][h], ms->red[wg][3][h]));
-          const float mn = fmaxf(mr[h], tm);
-          const float al = ex2(mr[h] - mn);
+          const float al = ex2(mr[h] - fmaxf(mr[h], tm));
           lpart[h] *= al;
           if (tid == wg * 128) ms->alpha[wg][h] = al;
-          mr[h] = mn;
         }
-        named_barrier(1 + wg, 128);
+        named_barrier(1 + wg, 128);  // everyone has read the old references
+        if (tid == wg * 128) {
+          for (int h = 0; h < HH; ++h) {
+            const float tm = fmaxf(fmaxf(ms->red[wg][0][h], ms->red[wg][1][h]),
+                                   fmaxf(ms->red[wg][2][h], ms->red[wg][3][h]));
+            ms->mref[wg * HH + h] = fmaxf(mr[h], tm);
+          }
+        }
+        named_barrier(1 + wg, 128);  // the new references are visible
         if (j > 0) {
           // O^T columns of this warpgroup's heads, all four 128-dim tiles:
           // wait for PV(j-1), then scale in place.
@@ -350,7 +361,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
       if (lane == 0) ms->red[wg][qd][h] = t;
-      if (tid == wg * 128) ms->m_fin[wg * HH + h] = mr[h];
     }
   } else if (warp == kMmaWarp) {
     // ---------------- MMA issuer ----------------
@@ -498,7 +508,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
   if (tid < H) {
     const int g = tid / HH, hh = tid % HH;
     const float l = ms->red[g][0][hh] + ms->red[g][1][hh] + ms->red[g][2][hh] + ms->red[g][3][hh];
-    const float m = ms->m_fin[tid];
+    const float m = ms->mref[tid];
     if (a.splits == 1) {
       float fac, lse;
       finish_head(m, nt > 0 ? l : 0.f, a.sink, tid, &fac, &lse);
