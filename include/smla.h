@@ -124,9 +124,10 @@ typedef struct smla_decode_params {
   float* lse;
   int32_t* n_valid;
   int32_t* status;
-  /* Chunks per row for split-KV ([P2] stage_split / stage_combine): 0 lets the
-   * planner choose from the row length, the batch and the SM count; k >= 1
-   * forces k chunks. */
+  /* Split-KV control ([P2] stage_split / stage_combine).  0 lets the planner
+   * choose from the row length, the batch and the SM count.  k >= 1: the
+   * CUDA-core kernel cuts every row into k chunks; the tensor-core kernel
+   * spreads the tiles over n_q * k CTAs (about k parts per row). */
   int32_t num_splits;
   /* Which kernel runs the call: SMLA_KERNEL_TENSOR_CORE (0, default) or
    * SMLA_KERNEL_CUDA_CORE (1, an fp32 CUDA-core kernel kept as a cross-check).
@@ -137,52 +138,65 @@ typedef struct smla_decode_params {
 #define SMLA_KERNEL_TENSOR_CORE 0
 #define SMLA_KERNEL_CUDA_CORE 1
 
-/* The split plan a decode call with these sizes would use on the current
- * device (or on a device with num_sms SMs when num_sms > 0).
- *   num_splits   chunks per row (1 = no split, no combine)
- *   chunk_len    slice positions per chunk (a multiple of tile_len); the last
- *                chunk of a row also takes every position past num_splits*chunk_len
- *   tile_len     keys per pipeline tile
- *   grid         CTAs of the decode launch
- *   workspace_bytes  bytes of workspace the call needs (0 when num_splits == 1)
- * Pure host arithmetic when num_sms > 0 (no CUDA call). */
+/* How a decode call with given params is laid out on the GPU.
+ *
+ * Tensor-core kernel (the default): a persistent, balanced schedule.  Each row
+ * r is cut into T_r = max(1, ceil(len_r / 64)) tiles of 64 slice positions;
+ * the rows' tiles are concatenated in row order into one tile space of
+ * T = sum_r T_r tiles, starting row r at tile P_r = sum_{r' < r} T_r'.  CTA c of
+ * G = grid takes the tiles [b_c, e_c) with b_c = floor(c T / G), and streams
+ * through them across row boundaries.  A row lying wholly inside one CTA's
+ * range is finished there; a row shared by CTAs c_a..c_b (the CTAs holding its
+ * first and last tile) gets one partial per CTA, stored in workspace slot
+ * 2 c + (P_r < b_c ? 0 : 1), and is merged from those slots ([P2]
+ * stage_combine) either by the last of its CTAs to finish (merge_kernel = 0)
+ * or by a second, small merge kernel launched right after (merge_kernel = 1,
+ * chosen when rows are shared by many CTAs).
+ * CUDA-core kernel: one CTA per (row, chunk); chunk c of a row covers slice
+ * positions [c chunk_len, (c + 1) chunk_len), the last chunk everything after;
+ * partial slot r * num_splits + c; the last chunk to finish merges.
+ *
+ * Fields: kernel (SMLA_KERNEL_*), grid (CTAs of the decode launch), tile_len
+ * (keys per tile), num_splits and chunk_len (CUDA-core kernel only),
+ * partial_slots, merge_kernel, workspace_bytes.  num_sms > 0 makes the plan
+ * pure host arithmetic (no CUDA call); num_sms = 0 asks the current device. */
 typedef struct smla_plan_info {
+  int32_t kernel;
+  int32_t grid;
+  int32_t tile_len;
   int32_t num_splits;
   int32_t chunk_len;
-  int32_t tile_len;
-  int32_t grid;
+  int32_t partial_slots;
+  int32_t merge_kernel;
+  int32_t pad;
   int64_t workspace_bytes;
 } smla_plan_info;
 
-int smla_plan(int32_t n_q, int32_t num_heads, int32_t max_row_len, int64_t n_indices,
-              int32_t num_splits, int32_t num_sms, smla_plan_info* plan);
+int smla_plan(const smla_decode_params* params, int32_t num_sms, smla_plan_info* plan);
 
-/* Workspace bytes smla_decode needs for these sizes on the current device
- * (same arguments as the params fields of the same names).  Returns 0 when
- * the call does not split, or when the sizes are invalid.
+/* Workspace bytes smla_decode needs for these params on the current device
+ * (0 when none; also 0 for invalid params).
  *
- * Workspace layout (all offsets 256-byte aligned), for C = plan.num_splits:
- *   ticket  int32 [n_q]                  per-row arrival counters
- *   o_part  f32 [n_q][C][H][512]         unnormalised chunk partial sum_t 2^(x_t - m) k_t
- *   ml_part f32 [n_q][C][H][2]           (m, l) of x_t = s_t * log2(e): m is the chunk's
- *                                        reference maximum (its max, or at most 8 below it),
- *                                        l = sum_t 2^(x_t - m), and o_part is taken against
- *                                        the same m; m = -inf, l = 0 if the chunk is empty
- *   nv_part int32 [n_q][C]               contributing keys of each chunk
+ * Layout (each part 256-byte aligned), S = plan.partial_slots:
+ *   ticket  int32 [n_q]          per-row arrival counters
+ *   o_part  f32 [S][H][512]      unnormalised partial sum_t 2^(x_t - m) v_t of a row part
+ *   ml_part f32 [S][H][2]        (m, l) of x_t = s_t * log2(e): m is the part's reference
+ *                                maximum (its max, or at most 8 below it), l = sum_t 2^(x_t - m);
+ *                                m = -inf, l = 0 for a part without keys
+ *   nv_part int32 [S]            contributing keys of the part
  * The ticket counters must be zero when a call starts (e.g. allocate the
  * workspace zeroed); every completed call returns them to zero.  A call with
  * other sizes may have written partials over that region, so re-zero bytes
  * [0, 4 n_q) before reusing a workspace across calls of different n_q,
- * num_heads or plan.  Calls that share a workspace must be ordered (same
- * stream); a call that reports SMLA_STATUS_TIMEOUT leaves it undefined. */
-size_t smla_decode_workspace_size(int32_t n_q, int32_t num_heads, int32_t max_row_len,
-                                  int64_t n_indices, int32_t num_splits);
+ * num_heads, kernel or plan.  Calls that share a workspace must be ordered
+ * (same stream); a call that reports SMLA_STATUS_TIMEOUT leaves it undefined. */
+size_t smla_decode_workspace_size(const smla_decode_params* params);
 
-/* Sparse MLA decode (the definition above) as one kernel launch: every
- * (row, chunk) unit gathers its records, dequantises them to bf16 (exact),
- * runs QK over 576 dims and PV over 512 dims on the tcgen05 tensor cores with
- * an online softmax in between; when a row is split, the last chunk of the row
- * to finish merges the partials ([P2] stage_combine) and writes out / lse.
+/* Sparse MLA decode (the definition above): one kernel launch (two when the
+ * plan has merge_kernel = 1).  Each CTA gathers its tiles' records,
+ * dequantises them to bf16 (exact), runs QK over 576 dims and PV over 512 dims
+ * on the tcgen05 tensor cores with an online softmax in between, and writes
+ * out / lse of its whole rows and partials of shared rows (see smla_plan).
  * `workspace` may be NULL only when smla_decode_workspace_size() returns 0.
  * Accuracy: q, k and v enter the products exactly; p is rounded to bf16, sums
  * are f32, out is rounded to bf16 (round to nearest even). */

@@ -66,10 +66,14 @@ class DecodeParams(ctypes.Structure):
 
 class PlanInfo(ctypes.Structure):
     _fields_ = [
+        ("kernel", ctypes.c_int32),
+        ("grid", ctypes.c_int32),
+        ("tile_len", ctypes.c_int32),
         ("num_splits", ctypes.c_int32),
         ("chunk_len", ctypes.c_int32),
-        ("tile_len", ctypes.c_int32),
-        ("grid", ctypes.c_int32),
+        ("partial_slots", ctypes.c_int32),
+        ("merge_kernel", ctypes.c_int32),
+        ("pad", ctypes.c_int32),
         ("workspace_bytes", ctypes.c_int64),
     ]
 
@@ -79,11 +83,9 @@ def _load():
         raise ImportError(
             f"{LIB_PATH} is not built: run `python -c \"import __graft_entry__ as g; g.build()\"`")
     lib = ctypes.CDLL(LIB_PATH)
-    lib.smla_plan.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
-                              ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(PlanInfo)]
+    lib.smla_plan.argtypes = [ctypes.POINTER(DecodeParams), ctypes.c_int32, ctypes.POINTER(PlanInfo)]
     lib.smla_plan.restype = ctypes.c_int
-    lib.smla_decode_workspace_size.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
-                                               ctypes.c_int64, ctypes.c_int32]
+    lib.smla_decode_workspace_size.argtypes = [ctypes.POINTER(DecodeParams)]
     lib.smla_decode_workspace_size.restype = ctypes.c_size_t
     lib.smla_decode.argtypes = [ctypes.POINTER(DecodeParams), ctypes.c_void_p, ctypes.c_size_t,
                                 ctypes.c_void_p]
@@ -121,19 +123,30 @@ def _stream(stream) -> Optional[int]:
     return int(stream)
 
 
+def _plan_params(n_q, num_heads, max_row_len=0, n_indices=0, num_splits=0,
+                 kernel=KERNEL_TENSOR_CORE) -> DecodeParams:
+    p = DecodeParams()
+    p.n_q, p.num_heads, p.max_row_len, p.n_indices = int(n_q), int(num_heads), int(max_row_len), int(n_indices)
+    p.num_splits, p.kernel = int(num_splits), int(kernel)
+    return p
+
+
 def smla_plan(n_q: int, num_heads: int, max_row_len: int = 0, n_indices: int = 0,
-              num_splits: int = 0, num_sms: int = 0) -> PlanInfo:
-    """The split plan of a decode call (pure host arithmetic when num_sms > 0)."""
+              num_splits: int = 0, num_sms: int = 0, kernel: int = KERNEL_TENSOR_CORE) -> PlanInfo:
+    """The launch plan of a decode call (pure host arithmetic when num_sms > 0)."""
     info = PlanInfo()
-    rc = lib.smla_plan(n_q, num_heads, max_row_len, n_indices, num_splits, num_sms, ctypes.byref(info))
+    p = _plan_params(n_q, num_heads, max_row_len, n_indices, num_splits, kernel)
+    rc = lib.smla_plan(ctypes.byref(p), int(num_sms), ctypes.byref(info))
     if rc != 0:
         raise SmlaError(rc, "smla_plan")
     return info
 
 
 def smla_decode_workspace_size(n_q: int, num_heads: int, max_row_len: int = 0,
-                               n_indices: int = 0, num_splits: int = 0) -> int:
-    return int(lib.smla_decode_workspace_size(n_q, num_heads, max_row_len, n_indices, num_splits))
+                               n_indices: int = 0, num_splits: int = 0,
+                               kernel: int = KERNEL_TENSOR_CORE) -> int:
+    p = _plan_params(n_q, num_heads, max_row_len, n_indices, num_splits, kernel)
+    return int(lib.smla_decode_workspace_size(ctypes.byref(p)))
 
 
 _WS: dict = {}
@@ -198,8 +211,12 @@ def smla_decode(q: torch.Tensor, kv_cache: torch.Tensor, n_kv_rows: int, indices
     p.kernel = int(kernel)
     ws = workspace_tensor
     if ws is None:
-        plan = smla_plan(n_q, heads, p.max_row_len, p.n_indices, p.num_splits)
-        ws = workspace(int(plan.workspace_bytes), q.device, (n_q, heads, plan.num_splits, plan.chunk_len))
+        plan = PlanInfo()
+        rc = lib.smla_plan(ctypes.byref(p), 0, ctypes.byref(plan))
+        if rc != 0:
+            raise SmlaError(rc, "smla_plan")
+        ws = workspace(int(plan.workspace_bytes), q.device,
+                       (n_q, heads, plan.kernel, plan.grid, plan.num_splits, plan.chunk_len))
     rc = lib.smla_decode(ctypes.byref(p), _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream))
     if rc != 0:
         raise SmlaError(rc, "smla_decode")

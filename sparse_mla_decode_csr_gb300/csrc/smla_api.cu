@@ -44,18 +44,18 @@ double split_cost(int64_t n_q, int heads, int64_t tiles, int s, int num_sms) {
 
 }  // namespace
 
-WorkspaceLayout workspace_layout(int32_t n_q, int32_t heads, int32_t splits) {
+WorkspaceLayout workspace_layout(int32_t n_q, int32_t heads, int32_t slots) {
   WorkspaceLayout w{};
-  if (splits <= 1) return w;
+  if (slots <= 0) return w;
   int64_t off = 0;
   w.ticket_off = off;
   off = align256(off + int64_t(n_q) * 4);
   w.o_off = off;
-  off = align256(off + int64_t(n_q) * splits * heads * kLatent * 4);
+  off = align256(off + int64_t(slots) * heads * kLatent * 4);
   w.ml_off = off;
-  off = align256(off + int64_t(n_q) * splits * heads * 2 * 4);
+  off = align256(off + int64_t(slots) * heads * 2 * 4);
   w.nv_off = off;
-  off = align256(off + int64_t(n_q) * splits * 4);
+  off = align256(off + int64_t(slots) * 4);
   w.total = off;
   return w;
 }
@@ -91,18 +91,36 @@ int smla_device_check(void) {
   return (major == 10 && minor == 3) ? SMLA_OK : SMLA_ERR_DEVICE;
 }
 
-int smla_plan(int32_t n_q, int32_t num_heads, int32_t max_row_len, int64_t n_indices,
-              int32_t num_splits, int32_t num_sms, smla_plan_info* plan) {
-  if (plan == nullptr) return SMLA_ERR_NULL;
-  if (n_q < 0 || num_heads < 1 || num_heads > SMLA_MAX_HEADS || n_indices < 0) return SMLA_ERR_SHAPE;
+int smla_plan(const smla_decode_params* p, int32_t num_sms, smla_plan_info* plan) {
+  if (plan == nullptr || p == nullptr) return SMLA_ERR_NULL;
+  const int32_t n_q = p->n_q, num_heads = p->num_heads, num_splits = p->num_splits;
+  if (n_q < 0 || num_heads < 1 || num_heads > SMLA_MAX_HEADS || p->n_indices < 0) return SMLA_ERR_SHAPE;
   if (num_splits < 0 || num_splits > SMLA_MAX_SPLITS) return SMLA_ERR_SPLITS;
+  if (p->kernel != SMLA_KERNEL_TENSOR_CORE && p->kernel != SMLA_KERNEL_CUDA_CORE) return SMLA_ERR_SHAPE;
   if (num_sms <= 0) {
     int rc = current_sm_count(&num_sms);
     if (rc != SMLA_OK) return rc;
   }
-  int64_t row_len = max_row_len;
-  if (row_len <= 0) row_len = n_q > 0 ? (n_indices + n_q - 1) / n_q : 0;
-  int64_t tiles = std::max<int64_t>(1, (row_len + kTile - 1) / kTile);
+  int64_t row_len = p->max_row_len;
+  if (row_len <= 0) row_len = n_q > 0 ? (p->n_indices + n_q - 1) / n_q : 0;
+  const int64_t tiles = std::max<int64_t>(1, (row_len + kTile - 1) / kTile);
+  *plan = smla_plan_info{};
+  plan->kernel = p->kernel;
+  plan->tile_len = kTile;
+  if (p->kernel == SMLA_KERNEL_TENSOR_CORE) {
+    // persistent: one CTA per SM, tiles balanced over them; forcing k splits
+    // spreads the tiles over n_q * k CTAs instead
+    int64_t g = num_splits > 0 ? int64_t(n_q) * num_splits : num_sms;
+    g = std::max<int64_t>(1, std::min<int64_t>(g, 65535));
+    plan->grid = n_q > 0 ? int32_t(g) : 0;
+    plan->num_splits = 0;
+    plan->chunk_len = 0;
+    plan->partial_slots = 2 * plan->grid;
+    // rows shared by many CTAs are merged by a separate, parallel kernel
+    plan->merge_kernel = (n_q > 0 && int64_t(plan->grid) > 4 * int64_t(n_q)) ? 1 : 0;
+    plan->workspace_bytes = n_q > 0 ? workspace_layout(n_q, num_heads, plan->partial_slots).total : 0;
+    return SMLA_OK;
+  }
   int s = 1;
   if (num_splits > 0) {
     s = num_splits;
@@ -117,19 +135,19 @@ int smla_plan(int32_t n_q, int32_t num_heads, int32_t max_row_len, int64_t n_ind
       }
     }
   }
-  int64_t per_chunk_tiles = (tiles + s - 1) / s;
+  const int64_t per_chunk_tiles = (tiles + s - 1) / s;
   plan->num_splits = s;
-  plan->tile_len = kTile;
   plan->chunk_len = int32_t(std::min<int64_t>(per_chunk_tiles * kTile, INT32_MAX / 2));
   plan->grid = int32_t(int64_t(n_q) * s);
-  plan->workspace_bytes = workspace_layout(n_q, num_heads, s).total;
+  plan->partial_slots = s > 1 ? n_q * s : 0;
+  plan->merge_kernel = 0;
+  plan->workspace_bytes = workspace_layout(n_q, num_heads, plan->partial_slots).total;
   return SMLA_OK;
 }
 
-size_t smla_decode_workspace_size(int32_t n_q, int32_t num_heads, int32_t max_row_len,
-                                  int64_t n_indices, int32_t num_splits) {
+size_t smla_decode_workspace_size(const smla_decode_params* params) {
   smla_plan_info plan{};
-  if (smla_plan(n_q, num_heads, max_row_len, n_indices, num_splits, 0, &plan) != SMLA_OK) return 0;
+  if (smla_plan(params, 0, &plan) != SMLA_OK) return 0;
   return size_t(plan.workspace_bytes);
 }
 
@@ -138,6 +156,7 @@ static int check_params(const smla_decode_params* p) {
   if (p->n_q < 0 || p->num_heads < 1 || p->num_heads > SMLA_MAX_HEADS) return SMLA_ERR_SHAPE;
   if (p->n_kv_rows < 0 || p->n_kv_rows > (int64_t(1) << 31) || p->n_indices < 0) return SMLA_ERR_SHAPE;
   if (p->num_splits < 0 || p->num_splits > SMLA_MAX_SPLITS) return SMLA_ERR_SPLITS;
+  if (p->kernel != SMLA_KERNEL_TENSOR_CORE && p->kernel != SMLA_KERNEL_CUDA_CORE) return SMLA_ERR_SHAPE;
   if (p->n_q == 0) return SMLA_OK;
   if (!p->q || !p->indptr || !p->out) return SMLA_ERR_NULL;
   if (p->n_kv_rows > 0 && !p->kv_cache) return SMLA_ERR_NULL;
@@ -155,7 +174,6 @@ static int check_params(const smla_decode_params* p) {
   if ((p->q_stride_row | p->q_stride_head | p->out_stride_row | p->out_stride_head) & 7)
     return SMLA_ERR_ALIGN;
   if (!std::isfinite(p->sm_scale)) return SMLA_ERR_SHAPE;
-  if (p->kernel != SMLA_KERNEL_TENSOR_CORE && p->kernel != SMLA_KERNEL_CUDA_CORE) return SMLA_ERR_SHAPE;
   return SMLA_OK;
 }
 
@@ -168,10 +186,9 @@ int smla_decode(const smla_decode_params* params, void* workspace, size_t worksp
   if (rc != SMLA_OK) return rc;
   DecodeLaunch L{};
   L.p = *params;
-  rc = smla_plan(params->n_q, params->num_heads, params->max_row_len, params->n_indices,
-                 params->num_splits, 0, &L.plan);
+  rc = smla_plan(params, 0, &L.plan);
   if (rc != SMLA_OK) return rc;
-  L.ws = workspace_layout(params->n_q, params->num_heads, L.plan.num_splits);
+  L.ws = workspace_layout(params->n_q, params->num_heads, L.plan.partial_slots);
   if (L.ws.total > 0 && (workspace == nullptr || int64_t(workspace_bytes) < L.ws.total))
     return SMLA_ERR_WORKSPACE;
   if (L.ws.total > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return SMLA_ERR_ALIGN;

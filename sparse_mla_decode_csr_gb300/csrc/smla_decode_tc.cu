@@ -1,32 +1,42 @@
-// Sparse MLA decode on the 5th-generation tensor cores (tcgen05, TMEM).
+// Sparse MLA decode on the 5th-generation tensor cores (tcgen05, TMEM),
+// persistent and balanced.
 //
-// One CTA per (row, chunk) unit; 64-key tiles, double-buffered.  Warp roles:
+// Schedule (documented with smla_plan in smla.h): every row is cut into 64-key
+// tiles, the rows' tiles are concatenated into one tile space, and CTA c of the
+// grid streams through the tiles [floor(c T / G), floor((c+1) T / G)) across
+// row boundaries.  A row wholly inside one CTA's range is finished there; a
+// shared row gets one (O, m, l) partial per CTA and is merged by its last CTA
+// to finish, or by the merge kernel below when rows are shared by many CTAs.
+//
+// Warp roles (16 warps):
 //   warps 0-3 (and 4-7 at 64 heads)  softmax: warpgroup g owns head columns
-//               [g*HH, (g+1)*HH), HH = all heads up to 32, 32 at 64 heads;
-//               they also stage q, rescale O when a running max moves, and run
-//               the epilogue with everyone else
-//   every other warp but 12  converters: gather the tile's 656-byte records (64-bit
-//               addressing), dequantise E4M3 * pow2 scale -> bf16 exactly, and
-//               write the 64 x 576 bf16 key tile in the 128-byte-swizzled
-//               K-major layout
+//               [g*HH, (g+1)*HH) (HH = all heads up to 32, 32 at 64 heads); they
+//               also stage q, move the reference maxima (rescaling O in TMEM),
+//               and run each row part's epilogue and merge
 //   warp 12     TMEM allocator and MMA issuer (one thread)
+//   all others  converters: gather each tile's 656-byte records (64-bit
+//               addressing; the next batch's loads in flight while this one is
+//               converted; records two tiles ahead prefetched into L2),
+//               dequantise E4M3 * pow2 scale -> bf16 exactly, and write the
+//               64 x 576 bf16 key tile in the 128-byte-swizzled K-major layout
+//               (the rope bytes go there by cp.async)
 //
-// Per tile i (stage s = i % 2):
+// Per tile i (stage s = i % 2), within the row part it belongs to:
 //   QK  S^T[64 keys, HP heads] = K_tile[64 x 576] . Q^T       (M=64, N=HP, K=576)
 //   softmax on S^T in log2 units with a lazily moved per-head reference max:
-//       p = 2^(x - m_ref) with x = s * sm_scale * log2 e, m_ref raised (and O
-//       rescaled in TMEM) only when a score exceeds m_ref + 8; p (<= 256) is
-//       written as bf16 P^T
+//       p = 2^(x - m_ref), x = s * sm_scale * log2 e; m_ref is raised (and O
+//       rescaled in TMEM) only when a score exceeds m_ref + 8, so p <= 256;
+//       p is written as bf16 P^T
 //   PV  O^T[128 d, HP] += V^T[128 d, 64 keys] . P^T[64 keys, HP], four 128-dim
 //       M tiles; V^T is the same shared-memory key tile read MN-major.
-// The split rows' partials and the last-arriver combine follow the CUDA-core
-// kernel (same workspace layout).
+// O has two TMEM buffers (alternating between row parts) where they fit.
 //
 // The maths is the sparse softmax attention of the gfx950 FlyDSL page (module
 // docstring: record layout, CSR tiles, masking; epilogue: out and LSE) with
-// the sink folded as the DeepSeek-V4.1 "K2 back" page's stage_combine does.
-// That page's design (scaled fp8 MFMA, LDS DMA) is prior art for other
-// hardware; this kernel dequantises to bf16 and uses tcgen05 instead.
+// the sink folded as the DeepSeek-V4.1 "K2 back" page's stage_combine does,
+// and its split/combine for rows shared between CTAs.  The pages' kernels
+// (scaled fp8 MFMA on gfx950, FP8 tcgen05 with a TMA gather4 front end on
+// SM100) are prior art; this kernel dequantises to bf16 (exact) instead.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
@@ -52,20 +62,24 @@ constexpr int kMmaWarp = 12;
 constexpr float kRescaleMargin = 8.f;            // p <= 2^8 before a max update
 constexpr float kInitMax = -1.0e30f;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
+constexpr int kMergeHeads = 8;                   // heads per merge-kernel CTA
+
+static_assert(kSchedTile == kTileK, "schedule and pipeline tiles must agree");
 
 struct Misc {
   uint32_t tmem_base;
   int32_t abort;
-  int32_t last_valid;
-  int32_t nvalid;
   int32_t is_last;
-  int32_t pad[3];
-  int32_t flag[2][2][4];         // [warpgroup][stage][quarter] rescale votes
+  int32_t first_row;      // schedule: first row of this CTA's range
+  int64_t first_tile;     // schedule: that row's first tile
+  int64_t total_tiles;    // schedule: T
+  int32_t flag[2][2][4];  // [warpgroup][stage][quarter] rescale votes
   uint8_t valid[kStages][kTileK];
-  float mref[64];                // per-head reference maxima (log2 units)
+  float mref[64];         // per-head reference maxima (log2 units)
   float alpha[2][32];
-  float red[2][4][32];           // tile maxima, then (after the last tile) key sums
+  float red[2][4][32];    // tile maxima; key sums at a part's end
   float fac[64];
+  int32_t nvr[4];         // key counts of a part, per quarter
 };
 
 template <int HP>
@@ -76,7 +90,8 @@ struct TcLayout {
   static constexpr int kSoftmaxWarps = 4 * SWG;
   static constexpr int kConvWarps = 15 - kSoftmaxWarps;
   static constexpr int kPerConv = (kTileK + kConvWarps - 1) / kConvWarps;  // records per converter warp and tile
-  static constexpr int kBatch = kPerConv <= 6 ? kPerConv : (kPerConv + 1) / 2;  // records in flight
+  static constexpr int kBatch = kPerConv <= 6 ? kPerConv : (kPerConv + 1) / 2;  // records per load batch
+  static constexpr int kSub = (kPerConv + kBatch - 1) / kBatch;                 // batches per tile
   static constexpr int HH = HP / SWG;             // head columns per softmax warpgroup
   static constexpr int q_bytes = kDChunks * HP * 128;
   static constexpr int p_row = 2 * HP;            // bytes of one key's P^T row
@@ -91,11 +106,15 @@ struct TcLayout {
   // slack to align the dynamic shared memory base to 1024 bytes, when it fits
   static constexpr int slack = used + 1024 <= 232448 ? 1024 : 0;
   static constexpr int total = used + slack;
-  static constexpr int tmem_cols = (6 * HP <= 128) ? 128 : (6 * HP <= 256 ? 256 : 512);
+  // TMEM: S stages [0, 2 HP), then n_ob O buffers of 4 HP columns each
+  static constexpr int n_ob = (2 * HP + 8 * HP <= 512) ? 2 : 1;
+  static constexpr int tmem_need = 2 * HP + n_ob * 4 * HP;
+  static constexpr int tmem_cols = tmem_need <= 128 ? 128 : (tmem_need <= 256 ? 256 : 512);
   static constexpr Swizzle p_swz = HP == 64 ? kSw128 : (HP == 32 ? kSw64 : kSw32);
   static constexpr uint32_t p_swmask = HP == 64 ? 7 : (HP == 32 ? 3 : 1);
   static constexpr uint32_t idesc_qk = idesc_bf16(64, HP, 0, 0);
   static constexpr uint32_t idesc_pv = idesc_bf16(128, HP, 1, 1);
+  __host__ __device__ static constexpr uint32_t o_col(int ob, int mt) { return 2 * HP + (ob * 4 + mt) * HP; }
 };
 
 // Offset of byte `b` (16-byte aligned) of row `r` inside a 128-byte-row
@@ -104,8 +123,8 @@ __device__ __forceinline__ uint32_t sw128_off(uint32_t r, uint32_t b) {
   return r * 128u + ((((b >> 4) ^ (r & 7u)) << 4) | (b & 15u));
 }
 
-// TMEM row of S^T for key r of the tile, for an M=64 MMA: rows 16 w .. 16 w + 15
-// sit in lanes 32 w .. 32 w + 15 of warp quarter w.
+// For an M=64 MMA, rows 16 w .. 16 w + 15 of S^T sit in lanes 32 w .. 32 w + 15
+// of TMEM lane quarter w: lanes 0-15 of each warp hold keys.
 __device__ __forceinline__ bool s_lane_active(int lane) { return lane < 16; }
 
 __device__ __forceinline__ void set_abort(Misc* ms, const DecodeArgs& a) {
@@ -128,6 +147,13 @@ __device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity, Mi
   return __all_sync(0xffffffffu, wait_bar(bar, parity, ms, a));
 }
 
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)),
+               "l"(__cvta_generic_to_global(gmem_src))
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // 16 E4M3 bytes times a power-of-two scale -> 16 bf16 (exact), as 2 x uint4.
 __device__ __forceinline__ void dequant16_bf16(uint4 v, float scale, uint4& lo, uint4& hi) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -145,15 +171,136 @@ __device__ __forceinline__ void dequant16_bf16(uint4 v, float scale, uint4& lo, 
   hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
+// Walks this CTA's tiles: row, slice positions, and where the row part starts
+// and ends.  Every role keeps its own copy and advances it tile by tile.
+struct Cursor {
+  int32_t row;      // current row
+  int32_t len;      // its slice length
+  int32_t ntiles;   // its tile count T_row
+  int32_t ta, tb;   // this CTA's tiles of the row: [ta, tb)
+  int32_t t;        // current tile of the row
+  int64_t P;        // the row's first tile in the tile space
+  int64_t beg;      // offset of the row's slice in indices[]
+  int64_t e;        // end of this CTA's range
+  bool live;
+
+  __device__ __forceinline__ void load_row(const DecodeArgs& a) {
+    len = row_len(a, row);
+    ntiles = tiles_of_len(len);
+    beg = __ldg(a.indptr + row);
+    tb = int32_t((e - P) < int64_t(ntiles) ? (e - P) : int64_t(ntiles));
+  }
+  __device__ __forceinline__ void init(const DecodeArgs& a, int32_t r0, int64_t P0, int64_t b, int64_t e_) {
+    row = r0;
+    P = P0;
+    e = e_;
+    live = b < e_ && r0 < a.n_q;
+    ta = tb = t = 0;
+    if (!live) return;
+    load_row(a);
+    ta = int32_t(b - P);
+    t = ta;
+  }
+  __device__ __forceinline__ void advance(const DecodeArgs& a) {
+    if (!live) return;
+    if (++t < tb) return;
+    P += ntiles;
+    ++row;
+    if (P >= e || row >= a.n_q) {
+      live = false;
+      return;
+    }
+    load_row(a);
+    ta = 0;
+    t = 0;
+  }
+  __device__ __forceinline__ bool first() const { return t == ta; }
+  __device__ __forceinline__ bool last() const { return t == tb - 1; }
+  __device__ __forceinline__ bool whole() const { return ta == 0 && tb == ntiles; }
+  __device__ __forceinline__ int32_t p0() const { return t * kTileK; }
+  __device__ __forceinline__ int32_t p1() const {
+    const int32_t x = t * kTileK + kTileK;
+    return x < len ? x : len;
+  }
+};
+
+// CTAs (with non-empty ranges) holding tiles of the row whose tiles are
+// [P, P + nt): their count, and the range [c_a, c_b] to scan.
+__device__ __forceinline__ int32_t row_parts(int64_t P, int32_t nt, int64_t T, int64_t G, int64_t* ca,
+                                             int64_t* cb) {
+  *ca = cta_of_tile(P, T, G);
+  *cb = cta_of_tile(P + nt - 1, T, G);
+  int32_t n = 0;
+  for (int64_t c = *ca; c <= *cb; ++c) n += cta_begin(c + 1, T, G) > cta_begin(c, T, G);
+  return n;
+}
+
+// Merge the partials of row `row` (tiles [P, P + nt)) for heads [h0, h1) and
+// write out / lse (and n_valid when write_nv).  Threads [0, nthr) of the
+// caller take latent dims tid, tid + nthr, ...
+__device__ void merge_row(const DecodeArgs& a, int32_t row, int64_t P, int32_t nt, int64_t T, int64_t G,
+                          int h0, int h1, int tid, int nthr, bool write_nv) {
+  const int H = a.heads;
+  int64_t ca, cb;
+  row_parts(P, nt, T, G, &ca, &cb);
+  for (int h = h0; h < h1; ++h) {
+    float mstar = -INFINITY;
+    for (int64_t c = ca; c <= cb; ++c) {
+      if (cta_begin(c + 1, T, G) == cta_begin(c, T, G)) continue;
+      const int64_t o = (part_slot(c, P, T, G) * H + h) * 2;
+      if (__ldcg(a.ml_part + o + 1) > 0.f) mstar = fmaxf(mstar, __ldcg(a.ml_part + o));
+    }
+    float L = 0.f;
+    for (int64_t c = ca; c <= cb; ++c) {
+      if (cta_begin(c + 1, T, G) == cta_begin(c, T, G)) continue;
+      const int64_t o = (part_slot(c, P, T, G) * H + h) * 2;
+      const float lc = __ldcg(a.ml_part + o + 1);
+      if (lc > 0.f) L += lc * exp2f(__ldcg(a.ml_part + o) - mstar);
+    }
+    float fac, lse;
+    finish_head(mstar, L, a.sink, h, &fac, &lse);
+    if (tid == 0 && a.lse) a.lse[int64_t(row) * H + h] = lse;
+    for (int d = tid; d < kLatent; d += nthr) {
+      float acc = 0.f;
+      for (int64_t c = ca; c <= cb; ++c) {
+        if (cta_begin(c + 1, T, G) == cta_begin(c, T, G)) continue;
+        const int64_t sl = part_slot(c, P, T, G);
+        const int64_t o = (sl * H + h) * 2;
+        const float lc = __ldcg(a.ml_part + o + 1);
+        if (lc > 0.f)
+          acc = fmaf(exp2f(__ldcg(a.ml_part + o) - mstar), __ldcg(a.o_part + (sl * H + h) * kLatent + d), acc);
+      }
+      a.out[row * a.out_stride_row + h * a.out_stride_head + d] = __bfloat16_as_ushort(__float2bfloat16_rn(acc * fac));
+    }
+  }
+  if (write_nv && tid == 0 && a.n_valid) {
+    int tot = 0;
+    for (int64_t c = ca; c <= cb; ++c) {
+      if (cta_begin(c + 1, T, G) == cta_begin(c, T, G)) continue;
+      tot += __ldcg(a.nv_part + part_slot(c, P, T, G));
+    }
+    a.n_valid[row] = tot;
+  }
+}
+
 template <int HP>
 __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) {
   using Lay = TcLayout<HP>;
   constexpr int HH = Lay::HH;
   constexpr int kSoftmaxWarps = Lay::kSoftmaxWarps;
+  constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
   constexpr int kConvWarps = Lay::kConvWarps;
   constexpr int kPerConv = Lay::kPerConv;
   constexpr int kBatch = Lay::kBatch;
+  constexpr int kSub = Lay::kSub;
+  static_assert(Lay::total <= 232448, "shared memory over the per-block limit");
   extern __shared__ uint8_t smem_raw[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (Lay::slack == 0 && (smem_u32(smem_raw) & 1023u) != 0) {
+    // no room to realign: refuse (uniformly, before any barrier or TMEM use)
+    if (tid == 0 && a.status) atomicOr(a.status, SMLA_STATUS_TIMEOUT);
+    return;
+  }
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* tiles = smem;
   uint8_t* q_s = smem + Lay::off_q;
@@ -165,18 +312,13 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
   uint64_t* s_empty = bars + 6;
   uint64_t* p_full = bars + 8;
   uint64_t* pv_done = bars + 10;
-  uint64_t* q_full = bars + 12;
-  uint64_t* mma_drain = bars + 13;
+  uint64_t* o_free = bars + 12;
+  uint64_t* q_full = bars + 14;
+  uint64_t* mma_drain = bars + 15;
   Misc* ms = reinterpret_cast<Misc*>(smem + Lay::off_misc);
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (Lay::slack == 0 && (smem_u32(smem_raw) & 1023u) != 0) {
-    // no room to realign: refuse (uniformly, before any barrier or TMEM use)
-    if (tid == 0 && a.status) atomicOr(a.status, SMLA_STATUS_TIMEOUT);
-    return;
-  }
-  const Unit u = unit_of(a, blockIdx.x);
   const int H = a.heads;
+  const int64_t G = gridDim.x;
+  const int64_t c_id = blockIdx.x;
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -186,66 +328,110 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
       mbar_init(s_empty + s, kSoftmaxWarps);
       mbar_init(p_full + s, kSoftmaxWarps);
       mbar_init(pv_done + s, 1);
+      mbar_init(o_free + s, kSoftmaxWarps);
     }
     mbar_init(q_full, kSoftmaxWarps);
     mbar_init(mma_drain, 1);
     ms->abort = 0;
-    for (int h = 0; h < 64; ++h) ms->mref[h] = kInitMax;
-    ms->last_valid = u.p0 - 1;
-    ms->nvalid = 0;
     ms->is_last = 0;
+    ms->first_row = a.n_q;
+    ms->first_tile = 0;
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
     tmem_alloc(&ms->tmem_base, Lay::tmem_cols);
     tmem_relinquish();
   }
-  // Rows padded with -1 (has_invalid): stop after the last entry >= 0.
-  int p1 = u.p1;
-  if (a.has_invalid && u.p1 > u.p0) {
+
+  // ---- schedule: tile counts of all rows, their prefix, and this CTA's first row.
+  {
+    int64_t* scan = reinterpret_cast<int64_t*>(tiles);  // tiles are free until the pipeline starts
+    const int n = a.n_q;
+    const int per = (n + kThreadsTC - 1) / kThreadsTC;
+    const int lo = min(tid * per, n), hi = min(lo + per, n);
+    int64_t local = 0;
+    for (int r = lo; r < hi; ++r) local += tiles_of_len(row_len(a, r));
+    scan[tid] = local;
     __syncthreads();
-    int last = u.p0 - 1;
-    for (int p = u.p0 + tid; p < u.p1; p += kThreadsTC) {
-      const int64_t off = u.beg + p;
-      if (off >= 0 && off < a.n_indices && __ldg(a.indices + off) >= 0) last = p;
+    if (warp == 0) {  // exclusive scan of the 512 partial sums by one warp
+      int64_t run = 0;
+      for (int base = 0; base < kThreadsTC; base += 32) {
+        const int64_t v = scan[base + lane];
+        int64_t x = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+          if (lane >= o) x += y;
+        }
+        scan[base + lane] = run + x - v;
+        run += __shfl_sync(0xffffffffu, x, 31);
+      }
+      if (lane == 0) ms->total_tiles = run;
     }
-    if (last >= u.p0) atomicMax(&ms->last_valid, last);
+    __syncthreads();
+    const int64_t Tt = ms->total_tiles;
+    const int64_t b = cta_begin(c_id, Tt, G);
+    int64_t P = scan[tid];
+    for (int r = lo; r < hi; ++r) {
+      const int32_t nt_r = tiles_of_len(row_len(a, r));
+      if (P <= b && b < P + nt_r) {
+        ms->first_row = r;
+        ms->first_tile = P;
+      }
+      P += nt_r;
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (a.has_invalid) p1 = ms->last_valid + 1 > u.p0 ? ms->last_valid + 1 : u.p0;
-  const int nt = (p1 - u.p0 + kTileK - 1) / kTileK;
+  const int64_t T = ms->total_tiles;
+  const int64_t cb = cta_begin(c_id, T, G), ce = cta_begin(c_id + 1, T, G);
+  const int32_t n_tiles = int32_t(ce - cb);  // this CTA's tiles
+  const int32_t row0 = ms->first_row;
+  const int64_t P0 = ms->first_tile;
   const uint32_t tmem = ms->tmem_base;
   const uint32_t tiles_u32 = smem_u32(tiles);
   const uint32_t q_u32 = smem_u32(q_s);
   const uint32_t p_u32 = smem_u32(p_s);
 
-  float lpart[HH];
-#pragma unroll
-  for (int h = 0; h < HH; ++h) lpart[h] = 0.f;
-
   if (warp < kSoftmaxWarps) {
-    // ---------------- softmax warpgroups ----------------
+    // =================== softmax warpgroups ===================
     const int wg = warp >> 2, qd = warp & 3;
-    for (int i = tid; i < HP * (kQK / 8); i += 32 * kSoftmaxWarps) {
-      const int h = i / (kQK / 8), c16 = i % (kQK / 8);
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (h < H)
-        v = __ldg(reinterpret_cast<const uint4*>(a.q + u.row * a.q_stride_row + h * a.q_stride_head + c16 * 8));
-      const uint32_t off = uint32_t(c16 >> 3) * (HP * 128) + uint32_t(h >> 3) * 1024u + sw128_off(h & 7, (c16 & 7) * 16);
-      *reinterpret_cast<uint4*>(q_s + off) = v;
-    }
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(q_full);
-
     const bool active = s_lane_active(lane);
     const int r = 16 * qd + lane;  // key of this thread within the tile (active lanes)
-    const float* mr = ms->mref + wg * HH;  // this warpgroup's reference maxima (uniform)
-    for (int j = 0; j < nt; ++j) {
-      const int s = j & 1;
-      const uint32_t ph = (j >> 1) & 1;
+    float* mr = ms->mref + wg * HH;  // this warpgroup's reference maxima (uniform)
+    float lpart[HH];
+#pragma unroll
+    for (int h = 0; h < HH; ++h) lpart[h] = 0.f;
+    int nv = 0;
+    Cursor c;
+    c.init(a, row0, P0, cb, ce);
+    int seg = 0;
+    for (int i = 0; i < n_tiles; ++i) {
+      const int s = i & 1;
+      const uint32_t ph = (i >> 1) & 1;
+      const bool first = c.first(), last = c.last();
+      const int ob = Lay::n_ob == 2 ? (seg & 1) : 0;
+      if (first) {
+        // stage this row's q (bf16, 128-byte swizzled K-major [9][HP][128]).
+        // Every QK that read the previous q has completed: this warpgroup
+        // has consumed their S.
+        for (int k = tid; k < HP * (kQK / 8); k += kSoftmaxThreads) {
+          const int h = k / (kQK / 8), c16 = k % (kQK / 8);
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (h < H)
+            v = __ldg(reinterpret_cast<const uint4*>(a.q + c.row * a.q_stride_row + h * a.q_stride_head + c16 * 8));
+          const uint32_t off =
+              uint32_t(c16 >> 3) * (HP * 128) + uint32_t(h >> 3) * 1024u + sw128_off(h & 7, (c16 & 7) * 16);
+          *reinterpret_cast<uint4*>(q_s + off) = v;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(q_full);
+#pragma unroll
+        for (int h = 0; h < HH; ++h) lpart[h] = 0.f;
+        nv = 0;
+      }
       wait_bar_warp(kv_full + s, ph, ms, a);
       wait_bar_warp(s_full + s, ph, ms, a);
       tc_fence_after();
@@ -253,19 +439,20 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
       {
         const uint32_t taddr = tmem + (uint32_t(32 * qd) << 16) + uint32_t(s * HP + wg * HH);
 #pragma unroll
-        for (int c = 0; c < HH / 8; ++c) {
+        for (int cc = 0; cc < HH / 8; ++cc) {
           uint32_t v[8];
-          tmem_ld8(taddr + 8 * c, v);
+          tmem_ld8(taddr + 8 * cc, v);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) x[8 * c + k] = __uint_as_float(v[k]);
+          for (int k = 0; k < 8; ++k) x[8 * cc + k] = __uint_as_float(v[k]);
         }
         tmem_wait_ld();
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(s_empty + s);
-      const bool valid = active && (r < kTileK) && ms->valid[s][active ? r : 0];
-      bool need = false;
+      const bool valid = active && ms->valid[s][r];
+      nv += valid;
+      bool need = first;
 #pragma unroll
       for (int h = 0; h < HH; ++h) {
         x[h] = valid ? x[h] * a.sm_scale_log2 : -INFINITY;
@@ -277,6 +464,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
       need = ms->flag[wg][s][0] | ms->flag[wg][s][1] | ms->flag[wg][s][2] | ms->flag[wg][s][3];
       if (need) {
         // exact tile max of this warpgroup's heads, then move the references
+        // (a row part starts from scratch: its old reference is -inf)
 #pragma unroll
         for (int h = 0; h < HH; ++h) {
           float t = x[h];
@@ -289,7 +477,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
         for (int h = 0; h < HH; ++h) {
           const float tm = fmaxf(fmaxf(ms->red[wg][0][h], ms->red[wg][1][h]),
                                  fmaxf(ms->red[wg][2][h], ms->red[wg][3][h]));
-          const float al = ex2(mr[h] - fmaxf(mr[h], tm));
+          const float old = first ? kInitMax : mr[h];
+          const float al = ex2(old - fmaxf(old, tm));
           lpart[h] *= al;
           if (tid == wg * 128) ms->alpha[wg][h] = al;
         }
@@ -298,27 +487,28 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
           for (int h = 0; h < HH; ++h) {
             const float tm = fmaxf(fmaxf(ms->red[wg][0][h], ms->red[wg][1][h]),
                                    fmaxf(ms->red[wg][2][h], ms->red[wg][3][h]));
-            ms->mref[wg * HH + h] = fmaxf(mr[h], tm);
+            const float old = first ? kInitMax : mr[h];
+            mr[h] = fmaxf(old, tm);
           }
         }
         named_barrier(1 + wg, 128);  // the new references are visible
-        if (j > 0) {
+        if (!first) {
           // O^T columns of this warpgroup's heads, all four 128-dim tiles:
-          // wait for PV(j-1), then scale in place.
-          wait_bar_warp(pv_done + ((j - 1) & 1), ((j - 1) >> 1) & 1, ms, a);
+          // wait for PV(i-1), then scale in place.
+          wait_bar_warp(pv_done + ((i - 1) & 1), ((i - 1) >> 1) & 1, ms, a);
           tc_fence_after();
 #pragma unroll 1
           for (int mt = 0; mt < 4; ++mt) {
-            const uint32_t taddr = tmem + (uint32_t(32 * qd) << 16) + uint32_t(2 * HP + mt * HP + wg * HH);
+            const uint32_t taddr = tmem + (uint32_t(32 * qd) << 16) + Lay::o_col(ob, mt) + uint32_t(wg * HH);
 #pragma unroll
-            for (int c = 0; c < HH / 8; ++c) {
+            for (int cc = 0; cc < HH / 8; ++cc) {
               uint32_t v[8];
-              tmem_ld8(taddr + 8 * c, v);
+              tmem_ld8(taddr + 8 * cc, v);
               tmem_wait_ld();
 #pragma unroll
               for (int k = 0; k < 8; ++k)
-                v[k] = __float_as_uint(__uint_as_float(v[k]) * ms->alpha[wg][8 * c + k]);
-              tmem_st8(taddr + 8 * c, v);
+                v[k] = __float_as_uint(__uint_as_float(v[k]) * ms->alpha[wg][8 * cc + k]);
+              tmem_st8(taddr + 8 * cc, v);
             }
           }
           tmem_wait_st();
@@ -329,66 +519,165 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
 #pragma unroll
       for (int h = 0; h < HH; h += 2) {
         const float p0 = ex2(x[h] - mr[h]);
-        const float p1v = ex2(x[h + 1] - mr[h + 1]);
+        const float p1 = ex2(x[h + 1] - mr[h + 1]);
         lpart[h] += p0;
-        lpart[h + 1] += p1v;
-        pk[h / 2] = pack_bf16x2(p0, p1v);
+        lpart[h + 1] += p1;
+        pk[h / 2] = pack_bf16x2(p0, p1);
       }
       // the P stage is free once the PV that last read it has completed
       if (Lay::p_stages == 2)
-        wait_bar_warp(pv_done + s, ph ^ 1, ms, a);  // PV(j-2)
-      else if (j > 0)
-        wait_bar_warp(pv_done + ((j - 1) & 1), ((j - 1) >> 1) & 1, ms, a);  // PV(j-1)
+        wait_bar_warp(pv_done + s, ph ^ 1, ms, a);  // PV(i-2)
+      else if (i > 0)
+        wait_bar_warp(pv_done + ((i - 1) & 1), ((i - 1) >> 1) & 1, ms, a);  // PV(i-1)
       const int ps = Lay::p_stages == 2 ? s : 0;
       if (active) {
         uint8_t* prow = p_s + ps * Lay::p_bytes;
 #pragma unroll
-        for (int c = 0; c < HH / 8; ++c) {
-          uint32_t off = uint32_t(r) * Lay::p_row + uint32_t(wg * (HH / 8) + c) * 16u;
+        for (int cc = 0; cc < HH / 8; ++cc) {
+          uint32_t off = uint32_t(r) * Lay::p_row + uint32_t(wg * (HH / 8) + cc) * 16u;
           off ^= ((off >> 7) & Lay::p_swmask) << 4;
-          *reinterpret_cast<uint4*>(prow + off) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+          *reinterpret_cast<uint4*>(prow + off) = make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full + s);
-    }
-    // per-head sums of this warpgroup over its 64 keys, and the final maxima
+
+      if (last) {
+        // ---------- epilogue of this row part ----------
 #pragma unroll
-    for (int h = 0; h < HH; ++h) {
-      float t = active ? lpart[h] : 0.f;
+        for (int h = 0; h < HH; ++h) {
+          float t = active ? lpart[h] : 0.f;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-      if (lane == 0) ms->red[wg][qd][h] = t;
+          for (int o = 1; o < 32; o <<= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+          if (lane == 0) ms->red[wg][qd][h] = t;
+        }
+        if (wg == 0) {
+          int t = nv;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+          if (lane == 0) ms->nvr[qd] = t;
+        }
+        named_barrier(3, kSoftmaxThreads);
+        const bool whole = c.whole();
+        const int64_t slot = whole ? -1 : part_slot(c_id, c.P, T, G);
+        const int row = c.row;
+        if (tid < H) {
+          const int g = tid / HH, hh = tid % HH;
+          const float l = ms->red[g][0][hh] + ms->red[g][1][hh] + ms->red[g][2][hh] + ms->red[g][3][hh];
+          const float m = ms->mref[tid];
+          if (whole) {
+            float fac, lse;
+            finish_head(m, l, a.sink, tid, &fac, &lse);
+            ms->fac[tid] = fac;
+            if (a.lse) a.lse[int64_t(row) * H + tid] = lse;
+          } else {
+            a.ml_part[(slot * H + tid) * 2] = l > 0.f ? m : -INFINITY;
+            a.ml_part[(slot * H + tid) * 2 + 1] = l > 0.f ? l : 0.f;
+          }
+        }
+        if (tid == 0) {
+          const int tot = ms->nvr[0] + ms->nvr[1] + ms->nvr[2] + ms->nvr[3];
+          if (whole) {
+            if (a.n_valid) a.n_valid[row] = tot;
+          } else {
+            a.nv_part[slot] = tot;
+          }
+        }
+        named_barrier(3, kSoftmaxThreads);
+        // O^T of the part: wait for its last PV, then read it out.
+        wait_bar_warp(pv_done + s, ph, ms, a);
+        tc_fence_after();
+#pragma unroll 1
+        for (int mt = wg; mt < 4; mt += Lay::SWG) {
+          const int dg = mt * 128 + qd * 32 + lane;
+#pragma unroll 1
+          for (int cc = 0; cc < HP / 8; ++cc) {
+            uint32_t v[8];
+            tmem_ld8(tmem + (uint32_t(32 * qd) << 16) + Lay::o_col(ob, mt) + uint32_t(8 * cc), v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const int h = 8 * cc + k;
+              if (h >= H) break;
+              const float o = __uint_as_float(v[k]);
+              if (whole)
+                a.out[row * a.out_stride_row + h * a.out_stride_head + dg] =
+                    __bfloat16_as_ushort(__float2bfloat16_rn(o * ms->fac[h]));
+              else
+                a.o_part[(slot * H + h) * kLatent + dg] = o;
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(o_free + ob);
+        if (!whole && !a.merge_kernel) {
+          // the row's last CTA to finish merges its partials
+          __threadfence();
+          named_barrier(3, kSoftmaxThreads);
+          if (tid == 0) {
+            int64_t ca, cbb;
+            const int32_t n = row_parts(c.P, c.ntiles, T, G, &ca, &cbb);
+            ms->is_last = (atomicAdd(a.ticket + row, 1) == n - 1);
+          }
+          named_barrier(3, kSoftmaxThreads);
+          if (ms->is_last) {
+            __threadfence();
+            merge_row(a, row, c.P, c.ntiles, T, G, 0, H, tid, kSoftmaxThreads, true);
+            if (tid == 0) a.ticket[row] = 0;  // leave the counter zero for the next call
+          }
+          named_barrier(3, kSoftmaxThreads);
+        }
+        ++seg;
+      }
+      c.advance(a);
     }
   } else if (warp == kMmaWarp) {
-    // ---------------- MMA issuer ----------------
+    // =================== MMA issuer ===================
     if (lane == 0) {
-      bool ok = wait_bar(q_full, 0, ms, a);
-      auto issue_pv = [&](int j) -> bool {
+      Cursor c;
+      c.init(a, row0, P0, cb, ce);
+      bool ok = true;
+      int seg = 0, q_uses = 0;
+      bool prev_first = false;
+      int prev_ob = 0, prev_seg = 0;
+      auto issue_pv = [&](int j, bool pfirst, int ob, int sg) -> bool {
         const int s = j & 1;
+        if (pfirst && !wait_bar(o_free + ob, ((sg / Lay::n_ob) & 1) ^ 1, ms, a)) return false;
         if (!wait_bar(p_full + s, (j >> 1) & 1, ms, a)) return false;
         tc_fence_after();
         const uint32_t tile = tiles_u32 + s * kTileBytes;
         const uint32_t pst = p_u32 + (Lay::p_stages == 2 ? s : 0) * Lay::p_bytes;
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt) {
-          const uint32_t d = tmem + uint32_t(2 * HP + mt * HP);
+          const uint32_t d = tmem + Lay::o_col(ob, mt);
 #pragma unroll
           for (int k = 0; k < kTileK / 16; ++k) {
             const uint64_t ad = smem_desc(tile + (2 * mt) * kChunkBytes + k * 2048, kChunkBytes, 1024, kSw128);
             const uint64_t bd = smem_desc(pst + k * 16 * Lay::p_row, 8 * Lay::p_row, 8 * Lay::p_row, Lay::p_swz);
-            mma_f16_ss(d, ad, bd, Lay::idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+            mma_f16_ss(d, ad, bd, Lay::idesc_pv, (pfirst && k == 0) ? 0u : 1u);
           }
         }
         mma_commit(kv_empty + s);
         mma_commit(pv_done + s);
         return true;
       };
-      for (int i = 0; ok && i < nt; ++i) {
+      for (int i = 0; ok && i < n_tiles; ++i) {
         const int s = i & 1;
         const uint32_t ph = (i >> 1) & 1;
+        const bool first = c.first();
+        // a row part's last PV goes out before the next part's QK, whose q
+        // the softmax stages only after that part's epilogue has read O
+        if (first && i > 0 && !issue_pv(i - 1, prev_first, prev_ob, prev_seg)) {
+          ok = false;
+          break;
+        }
+        if (first && !wait_bar(q_full, (q_uses++) & 1, ms, a)) {
+          ok = false;
+          break;
+        }
         if (!wait_bar(kv_full + s, ph, ms, a) || !wait_bar(s_empty + s, ph ^ 1, ms, a)) {
           ok = false;
           break;
@@ -398,217 +687,177 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
         const uint32_t d = tmem + uint32_t(s * HP);
 #pragma unroll
         for (int k = 0; k < kQK / 16; ++k) {
-          const int c = k >> 2, kk = k & 3;
-          const uint64_t ad = smem_desc(tile + c * kChunkBytes + kk * 32, 16, 1024, kSw128);
-          const uint64_t bd = smem_desc(q_u32 + c * (HP * 128) + kk * 32, 16, 1024, kSw128);
+          const int ch = k >> 2, kk = k & 3;
+          const uint64_t ad = smem_desc(tile + ch * kChunkBytes + kk * 32, 16, 1024, kSw128);
+          const uint64_t bd = smem_desc(q_u32 + ch * (HP * 128) + kk * 32, 16, 1024, kSw128);
           mma_f16_ss(d, ad, bd, Lay::idesc_qk, k > 0 ? 1u : 0u);
         }
         mma_commit(s_full + s);
-        if (i > 0 && !issue_pv(i - 1)) {
+        if (!first && i > 0 && !issue_pv(i - 1, prev_first, prev_ob, prev_seg)) {
           ok = false;
           break;
         }
+        prev_first = first;
+        prev_ob = Lay::n_ob == 2 ? (seg & 1) : 0;
+        prev_seg = seg;
+        if (c.last()) ++seg;
+        c.advance(a);
       }
-      if (ok && nt > 0) issue_pv(nt - 1);
-      // every issued MMA has completed before anyone reads O or frees TMEM
+      if (ok && n_tiles > 0) issue_pv(n_tiles - 1, prev_first, prev_ob, prev_seg);
+      // every issued MMA has completed before TMEM is freed
       mma_commit(mma_drain);
       if (!mbar_wait(mma_drain, 0, kWaitLimitNs)) set_abort(ms, a);
     }
     __syncwarp();
   } else {
-    // ---------------- converters ----------------
-    // Warp cw takes records cw, cw + 7, ... of each tile (kPerConv at most).
-    // Lane k holds the record row of the warp's k-th record; the records of
-    // tile i + 2 are prefetched into L2 while tile i is converted.
-    const int cw = warp < kMmaWarp ? warp - kSoftmaxWarps : warp - kSoftmaxWarps - 1;  // 0..6
-    int nvalid = 0;
+    // =================== converters ===================
+    // Warp cw takes records cw, cw + kConvWarps, ... of each tile (kPerConv at
+    // most), in kSub batches of kBatch; lane k holds the record row of the
+    // warp's k-th record of a tile.  The next batch's loads are in flight while
+    // this one is converted; tiles two ahead are prefetched into L2.
+    const int cw = warp < kMmaWarp ? warp - kSoftmaxWarps : warp - kSoftmaxWarps - 1;
     const int ck = lane >> 2;                 // 64-dim column block of this lane's 16 dims
     const int b0 = (lane & 3) * 32;           // byte offset of those dims within the 128-byte row
     const bool hi_first = (lane >> 2) & 1;    // alternate store order: conflict-free phases
-    auto tile_keys = [&](int i) -> int32_t {  // this lane's record row in tile i, or -1
-      const int r = cw + kConvWarps * lane;
-      const int p = u.p0 + i * kTileK + r;
-      return (i < nt && lane < kPerConv && r < kTileK && p < p1) ? key_of(a, u.beg, p) : -1;
+    auto tile_keys = [&](const Cursor& cu) -> int32_t {  // this lane's record row, or -1
+      const int rr = cw + kConvWarps * lane;
+      if (!cu.live || lane >= kPerConv || rr >= kTileK) return -1;
+      const int p = cu.p0() + rr;
+      return p < cu.p1() ? key_of(a, cu.beg, p) : -1;
     };
     auto prefetch = [&](int32_t id) {
       if (id >= 0) prefetch_l2(a.kv + int64_t(id) * kRecordBytes, kRecordBytes);
     };
-    int32_t key_cur = tile_keys(0);
-    int32_t key_nxt = tile_keys(1);
-    prefetch(key_cur);
-    prefetch(key_nxt);
-    for (int i = 0; i < nt; ++i) {
+    struct Batch {
+      int32_t id[kBatch];
+      uint4 lat[kBatch];
+      float sc[kBatch];
+    };
+    auto load_batch = [&](Batch& B, int32_t keys, int sub) {
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int kk = sub * kBatch + k;
+        const int32_t id = __shfl_sync(0xffffffffu, keys, kk & 31);
+        B.id[k] = kk < kPerConv ? id : -1;
+        B.lat[k] = make_uint4(0, 0, 0, 0);
+        B.sc[k] = 0.f;
+        if (B.id[k] >= 0) {
+          const uint8_t* rec = a.kv + int64_t(B.id[k]) * kRecordBytes;
+          B.lat[k] = __ldg(reinterpret_cast<const uint4*>(rec) + lane);
+          B.sc[k] = __ldg(reinterpret_cast<const float*>(rec + kScaleOffset) + (lane >> 3));
+        }
+      }
+    };
+    Cursor cl;  // the tile whose batches are being loaded
+    cl.init(a, row0, P0, cb, ce);
+    Cursor cp = cl;  // two tiles ahead of cl, for L2 prefetch
+    int32_t keys_l = tile_keys(cl);
+    prefetch(keys_l);
+    cp.advance(a);
+    prefetch(tile_keys(cp));
+    cp.advance(a);
+    prefetch(tile_keys(cp));
+    int sub_l = 0;  // batch index within cl
+    Batch A;
+    load_batch(A, keys_l, 0);
+    const int n_batches = n_tiles * kSub;
+    for (int q = 0; q < n_batches; ++q) {
+      const int i = q / kSub, sub = q % kSub;
       const int s = i & 1;
       const uint32_t ph = (i >> 1) & 1;
       uint8_t* tile = tiles + s * kTileBytes;
-      const int32_t key_nn = tile_keys(i + 2);
-      prefetch(key_nn);
-      bool waited = false;
-      bool ok = true;
-      for (int k0 = 0; k0 < kPerConv; k0 += kBatch) {
-        int32_t idx[kBatch];
-        uint4 lat[kBatch], rp[kBatch];
-        float sc[kBatch];
+      // loads of the next batch (the next tile's first, at a tile boundary)
+      Batch B;
+      if (++sub_l == kSub) {
+        sub_l = 0;
+        cl.advance(a);
+        keys_l = tile_keys(cl);
+        cp.advance(a);
+        prefetch(tile_keys(cp));
+      }
+      if (q + 1 < n_batches) {
+        load_batch(B, keys_l, sub_l);
+      } else {
 #pragma unroll
-        for (int b = 0; b < kBatch; ++b) {
-          const int32_t id = __shfl_sync(0xffffffffu, key_cur, (k0 + b) & 31);
-          idx[b] = (k0 + b < kPerConv) ? id : -1;
-          lat[b] = make_uint4(0, 0, 0, 0);
-          rp[b] = make_uint4(0, 0, 0, 0);
-          sc[b] = 0.f;
-          if (idx[b] >= 0) {
-            const uint8_t* rec = a.kv + int64_t(idx[b]) * kRecordBytes;
-            lat[b] = __ldg(reinterpret_cast<const uint4*>(rec) + lane);
-            sc[b] = __ldg(reinterpret_cast<const float*>(rec + kScaleOffset) + (lane >> 3));
-            if (lane < 8) rp[b] = __ldg(reinterpret_cast<const uint4*>(rec + kRopeOffset) + lane);
-          }
-        }
-        if (!waited) {
-          waited = true;
-          if (!wait_bar_warp(kv_empty + s, ph ^ 1, ms, a)) {
-            ok = false;
-            break;
-          }
-        }
-#pragma unroll
-        for (int b = 0; b < kBatch; ++b) {
-          const int r = cw + kConvWarps * (k0 + b);
-          if (k0 + b >= kPerConv || r >= kTileK) break;
-          uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
-          if (idx[b] >= 0) dequant16_bf16(lat[b], sc[b], lo, hi);
-          uint8_t* rowbase = tile + ck * kChunkBytes + (r >> 3) * 1024;
-          const uint4 first = hi_first ? hi : lo, second = hi_first ? lo : hi;
-          *reinterpret_cast<uint4*>(rowbase + sw128_off(r & 7, b0 + (hi_first ? 16 : 0))) = first;
-          *reinterpret_cast<uint4*>(rowbase + sw128_off(r & 7, b0 + (hi_first ? 0 : 16))) = second;
-          if (lane < 8)
-            *reinterpret_cast<uint4*>(tile + 8 * kChunkBytes + (r >> 3) * 1024 + sw128_off(r & 7, lane * 16)) = rp[b];
-          if (lane == 0) {
-            ms->valid[s][r] = idx[b] >= 0;
-            nvalid += idx[b] >= 0;
-          }
+        for (int k = 0; k < kBatch; ++k) {
+          B.id[k] = -1;
+          B.lat[k] = make_uint4(0, 0, 0, 0);
+          B.sc[k] = 0.f;
         }
       }
-      if (!ok) break;
-      if (!waited && !wait_bar_warp(kv_empty + s, ph ^ 1, ms, a)) break;
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(kv_full + s);
-      key_cur = key_nxt;
-      key_nxt = key_nn;
+      if (sub == 0 && !wait_bar_warp(kv_empty + s, ph ^ 1, ms, a)) break;
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int kk = sub * kBatch + k;
+        const int r = cw + kConvWarps * kk;
+        if (kk >= kPerConv || r >= kTileK) break;
+        uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+        if (A.id[k] >= 0) dequant16_bf16(A.lat[k], A.sc[k], lo, hi);
+        uint8_t* rowbase = tile + ck * kChunkBytes + (r >> 3) * 1024;
+        const uint4 first = hi_first ? hi : lo, second = hi_first ? lo : hi;
+        *reinterpret_cast<uint4*>(rowbase + sw128_off(r & 7, b0 + (hi_first ? 16 : 0))) = first;
+        *reinterpret_cast<uint4*>(rowbase + sw128_off(r & 7, b0 + (hi_first ? 0 : 16))) = second;
+        uint8_t* rope_dst = tile + 8 * kChunkBytes + (r >> 3) * 1024 + sw128_off(r & 7, (lane & 7) * 16);
+        if (lane < 8) {
+          if (A.id[k] >= 0)
+            cp_async16(rope_dst, a.kv + int64_t(A.id[k]) * kRecordBytes + kRopeOffset + lane * 16);
+          else
+            *reinterpret_cast<uint4*>(rope_dst) = make_uint4(0, 0, 0, 0);
+        }
+        if (lane == 0) ms->valid[s][r] = A.id[k] >= 0;
+      }
+      if (sub == kSub - 1) {
+        cp_async_wait_all();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(kv_full + s);
+      }
+      A = B;
     }
-    if (lane == 0 && nvalid) atomicAdd(&ms->nvalid, nvalid);
+    cp_async_wait_all();
   }
 
-  // ---------------- epilogue (all warps) ----------------
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const bool aborted = ms->abort != 0;
-  static_assert(TcLayout<HP>::total <= 232448, "shared memory over the per-block limit");
-  if (tid < H) {
-    const int g = tid / HH, hh = tid % HH;
-    const float l = ms->red[g][0][hh] + ms->red[g][1][hh] + ms->red[g][2][hh] + ms->red[g][3][hh];
-    const float m = ms->mref[tid];
-    if (a.splits == 1) {
-      float fac, lse;
-      finish_head(m, nt > 0 ? l : 0.f, a.sink, tid, &fac, &lse);
-      ms->fac[tid] = fac;
-      if (a.lse && !aborted) a.lse[int64_t(u.row) * H + tid] = lse;
-    } else {
-      const int64_t rc = int64_t(u.row) * a.splits + u.chunk;
-      const bool live = nt > 0 && l > 0.f;
-      if (!aborted) {
-        a.ml_part[(rc * H + tid) * 2] = live ? m : -INFINITY;
-        a.ml_part[(rc * H + tid) * 2 + 1] = live ? l : 0.f;
-      }
-    }
-  }
-  __syncthreads();
-  {
-    // O^T readout: warp w takes 128-dim tile w / 4, lanes of quarter w % 4.
-    const int mt = warp >> 2, qd = warp & 3;
-    const int dg = mt * 128 + qd * 32 + lane;
-    const int64_t rc = int64_t(u.row) * a.splits + u.chunk;
-#pragma unroll 1
-    for (int c = 0; c < HP / 8; ++c) {
-      uint32_t v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      if (nt > 0) {
-        tmem_ld8(tmem + (uint32_t(32 * qd) << 16) + uint32_t(2 * HP + mt * HP + 8 * c), v);
-        tmem_wait_ld();
-      }
-      if (aborted) continue;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int h = 8 * c + k;
-        if (h >= H) break;
-        const float o = nt > 0 ? __uint_as_float(v[k]) : 0.f;
-        if (a.splits == 1) {
-          const __nv_bfloat16 bv = __float2bfloat16_rn(o * ms->fac[h]);
-          *reinterpret_cast<__nv_bfloat16*>(a.out + u.row * a.out_stride_row + h * a.out_stride_head + dg) = bv;
-        } else {
-          a.o_part[(rc * H + h) * kLatent + dg] = o;
-        }
-      }
-    }
-  }
+  // ---------------- teardown ----------------
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, Lay::tmem_cols);
   }
-  if (aborted) return;
-  if (a.splits == 1) {
-    if (tid == 0 && a.n_valid) a.n_valid[u.row] = ms->nvalid;
-    return;
+}
+
+// Merge kernel: CTA (row, head group) merges the row's partials when the row
+// was shared between CTAs of the decode launch (rows finished whole there are
+// skipped).  128 threads, latent dims tid, tid + 128, ...
+__global__ void __launch_bounds__(128) merge_rows_kernel(DecodeArgs a) {
+  const int row = blockIdx.x;
+  const int h0 = blockIdx.y * kMergeHeads;
+  const int h1 = min(h0 + kMergeHeads, a.heads);
+  const int tid = threadIdx.x;
+  __shared__ int64_t red_before[128];
+  __shared__ int64_t red_all[128];
+  int64_t before = 0, all = 0;
+  for (int r = tid; r < a.n_q; r += 128) {
+    const int64_t nt = tiles_of_len(row_len(a, r));
+    all += nt;
+    if (r < row) before += nt;
   }
-  // ---- split row: the last chunk to finish merges the partials.
-  const int C = a.splits;
-  if (tid == 0) a.nv_part[int64_t(u.row) * C + u.chunk] = ms->nvalid;
-  __threadfence();
+  red_before[tid] = before;
+  red_all[tid] = all;
   __syncthreads();
-  if (tid == 0) ms->is_last = (atomicAdd(a.ticket + u.row, 1) == C - 1);
-  __syncthreads();
-  if (!ms->is_last) return;
-  __threadfence();
-  float* w_s = reinterpret_cast<float*>(tiles);  // [H][C] merge weights (tiles are free now)
-  if (tid < H) {
-    const int h = tid;
-    float mstar = -INFINITY;
-    for (int c = 0; c < C; ++c) {
-      const int64_t o = ((int64_t(u.row) * C + c) * H + h) * 2;
-      if (__ldcg(a.ml_part + o + 1) > 0.f) mstar = fmaxf(mstar, __ldcg(a.ml_part + o));
+  for (int o = 64; o > 0; o >>= 1) {
+    if (tid < o) {
+      red_before[tid] += red_before[tid + o];
+      red_all[tid] += red_all[tid + o];
     }
-    float L = 0.f;
-    for (int c = 0; c < C; ++c) {
-      const int64_t o = ((int64_t(u.row) * C + c) * H + h) * 2;
-      const float lc = __ldcg(a.ml_part + o + 1);
-      const float w = lc > 0.f ? exp2f(__ldcg(a.ml_part + o) - mstar) : 0.f;
-      w_s[h * C + c] = w;
-      L += lc * w;
-    }
-    float fac, lse;
-    finish_head(mstar, L, a.sink, h, &fac, &lse);
-    ms->fac[h] = fac;
-    if (a.lse) a.lse[int64_t(u.row) * H + h] = lse;
+    __syncthreads();
   }
-  if (tid == 0) {
-    int tot = 0;
-    for (int c = 0; c < C; ++c) tot += __ldcg(a.nv_part + int64_t(u.row) * C + c);
-    if (a.n_valid) a.n_valid[u.row] = tot;
-    a.ticket[u.row] = 0;  // leave the counter zero for the next call
-  }
-  __syncthreads();
-  const int d = tid;  // 512 threads, one latent dim each
-  for (int h = 0; h < H; ++h) {
-    float o = 0.f;
-    for (int c = 0; c < C; ++c) {
-      const float w = w_s[h * C + c];
-      if (w != 0.f) o = fmaf(w, __ldcg(a.o_part + ((int64_t(u.row) * C + c) * H + h) * kLatent + d), o);
-    }
-    a.out[u.row * a.out_stride_row + h * a.out_stride_head + d] =
-        __bfloat16_as_ushort(__float2bfloat16_rn(o * ms->fac[h]));
-  }
+  const int64_t P = red_before[0], T = red_all[0], G = a.grid;
+  const int32_t nt = tiles_of_len(row_len(a, row));
+  int64_t ca, cbb;
+  row_parts(P, nt, T, G, &ca, &cbb);
+  if (ca == cbb) return;  // finished whole by one CTA
+  merge_row(a, row, P, nt, T, G, h0, h1, tid, 128, blockIdx.y == 0);
 }
 
 template <int HP>
@@ -616,7 +865,12 @@ cudaError_t launch_tc_hp(const DecodeLaunch& L) {
   const int smem = TcLayout<HP>::total;
   cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<HP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  decode_tc_kernel<HP><<<L.plan.grid, kThreadsTC, smem, L.stream>>>(make_decode_args(L));
+  const DecodeArgs args = make_decode_args(L);
+  decode_tc_kernel<HP><<<L.plan.grid, kThreadsTC, smem, L.stream>>>(args);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || !L.plan.merge_kernel) return e;
+  dim3 grid(L.p.n_q, (L.p.num_heads + kMergeHeads - 1) / kMergeHeads);
+  merge_rows_kernel<<<grid, 128, 0, L.stream>>>(args);
   return cudaGetLastError();
 }
 

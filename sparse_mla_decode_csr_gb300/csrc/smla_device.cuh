@@ -31,6 +31,7 @@ struct DecodeArgs {
   int32_t* status;
   float sm_scale_log2;  // sm_scale * log2(e): scores are kept in log2 units
   int32_t n_q, heads, splits, chunk_len, has_invalid;
+  int32_t grid, merge_kernel;  // tensor-core schedule
   // split workspace
   int32_t* ticket;
   float* o_part;
@@ -63,7 +64,9 @@ inline DecodeArgs make_decode_args(const DecodeLaunch& L) {
   a.splits = L.plan.num_splits;
   a.chunk_len = L.plan.chunk_len;
   a.has_invalid = p.has_invalid;
-  if (L.plan.num_splits > 1) {
+  a.grid = L.plan.grid;
+  a.merge_kernel = L.plan.merge_kernel;
+  if (L.ws.total > 0) {
     char* ws = static_cast<char*>(L.workspace);
     a.ticket = reinterpret_cast<int32_t*>(ws + L.ws.ticket_off);
     a.o_part = reinterpret_cast<float*>(ws + L.ws.o_off);
@@ -143,6 +146,44 @@ __device__ __forceinline__ void finish_head(float m, float l, const float* sink,
   const float mf = fmaxf(m, s);
   const float wm = exp2f(m - mf);
   *factor = wm / (exp2f(s - mf) + l * wm);
+}
+
+}  // namespace smla
+
+namespace smla {
+
+// ---- the tensor-core kernel's balanced schedule (see smla_plan in smla.h) ----
+
+constexpr int kSchedTile = 64;
+
+// Slice length of row r: max(indptr[r+1] - indptr[r], 0), capped by lens.
+__device__ __forceinline__ int32_t row_len(const DecodeArgs& a, int32_t r) {
+  int64_t len = int64_t(__ldg(a.indptr + r + 1)) - __ldg(a.indptr + r);
+  if (len < 0) len = 0;
+  if (a.lens) {
+    const int64_t cap = __ldg(a.lens + r);
+    len = cap < len ? (cap < 0 ? 0 : cap) : len;
+  }
+  return int32_t(len > INT32_MAX ? INT32_MAX : len);
+}
+
+// Tiles of a row: every row has at least one (an empty row's tile has no keys
+// and yields out = 0, lse = -inf).
+__device__ __forceinline__ int32_t tiles_of_len(int32_t len) {
+  return len > 0 ? (len + kSchedTile - 1) / kSchedTile : 1;
+}
+
+// First tile of CTA c: floor(c T / G).
+__device__ __forceinline__ int64_t cta_begin(int64_t c, int64_t T, int64_t G) { return (c * T) / G; }
+
+// The CTA whose range holds tile t: the largest c with floor(c T / G) <= t.
+__device__ __forceinline__ int64_t cta_of_tile(int64_t t, int64_t T, int64_t G) {
+  return ((t + 1) * G - 1) / T;
+}
+
+// Partial slot of row part (CTA c, row starting at tile P).
+__device__ __forceinline__ int64_t part_slot(int64_t c, int64_t P, int64_t T, int64_t G) {
+  return 2 * c + (P < cta_begin(c, T, G) ? 0 : 1);
 }
 
 }  // namespace smla

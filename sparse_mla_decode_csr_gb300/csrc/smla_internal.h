@@ -22,7 +22,7 @@ struct WorkspaceLayout {
   int64_t ticket_off, o_off, ml_off, nv_off, total;
 };
 
-WorkspaceLayout workspace_layout(int32_t n_q, int32_t heads, int32_t splits);
+WorkspaceLayout workspace_layout(int32_t n_q, int32_t heads, int32_t slots);
 
 // Everything a decode kernel needs, resolved on the host.
 struct DecodeLaunch {

@@ -155,45 +155,112 @@ def test_repeated_split_calls_reuse_workspace(kernel):
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
-def test_split_partials_match_oracle(kernel):
+def _oracle_part(c, row, lo, hi, sm_scale=0.0625):
+    """(O, m, l, n) of slice positions [lo, hi) of a row, from the oracle's primitives."""
+    q = c["q"].double().numpy()
+    pos, ids = oracle.row_positions(row, c["indices"].numpy(), c["indptr"].numpy(), None, c["n_kv"])
+    sel = (pos >= lo) & (pos < hi)
+    if not sel.any():
+        return np.zeros((q.shape[1], 512)), np.full(q.shape[1], -np.inf), np.zeros(q.shape[1]), 0
+    keys, values = oracle.row_keys(c["rec"], ids[sel])
+    s_ = oracle.row_scores(q[row], keys, sm_scale)
+    m = s_.max(axis=1)
+    e = np.exp(s_ - m[:, None])
+    return e @ values, m, e.sum(axis=1), int(sel.sum())
+
+
+def _read_workspace(ws, n_q, heads, slots):
+    a256 = lambda x: (x + 255) // 256 * 256
+    off_o = a256(4 * n_q)
+    off_ml = a256(off_o + slots * heads * 512 * 4)
+    off_nv = a256(off_ml + slots * heads * 2 * 4)
+    raw = ws.cpu()
+    ticket = raw[:4 * n_q].view(torch.int32).numpy()
+    o = raw[off_o:off_o + slots * heads * 512 * 4].view(torch.float32).numpy().reshape(slots, heads, 512)
+    ml = raw[off_ml:off_ml + slots * heads * 8].view(torch.float32).numpy().reshape(slots, heads, 2)
+    nv = raw[off_nv:off_nv + slots * 4].view(torch.int32).numpy()
+    return ticket, o, ml, nv
+
+
+def _check_part(o, ml, nv, ref, what):
+    o_ref, m_ref, l_ref, n_ref = ref
+    assert nv == n_ref, what
+    live = l_ref > 0
+    np.testing.assert_array_equal(ml[:, 1] > 0, live, err_msg=what)
+    # (m, l, O) of a part are taken against a reference maximum m (log2 units):
+    # l 2^m and O 2^m are what the oracle's part max and sums fix.
+    with np.errstate(invalid="ignore"):
+        shift = np.where(live, ml[:, 0] - m_ref / np.log(2.0), 0.0)
+    assert np.all(shift[live] < 1e-3) and np.all(shift[live] > -8.0 - 1e-3), what
+    np.testing.assert_allclose((ml[:, 1] * np.exp2(shift))[live], l_ref[live], rtol=1e-2, err_msg=what)
+    o_scaled = o * np.exp2(shift)[:, None]
+    scale = np.maximum(np.abs(o_ref).max(axis=-1, keepdims=True), 1e-30)
+    assert np.all(np.abs(o_scaled - o_ref) <= 2e-2 * scale + 1e-6), what
+
+
+def test_split_partials_match_oracle_cuda_core():
     c = small_case(3, 16, 1500, [700, 640, 129], seed=81, invalid=0.1)
     splits = 4
-    plan = smla.smla_plan(3, 16, 700, int(c["indices"].numel()), splits)
+    plan = smla.smla_plan(3, 16, 700, int(c["indices"].numel()), splits, kernel=smla.KERNEL_CUDA_CORE)
     ws = torch.zeros(plan.workspace_bytes + 4096, dtype=torch.uint8, device=DEV)
     out = torch.empty(3, 16, 512, dtype=torch.bfloat16, device=DEV)
     lse = torch.empty(3, 16, dtype=torch.float32, device=DEV)
     smla.smla_decode(c["q"].to(DEV), c["kv"], 1500, c["indices"].to(DEV), c["indptr"].to(DEV), None,
                      0.0625, None, out, lse, max_row_len=700, num_splits=splits, workspace_tensor=ws,
-                     kernel=KERNELS[kernel])
+                     kernel=smla.KERNEL_CUDA_CORE)
     torch.cuda.synchronize()
-    o_ref, m_ref, l_ref, nv_ref = oracle.split_partials(
-        c["q"].double().numpy(), c["rec"], c["indices"].numpy(), c["indptr"].numpy(), None, 0.0625,
-        chunk_len=plan.chunk_len, n_chunks=splits)
-    H, C = 16, splits
-    base = 0
-    off_o = (3 * 4 + 255) // 256 * 256
-    n_o = 3 * C * H * 512
-    off_ml = (off_o + n_o * 4 + 255) // 256 * 256
-    off_nv = (off_ml + 3 * C * H * 2 * 4 + 255) // 256 * 256
-    raw = ws.cpu()
-    ticket = raw[base:base + 12].view(torch.int32).numpy()
-    o = raw[off_o:off_o + n_o * 4].view(torch.float32).numpy().reshape(3, C, H, 512)
-    ml = raw[off_ml:off_ml + 3 * C * H * 8].view(torch.float32).numpy().reshape(3, C, H, 2)
-    nv = raw[off_nv:off_nv + 3 * C * 4].view(torch.int32).numpy().reshape(3, C)
+    ticket, o, ml, nv = _read_workspace(ws, 3, 16, plan.partial_slots)
     assert np.all(ticket == 0), "ticket counters must return to zero"
-    assert np.array_equal(nv, nv_ref)
-    live = l_ref > 0
-    np.testing.assert_array_equal(ml[..., 1] > 0, live)
-    # (m, l, O) of a chunk are taken against a reference maximum m (log2 units):
-    # l 2^m and O 2^m are what the oracle's chunk max and sums fix.
-    with np.errstate(invalid="ignore"):
-        shift = np.where(live, ml[..., 0] - m_ref / np.log(2.0), 0.0)
-    np.testing.assert_array_less(shift[live], 1e-3)
-    np.testing.assert_array_less(-shift[live], 8.0 + 1e-3)
-    np.testing.assert_allclose((ml[..., 1] * np.exp2(shift))[live], l_ref[live], rtol=1e-2)
-    o_scaled = o * np.exp2(shift)[..., None]
-    scale = np.maximum(np.abs(o_ref).max(axis=-1, keepdims=True), 1e-30)
-    assert np.all(np.abs(o_scaled - o_ref) <= 2e-2 * scale + 1e-6)
+    lens = [700, 640, 129]
+    for r in range(3):
+        for ch in range(splits):
+            lo = ch * plan.chunk_len
+            hi = lens[r] if ch == splits - 1 else min(lens[r], lo + plan.chunk_len)
+            sl = r * splits + ch
+            _check_part(o[sl], ml[sl], nv[sl], _oracle_part(c, r, lo, max(lo, hi)), f"row {r} chunk {ch}")
+
+
+def tc_schedule(lens, G):
+    """The tensor-core kernel's row parts, restated from smla.h: rows cut into
+    64-key tiles, concatenated; CTA c takes tiles [c T / G, (c+1) T / G); a part
+    of a shared row lands in slot 2 c + (P_r < b_c ? 0 : 1).  Returns
+    {row: [(cta, slot, first position, end position), ...]}."""
+    tiles = [max(1, -(-L // 64)) for L in lens]
+    starts = np.concatenate([[0], np.cumsum(tiles)]).astype(np.int64)
+    T = int(starts[-1])
+    b = [c * T // G for c in range(G + 1)]
+    parts = {}
+    for r, L in enumerate(lens):
+        P, nt = int(starts[r]), tiles[r]
+        for c in range(G):
+            lo_t, hi_t = max(b[c], P), min(b[c + 1], P + nt)
+            if lo_t < hi_t:
+                slot = 2 * c + (0 if P < b[c] else 1)
+                parts.setdefault(r, []).append((c, slot, (lo_t - P) * 64, min((hi_t - P) * 64, L)))
+    return parts
+
+
+@pytest.mark.parametrize("k", [2, 3, 7])
+def test_tensor_core_schedule_partials_match_oracle(k):
+    lens = [700, 640, 129, 0, 64, 1000]
+    c = small_case(len(lens), 16, 1500, lens, seed=90 + k, invalid=0.1)
+    n_q = len(lens)
+    plan = smla.smla_plan(n_q, 16, 1000, int(c["indices"].numel()), k)
+    assert plan.grid == n_q * k
+    ws = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device=DEV)
+    out, lse = run_small(c, num_splits=k, max_row_len=1000, what=f"tc schedule k={k}", kernel="tc")[:2]
+    smla.smla_decode(c["q"].to(DEV), c["kv"], 1500, c["indices"].to(DEV), c["indptr"].to(DEV), None,
+                     0.0625, None, torch.empty_like(out), torch.empty_like(lse), max_row_len=1000,
+                     num_splits=k, workspace_tensor=ws)
+    torch.cuda.synchronize()
+    ticket, o, ml, nv = _read_workspace(ws, n_q, 16, plan.partial_slots)
+    assert np.all(ticket == 0), "ticket counters must return to zero"
+    parts = tc_schedule(lens, plan.grid)
+    shared = [r for r, pr in parts.items() if len(pr) > 1]
+    assert shared, "the case must exercise shared rows"
+    for r in shared:
+        for cta, slot, lo, hi in parts[r]:
+            _check_part(o[slot], ml[slot], nv[slot], _oracle_part(c, r, lo, hi), f"row {r} cta {cta}")
 
 
 @pytest.mark.parametrize("name,rows", [("tiny", None), ("decode", [0, 1, 31, 62, 63]),

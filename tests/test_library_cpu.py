@@ -38,30 +38,50 @@ def test_strerror_names_every_code():
 @pytest.mark.parametrize("n_q,heads,row_len", [
     (4, 16, 128), (64, 16, 2048), (256, 16, 2048), (128, 64, 2048), (4, 64, 16384),
     (1, 1, 1), (1000, 64, 100), (7, 33, 5000), (3, 16, 0)])
-def test_plan_properties(n_q, heads, row_len):
-    p = smla.smla_plan(n_q, heads, row_len, n_q * row_len, 0, 152)
+def test_plan_properties_cuda_core(n_q, heads, row_len):
+    p = smla.smla_plan(n_q, heads, row_len, n_q * row_len, 0, 152, kernel=smla.KERNEL_CUDA_CORE)
+    assert p.kernel == smla.KERNEL_CUDA_CORE
     assert 1 <= p.num_splits <= smla.MAX_SPLITS
     assert p.tile_len == 64 and p.chunk_len % p.tile_len == 0 and p.chunk_len > 0
     assert p.num_splits * p.chunk_len >= row_len
     assert (p.num_splits - 1) * p.chunk_len < max(row_len, 1)  # no chunk wholly past the row
     assert p.grid == n_q * p.num_splits
+    assert p.partial_slots == (n_q * p.num_splits if p.num_splits > 1 else 0)
     assert (p.workspace_bytes == 0) == (p.num_splits == 1)
     if p.num_splits > 1:
-        need = n_q * 4 + n_q * p.num_splits * heads * (512 + 2) * 4 + n_q * p.num_splits * 4
+        need = n_q * 4 + p.partial_slots * heads * (512 + 2) * 4 + p.partial_slots * 4
         assert p.workspace_bytes >= need
 
 
+@pytest.mark.parametrize("n_q,heads,row_len", [
+    (4, 16, 128), (64, 16, 2048), (256, 16, 2048), (128, 64, 2048), (4, 64, 16384), (1, 1, 1)])
+def test_plan_properties_tensor_core(n_q, heads, row_len):
+    p = smla.smla_plan(n_q, heads, row_len, n_q * row_len, 0, 152)
+    assert p.kernel == smla.KERNEL_TENSOR_CORE
+    assert p.grid == 152 and p.tile_len == 64  # persistent: one CTA per SM
+    assert p.partial_slots == 2 * p.grid
+    assert p.merge_kernel == (p.grid > 4 * n_q)
+    need = n_q * 4 + p.partial_slots * heads * (512 + 2) * 4 + p.partial_slots * 4
+    assert p.workspace_bytes >= need
+    for k in (1, 3, 64):
+        f = smla.smla_plan(n_q, heads, row_len, n_q * row_len, k, 152)
+        assert f.grid == min(n_q * k, 65535)
+
+
 def test_plan_splits_short_batches_and_respects_forcing():
-    assert smla.smla_plan(4, 64, 16384, 4 * 16384, 0, 152).num_splits > 16  # long rows split
-    assert smla.smla_plan(2048, 16, 2048, 2048 * 2048, 0, 152).num_splits == 1  # big batch does not
+    cc = smla.KERNEL_CUDA_CORE
+    assert smla.smla_plan(4, 64, 16384, 4 * 16384, 0, 152, kernel=cc).num_splits > 16  # long rows split
+    assert smla.smla_plan(2048, 16, 2048, 2048 * 2048, 0, 152, kernel=cc).num_splits == 1
     for k in (1, 2, 5, 64):
-        assert smla.smla_plan(3, 16, 700, 2100, k, 152).num_splits == k
+        assert smla.smla_plan(3, 16, 700, 2100, k, 152, kernel=cc).num_splits == k
     with pytest.raises(smla.SmlaError):
         smla.smla_plan(3, 16, 700, 2100, 65, 152)
     with pytest.raises(smla.SmlaError):
         smla.smla_plan(3, 65, 700, 2100, 0, 152)
     with pytest.raises(smla.SmlaError):
         smla.smla_plan(-1, 16, 700, 2100, 0, 152)
+    with pytest.raises(smla.SmlaError):
+        smla.smla_plan(3, 16, 700, 2100, 0, 152, kernel=7)
 
 
 def _params(**kw):
@@ -83,7 +103,7 @@ def _params(**kw):
     (dict(n_kv_rows=(1 << 31) + 1), -2), (dict(sm_scale=float("nan")), -2),
     (dict(q_stride_head=100), -3), (dict(out_stride_row=512), -3),
     (dict(q=0x1008), -4), (dict(out_stride_head=516, out_stride_row=16 * 516), -4), (dict(kv_cache=0x2004), -4),
-    (dict(num_splits=65), -6), (dict(num_splits=-1), -6),
+    (dict(num_splits=65), -6), (dict(num_splits=-1), -6), (dict(kernel=2), -2),
 ])
 def test_decode_rejects_bad_arguments_on_host(kw, code):
     p = _params(**kw)
