@@ -149,9 +149,8 @@ typedef struct smla_decode_params {
  * range is finished there; a row shared by CTAs c_a..c_b (the CTAs holding its
  * first and last tile) gets one partial per CTA, stored in workspace slot
  * 2 c + (P_r < b_c ? 0 : 1), and is merged from those slots ([P2]
- * stage_combine) either by the last of its CTAs to finish (merge_kernel = 0)
- * or by a second, small merge kernel launched right after (merge_kernel = 1,
- * chosen when rows are shared by many CTAs).
+ * stage_combine) by a second, small kernel launched right after
+ * (merge_kernel = 1 whenever grid > 1; its CTA (r, h) merges head h of row r).
  * CUDA-core kernel: one CTA per (row, chunk); chunk c of a row covers slice
  * positions [c chunk_len, (c + 1) chunk_len), the last chunk everything after;
  * partial slot r * num_splits + c; the last chunk to finish merges.
@@ -178,8 +177,9 @@ int smla_plan(const smla_decode_params* params, int32_t num_sms, smla_plan_info*
  * (0 when none; also 0 for invalid params).
  *
  * Layout (each part 256-byte aligned), S = plan.partial_slots:
- *   ticket  int32 [n_q]          per-row arrival counters
- *   o_part  f32 [S][H][512]      unnormalised partial sum_t 2^(x_t - m) v_t of a row part
+ *   ticket   int32 [n_q]         per-row arrival counters (CUDA-core kernel)
+ *   row_tile int64 [n_q + 1]     tensor-core kernel: P_r of every row, then T
+ *   o_part   f32 [S][H][512]     unnormalised partial sum_t 2^(x_t - m) v_t of a row part
  *   ml_part f32 [S][H][2]        (m, l) of x_t = s_t * log2(e): m is the part's reference
  *                                maximum (its max, or at most 8 below it), l = sum_t 2^(x_t - m);
  *                                m = -inf, l = 0 for a part without keys

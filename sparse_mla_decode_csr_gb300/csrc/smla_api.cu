@@ -50,6 +50,8 @@ WorkspaceLayout workspace_layout(int32_t n_q, int32_t heads, int32_t slots) {
   int64_t off = 0;
   w.ticket_off = off;
   off = align256(off + int64_t(n_q) * 4);
+  w.rowtile_off = off;
+  off = align256(off + (int64_t(n_q) + 1) * 8);
   w.o_off = off;
   off = align256(off + int64_t(slots) * heads * kLatent * 4);
   w.ml_off = off;
@@ -116,8 +118,8 @@ int smla_plan(const smla_decode_params* p, int32_t num_sms, smla_plan_info* plan
     plan->num_splits = 0;
     plan->chunk_len = 0;
     plan->partial_slots = 2 * plan->grid;
-    // rows shared by many CTAs are merged by a separate, parallel kernel
-    plan->merge_kernel = (n_q > 0 && int64_t(plan->grid) > 4 * int64_t(n_q)) ? 1 : 0;
+    // rows shared between CTAs are merged by a second, parallel kernel
+    plan->merge_kernel = (n_q > 0 && plan->grid > 1) ? 1 : 0;
     plan->workspace_bytes = n_q > 0 ? workspace_layout(n_q, num_heads, plan->partial_slots).total : 0;
     return SMLA_OK;
   }

@@ -5,15 +5,18 @@
 // tiles, the rows' tiles are concatenated into one tile space, and CTA c of the
 // grid streams through the tiles [floor(c T / G), floor((c+1) T / G)) across
 // row boundaries.  A row wholly inside one CTA's range is finished there; a
-// shared row gets one (O, m, l) partial per CTA and is merged by its last CTA
-// to finish, or by the merge kernel below when rows are shared by many CTAs.
+// shared row gets one (O, m, l) partial per CTA and is merged by the merge
+// kernel below.
 //
 // Warp roles (16 warps):
 //   warps 0-3 (and 4-7 at 64 heads)  softmax: warpgroup g owns head columns
 //               [g*HH, (g+1)*HH) (HH = all heads up to 32, 32 at 64 heads); they
 //               also stage q, move the reference maxima (rescaling O in TMEM),
 //               and run each row part's epilogue and merge
-//   warp 12     TMEM allocator and MMA issuer (one thread)
+//   warps 12-14 MMA issuers, one thread each on three different SM
+//               sub-partitions (a single thread issues a tcgen05.mma only every
+//               ~55 cycles): 12 and 13 issue the two halves of QK's K = 576
+//               into two S accumulators, 14 issues PV; warp 12 owns TMEM
 //   all others  converters: gather each tile's 656-byte records (64-bit
 //               addressing; the next batch's loads in flight while this one is
 //               converted; records two tiles ahead prefetched into L2),
@@ -30,6 +33,7 @@
 //   PV  O^T[128 d, HP] += V^T[128 d, 64 keys] . P^T[64 keys, HP], four 128-dim
 //       M tiles; V^T is the same shared-memory key tile read MN-major.
 // O has two TMEM buffers (alternating between row parts) where they fit.
+// Shared rows are merged by merge_rows_kernel, launched right after.
 //
 // The maths is the sparse softmax attention of the gfx950 FlyDSL page (module
 // docstring: record layout, CSR tiles, masking; epilogue: out and LSE) with
@@ -58,11 +62,13 @@ constexpr int kDChunks = 9;                      // 576 dims = 9 x 64 (128-byte 
 constexpr int kChunkBytes = kTileK * 128;        // one 64-dim column block of a tile
 constexpr int kTileBytes = kDChunks * kChunkBytes;
 constexpr int kStages = 2;
-constexpr int kMmaWarp = 12;
+constexpr int kQkWarpA = 12;   // QK K-steps [0, 18) -> S accumulator 0; owns TMEM
+constexpr int kQkWarpB = 13;   // QK K-steps [18, 36) -> S accumulator 1
+constexpr int kPvWarp = 14;    // PV
+constexpr int kQkSteps = kQK / 16;
 constexpr float kRescaleMargin = 8.f;            // p <= 2^8 before a max update
 constexpr float kInitMax = -1.0e30f;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
-constexpr int kMergeHeads = 8;                   // heads per merge-kernel CTA
 
 static_assert(kSchedTile == kTileK, "schedule and pipeline tiles must agree");
 
@@ -88,7 +94,7 @@ struct TcLayout {
   // every other warp but the MMA issuer converts records
   static constexpr int SWG = HP == 64 ? 2 : 1;
   static constexpr int kSoftmaxWarps = 4 * SWG;
-  static constexpr int kConvWarps = 15 - kSoftmaxWarps;
+  static constexpr int kConvWarps = 13 - kSoftmaxWarps;  // warps [4 SWG, 12) and 15
   static constexpr int kPerConv = (kTileK + kConvWarps - 1) / kConvWarps;  // records per converter warp and tile
   static constexpr int kBatch = kPerConv <= 6 ? kPerConv : (kPerConv + 1) / 2;  // records per load batch
   static constexpr int kSub = (kPerConv + kBatch - 1) / kBatch;                 // batches per tile
@@ -106,15 +112,16 @@ struct TcLayout {
   // slack to align the dynamic shared memory base to 1024 bytes, when it fits
   static constexpr int slack = used + 1024 <= 232448 ? 1024 : 0;
   static constexpr int total = used + slack;
-  // TMEM: S stages [0, 2 HP), then n_ob O buffers of 4 HP columns each
-  static constexpr int n_ob = (2 * HP + 8 * HP <= 512) ? 2 : 1;
-  static constexpr int tmem_need = 2 * HP + n_ob * 4 * HP;
+  // TMEM: S (2 stages x 2 accumulators) in [0, 4 HP), then n_ob O buffers of 4 HP columns
+  static constexpr int n_ob = (4 * HP + 8 * HP <= 512) ? 2 : 1;
+  static constexpr int tmem_need = 4 * HP + n_ob * 4 * HP;
   static constexpr int tmem_cols = tmem_need <= 128 ? 128 : (tmem_need <= 256 ? 256 : 512);
   static constexpr Swizzle p_swz = HP == 64 ? kSw128 : (HP == 32 ? kSw64 : kSw32);
   static constexpr uint32_t p_swmask = HP == 64 ? 7 : (HP == 32 ? 3 : 1);
   static constexpr uint32_t idesc_qk = idesc_bf16(64, HP, 0, 0);
   static constexpr uint32_t idesc_pv = idesc_bf16(128, HP, 1, 1);
-  __host__ __device__ static constexpr uint32_t o_col(int ob, int mt) { return 2 * HP + (ob * 4 + mt) * HP; }
+  __host__ __device__ static constexpr uint32_t s_col(int stage, int acc) { return (2 * stage + acc) * HP; }
+  __host__ __device__ static constexpr uint32_t o_col(int ob, int mt) { return 4 * HP + (ob * 4 + mt) * HP; }
 };
 
 // Offset of byte `b` (16-byte aligned) of row `r` inside a 128-byte-row
@@ -235,54 +242,6 @@ __device__ __forceinline__ int32_t row_parts(int64_t P, int32_t nt, int64_t T, i
   return n;
 }
 
-// Merge the partials of row `row` (tiles [P, P + nt)) for heads [h0, h1) and
-// write out / lse (and n_valid when write_nv).  Threads [0, nthr) of the
-// caller take latent dims tid, tid + nthr, ...
-__device__ void merge_row(const DecodeArgs& a, int32_t row, int64_t P, int32_t nt, int64_t T, int64_t G,
-                          int h0, int h1, int tid, int nthr, bool write_nv) {
-  const int H = a.heads;
-  int64_t ca, cb;
-  row_parts(P, nt, T, G, &ca, &cb);
-  for (int h = h0; h < h1; ++h) {
-    float mstar = -INFINITY;
-    for (int64_t c = ca; c <= cb; ++c) {
-      if (cta_begin(c + 1, T, G) == cta_begin(c, T, G)) continue;
-      const int64_t o = (part_slot(c, P, T, G) * H + h) * 2;
-      if (__ldcg(a.ml_part + o + 1) > 0.f) mstar = fmaxf(mstar, __ldcg(a.ml_part + o));
-    }
-    float L = 0.f;
-    for (int64_t c = ca; c <= cb; ++c) {
-      if (cta_begin(c + 1, T, G) == cta_begin(c, T, G)) continue;
-      const int64_t o = (part_slot(c, P, T, G) * H + h) * 2;
-      const float lc = __ldcg(a.ml_part + o + 1);
-      if (lc > 0.f) L += lc * exp2f(__ldcg(a.ml_part + o) - mstar);
-    }
-    float fac, lse;
-    finish_head(mstar, L, a.sink, h, &fac, &lse);
-    if (tid == 0 && a.lse) a.lse[int64_t(row) * H + h] = lse;
-    for (int d = tid; d < kLatent; d += nthr) {
-      float acc = 0.f;
-      for (int64_t c = ca; c <= cb; ++c) {
-        if (cta_begin(c + 1, T, G) == cta_begin(c, T, G)) continue;
-        const int64_t sl = part_slot(c, P, T, G);
-        const int64_t o = (sl * H + h) * 2;
-        const float lc = __ldcg(a.ml_part + o + 1);
-        if (lc > 0.f)
-          acc = fmaf(exp2f(__ldcg(a.ml_part + o) - mstar), __ldcg(a.o_part + (sl * H + h) * kLatent + d), acc);
-      }
-      a.out[row * a.out_stride_row + h * a.out_stride_head + d] = __bfloat16_as_ushort(__float2bfloat16_rn(acc * fac));
-    }
-  }
-  if (write_nv && tid == 0 && a.n_valid) {
-    int tot = 0;
-    for (int64_t c = ca; c <= cb; ++c) {
-      if (cta_begin(c + 1, T, G) == cta_begin(c, T, G)) continue;
-      tot += __ldcg(a.nv_part + part_slot(c, P, T, G));
-    }
-    a.n_valid[row] = tot;
-  }
-}
-
 template <int HP>
 __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) {
   using Lay = TcLayout<HP>;
@@ -324,21 +283,21 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
     for (int s = 0; s < kStages; ++s) {
       mbar_init(kv_full + s, kConvWarps);
       mbar_init(kv_empty + s, 1);
-      mbar_init(s_full + s, 1);
+      mbar_init(s_full + s, 2);  // both QK halves
       mbar_init(s_empty + s, kSoftmaxWarps);
       mbar_init(p_full + s, kSoftmaxWarps);
       mbar_init(pv_done + s, 1);
       mbar_init(o_free + s, kSoftmaxWarps);
     }
     mbar_init(q_full, kSoftmaxWarps);
-    mbar_init(mma_drain, 1);
+    mbar_init(mma_drain, 3);  // the three issuers
     ms->abort = 0;
     ms->is_last = 0;
     ms->first_row = a.n_q;
     ms->first_tile = 0;
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == kQkWarpA) {
     tmem_alloc(&ms->tmem_base, Lay::tmem_cols);
     tmem_relinquish();
   }
@@ -378,8 +337,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
         ms->first_row = r;
         ms->first_tile = P;
       }
+      if (c_id == 0 && a.row_tile) a.row_tile[r] = P;  // for the merge kernel
       P += nt_r;
     }
+    if (c_id == 0 && tid == 0 && a.row_tile) a.row_tile[n] = Tt;
   }
   tc_fence_before();
   __syncthreads();
@@ -437,15 +398,18 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
       tc_fence_after();
       float x[HH];
       {
-        const uint32_t taddr = tmem + (uint32_t(32 * qd) << 16) + uint32_t(s * HP + wg * HH);
+        // S = the two QK halves' accumulators
+        const uint32_t ta = tmem + (uint32_t(32 * qd) << 16) + Lay::s_col(s, 0) + uint32_t(wg * HH);
+        const uint32_t tb = tmem + (uint32_t(32 * qd) << 16) + Lay::s_col(s, 1) + uint32_t(wg * HH);
 #pragma unroll
         for (int cc = 0; cc < HH / 8; ++cc) {
-          uint32_t v[8];
-          tmem_ld8(taddr + 8 * cc, v);
+          uint32_t v[8], w8[8];
+          tmem_ld8(ta + 8 * cc, v);
+          tmem_ld8(tb + 8 * cc, w8);
+          tmem_wait_ld();
 #pragma unroll
-          for (int k = 0; k < 8; ++k) x[8 * cc + k] = __uint_as_float(v[k]);
+          for (int k = 0; k < 8; ++k) x[8 * cc + k] = __uint_as_float(v[k]) + __uint_as_float(w8[k]);
         }
-        tmem_wait_ld();
       }
       tc_fence_before();
       __syncwarp();
@@ -613,98 +577,73 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(o_free + ob);
-        if (!whole && !a.merge_kernel) {
-          // the row's last CTA to finish merges its partials
-          __threadfence();
-          named_barrier(3, kSoftmaxThreads);
-          if (tid == 0) {
-            int64_t ca, cbb;
-            const int32_t n = row_parts(c.P, c.ntiles, T, G, &ca, &cbb);
-            ms->is_last = (atomicAdd(a.ticket + row, 1) == n - 1);
-          }
-          named_barrier(3, kSoftmaxThreads);
-          if (ms->is_last) {
-            __threadfence();
-            merge_row(a, row, c.P, c.ntiles, T, G, 0, H, tid, kSoftmaxThreads, true);
-            if (tid == 0) a.ticket[row] = 0;  // leave the counter zero for the next call
-          }
-          named_barrier(3, kSoftmaxThreads);
-        }
         ++seg;
       }
       c.advance(a);
     }
-  } else if (warp == kMmaWarp) {
-    // =================== MMA issuer ===================
+  } else if (warp == kQkWarpA || warp == kQkWarpB) {
+    // =================== QK issuers (one K half each) ===================
+    if (lane == 0) {
+      const int half = warp == kQkWarpA ? 0 : 1;
+      const int k0 = half * (kQkSteps / 2), k1 = k0 + kQkSteps / 2;
+      Cursor c;
+      c.init(a, row0, P0, cb, ce);
+      int q_uses = 0;
+      for (int i = 0; i < n_tiles; ++i) {
+        const int s = i & 1;
+        const uint32_t ph = (i >> 1) & 1;
+        if (c.first() && !wait_bar(q_full, (q_uses++) & 1, ms, a)) break;
+        if (!wait_bar(kv_full + s, ph, ms, a) || !wait_bar(s_empty + s, ph ^ 1, ms, a)) break;
+        tc_fence_after();
+        const uint32_t tile = tiles_u32 + s * kTileBytes;
+        const uint32_t d = tmem + Lay::s_col(s, half);
+#pragma unroll
+        for (int k = k0; k < k1; ++k) {
+          const int ch = k >> 2, kk = k & 3;
+          const uint64_t ad = smem_desc(tile + ch * kChunkBytes + kk * 32, 16, 1024, kSw128);
+          const uint64_t bd = smem_desc(q_u32 + ch * (HP * 128) + kk * 32, 16, 1024, kSw128);
+          mma_f16_ss(d, ad, bd, Lay::idesc_qk, k > k0 ? 1u : 0u);
+        }
+        mma_commit(s_full + s);
+        c.advance(a);
+      }
+      // every issued MMA has completed before TMEM is freed
+      mma_commit(mma_drain);
+      if (!mbar_wait(mma_drain, 0, kWaitLimitNs)) set_abort(ms, a);
+    }
+    __syncwarp();
+  } else if (warp == kPvWarp) {
+    // =================== PV issuer ===================
     if (lane == 0) {
       Cursor c;
       c.init(a, row0, P0, cb, ce);
-      bool ok = true;
-      int seg = 0, q_uses = 0;
-      bool prev_first = false;
-      int prev_ob = 0, prev_seg = 0;
-      auto issue_pv = [&](int j, bool pfirst, int ob, int sg) -> bool {
-        const int s = j & 1;
-        if (pfirst && !wait_bar(o_free + ob, ((sg / Lay::n_ob) & 1) ^ 1, ms, a)) return false;
-        if (!wait_bar(p_full + s, (j >> 1) & 1, ms, a)) return false;
+      int seg = 0;
+      for (int i = 0; i < n_tiles; ++i) {
+        const int s = i & 1;
+        const bool first = c.first();
+        const int ob = Lay::n_ob == 2 ? (seg & 1) : 0;
+        // a row part's first PV overwrites its O buffer: the epilogue of the
+        // part that used it before must have read it out
+        if (first && !wait_bar(o_free + ob, ((seg / Lay::n_ob) & 1) ^ 1, ms, a)) break;
+        if (!wait_bar(p_full + s, (i >> 1) & 1, ms, a)) break;
         tc_fence_after();
         const uint32_t tile = tiles_u32 + s * kTileBytes;
         const uint32_t pst = p_u32 + (Lay::p_stages == 2 ? s : 0) * Lay::p_bytes;
+        // k-major order: consecutive MMAs go to different O tiles
 #pragma unroll
-        for (int mt = 0; mt < 4; ++mt) {
-          const uint32_t d = tmem + Lay::o_col(ob, mt);
+        for (int k = 0; k < kTileK / 16; ++k) {
 #pragma unroll
-          for (int k = 0; k < kTileK / 16; ++k) {
+          for (int mt = 0; mt < 4; ++mt) {
             const uint64_t ad = smem_desc(tile + (2 * mt) * kChunkBytes + k * 2048, kChunkBytes, 1024, kSw128);
             const uint64_t bd = smem_desc(pst + k * 16 * Lay::p_row, 8 * Lay::p_row, 8 * Lay::p_row, Lay::p_swz);
-            mma_f16_ss(d, ad, bd, Lay::idesc_pv, (pfirst && k == 0) ? 0u : 1u);
+            mma_f16_ss(tmem + Lay::o_col(ob, mt), ad, bd, Lay::idesc_pv, (first && k == 0) ? 0u : 1u);
           }
         }
         mma_commit(kv_empty + s);
         mma_commit(pv_done + s);
-        return true;
-      };
-      for (int i = 0; ok && i < n_tiles; ++i) {
-        const int s = i & 1;
-        const uint32_t ph = (i >> 1) & 1;
-        const bool first = c.first();
-        // a row part's last PV goes out before the next part's QK, whose q
-        // the softmax stages only after that part's epilogue has read O
-        if (first && i > 0 && !issue_pv(i - 1, prev_first, prev_ob, prev_seg)) {
-          ok = false;
-          break;
-        }
-        if (first && !wait_bar(q_full, (q_uses++) & 1, ms, a)) {
-          ok = false;
-          break;
-        }
-        if (!wait_bar(kv_full + s, ph, ms, a) || !wait_bar(s_empty + s, ph ^ 1, ms, a)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t tile = tiles_u32 + s * kTileBytes;
-        const uint32_t d = tmem + uint32_t(s * HP);
-#pragma unroll
-        for (int k = 0; k < kQK / 16; ++k) {
-          const int ch = k >> 2, kk = k & 3;
-          const uint64_t ad = smem_desc(tile + ch * kChunkBytes + kk * 32, 16, 1024, kSw128);
-          const uint64_t bd = smem_desc(q_u32 + ch * (HP * 128) + kk * 32, 16, 1024, kSw128);
-          mma_f16_ss(d, ad, bd, Lay::idesc_qk, k > 0 ? 1u : 0u);
-        }
-        mma_commit(s_full + s);
-        if (!first && i > 0 && !issue_pv(i - 1, prev_first, prev_ob, prev_seg)) {
-          ok = false;
-          break;
-        }
-        prev_first = first;
-        prev_ob = Lay::n_ob == 2 ? (seg & 1) : 0;
-        prev_seg = seg;
         if (c.last()) ++seg;
         c.advance(a);
       }
-      if (ok && n_tiles > 0) issue_pv(n_tiles - 1, prev_first, prev_ob, prev_seg);
-      // every issued MMA has completed before TMEM is freed
       mma_commit(mma_drain);
       if (!mbar_wait(mma_drain, 0, kWaitLimitNs)) set_abort(ms, a);
     }
@@ -715,7 +654,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
     // most), in kSub batches of kBatch; lane k holds the record row of the
     // warp's k-th record of a tile.  The next batch's loads are in flight while
     // this one is converted; tiles two ahead are prefetched into L2.
-    const int cw = warp < kMmaWarp ? warp - kSoftmaxWarps : warp - kSoftmaxWarps - 1;
+    const int cw = warp < kQkWarpA ? warp - kSoftmaxWarps : kConvWarps - 1;  // warps [4 SWG, 12), then 15
     const int ck = lane >> 2;                 // 64-dim column block of this lane's 16 dims
     const int b0 = (lane & 3) * 32;           // byte offset of those dims within the 128-byte row
     const bool hi_first = (lane >> 2) & 1;    // alternate store order: conflict-free phases
@@ -820,44 +759,107 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
   // ---------------- teardown ----------------
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kQkWarpA) {
     tc_fence_after();
     tmem_dealloc(tmem, Lay::tmem_cols);
   }
 }
 
-// Merge kernel: CTA (row, head group) merges the row's partials when the row
-// was shared between CTAs of the decode launch (rows finished whole there are
-// skipped).  128 threads, latent dims tid, tid + 128, ...
+// Merge kernel: CTA (row, head) merges the head's partials of a row that was
+// shared between CTAs of the decode launch ([P2] stage_combine: max of the
+// parts' maxima, rescaled sums, sink in the denominator); rows finished whole
+// there are skipped.  The decode launch's CTA 0 left every row's first tile
+// and the tile total in the workspace.  128 threads x 4 latent dims.
+constexpr int kMergeChunk = 512;  // parts handled per pass
+
 __global__ void __launch_bounds__(128) merge_rows_kernel(DecodeArgs a) {
-  const int row = blockIdx.x;
-  const int h0 = blockIdx.y * kMergeHeads;
-  const int h1 = min(h0 + kMergeHeads, a.heads);
-  const int tid = threadIdx.x;
-  __shared__ int64_t red_before[128];
-  __shared__ int64_t red_all[128];
-  int64_t before = 0, all = 0;
-  for (int r = tid; r < a.n_q; r += 128) {
-    const int64_t nt = tiles_of_len(row_len(a, r));
-    all += nt;
-    if (r < row) before += nt;
+  const int row = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  const int H = a.heads;
+  __shared__ int32_t slot_s[kMergeChunk];
+  __shared__ float w_s[kMergeChunk];
+  __shared__ float red_s[128];
+  __shared__ float bc_s[2];
+  const int64_t P = a.row_tile[row], T = a.row_tile[a.n_q], G = a.grid;
+  const int32_t nt = int32_t(a.row_tile[row + 1] - P);
+  int64_t ca, cb;
+  row_parts(P, nt, T, G, &ca, &cb);
+  if (ca == cb) return;  // finished whole by one CTA
+  const int64_t nscan = cb - ca + 1;
+  // pass 1: the largest part maximum
+  float mloc = -INFINITY;
+  for (int64_t j = tid; j < nscan; j += 128) {
+    const int64_t c = ca + j;
+    if (cta_begin(c + 1, T, G) == cta_begin(c, T, G)) continue;
+    const int64_t o = (part_slot(c, P, T, G) * H + h) * 2;
+    if (__ldcg(a.ml_part + o + 1) > 0.f) mloc = fmaxf(mloc, __ldcg(a.ml_part + o));
   }
-  red_before[tid] = before;
-  red_all[tid] = all;
+  red_s[tid] = mloc;
   __syncthreads();
   for (int o = 64; o > 0; o >>= 1) {
-    if (tid < o) {
-      red_before[tid] += red_before[tid + o];
-      red_all[tid] += red_all[tid + o];
+    if (tid < o) red_s[tid] = fmaxf(red_s[tid], red_s[tid + o]);
+    __syncthreads();
+  }
+  const float mstar = red_s[0];
+  __syncthreads();
+  // pass 2: weights of the parts, their sum and the merged numerator
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float lsum = 0.f;
+  const int d4 = 4 * tid;
+  for (int64_t j0 = 0; j0 < nscan; j0 += kMergeChunk) {
+    const int n = int(nscan - j0 < kMergeChunk ? nscan - j0 : kMergeChunk);
+    for (int j = tid; j < n; j += 128) {
+      const int64_t c = ca + j0 + j;
+      int32_t sl = -1;
+      float w = 0.f;
+      if (cta_begin(c + 1, T, G) > cta_begin(c, T, G)) {
+        sl = int32_t(part_slot(c, P, T, G));
+        const int64_t o = (int64_t(sl) * H + h) * 2;
+        const float lc = __ldcg(a.ml_part + o + 1);
+        if (lc > 0.f) {
+          w = exp2f(__ldcg(a.ml_part + o) - mstar);
+          lsum += lc * w;
+        }
+      }
+      slot_s[j] = sl;
+      w_s[j] = w;
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int j = 0; j < n; ++j) {
+      const float w = w_s[j];
+      if (w == 0.f) continue;
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(a.o_part + (int64_t(slot_s[j]) * H + h) * kLatent + d4));
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
     }
     __syncthreads();
   }
-  const int64_t P = red_before[0], T = red_all[0], G = a.grid;
-  const int32_t nt = tiles_of_len(row_len(a, row));
-  int64_t ca, cbb;
-  row_parts(P, nt, T, G, &ca, &cbb);
-  if (ca == cbb) return;  // finished whole by one CTA
-  merge_row(a, row, P, nt, T, G, h0, h1, tid, 128, blockIdx.y == 0);
+  red_s[tid] = lsum;
+  __syncthreads();
+  for (int o = 64; o > 0; o >>= 1) {
+    if (tid < o) red_s[tid] += red_s[tid + o];
+    __syncthreads();
+  }
+  if (tid == 0) {
+    float fac, lse;
+    finish_head(mstar, red_s[0], a.sink, h, &fac, &lse);
+    bc_s[0] = fac;
+    if (a.lse) a.lse[int64_t(row) * H + h] = lse;
+    if (h == 0 && a.n_valid) {
+      int tot = 0;
+      for (int64_t c = ca; c <= cb; ++c)
+        if (cta_begin(c + 1, T, G) > cta_begin(c, T, G)) tot += __ldcg(a.nv_part + part_slot(c, P, T, G));
+      a.n_valid[row] = tot;
+    }
+  }
+  __syncthreads();
+  const float fac = bc_s[0];
+  uint2 packed;
+  packed.x = pack_bf16x2(acc.x * fac, acc.y * fac);
+  packed.y = pack_bf16x2(acc.z * fac, acc.w * fac);
+  *reinterpret_cast<uint2*>(a.out + row * a.out_stride_row + h * a.out_stride_head + d4) = packed;
 }
 
 template <int HP>
@@ -869,7 +871,7 @@ cudaError_t launch_tc_hp(const DecodeLaunch& L) {
   decode_tc_kernel<HP><<<L.plan.grid, kThreadsTC, smem, L.stream>>>(args);
   e = cudaGetLastError();
   if (e != cudaSuccess || !L.plan.merge_kernel) return e;
-  dim3 grid(L.p.n_q, (L.p.num_heads + kMergeHeads - 1) / kMergeHeads);
+  dim3 grid(L.p.n_q, L.p.num_heads);
   merge_rows_kernel<<<grid, 128, 0, L.stream>>>(args);
   return cudaGetLastError();
 }

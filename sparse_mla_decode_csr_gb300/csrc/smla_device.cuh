@@ -34,6 +34,7 @@ struct DecodeArgs {
   int32_t grid, merge_kernel;  // tensor-core schedule
   // split workspace
   int32_t* ticket;
+  int64_t* row_tile;  // tensor-core schedule: first tile of each row, then T
   float* o_part;
   float* ml_part;
   int32_t* nv_part;
@@ -69,6 +70,7 @@ inline DecodeArgs make_decode_args(const DecodeLaunch& L) {
   if (L.ws.total > 0) {
     char* ws = static_cast<char*>(L.workspace);
     a.ticket = reinterpret_cast<int32_t*>(ws + L.ws.ticket_off);
+    a.row_tile = reinterpret_cast<int64_t*>(ws + L.ws.rowtile_off);
     a.o_part = reinterpret_cast<float*>(ws + L.ws.o_off);
     a.ml_part = reinterpret_cast<float*>(ws + L.ws.ml_off);
     a.nv_part = reinterpret_cast<int32_t*>(ws + L.ws.nv_off);

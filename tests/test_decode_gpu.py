@@ -171,7 +171,7 @@ def _oracle_part(c, row, lo, hi, sm_scale=0.0625):
 
 def _read_workspace(ws, n_q, heads, slots):
     a256 = lambda x: (x + 255) // 256 * 256
-    off_o = a256(4 * n_q)
+    off_o = a256(a256(4 * n_q) + 8 * (n_q + 1))
     off_ml = a256(off_o + slots * heads * 512 * 4)
     off_nv = a256(off_ml + slots * heads * 2 * 4)
     raw = ws.cpu()

@@ -60,8 +60,8 @@ def test_plan_properties_tensor_core(n_q, heads, row_len):
     assert p.kernel == smla.KERNEL_TENSOR_CORE
     assert p.grid == 152 and p.tile_len == 64  # persistent: one CTA per SM
     assert p.partial_slots == 2 * p.grid
-    assert p.merge_kernel == (p.grid > 4 * n_q)
-    need = n_q * 4 + p.partial_slots * heads * (512 + 2) * 4 + p.partial_slots * 4
+    assert p.merge_kernel == (p.grid > 1)
+    need = n_q * 4 + (n_q + 1) * 8 + p.partial_slots * heads * (512 + 2) * 4 + p.partial_slots * 4
     assert p.workspace_bytes >= need
     for k in (1, 3, 64):
         f = smla.smla_plan(n_q, heads, row_len, n_q * row_len, k, 152)
