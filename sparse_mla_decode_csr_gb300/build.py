@@ -18,12 +18,13 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
-BUILD = os.path.join(ROOT, "_build")
-LIB = os.path.join(PKG, "libsmla.so")
+TRACE = os.environ.get("SMLA_TRACE", "") == "1"  # stage-trace build (debugging only)
+BUILD = os.path.join(ROOT, "_build_trace" if TRACE else "_build")
+LIB = os.path.join(PKG, "libsmla_trace.so" if TRACE else "libsmla.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas=-warn-spills",
-              "-I", INCLUDE, "-I", CSRC]
+              "-I", INCLUDE, "-I", CSRC] + (["-DSMLA_TRACE"] if TRACE else [])
 
 
 def nvcc() -> str:

@@ -51,10 +51,36 @@
 #include "smla_internal.h"
 #include "smla_ptx.cuh"
 
+#ifdef SMLA_TRACE
+// Optional stage trace (compile with -DSMLA_TRACE): lane 0 of each warp writes
+// (%globaltimer ns | tag << 48 | tile << 56) into
+// g_smla_trace[(cta * 16 + warp) * kTraceEvents + k].  Off in normal builds.
+__device__ unsigned long long* g_smla_trace;
+extern "C" int smla_trace_set(void* buf) {
+  unsigned long long* p = static_cast<unsigned long long*>(buf);
+  return int(cudaMemcpyToSymbol(g_smla_trace, &p, sizeof(p)));
+}
+#endif
+
 namespace smla {
 namespace {
 
 using namespace ptx;
+
+#ifdef SMLA_TRACE
+constexpr int kTraceEvents = 256;
+__device__ __forceinline__ void trace_event(int* cnt, int tag, int tile) {
+  if (g_smla_trace == nullptr || (threadIdx.x & 31) != 0) return;
+  const int w = threadIdx.x >> 5;
+  const int k = atomicAdd(cnt + w, 1);
+  if (k >= kTraceEvents) return;
+  g_smla_trace[(size_t(blockIdx.x) * 16 + w) * kTraceEvents + k] =
+      (globaltimer() & 0xFFFFFFFFFFFFull) | (uint64_t(tag & 0xFF) << 48) | (uint64_t(tile & 0xFF) << 56);
+}
+#define SMLA_TR(tag, tile) trace_event(tr_cnt, (tag), (tile))
+#else
+#define SMLA_TR(tag, tile) ((void)0)
+#endif
 
 constexpr int kThreadsTC = 512;
 constexpr int kTileK = 64;                       // keys per tile
@@ -255,6 +281,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
   static_assert(Lay::total <= 232448, "shared memory over the per-block limit");
   extern __shared__ uint8_t smem_raw[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+#ifdef SMLA_TRACE
+  __shared__ int tr_cnt[16];
+  if (tid < 16) tr_cnt[tid] = 0;
+#endif
   if (Lay::slack == 0 && (smem_u32(smem_raw) & 1023u) != 0) {
     // no room to realign: refuse (uniformly, before any barrier or TMEM use)
     if (tid == 0 && a.status) atomicOr(a.status, SMLA_STATUS_TIMEOUT);
@@ -345,6 +375,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  SMLA_TR(1, 0);  // schedule known
   const int64_t T = ms->total_tiles;
   const int64_t cb = cta_begin(c_id, T, G), ce = cta_begin(c_id + 1, T, G);
   const int32_t n_tiles = int32_t(ce - cb);  // this CTA's tiles
@@ -393,8 +424,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
         for (int h = 0; h < HH; ++h) lpart[h] = 0.f;
         nv = 0;
       }
+      SMLA_TR(10, i);
       wait_bar_warp(kv_full + s, ph, ms, a);
       wait_bar_warp(s_full + s, ph, ms, a);
+      SMLA_TR(11, i);
       tc_fence_after();
       float x[HH];
       {
@@ -507,6 +540,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full + s);
+      SMLA_TR(12, i);
 
       if (last) {
         // ---------- epilogue of this row part ----------
@@ -577,6 +611,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(o_free + ob);
+        SMLA_TR(13, i);
         ++seg;
       }
       c.advance(a);
@@ -593,7 +628,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
         const int s = i & 1;
         const uint32_t ph = (i >> 1) & 1;
         if (c.first() && !wait_bar(q_full, (q_uses++) & 1, ms, a)) break;
+        SMLA_TR(20, i);
         if (!wait_bar(kv_full + s, ph, ms, a) || !wait_bar(s_empty + s, ph ^ 1, ms, a)) break;
+        SMLA_TR(21, i);
         tc_fence_after();
         const uint32_t tile = tiles_u32 + s * kTileBytes;
         const uint32_t d = tmem + Lay::s_col(s, half);
@@ -605,6 +642,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
           mma_f16_ss(d, ad, bd, Lay::idesc_qk, k > k0 ? 1u : 0u);
         }
         mma_commit(s_full + s);
+        SMLA_TR(22, i);
         c.advance(a);
       }
       // every issued MMA has completed before TMEM is freed
@@ -625,7 +663,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
         // a row part's first PV overwrites its O buffer: the epilogue of the
         // part that used it before must have read it out
         if (first && !wait_bar(o_free + ob, ((seg / Lay::n_ob) & 1) ^ 1, ms, a)) break;
+        SMLA_TR(40, i);
         if (!wait_bar(p_full + s, (i >> 1) & 1, ms, a)) break;
+        SMLA_TR(41, i);
         tc_fence_after();
         const uint32_t tile = tiles_u32 + s * kTileBytes;
         const uint32_t pst = p_u32 + (Lay::p_stages == 2 ? s : 0) * Lay::p_bytes;
@@ -641,6 +681,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
         }
         mma_commit(kv_empty + s);
         mma_commit(pv_done + s);
+        SMLA_TR(42, i);
         if (c.last()) ++seg;
         c.advance(a);
       }
@@ -658,14 +699,26 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
     const int ck = lane >> 2;                 // 64-dim column block of this lane's 16 dims
     const int b0 = (lane & 3) * 32;           // byte offset of those dims within the 128-byte row
     const bool hi_first = (lane >> 2) & 1;    // alternate store order: conflict-free phases
-    auto tile_keys = [&](const Cursor& cu) -> int32_t {  // this lane's record row, or -1
+    // Index pipeline: raw entries are loaded three tiles ahead (no use of the
+    // value at load time), validated when their tile's loads are issued, and
+    // used for an L2 prefetch of the records two tiles ahead.
+    auto raw_key = [&](const Cursor& cu) -> int32_t {  // this lane's raw entry, or INT32_MIN
       const int rr = cw + kConvWarps * lane;
-      if (!cu.live || lane >= kPerConv || rr >= kTileK) return -1;
+      if (!cu.live || lane >= kPerConv || rr >= kTileK) return INT32_MIN;
       const int p = cu.p0() + rr;
-      return p < cu.p1() ? key_of(a, cu.beg, p) : -1;
+      const int64_t off = cu.beg + p;
+      if (p >= cu.p1() || off < 0 || off >= a.n_indices) return INT32_MIN;
+      return __ldg(a.indices + off);
     };
-    auto prefetch = [&](int32_t id) {
-      if (id >= 0) prefetch_l2(a.kv + int64_t(id) * kRecordBytes, kRecordBytes);
+    auto valid_key = [&](int32_t raw) -> int32_t {  // record row, or -1 when masked
+      if (raw >= a.n_kv_rows) {
+        if (a.status) atomicOr(a.status, SMLA_STATUS_INDEX_OOB);
+        return -1;
+      }
+      return raw < 0 ? -1 : raw;
+    };
+    auto prefetch = [&](int32_t raw) {
+      if (raw >= 0 && raw < a.n_kv_rows) prefetch_l2(a.kv + int64_t(raw) * kRecordBytes, kRecordBytes);
     };
     struct Batch {
       int32_t id[kBatch];
@@ -689,13 +742,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
     };
     Cursor cl;  // the tile whose batches are being loaded
     cl.init(a, row0, P0, cb, ce);
-    Cursor cp = cl;  // two tiles ahead of cl, for L2 prefetch
-    int32_t keys_l = tile_keys(cl);
-    prefetch(keys_l);
-    cp.advance(a);
-    prefetch(tile_keys(cp));
-    cp.advance(a);
-    prefetch(tile_keys(cp));
+    Cursor c3 = cl;  // three tiles ahead of cl: its raw entries are being loaded
+    const int32_t raw0 = raw_key(cl);
+    c3.advance(a);
+    int32_t raw1 = raw_key(c3);
+    c3.advance(a);
+    int32_t raw2 = raw_key(c3);
+    c3.advance(a);
+    int32_t raw3 = raw_key(c3);
+    int32_t keys_l = valid_key(raw0);
+    prefetch(raw1);
+    prefetch(raw2);
     int sub_l = 0;  // batch index within cl
     Batch A;
     load_batch(A, keys_l, 0);
@@ -710,9 +767,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
       if (++sub_l == kSub) {
         sub_l = 0;
         cl.advance(a);
-        keys_l = tile_keys(cl);
-        cp.advance(a);
-        prefetch(tile_keys(cp));
+        keys_l = valid_key(raw1);
+        prefetch(raw3);  // loaded a tile ago
+        raw1 = raw2;
+        raw2 = raw3;
+        c3.advance(a);
+        raw3 = raw_key(c3);
       }
       if (q + 1 < n_batches) {
         load_batch(B, keys_l, sub_l);
@@ -724,7 +784,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
           B.sc[k] = 0.f;
         }
       }
+      SMLA_TR(30, i);
       if (sub == 0 && !wait_bar_warp(kv_empty + s, ph ^ 1, ms, a)) break;
+      SMLA_TR(31, i);
 #pragma unroll
       for (int k = 0; k < kBatch; ++k) {
         const int kk = sub * kBatch + k;
@@ -750,12 +812,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(kv_full + s);
+        SMLA_TR(32, i);
       }
       A = B;
     }
     cp_async_wait_all();
   }
 
+  SMLA_TR(2, 0);
   // ---------------- teardown ----------------
   tc_fence_before();
   __syncthreads();
