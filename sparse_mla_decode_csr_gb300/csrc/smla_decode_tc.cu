@@ -22,7 +22,6 @@
 //               converted; records two tiles ahead prefetched into L2),
 //               dequantise E4M3 * pow2 scale -> bf16 exactly, and write the
 //               64 x 576 bf16 key tile in the 128-byte-swizzled K-major layout
-//               (the rope bytes go there by cp.async)
 //
 // Per tile i (stage s = i % 2), within the row part it belongs to:
 //   QK  S^T[64 keys, HP heads] = K_tile[64 x 576] . Q^T       (M=64, N=HP, K=576)
@@ -122,7 +121,7 @@ struct TcLayout {
   static constexpr int kSoftmaxWarps = 4 * SWG;
   static constexpr int kConvWarps = 13 - kSoftmaxWarps;  // warps [4 SWG, 12) and 15
   static constexpr int kPerConv = (kTileK + kConvWarps - 1) / kConvWarps;  // records per converter warp and tile
-  static constexpr int kBatch = kPerConv <= 6 ? kPerConv : (kPerConv + 1) / 2;  // records per load batch
+  static constexpr int kBatch = kPerConv <= 4 ? kPerConv : 4;  // records per load batch
   static constexpr int kSub = (kPerConv + kBatch - 1) / kBatch;                 // batches per tile
   static constexpr int HH = HP / SWG;             // head columns per softmax warpgroup
   static constexpr int q_bytes = kDChunks * HP * 128;
@@ -179,13 +178,6 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Misc* m
 __device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity, Misc* ms, const DecodeArgs& a) {
   return __all_sync(0xffffffffu, wait_bar(bar, parity, ms, a));
 }
-
-__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)),
-               "l"(__cvta_generic_to_global(gmem_src))
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // 16 E4M3 bytes times a power-of-two scale -> 16 bf16 (exact), as 2 x uint4.
 __device__ __forceinline__ void dequant16_bf16(uint4 v, float scale, uint4& lo, uint4& hi) {
@@ -720,10 +712,13 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
     auto prefetch = [&](int32_t raw) {
       if (raw >= 0 && raw < a.n_kv_rows) prefetch_l2(a.kv + int64_t(raw) * kRecordBytes, kRecordBytes);
     };
+    // A record is two 16-byte loads per lane: latent bytes [16 lane, 16 lane + 16)
+    // on every lane, and the 144-byte tail (4 f32 scales, then 64 bf16 rope) on
+    // lanes 0-8 (tail chunk `lane`).
     struct Batch {
       int32_t id[kBatch];
       uint4 lat[kBatch];
-      float sc[kBatch];
+      uint4 tail[kBatch];
     };
     auto load_batch = [&](Batch& B, int32_t keys, int sub) {
 #pragma unroll
@@ -732,11 +727,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
         const int32_t id = __shfl_sync(0xffffffffu, keys, kk & 31);
         B.id[k] = kk < kPerConv ? id : -1;
         B.lat[k] = make_uint4(0, 0, 0, 0);
-        B.sc[k] = 0.f;
+        B.tail[k] = make_uint4(0, 0, 0, 0);
         if (B.id[k] >= 0) {
-          const uint8_t* rec = a.kv + int64_t(B.id[k]) * kRecordBytes;
-          B.lat[k] = __ldg(reinterpret_cast<const uint4*>(rec) + lane);
-          B.sc[k] = __ldg(reinterpret_cast<const float*>(rec + kScaleOffset) + (lane >> 3));
+          const uint4* rec = reinterpret_cast<const uint4*>(a.kv + int64_t(B.id[k]) * kRecordBytes);
+          B.lat[k] = __ldg(rec + lane);
+          if (lane < 9) B.tail[k] = __ldg(rec + kScaleOffset / 16 + lane);
         }
       }
     };
@@ -781,7 +776,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
         for (int k = 0; k < kBatch; ++k) {
           B.id[k] = -1;
           B.lat[k] = make_uint4(0, 0, 0, 0);
-          B.sc[k] = 0.f;
+          B.tail[k] = make_uint4(0, 0, 0, 0);
         }
       }
       SMLA_TR(30, i);
@@ -792,23 +787,25 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
         const int kk = sub * kBatch + k;
         const int r = cw + kConvWarps * kk;
         if (kk >= kPerConv || r >= kTileK) break;
+        // this lane's scale: f32 word (lane / 8) of lane 0's tail chunk
+        const uint32_t sw0 = __shfl_sync(0xffffffffu, A.tail[k].x, 0);
+        const uint32_t sw1 = __shfl_sync(0xffffffffu, A.tail[k].y, 0);
+        const uint32_t sw2 = __shfl_sync(0xffffffffu, A.tail[k].z, 0);
+        const uint32_t sw3 = __shfl_sync(0xffffffffu, A.tail[k].w, 0);
+        const int blk = lane >> 3;
+        const float sc = __uint_as_float(blk == 0 ? sw0 : blk == 1 ? sw1 : blk == 2 ? sw2 : sw3);
         uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
-        if (A.id[k] >= 0) dequant16_bf16(A.lat[k], A.sc[k], lo, hi);
+        if (A.id[k] >= 0) dequant16_bf16(A.lat[k], sc, lo, hi);
         uint8_t* rowbase = tile + ck * kChunkBytes + (r >> 3) * 1024;
         const uint4 first = hi_first ? hi : lo, second = hi_first ? lo : hi;
         *reinterpret_cast<uint4*>(rowbase + sw128_off(r & 7, b0 + (hi_first ? 16 : 0))) = first;
         *reinterpret_cast<uint4*>(rowbase + sw128_off(r & 7, b0 + (hi_first ? 0 : 16))) = second;
-        uint8_t* rope_dst = tile + 8 * kChunkBytes + (r >> 3) * 1024 + sw128_off(r & 7, (lane & 7) * 16);
-        if (lane < 8) {
-          if (A.id[k] >= 0)
-            cp_async16(rope_dst, a.kv + int64_t(A.id[k]) * kRecordBytes + kRopeOffset + lane * 16);
-          else
-            *reinterpret_cast<uint4*>(rope_dst) = make_uint4(0, 0, 0, 0);
-        }
+        if (lane >= 1 && lane < 9)  // rope chunk lane - 1, bit for bit (zero for a masked key)
+          *reinterpret_cast<uint4*>(tile + 8 * kChunkBytes + (r >> 3) * 1024 + sw128_off(r & 7, (lane - 1) * 16)) =
+              A.tail[k];
         if (lane == 0) ms->valid[s][r] = A.id[k] >= 0;
       }
       if (sub == kSub - 1) {
-        cp_async_wait_all();
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(kv_full + s);
@@ -816,7 +813,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
       }
       A = B;
     }
-    cp_async_wait_all();
   }
 
   SMLA_TR(2, 0);
