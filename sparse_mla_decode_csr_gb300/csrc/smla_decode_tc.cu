@@ -179,18 +179,34 @@ __device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity, Mi
   return __all_sync(0xffffffffu, wait_bar(bar, parity, ms, a));
 }
 
-// 16 E4M3 bytes times a power-of-two scale -> 16 bf16 (exact), as 2 x uint4.
+// 16 E4M3 bytes times a power-of-two scale -> 16 bf16 (exact), as 2 x uint4,
+// with integer and packed-bf16 arithmetic only (no float-format conversions,
+// which run at a fraction of the ALU rate).  An E4M3 byte s.eeee.mmm put into
+// bf16 bits as s | eeee.mmm << 4 is a bf16 of value e4m3 * 2^-120 (E4M3
+// subnormals become bf16 subnormals); two exact multiplies, by 2^120 and by the
+// scale, give e4m3 * scale.  Codes 0x7F / 0xFF (E4M3 NaN, never written by the
+// record writer) decode as finite values here.
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2_scaled(uint32_t x, uint32_t scale2) {
+  // x: byte 0 -> bits 0-7, byte 1 -> bits 16-23
+  const uint32_t bits = ((x << 4) & 0x07F007F0u) | ((x << 8) & 0x80008000u);
+  return bf16x2_mul(bf16x2_mul(bits, 0x7B807B80u /* 2^120, 2^120 */), scale2);
+}
+
 __device__ __forceinline__ void dequant16_bf16(uint4 v, float scale, uint4& lo, uint4& hi) {
+  const uint32_t sb = __float_as_uint(scale) >> 16;  // a power of two is exact in bf16
+  const uint32_t scale2 = sb | (sb << 16);
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
   uint32_t o[8];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(w[i] >> (16 * j)), __NV_E4M3);
-      float2 f = __half22float2(*reinterpret_cast<__half2*>(&h));
-      o[2 * i + j] = pack_bf16x2(f.x * scale, f.y * scale);
-    }
+    o[2 * i] = e4m3x2_to_bf16x2_scaled(__byte_perm(w[i], 0u, 0x4140), scale2);      // bytes 0, 1
+    o[2 * i + 1] = e4m3x2_to_bf16x2_scaled(__byte_perm(w[i], 0u, 0x4342), scale2);  // bytes 2, 3
   }
   lo = make_uint4(o[0], o[1], o[2], o[3]);
   hi = make_uint4(o[4], o[5], o[6], o[7]);
@@ -730,8 +746,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
         B.tail[k] = make_uint4(0, 0, 0, 0);
         if (B.id[k] >= 0) {
           const uint4* rec = reinterpret_cast<const uint4*>(a.kv + int64_t(B.id[k]) * kRecordBytes);
-          B.lat[k] = __ldg(rec + lane);
-          if (lane < 9) B.tail[k] = __ldg(rec + kScaleOffset / 16 + lane);
+          B.lat[k] = ldg_v4_now(rec + lane);
+          if (lane < 9) B.tail[k] = ldg_v4_now(rec + kScaleOffset / 16 + lane);
         }
       }
     };
@@ -792,6 +808,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
         const uint32_t sw1 = __shfl_sync(0xffffffffu, A.tail[k].y, 0);
         const uint32_t sw2 = __shfl_sync(0xffffffffu, A.tail[k].z, 0);
         const uint32_t sw3 = __shfl_sync(0xffffffffu, A.tail[k].w, 0);
+        SMLA_TR(33 + k, i);  // record k of the batch has arrived
         const int blk = lane >> 3;
         const float sc = __uint_as_float(blk == 0 ? sw0 : blk == 1 ? sw1 : blk == 2 ? sw2 : sw3);
         uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
@@ -805,6 +822,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
               A.tail[k];
         if (lane == 0) ms->valid[s][r] = A.id[k] >= 0;
       }
+      SMLA_TR(38, i);  // batch stored
       if (sub == kSub - 1) {
         fence_proxy_async_smem();
         __syncwarp();

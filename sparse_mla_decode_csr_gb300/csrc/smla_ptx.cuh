@@ -53,6 +53,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   }
 }
 
+// 16-byte read-only global load that the compiler keeps at this point of the
+// program (volatile): a gather pipeline relies on loads being issued early.
+__device__ __forceinline__ uint4 ldg_v4_now(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(__cvta_generic_to_global(p)));
+  return v;
+}
+
 // Non-blocking prefetch of `bytes` (a multiple of 16, 16-byte aligned) of
 // global memory into L2.
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {

@@ -285,3 +285,38 @@ def test_workload_parity(name, rows, kernel):
     print(f"{name}: max norm-relative error {rel:.3g}")
     del kv
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("heads", [16, 33])
+def test_single_key_rows_return_every_e4m3_code_exactly(heads, kernel):
+    """A row with one key has softmax weight exactly 1, so its output is the
+    key's dequantised latent, which is exact in bf16 for every finite E4M3
+    code times a power-of-two scale.  Records are written byte by byte (not by
+    the writer) so that all 254 finite codes, both zeros and the subnormals
+    appear in every scale block, under scales 2^-20 .. 2^20."""
+    rng = np.random.default_rng(heads)
+    finite = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    n = 48
+    rec = np.zeros((n, 656), dtype=np.uint8)
+    for i in range(n):
+        for b in range(4):
+            rec[i, 128 * b:128 * (b + 1)] = rng.permutation(finite)[:128] if i % 2 else \
+                rng.permutation(finite)[126:]
+    scales = np.exp2(rng.integers(-20, 21, size=(n, 4))).astype("<f4")
+    rec[:, 512:528] = scales.view(np.uint8).reshape(n, 16)
+    rope = torch.randn(n, 64, generator=torch.Generator().manual_seed(heads)).to(torch.bfloat16)
+    rec[:, 528:] = bits(rope).view(np.uint8).reshape(n, 128)
+    # every finite code shows up in some record of every block position
+    assert all(np.isin(finite, rec[:, 128 * b:128 * (b + 1)]).all() for b in range(4))
+    q = torch.randn(n, heads, 576, generator=torch.Generator().manual_seed(1)).to(torch.bfloat16)
+    indices = torch.from_numpy(rng.permutation(n).astype(np.int32))
+    indptr = torch.arange(n + 1, dtype=torch.int32)
+    kv = torch.from_numpy(rec).to(DEV)
+    out, lse, nv, st = run_gpu(q.to(DEV), kv, n, indices.to(DEV), indptr.to(DEV), None, 0.0625, None,
+                               max_row_len=1, kernel=kernel)
+    latent, _, _ = oracle.unpack_records(rec)
+    want = latent[indices.numpy()]
+    got = out.float().cpu().double().numpy()
+    assert st == 0 and (nv.cpu().numpy() == 1).all()
+    assert np.array_equal(got, np.broadcast_to(want[:, None, :], got.shape)), \
+        f"max |diff| {np.abs(got - want[:, None, :]).max()}"
