@@ -203,6 +203,38 @@ size_t smla_decode_workspace_size(const smla_decode_params* params);
 int smla_decode(const smla_decode_params* params, void* workspace, size_t workspace_bytes,
                 void* stream);
 
+/* Bytes of the fixed device array behind smla_decode_noalloc: 64 MiB per
+ * device.  A default tensor-core plan on a 152-SM GPU needs about 40 MiB at 64
+ * heads (304 partial slots x 64 heads x 2 KiB) plus 12 bytes per query row. */
+#define SMLA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/* smla_decode without a caller-supplied workspace, for callers that cannot
+ * allocate device memory at call time: code running inside another runtime's
+ * memory pool or allocation-free serving loop, where a cudaMalloc (or a
+ * framework allocation) on the call path is not allowed or would stall other
+ * work.  The pages describe no such entry point; it is an addition of this
+ * library.
+ *
+ * Same params, outputs, accuracy and launches as smla_decode; the split-KV
+ * workspace (the layout of smla_decode_workspace_size) lives instead in a
+ * file-scope device array of SMLA_NOALLOC_SCRATCH_BYTES bytes inside
+ * libsmla.so.  The call allocates nothing.
+ *   - Set-up: the first call on a device (the current device) looks up the
+ *     device address of that array once (cudaGetSymbolAddress, which may load
+ *     the library's module on that device).  Make that first call before any
+ *     stream capture.
+ *   - Limit: a call whose workspace would exceed SMLA_NOALLOC_SCRATCH_BYTES
+ *     returns SMLA_ERR_WORKSPACE and launches nothing (use smla_decode with a
+ *     workspace of smla_decode_workspace_size bytes instead).
+ *   - Sharing: every call on a device uses the same array and leaves its last
+ *     contents there.  Calls whose work may overlap on the GPU (different
+ *     streams without an ordering event) race on it and give wrong results;
+ *     order them.  With the CUDA-core kernel the call first clears the
+ *     ticket counters (bytes [0, 4 n_q)) on `stream`; the tensor-core kernel
+ *     writes every part of the array it reads and needs nothing cleared.
+ * Errors as smla_decode, plus SMLA_ERR_DEVICE when the set-up fails. */
+int smla_decode_noalloc(const smla_decode_params* params, void* stream);
+
 /* The record writer ([P1] module docstring, "Preconditions": vLLM's
  * concat_and_cache_ds_mla rule).  For each of n records:
  *   scale_b = pow2ceil(max(amax_b, 1e-4) / 448), amax_b = max |latent[128 b .. 128 b + 127]|

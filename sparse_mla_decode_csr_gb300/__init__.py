@@ -28,6 +28,8 @@ STATUS_INDEX_OOB = 0x1
 STATUS_TIMEOUT = 0x2
 KERNEL_TENSOR_CORE = 0
 KERNEL_CUDA_CORE = 1
+NOALLOC_SCRATCH_BYTES = 64 << 20  # SMLA_NOALLOC_SCRATCH_BYTES
+SMLA_ERR_WORKSPACE = -5
 
 
 class SmlaError(RuntimeError):
@@ -90,6 +92,8 @@ def _load():
     lib.smla_decode.argtypes = [ctypes.POINTER(DecodeParams), ctypes.c_void_p, ctypes.c_size_t,
                                 ctypes.c_void_p]
     lib.smla_decode.restype = ctypes.c_int
+    lib.smla_decode_noalloc.argtypes = [ctypes.POINTER(DecodeParams), ctypes.c_void_p]
+    lib.smla_decode_noalloc.restype = ctypes.c_int
     lib.smla_pack_records.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
                                       ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
                                       ctypes.c_void_p]
@@ -103,7 +107,7 @@ def _load():
 
 lib = _load()
 
-EXPORTED_SYMBOLS = ("smla_plan", "smla_decode_workspace_size", "smla_decode",
+EXPORTED_SYMBOLS = ("smla_plan", "smla_decode_workspace_size", "smla_decode", "smla_decode_noalloc",
                     "smla_pack_records", "smla_strerror", "smla_device_check")
 
 
@@ -220,6 +224,46 @@ def smla_decode(q: torch.Tensor, kv_cache: torch.Tensor, n_kv_rows: int, indices
     rc = lib.smla_decode(ctypes.byref(p), _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream))
     if rc != 0:
         raise SmlaError(rc, "smla_decode")
+
+
+def smla_decode_noalloc(q: torch.Tensor, kv_cache: torch.Tensor, n_kv_rows: int,
+                        indices: torch.Tensor, indptr: torch.Tensor, lens: Optional[torch.Tensor],
+                        sm_scale: float, sink: Optional[torch.Tensor], out: torch.Tensor,
+                        lse: Optional[torch.Tensor], stream=None, *, max_row_len: int = 0,
+                        has_invalid: bool = False, n_valid: Optional[torch.Tensor] = None,
+                        status: Optional[torch.Tensor] = None, num_splits: int = 0,
+                        kernel: int = KERNEL_TENSOR_CORE) -> None:
+    """smla_decode with the library's fixed device scratch as workspace (no
+    allocation on the call path; for callers that cannot allocate device
+    memory at call time).  Arguments as smla_decode.  Calls on one device
+    share that scratch: calls that may overlap on the GPU must be ordered.
+    The first call on a device sets up the scratch address; make it before
+    any stream capture.  See include/smla.h."""
+    assert q.dtype == torch.bfloat16 and q.dim() == 3 and q.stride(2) == 1
+    assert out.dtype == torch.bfloat16 and out.dim() == 3 and out.stride(2) == 1
+    assert kv_cache.dtype == torch.uint8
+    for t in (indices, indptr, lens, n_valid, status):
+        assert t is None or t.dtype == torch.int32
+    assert sink is None or sink.dtype == torch.float32
+    assert lse is None or (lse.dtype == torch.float32 and lse.is_contiguous())
+    p = DecodeParams()
+    p.n_q, p.num_heads = int(q.shape[0]), int(q.shape[1])
+    p.q, p.q_stride_row, p.q_stride_head = q.data_ptr(), q.stride(0), q.stride(1)
+    p.kv_cache, p.n_kv_rows = kv_cache.data_ptr(), int(n_kv_rows)
+    p.indices, p.n_indices = _ptr(indices), int(indices.numel())
+    p.indptr, p.lens = _ptr(indptr), _ptr(lens)
+    p.max_row_len, p.has_invalid = int(max_row_len), int(bool(has_invalid))
+    p.sm_scale = float(sm_scale)
+    p.sink = _ptr(sink)
+    p.out, p.out_stride_row, p.out_stride_head = out.data_ptr(), out.stride(0), out.stride(1)
+    p.lse, p.n_valid, p.status = _ptr(lse), _ptr(n_valid), _ptr(status)
+    p.num_splits, p.kernel = int(num_splits), int(kernel)
+    rc = lib.smla_decode_noalloc(ctypes.byref(p), _stream(stream))
+    if rc == SMLA_ERR_WORKSPACE:
+        raise SmlaError(rc, f"smla_decode_noalloc: the call needs more than the "
+                            f"{NOALLOC_SCRATCH_BYTES}-byte fixed scratch")
+    if rc != 0:
+        raise SmlaError(rc, "smla_decode_noalloc")
 
 
 def smla_pack_records(latent: torch.Tensor, rope: torch.Tensor, kv_out: torch.Tensor,
