@@ -17,11 +17,18 @@
 //               sub-partitions (a single thread issues a tcgen05.mma only every
 //               ~55 cycles): 12 and 13 issue the two halves of QK's K = 576
 //               into two S accumulators, 14 issues PV; warp 12 owns TMEM
-//   all others  converters: gather each tile's 656-byte records (64-bit
-//               addressing; the next batch's loads in flight while this one is
-//               converted; records two tiles ahead prefetched into L2),
-//               dequantise E4M3 * pow2 scale -> bf16 exactly, and write the
-//               64 x 576 bf16 key tile in the 128-byte-swizzled K-major layout
+//   warps 4-11 (8-11 at 64 heads)  latent converters: gather the 512 E4M3
+//               bytes and the four scales of each tile's records (64-bit
+//               addressing), dequantise E4M3 * pow2 scale -> bf16 exactly, and
+//               write the 64 x 512 bf16 latent of the key tile in the
+//               128-byte-swizzled K-major layout.  Up to 32 heads the latent
+//               bytes travel by cp.async into a per-warp shared-memory ring
+//               about a tile and a half ahead of the conversion; at 64 heads
+//               (no shared memory left) into registers one batch ahead
+//   warp 15     rope copier: the records' 128-byte bf16 rope goes straight into
+//               the key tile by cp.async (completion tracked by the tile's
+//               mbarrier), zeros for masked keys; it also writes the keys'
+//               validity flags and flags out-of-range indices
 //
 // Per tile i (stage s = i % 2), within the row part it belongs to:
 //   QK  S^T[64 keys, HP heads] = K_tile[64 x 576] . Q^T       (M=64, N=HP, K=576)
@@ -33,6 +40,8 @@
 //       M tiles; V^T is the same shared-memory key tile read MN-major.
 // O has two TMEM buffers (alternating between row parts) where they fit.
 // Shared rows are merged by merge_rows_kernel, launched right after.
+// The latent dims are stored permuted within each 4-dim group (see
+// latent_dim_of); q is staged in the same order and the epilogue undoes it.
 //
 // The maths is the sparse softmax attention of the gfx950 FlyDSL page (module
 // docstring: record layout, CSR tiles, masking; epilogue: out and LSE) with
@@ -68,15 +77,15 @@ using namespace ptx;
 
 #ifdef SMLA_TRACE
 constexpr int kTraceEvents = 256;
-__device__ __forceinline__ void trace_event(int* cnt, int tag, int tile) {
-  if (g_smla_trace == nullptr || (threadIdx.x & 31) != 0) return;
-  const int w = threadIdx.x >> 5;
-  const int k = atomicAdd(cnt + w, 1);
-  if (k >= kTraceEvents) return;
-  g_smla_trace[(size_t(blockIdx.x) * 16 + w) * kTraceEvents + k] =
-      (globaltimer() & 0xFFFFFFFFFFFFull) | (uint64_t(tag & 0xFF) << 48) | (uint64_t(tile & 0xFF) << 56);
-}
-#define SMLA_TR(tag, tile) trace_event(tr_cnt, (tag), (tile))
+// tr_buf (the buffer, read once per thread) and tr_k (this warp's event
+// count, kept equal in all lanes) are locals of the kernel.
+#define SMLA_TR(tag, tile)                                                                              \
+  do {                                                                                                  \
+    if (tr_buf != nullptr && (threadIdx.x & 31) == 0 && tr_k < kTraceEvents)                            \
+      tr_buf[(size_t(blockIdx.x) * 16 + (threadIdx.x >> 5)) * kTraceEvents + tr_k] =                    \
+          (globaltimer() & 0xFFFFFFFFFFFFull) | (uint64_t((tag) & 0xFF) << 48) | (uint64_t((tile) & 0xFF) << 56); \
+    ++tr_k;                                                                                             \
+  } while (0)
 #else
 #define SMLA_TR(tag, tile) ((void)0)
 #endif
@@ -90,6 +99,7 @@ constexpr int kStages = 2;
 constexpr int kQkWarpA = 12;   // QK K-steps [0, 18) -> S accumulator 0; owns TMEM
 constexpr int kQkWarpB = 13;   // QK K-steps [18, 36) -> S accumulator 1
 constexpr int kPvWarp = 14;    // PV
+constexpr int kRopeWarp = 15;  // rope copier
 constexpr int kQkSteps = kQK / 16;
 constexpr float kRescaleMargin = 8.f;            // p <= 2^8 before a max update
 constexpr float kInitMax = -1.0e30f;
@@ -116,13 +126,14 @@ struct Misc {
 template <int HP>
 struct TcLayout {
   // softmax warpgroups: one holds all head columns up to 32 heads, two at 64;
-  // every other warp but the MMA issuer converts records
+  // the warps between them and the MMA issuers convert latents
   static constexpr int SWG = HP == 64 ? 2 : 1;
   static constexpr int kSoftmaxWarps = 4 * SWG;
-  static constexpr int kConvWarps = 13 - kSoftmaxWarps;  // warps [4 SWG, 12) and 15
-  static constexpr int kPerConv = (kTileK + kConvWarps - 1) / kConvWarps;  // records per converter warp and tile
-  static constexpr int kBatch = kPerConv <= 4 ? kPerConv : 4;  // records per load batch
-  static constexpr int kSub = (kPerConv + kBatch - 1) / kBatch;                 // batches per tile
+  static constexpr int kConvWarps = 12 - kSoftmaxWarps;            // warps [4 SWG, 12)
+  static constexpr int kPerConv = kTileK / kConvWarps;              // records per converter warp and tile
+  static constexpr int kBatch = 8;                                   // records per load batch
+  static constexpr int kSub = kPerConv / kBatch;                     // batches per tile
+  static_assert(kPerConv * kConvWarps == kTileK && kSub * kBatch == kPerConv, "converter split");
   static constexpr int HH = HP / SWG;             // head columns per softmax warpgroup
   static constexpr int q_bytes = kDChunks * HP * 128;
   static constexpr int p_row = 2 * HP;            // bytes of one key's P^T row
@@ -133,7 +144,15 @@ struct TcLayout {
   static constexpr int off_p = off_q + q_bytes;
   static constexpr int off_bar = off_p + p_stages * p_bytes;
   static constexpr int off_misc = off_bar + 16 * 8;
-  static constexpr int used = off_misc + int(sizeof(Misc));
+  // Up to 32 heads each converter warp also owns a ring of kRing raw-latent
+  // slots (512 B) in shared memory, filled by cp.async kRing - 1 records ahead
+  // of the conversion; at 64 heads there is no room and latents are gathered
+  // into registers one batch ahead instead (kRing = 0).
+  static constexpr int off_ring = (off_misc + int(sizeof(Misc)) + 127) / 128 * 128;
+  static constexpr int ring_fit = (232448 - 1024 - off_ring) / (kConvWarps * kLatent);
+  static constexpr int kRing = HP == 64 ? 0 : (ring_fit > 16 ? 16 : ring_fit);
+  static_assert(HP == 64 || kRing >= 4, "ring too small");
+  static constexpr int used = off_ring + kConvWarps * kRing * kLatent;
   // slack to align the dynamic shared memory base to 1024 bytes, when it fits
   static constexpr int slack = used + 1024 <= 232448 ? 1024 : 0;
   static constexpr int total = used + slack;
@@ -179,37 +198,46 @@ __device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity, Mi
   return __all_sync(0xffffffffu, wait_bar(bar, parity, ms, a));
 }
 
-// 16 E4M3 bytes times a power-of-two scale -> 16 bf16 (exact), as 2 x uint4,
-// with integer and packed-bf16 arithmetic only (no float-format conversions,
-// which run at a fraction of the ALU rate).  An E4M3 byte s.eeee.mmm put into
-// bf16 bits as s | eeee.mmm << 4 is a bf16 of value e4m3 * 2^-120 (E4M3
-// subnormals become bf16 subnormals); two exact multiplies, by 2^120 and by the
-// scale, give e4m3 * scale.  Codes 0x7F / 0xFF (E4M3 NaN, never written by the
-// record writer) decode as finite values here.
+// 16 E4M3 bytes (one lane's uint4) times a power-of-two scale -> 16 bf16,
+// exactly, with integer bit placement and packed-bf16 multiplies (no
+// float-format conversions, which run at a fraction of the ALU rate).  A byte
+// s.eeee.mmm put into bf16 bits as s | eeee.mmm << 4 is the bf16 of value
+// e4m3 * 2^-120 (E4M3 subnormals land on bf16 subnormals).  One exact multiply
+// by scale * 2^120 finishes it when that is a bf16, i.e. scale <= 2^7 (the
+// record writer's scales for |latent| <= 57344); otherwise two, by 2^120 and
+// then by the scale.  Codes 0x7F / 0xFF (E4M3 NaN, never written by the
+// writer) decode as finite values.
+//
+// Each 32-bit word [b0 b1 b2 b3] yields the pairs (b0, b2) and (b1, b3): five
+// integer operations per four values.  So the lane's dims come out in the
+// order 0 2 1 3 4 6 5 7 | 8 10 9 11 12 14 13 15; see latent_dim_of.
 __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
 }
 
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2_scaled(uint32_t x, uint32_t scale2) {
-  // x: byte 0 -> bits 0-7, byte 1 -> bits 16-23
-  const uint32_t bits = ((x << 4) & 0x07F007F0u) | ((x << 8) & 0x80008000u);
-  return bf16x2_mul(bf16x2_mul(bits, 0x7B807B80u /* 2^120, 2^120 */), scale2);
+__device__ __forceinline__ void dequant16(uint4 v, uint32_t m1, uint32_t (&o)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t e = ((w[j] << 4) & 0x07F007F0u) | ((w[j] << 8) & 0x80008000u);  // b0, b2
+    const uint32_t d = ((w[j] >> 4) & 0x07F007F0u) | (w[j] & 0x80008000u);         // b1, b3
+    o[2 * j] = bf16x2_mul(e, m1);
+    o[2 * j + 1] = bf16x2_mul(d, m1);
+  }
 }
 
-__device__ __forceinline__ void dequant16_bf16(uint4 v, float scale, uint4& lo, uint4& hi) {
-  const uint32_t sb = __float_as_uint(scale) >> 16;  // a power of two is exact in bf16
-  const uint32_t scale2 = sb | (sb << 16);
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t o[8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    o[2 * i] = e4m3x2_to_bf16x2_scaled(__byte_perm(w[i], 0u, 0x4140), scale2);      // bytes 0, 1
-    o[2 * i + 1] = e4m3x2_to_bf16x2_scaled(__byte_perm(w[i], 0u, 0x4342), scale2);  // bytes 2, 3
-  }
-  lo = make_uint4(o[0], o[1], o[2], o[3]);
-  hi = make_uint4(o[4], o[5], o[6], o[7]);
+// Latent position p (0..511) of the shared-memory key tile, and of the staged
+// q, holds latent dim latent_dim_of(p): bits 0 and 1 of p swapped (the pair
+// order above) and, in odd 64-dim column blocks, bit 3 flipped (there the two
+// 8-dim halves of a lane's 16 dims are stored in the opposite order, which
+// keeps the converters' shared-memory stores free of bank conflicts).  The map
+// is its own inverse.  QK contracts over positions, so it only has to be the
+// same for K and q; the epilogue writes O^T lane p to dim latent_dim_of(p).
+__device__ __forceinline__ int latent_dim_of(int p) {
+  const int t = p ^ (((p >> 6) & 1) << 3);
+  return (t & ~3) | ((t & 1) << 1) | ((t >> 1) & 1);
 }
 
 // Walks this CTA's tiles: row, slice positions, and where the row part starts
@@ -290,8 +318,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
   extern __shared__ uint8_t smem_raw[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 #ifdef SMLA_TRACE
-  __shared__ int tr_cnt[16];
-  if (tid < 16) tr_cnt[tid] = 0;
+  unsigned long long* const tr_buf = g_smla_trace;
+  int tr_k = 0;
 #endif
   if (Lay::slack == 0 && (smem_u32(smem_raw) & 1023u) != 0) {
     // no room to realign: refuse (uniformly, before any barrier or TMEM use)
@@ -319,7 +347,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(kv_full + s, kConvWarps);
+      mbar_init(kv_full + s, kConvWarps + 1);  // latent converters and the rope copier
       mbar_init(kv_empty + s, 1);
       mbar_init(s_full + s, 2);  // both QK halves
       mbar_init(s_empty + s, kSoftmaxWarps);
@@ -421,8 +449,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
           uint4 v = make_uint4(0, 0, 0, 0);
           if (h < H)
             v = __ldg(reinterpret_cast<const uint4*>(a.q + c.row * a.q_stride_row + h * a.q_stride_head + c16 * 8));
+          int pc = c16;  // position chunk of these 8 dims (latent_dim_of, applied per chunk)
+          if (c16 < kLatent / 8) {
+            pc = c16 ^ ((c16 >> 3) & 1);
+            v = make_uint4(__byte_perm(v.x, v.y, 0x5410), __byte_perm(v.x, v.y, 0x7632),
+                           __byte_perm(v.z, v.w, 0x5410), __byte_perm(v.z, v.w, 0x7632));
+          }
           const uint32_t off =
-              uint32_t(c16 >> 3) * (HP * 128) + uint32_t(h >> 3) * 1024u + sw128_off(h & 7, (c16 & 7) * 16);
+              uint32_t(pc >> 3) * (HP * 128) + uint32_t(h >> 3) * 1024u + sw128_off(h & 7, (pc & 7) * 16);
           *reinterpret_cast<uint4*>(q_s + off) = v;
         }
         fence_proxy_async_smem();
@@ -597,7 +631,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
         tc_fence_after();
 #pragma unroll 1
         for (int mt = wg; mt < 4; mt += Lay::SWG) {
-          const int dg = mt * 128 + qd * 32 + lane;
+          const int dg = latent_dim_of(mt * 128 + qd * 32 + lane);
 #pragma unroll 1
           for (int cc = 0; cc < HP / 8; ++cc) {
             uint32_t v[8];
@@ -697,23 +731,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
       if (!mbar_wait(mma_drain, 0, kWaitLimitNs)) set_abort(ms, a);
     }
     __syncwarp();
-  } else {
-    // =================== converters ===================
-    // Warp cw takes records cw, cw + kConvWarps, ... of each tile (kPerConv at
-    // most), in kSub batches of kBatch; lane k holds the record row of the
-    // warp's k-th record of a tile.  The next batch's loads are in flight while
-    // this one is converted; tiles two ahead are prefetched into L2.
-    const int cw = warp < kQkWarpA ? warp - kSoftmaxWarps : kConvWarps - 1;  // warps [4 SWG, 12), then 15
-    const int ck = lane >> 2;                 // 64-dim column block of this lane's 16 dims
-    const int b0 = (lane & 3) * 32;           // byte offset of those dims within the 128-byte row
-    const bool hi_first = (lane >> 2) & 1;    // alternate store order: conflict-free phases
-    // Index pipeline: raw entries are loaded three tiles ahead (no use of the
-    // value at load time), validated when their tile's loads are issued, and
-    // used for an L2 prefetch of the records two tiles ahead.
-    auto raw_key = [&](const Cursor& cu) -> int32_t {  // this lane's raw entry, or INT32_MIN
-      const int rr = cw + kConvWarps * lane;
-      if (!cu.live || lane >= kPerConv || rr >= kTileK) return INT32_MIN;
-      const int p = cu.p0() + rr;
+  } else if (warp == kRopeWarp) {
+    // =================== rope copier ===================
+    // Lane L holds the raw index entries of keys L and L + 32 of a tile, loaded
+    // three tiles ahead and validated when their tile's copies are issued.
+    auto raw_pair = [&](const Cursor& cu, int j) -> int32_t {
+      const int kk = lane + 32 * j;
+      if (!cu.live) return INT32_MIN;
+      const int p = cu.p0() + kk;
       const int64_t off = cu.beg + p;
       if (p >= cu.p1() || off < 0 || off >= a.n_indices) return INT32_MIN;
       return __ldg(a.indices + off);
@@ -725,111 +750,317 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
       }
       return raw < 0 ? -1 : raw;
     };
-    auto prefetch = [&](int32_t raw) {
-      if (raw >= 0 && raw < a.n_kv_rows) prefetch_l2(a.kv + int64_t(raw) * kRecordBytes, kRecordBytes);
-    };
-    // A record is two 16-byte loads per lane: latent bytes [16 lane, 16 lane + 16)
-    // on every lane, and the 144-byte tail (4 f32 scales, then 64 bf16 rope) on
-    // lanes 0-8 (tail chunk `lane`).
-    struct Batch {
-      int32_t id[kBatch];
-      uint4 lat[kBatch];
-      uint4 tail[kBatch];
-    };
-    auto load_batch = [&](Batch& B, int32_t keys, int sub) {
+    Cursor c3;
+    c3.init(a, row0, P0, cb, ce);
+    int32_t ra0 = raw_pair(c3, 0), rb0 = raw_pair(c3, 1);
+    c3.advance(a);
+    int32_t ra1 = raw_pair(c3, 0), rb1 = raw_pair(c3, 1);
+    c3.advance(a);
+    int32_t ra2 = raw_pair(c3, 0), rb2 = raw_pair(c3, 1);
+    const uint8_t* kv_rope = a.kv + kScaleOffset + 16 + 16 * (lane & 7);  // rope chunk lane % 8
+    for (int i = 0; i < n_tiles; ++i) {
+      const int s = i & 1;
+      const uint32_t ph = (i >> 1) & 1;
+      c3.advance(a);
+      const int32_t ra3 = raw_pair(c3, 0), rb3 = raw_pair(c3, 1);
+      SMLA_TR(50, i);
+      if (!wait_bar_warp(kv_empty + s, ph ^ 1, ms, a)) break;
+      SMLA_TR(51, i);
+      const int32_t ka = valid_key(ra0), kb = valid_key(rb0);
+      ms->valid[s][lane] = ka >= 0;
+      ms->valid[s][lane + 32] = kb >= 0;
+      uint8_t* rope_blk = tiles + s * kTileBytes + 8 * kChunkBytes;
+#pragma unroll 1
+      for (int m = 0; m < kTileK / 4; ++m) {
+        const int key = 4 * m + (lane >> 3);
+        const int32_t id = __shfl_sync(0xffffffffu, m < 8 ? ka : kb, key & 31);
+        const uint32_t off = uint32_t(key) * 128u + ((uint32_t(lane & 7) ^ uint32_t(key & 7)) << 4);
+        if (id >= 0)
+          cp_async16(smem_u32(rope_blk + off), kv_rope + int64_t(id) * kRecordBytes);
+        else
+          *reinterpret_cast<uint4*>(rope_blk + off) = make_uint4(0, 0, 0, 0);
+      }
+      fence_proxy_async_smem();        // the zero rows, for the tensor core
+      cp_async_mbar_arrive(kv_full + s);  // the copies land before the tile is full
+      __syncwarp();
+      if (lane == 0) mbar_arrive(kv_full + s);
+      SMLA_TR(52, i);
+      ra0 = ra1; rb0 = rb1;
+      ra1 = ra2; rb1 = rb2;
+      ra2 = ra3; rb2 = rb3;
+    }
+    cp_async_wait_all();
+  } else {
+    // =================== latent converters ===================
+    // Converter cw takes records cw, cw + kConvWarps, ... of each tile
+    // (kPerConv of them), in kSub batches of kBatch; lane k of a key word holds
+    // the record row of the warp's k-th record of a tile (-1 when masked).
+    // Raw index entries are loaded three tiles ahead and validated when their
+    // tile's first batch is loaded; each batch's loads are in flight while
+    // the previous batch is converted.  Lane L converts latent bytes
+    // [16 L, 16 L + 16) of every record (scale L / 8).
+    const int cw = warp - kSoftmaxWarps;
+    if constexpr (Lay::kRing > 0) {
+      // Ring pipeline.  Record j of this warp's sequence (tile j / kPerConv,
+      // record j % kPerConv) is copied into ring slot j % R by cp.async when
+      // record j - R + 1 is converted; every lane copies and later reads only
+      // its own 16 bytes of a slot, so a lane's cp.async.wait_group is all the
+      // synchronisation the ring needs.  Keys of tiles t .. t+2 are held
+      // validated, raw entries of tiles t+3 and t+4 are in flight; each tile's
+      // scales (lane L: word L % 4 of record L / 4) are loaded a tile ahead.
+      constexpr int R = Lay::kRing;
+      static_assert(kPerConv * 4 == 32 && R <= 2 * kPerConv, "ring pipeline shape");
+      const uint32_t ring_lane = smem_u32(smem + Lay::off_ring) + uint32_t(cw * R * kLatent) + 16u * lane;
+      const uint8_t* kv_lat = a.kv + 16 * lane;
+      const uint8_t* kv_sc = a.kv + kScaleOffset + 4 * (lane & 3);
+      const uint32_t c_off = uint32_t(lane >> 2) * kChunkBytes;
+      const uint32_t hf = (lane >> 2) & 1;
+      const uint32_t slot_lo = ((uint32_t(lane & 3) * 2 + hf) << 4);
+      const uint32_t slot_hi = ((uint32_t(lane & 3) * 2 + (hf ^ 1)) << 4);
+      auto raw_key = [&](const Cursor& cu) -> int32_t {
+        const int rr = cw + kConvWarps * lane;
+        if (!cu.live || lane >= kPerConv) return INT32_MIN;
+        const int p = cu.p0() + rr;
+        const int64_t off = cu.beg + p;
+        if (p >= cu.p1() || off < 0 || off >= a.n_indices) return INT32_MIN;
+        return __ldg(a.indices + off);
+      };
+      auto key_id = [&](int32_t raw) -> int32_t { return (raw < 0 || raw >= a.n_kv_rows) ? -1 : raw; };
+      auto load_scales = [&](int32_t keys) -> uint32_t {
+        const int32_t id = __shfl_sync(0xffffffffu, keys, lane >> 2);
+        return id >= 0 ? ldg_u32_now(kv_sc + int64_t(id) * kRecordBytes) : 0u;
+      };
+      Cursor cr;  // tile of the newest raw entries
+      cr.init(a, row0, P0, cb, ce);
+      int32_t k0 = key_id(raw_key(cr));
+      cr.advance(a);
+      int32_t k1 = key_id(raw_key(cr));
+      cr.advance(a);
+      int32_t k2 = key_id(raw_key(cr));
+      cr.advance(a);
+      int32_t r3 = raw_key(cr);
+      cr.advance(a);
+      int32_t r4 = raw_key(cr);
+      uint32_t sc_cur = load_scales(k0), sc_next = load_scales(k1);
+      const int n_total = n_tiles * kPerConv;
+      // Records go in groups of G (one cp.async group each), converted
+      // together so that their dependency chains overlap.
+      constexpr int G = R >= 12 ? 4 : 2;
+      constexpr int RG = R / G;  // ring slots in groups
+      static_assert(kPerConv % G == 0, "groups within a tile");
+      static_assert(RG >= 3, "at least two groups in flight");
+      int t = 0;       // tile being converted (keys k0)
+      bool fast = false;  // this tile takes the fast path
+      // the warp's rows cw + kConvWarps kk all have r % 8 == cw % 8 (kConvWarps is 8)
+      static_assert(kConvWarps == 8, "row swizzle constant per warp");
+      const uint32_t x_row = uint32_t(cw & 7) << 4;
+      int gslot = 0;   // ring group slot of the group being converted
+      int igslot = 0;  // ring group slot of the group being issued
+      auto issue = [&](int jj0) {  // copy records jj0 .. jj0+G-1 (tiles t .. t+2) into group slot igslot
 #pragma unroll
-      for (int k = 0; k < kBatch; ++k) {
-        const int kk = sub * kBatch + k;
-        const int32_t id = __shfl_sync(0xffffffffu, keys, kk & 31);
-        B.id[k] = kk < kPerConv ? id : -1;
-        B.lat[k] = make_uint4(0, 0, 0, 0);
-        B.tail[k] = make_uint4(0, 0, 0, 0);
-        if (B.id[k] >= 0) {
-          const uint4* rec = reinterpret_cast<const uint4*>(a.kv + int64_t(B.id[k]) * kRecordBytes);
-          B.lat[k] = ldg_v4_now(rec + lane);
-          if (lane < 9) B.tail[k] = ldg_v4_now(rec + kScaleOffset / 16 + lane);
+        for (int g = 0; g < G; ++g) {
+          const int jj = jj0 + g;
+          const int d = jj / kPerConv - t;
+          const int32_t id =
+              jj < n_total ? __shfl_sync(0xffffffffu, d == 0 ? k0 : (d == 1 ? k1 : k2), jj % kPerConv) : -1;
+          if (id >= 0)
+            cp_async16(ring_lane + uint32_t((igslot * G + g) * kLatent), kv_lat + int64_t(id) * kRecordBytes);
+        }
+        cp_async_commit();
+        igslot = igslot + 1 == RG ? 0 : igslot + 1;
+      };
+#pragma unroll 1
+      for (int jj = 0; jj < (RG - 1) * G; jj += G) issue(jj);
+#pragma unroll 1
+      for (int j = 0; j < n_total; j += G) {
+        const int k = j % kPerConv;
+        if (k == 0) {
+          if (j > 0) {  // next tile: move the key and scale pipelines on
+            ++t;
+            k0 = k1;
+            k1 = k2;
+            k2 = key_id(r3);
+            r3 = r4;
+            cr.advance(a);
+            r4 = raw_key(cr);
+            sc_cur = sc_next;
+            sc_next = load_scales(k1);
+          }
+          SMLA_TR(30, t);
+          if (!wait_bar_warp(kv_empty + (t & 1), ((t >> 1) & 1) ^ 1, ms, a)) break;
+          SMLA_TR(31, t);
+        }
+        const int s = t & 1;
+        if (k == 0) {
+          // per tile: every key valid and every scale <= 2^7 -> the fast path
+          const bool ok = (lane >= kPerConv || k0 >= 0) && sc_cur <= 0x43000000u;
+          fast = __all_sync(0xffffffffu, ok);
+        }
+        cp_async_wait_group<RG - 2>();  // this lane's 16 bytes of records j .. j+G-1 have landed
+        uint8_t* tile_base = tiles + s * kTileBytes + c_off + uint32_t(cw) * 128u;  // row r = cw + kConvWarps kk
+        if (fast) {
+          uint4 v[G];
+          uint32_t m1[G];
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            v[g] = ld_shared_v4(ring_lane + uint32_t((gslot * G + g) * kLatent));
+            const uint32_t scw = __shfl_sync(0xffffffffu, sc_cur, 4 * (k + g) + (lane >> 3));
+            m1[g] = __byte_perm(scw, 0u, 0x3232) + 0x3C003C00u;  // bf16 scale * 2^120, twice
+          }
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            uint32_t o[8];
+            dequant16(v[g], m1[g], o);
+            uint8_t* rb = tile_base + uint32_t(kConvWarps * (k + g)) * 128u;
+            *reinterpret_cast<uint4*>(rb + (slot_lo ^ x_row)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(rb + (slot_hi ^ x_row)) = make_uint4(o[4], o[5], o[6], o[7]);
+          }
+        } else {
+#pragma unroll 1
+          for (int g = 0; g < G; ++g) {
+            const int32_t id = __shfl_sync(0xffffffffu, k0, k + g);
+            uint32_t o[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            if (id >= 0) {  // uniform over the warp
+              const uint4 v = ld_shared_v4(ring_lane + uint32_t((gslot * G + g) * kLatent));
+              const uint32_t scw = __shfl_sync(0xffffffffu, sc_cur, 4 * (k + g) + (lane >> 3));
+              const uint32_t sb2 = __byte_perm(scw, 0u, 0x3232);
+              const bool big = scw > 0x43000000u;  // scale above 2^7 (or not positive)
+              dequant16(v, big ? 0x7B807B80u /* 2^120 */ : sb2 + 0x3C003C00u /* scale 2^120 */, o);
+              if (__any_sync(0xffffffffu, big)) {
+                const uint32_t m2 = big ? sb2 : 0x3F803F80u;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) o[q] = bf16x2_mul(o[q], m2);
+              }
+            }
+            uint8_t* rb = tile_base + uint32_t(kConvWarps * (k + g)) * 128u;
+            *reinterpret_cast<uint4*>(rb + (slot_lo ^ x_row)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(rb + (slot_hi ^ x_row)) = make_uint4(o[4], o[5], o[6], o[7]);
+          }
+        }
+        issue(j + (RG - 1) * G);  // into the group slot read one step ago
+        gslot = gslot + 1 == RG ? 0 : gslot + 1;
+        if (k + G == kPerConv) {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(kv_full + s);
+          SMLA_TR(32, t);
         }
       }
+      cp_async_wait_all();
+    } else {
+    const uint8_t* kv_lat = a.kv + 16 * lane;
+    const uint8_t* kv_sc = a.kv + kScaleOffset + 4 * (lane & 3);  // scale word lane % 4 of a record
+    const uint32_t c_off = uint32_t(lane >> 2) * kChunkBytes;  // 64-dim column block of the lane's dims
+    const uint32_t hf = (lane >> 2) & 1;                      // odd block: halves stored swapped
+    const uint32_t slot_lo = ((uint32_t(lane & 3) * 2 + hf) << 4);
+    const uint32_t slot_hi = ((uint32_t(lane & 3) * 2 + (hf ^ 1)) << 4);
+    auto raw_key = [&](const Cursor& cu) -> int32_t {
+      const int rr = cw + kConvWarps * lane;
+      if (!cu.live || lane >= kPerConv) return INT32_MIN;
+      const int p = cu.p0() + rr;
+      const int64_t off = cu.beg + p;
+      if (p >= cu.p1() || off < 0 || off >= a.n_indices) return INT32_MIN;
+      return __ldg(a.indices + off);
     };
-    Cursor cl;  // the tile whose batches are being loaded
-    cl.init(a, row0, P0, cb, ce);
-    Cursor c3 = cl;  // three tiles ahead of cl: its raw entries are being loaded
-    const int32_t raw0 = raw_key(cl);
+    auto key_id = [&](int32_t raw) -> int32_t { return (raw < 0 || raw >= a.n_kv_rows) ? -1 : raw; };
+    // A batch: kBatch records' latent bytes (lane L: bytes [16 L, 16 L + 16)),
+    // their scales (lane L: word L % 4 of record L / 4) and the key word.
+    struct Batch {
+      uint4 lat[kBatch];
+      uint32_t sc;
+      int32_t keys;
+    };
+    static_assert(kBatch * 4 == 32, "one scale word per lane");
+    auto load_rec = [&](Batch& B, int k, int sub) {
+      const int32_t id = __shfl_sync(0xffffffffu, B.keys, (sub * kBatch + k) & 31);
+      B.lat[k] = make_uint4(0, 0, 0, 0);  // a masked record converts to zeros
+      if (id >= 0) B.lat[k] = ldg_v4_now(kv_lat + int64_t(id) * kRecordBytes);
+    };
+    auto load_scales = [&](Batch& B, int32_t keys, int sub) {
+      B.keys = keys;
+      const int32_t id = __shfl_sync(0xffffffffu, keys, (sub * kBatch + (lane >> 2)) & 31);
+      B.sc = 0u;
+      if (id >= 0) B.sc = ldg_u32_now(kv_sc + int64_t(id) * kRecordBytes);
+    };
+    // Record k of a batch: dequantise and store row r = cw + kConvWarps kk of
+    // the tile (16-byte slots swizzled with r % 8).
+    auto convert_rec = [&](const Batch& B, int k, uint8_t* tile, int sub) {
+      const int kk = sub * kBatch + k;
+      const int r = cw + kConvWarps * kk;
+      const uint32_t scw = __shfl_sync(0xffffffffu, B.sc, 4 * k + (lane >> 3));  // scale of lane's block
+      const uint32_t sb2 = __byte_perm(scw, 0u, 0x3232);  // the scale's bf16 bits, twice
+      const bool big = scw > 0x43000000u;                 // scale above 2^7 (or not positive)
+      uint32_t o[8];
+      dequant16(B.lat[k], big ? 0x7B807B80u /* 2^120 */ : sb2 + 0x3C003C00u /* scale 2^120 */, o);
+      if (__any_sync(0xffffffffu, big)) {
+        const uint32_t m2 = big ? sb2 : 0x3F803F80u;  // then times the scale (1 where done)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) o[j] = bf16x2_mul(o[j], m2);
+      }
+      uint8_t* rb = tile + c_off + uint32_t(r) * 128u;
+      const uint32_t x = uint32_t(r & 7) << 4;
+      *reinterpret_cast<uint4*>(rb + (slot_lo ^ x)) = make_uint4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<uint4*>(rb + (slot_hi ^ x)) = make_uint4(o[4], o[5], o[6], o[7]);
+    };
+    Cursor c3;  // the tile whose raw entries are loaded next
+    c3.init(a, row0, P0, cb, ce);
+    int32_t rk0 = raw_key(c3);
     c3.advance(a);
-    int32_t raw1 = raw_key(c3);
+    int32_t rk1 = raw_key(c3);
     c3.advance(a);
-    int32_t raw2 = raw_key(c3);
-    c3.advance(a);
-    int32_t raw3 = raw_key(c3);
-    int32_t keys_l = valid_key(raw0);
-    prefetch(raw1);
-    prefetch(raw2);
-    int sub_l = 0;  // batch index within cl
-    Batch A;
-    load_batch(A, keys_l, 0);
+    int32_t rk2 = raw_key(c3);
+    int sub_l = 0;            // batch of the loading tile
+    int32_t keys_l = key_id(rk0);
+    auto next_load = [&]() {  // move the loading point one batch on
+      if (++sub_l == kSub) {
+        sub_l = 0;
+        c3.advance(a);
+        const int32_t rk3 = raw_key(c3);
+        keys_l = key_id(rk1);
+        rk1 = rk2;
+        rk2 = rk3;
+      }
+    };
     const int n_batches = n_tiles * kSub;
-    for (int q = 0; q < n_batches; ++q) {
+    // One batch step: convert `cur` record by record, issuing the loads of
+    // `nxt` (the next batch) in between, so that the gathers' L1 work and the
+    // conversion overlap.
+    auto step = [&](int q, const Batch& cur, Batch& nxt) -> bool {
       const int i = q / kSub, sub = q % kSub;
       const int s = i & 1;
       const uint32_t ph = (i >> 1) & 1;
-      uint8_t* tile = tiles + s * kTileBytes;
-      // loads of the next batch (the next tile's first, at a tile boundary)
-      Batch B;
-      if (++sub_l == kSub) {
-        sub_l = 0;
-        cl.advance(a);
-        keys_l = valid_key(raw1);
-        prefetch(raw3);  // loaded a tile ago
-        raw1 = raw2;
-        raw2 = raw3;
-        c3.advance(a);
-        raw3 = raw_key(c3);
-      }
-      if (q + 1 < n_batches) {
-        load_batch(B, keys_l, sub_l);
-      } else {
-#pragma unroll
-        for (int k = 0; k < kBatch; ++k) {
-          B.id[k] = -1;
-          B.lat[k] = make_uint4(0, 0, 0, 0);
-          B.tail[k] = make_uint4(0, 0, 0, 0);
-        }
-      }
+      const bool more = q + 1 < n_batches;
+      const int nsub = sub_l;
+      if (more) load_scales(nxt, keys_l, nsub);
       SMLA_TR(30, i);
-      if (sub == 0 && !wait_bar_warp(kv_empty + s, ph ^ 1, ms, a)) break;
+      if (sub == 0 && !wait_bar_warp(kv_empty + s, ph ^ 1, ms, a)) return false;
       SMLA_TR(31, i);
+      uint8_t* tile = tiles + s * kTileBytes;
 #pragma unroll
       for (int k = 0; k < kBatch; ++k) {
-        const int kk = sub * kBatch + k;
-        const int r = cw + kConvWarps * kk;
-        if (kk >= kPerConv || r >= kTileK) break;
-        // this lane's scale: f32 word (lane / 8) of lane 0's tail chunk
-        const uint32_t sw0 = __shfl_sync(0xffffffffu, A.tail[k].x, 0);
-        const uint32_t sw1 = __shfl_sync(0xffffffffu, A.tail[k].y, 0);
-        const uint32_t sw2 = __shfl_sync(0xffffffffu, A.tail[k].z, 0);
-        const uint32_t sw3 = __shfl_sync(0xffffffffu, A.tail[k].w, 0);
-        SMLA_TR(33 + k, i);  // record k of the batch has arrived
-        const int blk = lane >> 3;
-        const float sc = __uint_as_float(blk == 0 ? sw0 : blk == 1 ? sw1 : blk == 2 ? sw2 : sw3);
-        uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
-        if (A.id[k] >= 0) dequant16_bf16(A.lat[k], sc, lo, hi);
-        uint8_t* rowbase = tile + ck * kChunkBytes + (r >> 3) * 1024;
-        const uint4 first = hi_first ? hi : lo, second = hi_first ? lo : hi;
-        *reinterpret_cast<uint4*>(rowbase + sw128_off(r & 7, b0 + (hi_first ? 16 : 0))) = first;
-        *reinterpret_cast<uint4*>(rowbase + sw128_off(r & 7, b0 + (hi_first ? 0 : 16))) = second;
-        if (lane >= 1 && lane < 9)  // rope chunk lane - 1, bit for bit (zero for a masked key)
-          *reinterpret_cast<uint4*>(tile + 8 * kChunkBytes + (r >> 3) * 1024 + sw128_off(r & 7, (lane - 1) * 16)) =
-              A.tail[k];
-        if (lane == 0) ms->valid[s][r] = A.id[k] >= 0;
+        convert_rec(cur, k, tile, sub);
+        if (more) load_rec(nxt, k, nsub);
       }
-      SMLA_TR(38, i);  // batch stored
+      if (more) next_load();
       if (sub == kSub - 1) {
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(kv_full + s);
         SMLA_TR(32, i);
       }
-      A = B;
+      return true;
+    };
+    Batch A, B;
+    if (n_batches > 0) {
+      load_scales(A, keys_l, 0);
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) load_rec(A, k, 0);
+      next_load();
+    }
+    for (int q = 0; q < n_batches; q += 2) {
+      if (!step(q, A, B)) break;
+      if (q + 1 < n_batches && !step(q + 1, B, A)) break;
+    }
     }
   }
 
@@ -843,101 +1074,102 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
   }
 }
 
-// Merge kernel: CTA (row, head) merges the head's partials of a row that was
+// Merge kernel: warp (row, head) merges the head's partials of a row that was
 // shared between CTAs of the decode launch ([P2] stage_combine: max of the
 // parts' maxima, rescaled sums, sink in the denominator); rows finished whole
 // there are skipped.  The decode launch's CTA 0 left every row's first tile
-// and the tile total in the workspace.  128 threads x 4 latent dims.
-constexpr int kMergeChunk = 512;  // parts handled per pass
+// and the tile total in the workspace.  Lane L owns latent dims
+// [16 L, 16 L + 16); four parts' loads are in flight at a time.
+constexpr int kMergeWarps = 4;
 
-__global__ void __launch_bounds__(128) merge_rows_kernel(DecodeArgs a) {
-  const int row = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+__global__ void __launch_bounds__(32 * kMergeWarps) merge_rows_kernel(DecodeArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t pair = int64_t(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
   const int H = a.heads;
-  __shared__ int32_t slot_s[kMergeChunk];
-  __shared__ float w_s[kMergeChunk];
-  __shared__ float red_s[128];
-  __shared__ float bc_s[2];
-  const int64_t P = a.row_tile[row], T = a.row_tile[a.n_q], G = a.grid;
-  const int32_t nt = int32_t(a.row_tile[row + 1] - P);
-  int64_t ca, cb;
-  row_parts(P, nt, T, G, &ca, &cb);
+  if (pair >= int64_t(a.n_q) * H) return;
+  const int row = int(pair / H), h = int(pair % H);
+  const int64_t P = __ldcg(a.row_tile + row), T = __ldcg(a.row_tile + a.n_q), G = a.grid;
+  const int32_t nt = int32_t(__ldcg(a.row_tile + row + 1) - P);
+  const int64_t ca = cta_of_tile(P, T, G), cb = cta_of_tile(P + nt - 1, T, G);
   if (ca == cb) return;  // finished whole by one CTA
-  const int64_t nscan = cb - ca + 1;
-  // pass 1: the largest part maximum
+  // pass 1: each lane takes parts ca + lane, ca + lane + 32, ...: their maximum
   float mloc = -INFINITY;
-  for (int64_t j = tid; j < nscan; j += 128) {
-    const int64_t c = ca + j;
-    if (cta_begin(c + 1, T, G) == cta_begin(c, T, G)) continue;
+  for (int64_t c = ca + lane; c <= cb; c += 32) {
+    if (cta_begin(c + 1, T, G) == cta_begin(c, T, G)) continue;  // a CTA without tiles
     const int64_t o = (part_slot(c, P, T, G) * H + h) * 2;
     if (__ldcg(a.ml_part + o + 1) > 0.f) mloc = fmaxf(mloc, __ldcg(a.ml_part + o));
   }
-  red_s[tid] = mloc;
-  __syncthreads();
-  for (int o = 64; o > 0; o >>= 1) {
-    if (tid < o) red_s[tid] = fmaxf(red_s[tid], red_s[tid + o]);
-    __syncthreads();
-  }
-  const float mstar = red_s[0];
-  __syncthreads();
-  // pass 2: weights of the parts, their sum and the merged numerator
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
+  const float mstar = mloc;
+  // pass 2: weights, their sum and the merged numerator (32 parts per round)
+  float acc[16];
+#pragma unroll
+  for (int q = 0; q < 16; ++q) acc[q] = 0.f;
   float lsum = 0.f;
-  const int d4 = 4 * tid;
-  for (int64_t j0 = 0; j0 < nscan; j0 += kMergeChunk) {
-    const int n = int(nscan - j0 < kMergeChunk ? nscan - j0 : kMergeChunk);
-    for (int j = tid; j < n; j += 128) {
-      const int64_t c = ca + j0 + j;
-      int32_t sl = -1;
-      float w = 0.f;
-      if (cta_begin(c + 1, T, G) > cta_begin(c, T, G)) {
-        sl = int32_t(part_slot(c, P, T, G));
-        const int64_t o = (int64_t(sl) * H + h) * 2;
-        const float lc = __ldcg(a.ml_part + o + 1);
-        if (lc > 0.f) {
-          w = exp2f(__ldcg(a.ml_part + o) - mstar);
-          lsum += lc * w;
+  int nvsum = 0;
+  for (int64_t c0 = ca; c0 <= cb; c0 += 32) {
+    const int64_t c = c0 + lane;
+    int64_t sl = -1;
+    float w = 0.f;
+    if (c <= cb && cta_begin(c + 1, T, G) > cta_begin(c, T, G)) {
+      sl = part_slot(c, P, T, G);
+      const int64_t o = (sl * H + h) * 2;
+      const float lc = __ldcg(a.ml_part + o + 1);
+      if (lc > 0.f) {
+        w = exp2f(__ldcg(a.ml_part + o) - mstar);
+        lsum += lc * w;
+      }
+      if (h == 0) nvsum += __ldcg(a.nv_part + sl);
+    }
+    const int n = int(cb - c0 + 1 < 32 ? cb - c0 + 1 : 32);
+    for (int j = 0; j < n; j += 4) {  // four parts' loads in flight at once
+      float wj[4];
+      float4 v[4][4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        wj[u] = __shfl_sync(0xffffffffu, w, (j + u) & 31);
+        const int64_t slj = __shfl_sync(0xffffffffu, sl, (j + u) & 31);
+        if (j + u >= n) wj[u] = 0.f;
+        const float4* src = reinterpret_cast<const float4*>(a.o_part + (slj * H + h) * kLatent + 16 * lane);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[u][q] = wj[u] != 0.f ? __ldcg(src + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          acc[4 * q] = fmaf(wj[u], v[u][q].x, acc[4 * q]);
+          acc[4 * q + 1] = fmaf(wj[u], v[u][q].y, acc[4 * q + 1]);
+          acc[4 * q + 2] = fmaf(wj[u], v[u][q].z, acc[4 * q + 2]);
+          acc[4 * q + 3] = fmaf(wj[u], v[u][q].w, acc[4 * q + 3]);
         }
       }
-      slot_s[j] = sl;
-      w_s[j] = w;
     }
-    __syncthreads();
-#pragma unroll 4
-    for (int j = 0; j < n; ++j) {
-      const float w = w_s[j];
-      if (w == 0.f) continue;
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(a.o_part + (int64_t(slot_s[j]) * H + h) * kLatent + d4));
-      acc.x = fmaf(w, v.x, acc.x);
-      acc.y = fmaf(w, v.y, acc.y);
-      acc.z = fmaf(w, v.z, acc.z);
-      acc.w = fmaf(w, v.w, acc.w);
-    }
-    __syncthreads();
   }
-  red_s[tid] = lsum;
-  __syncthreads();
-  for (int o = 64; o > 0; o >>= 1) {
-    if (tid < o) red_s[tid] += red_s[tid + o];
-    __syncthreads();
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+    nvsum += __shfl_xor_sync(0xffffffffu, nvsum, o);
   }
-  if (tid == 0) {
-    float fac, lse;
-    finish_head(mstar, red_s[0], a.sink, h, &fac, &lse);
-    bc_s[0] = fac;
+  float fac = 0.f, lse = 0.f;
+  finish_head(mstar, lsum, a.sink, h, &fac, &lse);
+  if (lane == 0) {
     if (a.lse) a.lse[int64_t(row) * H + h] = lse;
-    if (h == 0 && a.n_valid) {
-      int tot = 0;
-      for (int64_t c = ca; c <= cb; ++c)
-        if (cta_begin(c + 1, T, G) > cta_begin(c, T, G)) tot += __ldcg(a.nv_part + part_slot(c, P, T, G));
-      a.n_valid[row] = tot;
-    }
+    if (h == 0 && a.n_valid) a.n_valid[row] = nvsum;
   }
-  __syncthreads();
-  const float fac = bc_s[0];
-  uint2 packed;
-  packed.x = pack_bf16x2(acc.x * fac, acc.y * fac);
-  packed.y = pack_bf16x2(acc.z * fac, acc.w * fac);
-  *reinterpret_cast<uint2*>(a.out + row * a.out_stride_row + h * a.out_stride_head + d4) = packed;
+  uint4 lo, hi;
+  lo.x = pack_bf16x2(acc[0] * fac, acc[1] * fac);
+  lo.y = pack_bf16x2(acc[2] * fac, acc[3] * fac);
+  lo.z = pack_bf16x2(acc[4] * fac, acc[5] * fac);
+  lo.w = pack_bf16x2(acc[6] * fac, acc[7] * fac);
+  hi.x = pack_bf16x2(acc[8] * fac, acc[9] * fac);
+  hi.y = pack_bf16x2(acc[10] * fac, acc[11] * fac);
+  hi.z = pack_bf16x2(acc[12] * fac, acc[13] * fac);
+  hi.w = pack_bf16x2(acc[14] * fac, acc[15] * fac);
+  uint4* dst = reinterpret_cast<uint4*>(a.out + row * a.out_stride_row + h * a.out_stride_head + 16 * lane);
+  dst[0] = lo;
+  dst[1] = hi;
 }
 
 template <int HP>
@@ -949,8 +1181,8 @@ cudaError_t launch_tc_hp(const DecodeLaunch& L) {
   decode_tc_kernel<HP><<<L.plan.grid, kThreadsTC, smem, L.stream>>>(args);
   e = cudaGetLastError();
   if (e != cudaSuccess || !L.plan.merge_kernel) return e;
-  dim3 grid(L.p.n_q, L.p.num_heads);
-  merge_rows_kernel<<<grid, 128, 0, L.stream>>>(args);
+  const int64_t pairs = int64_t(L.p.n_q) * L.p.num_heads;
+  merge_rows_kernel<<<unsigned((pairs + kMergeWarps - 1) / kMergeWarps), 32 * kMergeWarps, 0, L.stream>>>(args);
   return cudaGetLastError();
 }
 

@@ -63,6 +63,41 @@ __device__ __forceinline__ uint4 ldg_v4_now(const void* p) {
   return v;
 }
 
+// 4-byte read-only global load kept at this point of the program (volatile).
+__device__ __forceinline__ uint32_t ldg_u32_now(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(__cvta_generic_to_global(p)));
+  return v;
+}
+
+// 16-byte asynchronous global -> shared copy (L2 only), both 16-byte aligned.
+__device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(__cvta_generic_to_global(src))
+               : "memory");
+}
+
+// Makes `bar` wait for this thread's cp.async copies issued so far: its
+// pending count goes up by one now and back down when they have landed.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Waits until at most N of this thread's committed cp.async groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Non-blocking prefetch of `bytes` (a multiple of 16, 16-byte aligned) of
 // global memory into L2.
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
