@@ -345,6 +345,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
   const int64_t G = gridDim.x;
   const int64_t c_id = blockIdx.x;
 
+  SMLA_TR(3, 0);  // kernel entry
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(kv_full + s, kConvWarps + 1);  // latent converters and the rope copier
@@ -376,27 +377,31 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
     const int lo = min(tid * per, n), hi = min(lo + per, n);
     int64_t local = 0;
     for (int r = lo; r < hi; ++r) local += tiles_of_len(row_len(a, r));
-    scan[tid] = local;
-    __syncthreads();
-    if (warp == 0) {  // exclusive scan of the 512 partial sums by one warp
-      int64_t run = 0;
-      for (int base = 0; base < kThreadsTC; base += 32) {
-        const int64_t v = scan[base + lane];
-        int64_t x = v;
+    // exclusive scan of the 512 partial sums: within each warp, then over the
+    // 16 warp totals
+    int64_t x = local;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
-          if (lane >= o) x += y;
-        }
-        scan[base + lane] = run + x - v;
-        run += __shfl_sync(0xffffffffu, x, 31);
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) scan[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      const int64_t v = lane < kThreadsTC / 32 ? scan[lane] : 0;
+      int64_t t = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t y = __shfl_up_sync(0xffffffffu, t, o);
+        if (lane >= o) t += y;
       }
-      if (lane == 0) ms->total_tiles = run;
+      if (lane < kThreadsTC / 32) scan[32 + lane] = t - v;  // warp offsets
+      if (lane == 31) ms->total_tiles = t;
     }
     __syncthreads();
     const int64_t Tt = ms->total_tiles;
     const int64_t b = cta_begin(c_id, Tt, G);
-    int64_t P = scan[tid];
+    int64_t P = scan[32 + warp] + x - local;  // tiles before this thread's rows
     for (int r = lo; r < hi; ++r) {
       const int32_t nt_r = tiles_of_len(row_len(a, r));
       if (P <= b && b < P + nt_r) {
@@ -432,6 +437,30 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
 #pragma unroll
     for (int h = 0; h < HH; ++h) lpart[h] = 0.f;
     int nv = 0;
+    // Stage row `row`'s q (bf16, 128-byte swizzled K-major [9][HP][128],
+    // latent dims in latent_dim_of order) and signal the QK issuers.  Called
+    // when every QK that read the previous q has completed.
+    auto stage_q = [&](int row) {
+      SMLA_TR(25, row);
+      for (int k = tid; k < HP * (kQK / 8); k += kSoftmaxThreads) {
+        const int h = k / (kQK / 8), c16 = k % (kQK / 8);
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (h < H)
+          v = __ldg(reinterpret_cast<const uint4*>(a.q + row * a.q_stride_row + h * a.q_stride_head + c16 * 8));
+        int pc = c16;  // position chunk of these 8 dims (latent_dim_of, applied per chunk)
+        if (c16 < kLatent / 8) {
+          pc = c16 ^ ((c16 >> 3) & 1);
+          v = make_uint4(__byte_perm(v.x, v.y, 0x5410), __byte_perm(v.x, v.y, 0x7632),
+                         __byte_perm(v.z, v.w, 0x5410), __byte_perm(v.z, v.w, 0x7632));
+        }
+        const uint32_t off =
+            uint32_t(pc >> 3) * (HP * 128) + uint32_t(h >> 3) * 1024u + sw128_off(h & 7, (pc & 7) * 16);
+        *reinterpret_cast<uint4*>(q_s + off) = v;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_full);
+    };
     Cursor c;
     c.init(a, row0, P0, cb, ce);
     int seg = 0;
@@ -440,28 +469,16 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
       const uint32_t ph = (i >> 1) & 1;
       const bool first = c.first(), last = c.last();
       const int ob = Lay::n_ob == 2 ? (seg & 1) : 0;
-      if (first) {
-        // stage this row's q (bf16, 128-byte swizzled K-major [9][HP][128]).
-        // Every QK that read the previous q has completed: this warpgroup
-        // has consumed their S.
-        for (int k = tid; k < HP * (kQK / 8); k += kSoftmaxThreads) {
-          const int h = k / (kQK / 8), c16 = k % (kQK / 8);
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (h < H)
-            v = __ldg(reinterpret_cast<const uint4*>(a.q + c.row * a.q_stride_row + h * a.q_stride_head + c16 * 8));
-          int pc = c16;  // position chunk of these 8 dims (latent_dim_of, applied per chunk)
-          if (c16 < kLatent / 8) {
-            pc = c16 ^ ((c16 >> 3) & 1);
-            v = make_uint4(__byte_perm(v.x, v.y, 0x5410), __byte_perm(v.x, v.y, 0x7632),
-                           __byte_perm(v.z, v.w, 0x5410), __byte_perm(v.z, v.w, 0x7632));
-          }
-          const uint32_t off =
-              uint32_t(pc >> 3) * (HP * 128) + uint32_t(h >> 3) * 1024u + sw128_off(h & 7, (pc & 7) * 16);
-          *reinterpret_cast<uint4*>(q_s + off) = v;
+      if (first) stage_q(c.row);  // every QK that read the previous q has completed
+      if (last && i + 1 < n_tiles) {
+        // the next row's q is staged at its first tile: bring it into L2 now
+        const char* qn = reinterpret_cast<const char*>(a.q + int64_t(c.row + 1) * a.q_stride_row);
+        for (int k = tid; k < H * (kQK * 2 / 128); k += kSoftmaxThreads) {
+          const int h = k / (kQK * 2 / 128), line = k % (kQK * 2 / 128);
+          prefetch_l2_line(qn + int64_t(h) * a.q_stride_head * 2 + line * 128);
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(q_full);
+      }
+      if (first) {
 #pragma unroll
         for (int h = 0; h < HH; ++h) lpart[h] = 0.f;
         nv = 0;
@@ -489,6 +506,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(s_empty + s);
+      SMLA_TR(14, i);
       const bool valid = active && ms->valid[s][r];
       nv += valid;
       bool need = first;
@@ -501,6 +519,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
       if (lane == 0) ms->flag[wg][s][qd] = need;
       named_barrier(1 + wg, 128);
       need = ms->flag[wg][s][0] | ms->flag[wg][s][1] | ms->flag[wg][s][2] | ms->flag[wg][s][3];
+      SMLA_TR(15, i);
       if (need) {
         // exact tile max of this warpgroup's heads, then move the references
         // (a row part starts from scratch: its old reference is -inf)
@@ -563,11 +582,13 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
         lpart[h + 1] += p1;
         pk[h / 2] = pack_bf16x2(p0, p1);
       }
+      SMLA_TR(16, i);
       // the P stage is free once the PV that last read it has completed
       if (Lay::p_stages == 2)
         wait_bar_warp(pv_done + s, ph ^ 1, ms, a);  // PV(i-2)
       else if (i > 0)
         wait_bar_warp(pv_done + ((i - 1) & 1), ((i - 1) >> 1) & 1, ms, a);  // PV(i-1)
+      SMLA_TR(17, i);
       const int ps = Lay::p_stages == 2 ? s : 0;
       if (active) {
         uint8_t* prow = p_s + ps * Lay::p_bytes;
@@ -586,12 +607,27 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
 
       if (last) {
         // ---------- epilogue of this row part ----------
+        {
+          // per-head key sums of this warp by a butterfly reduce-scatter: at
+          // the step of half width hs a lane keeps the upper half of its heads
+          // when its lane bit hs is set; after the steps lane L (< HH) holds
+          // head L's sum over its 16-lane half, then the halves are added.
+          float v[HH];
 #pragma unroll
-        for (int h = 0; h < HH; ++h) {
-          float t = active ? lpart[h] : 0.f;
+          for (int h = 0; h < HH; ++h) v[h] = active ? lpart[h] : 0.f;
 #pragma unroll
-          for (int o = 1; o < 32; o <<= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-          if (lane == 0) ms->red[wg][qd][h] = t;
+          for (int hs = HH / 2; hs >= 1; hs >>= 1) {
+            const bool up = (lane & hs) != 0;
+#pragma unroll
+            for (int j = 0; j < hs; ++j) {
+              const float send = up ? v[j] : v[j + hs];
+              const float keep = up ? v[j + hs] : v[j];
+              v[j] = keep + __shfl_xor_sync(0xffffffffu, send, hs);
+            }
+          }
+          float t = v[0];
+          if (HH < 32) t += __shfl_xor_sync(0xffffffffu, t, HH);
+          if (lane < HH) ms->red[wg][qd][lane] = t;
         }
         if (wg == 0) {
           int t = nv;
@@ -600,6 +636,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
           if (lane == 0) ms->nvr[qd] = t;
         }
         named_barrier(3, kSoftmaxThreads);
+        SMLA_TR(24, i);
         const bool whole = c.whole();
         const int64_t slot = whole ? -1 : part_slot(c_id, c.P, T, G);
         const int row = c.row;
@@ -626,9 +663,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
           }
         }
         named_barrier(3, kSoftmaxThreads);
+        SMLA_TR(18, i);
         // O^T of the part: wait for its last PV, then read it out.
         wait_bar_warp(pv_done + s, ph, ms, a);
         tc_fence_after();
+        SMLA_TR(19, i);
 #pragma unroll 1
         for (int mt = wg; mt < 4; mt += Lay::SWG) {
           const int dg = latent_dim_of(mt * 128 + qd * 32 + lane);
@@ -832,15 +871,16 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
       };
       Cursor cr;  // tile of the newest raw entries
       cr.init(a, row0, P0, cb, ce);
-      int32_t k0 = key_id(raw_key(cr));
+      const int32_t r0 = raw_key(cr);  // all five loads in flight before any is used
       cr.advance(a);
-      int32_t k1 = key_id(raw_key(cr));
+      const int32_t r1 = raw_key(cr);
       cr.advance(a);
-      int32_t k2 = key_id(raw_key(cr));
+      const int32_t r2 = raw_key(cr);
       cr.advance(a);
       int32_t r3 = raw_key(cr);
       cr.advance(a);
       int32_t r4 = raw_key(cr);
+      int32_t k0 = key_id(r0), k1 = key_id(r1), k2 = key_id(r2);
       uint32_t sc_cur = load_scales(k0), sc_next = load_scales(k1);
       const int n_total = n_tiles * kPerConv;
       // Records go in groups of G (one cp.async group each), converted
@@ -1092,12 +1132,27 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_rows_kernel(DecodeArgs
   const int32_t nt = int32_t(__ldcg(a.row_tile + row + 1) - P);
   const int64_t ca = cta_of_tile(P, T, G), cb = cta_of_tile(P + nt - 1, T, G);
   if (ca == cb) return;  // finished whole by one CTA
-  // pass 1: each lane takes parts ca + lane, ca + lane + 32, ...: their maximum
-  float mloc = -INFINITY;
-  for (int64_t c = ca + lane; c <= cb; c += 32) {
-    if (cta_begin(c + 1, T, G) == cta_begin(c, T, G)) continue;  // a CTA without tiles
-    const int64_t o = (part_slot(c, P, T, G) * H + h) * 2;
-    if (__ldcg(a.ml_part + o + 1) > 0.f) mloc = fmaxf(mloc, __ldcg(a.ml_part + o));
+  // Lane j holds part ca + j + 32 k of round k: its slot and (m, l), read once.
+  auto part_of = [&](int64_t c, int64_t* sl, float* m, float* l) {
+    *sl = -1;
+    *m = -INFINITY;
+    *l = 0.f;
+    if (c > cb || cta_begin(c + 1, T, G) == cta_begin(c, T, G)) return;  // past the end / CTA without tiles
+    *sl = part_slot(c, P, T, G);
+    const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.ml_part + (*sl * H + h) * 2));
+    *m = ml.x;
+    *l = ml.y;
+  };
+  // pass 1: the largest part maximum (the first round's parts stay in registers)
+  int64_t sl0;
+  float m0, l0;
+  part_of(ca + lane, &sl0, &m0, &l0);
+  float mloc = l0 > 0.f ? m0 : -INFINITY;
+  for (int64_t c = ca + 32 + lane; c <= cb; c += 32) {
+    int64_t sl;
+    float m, l;
+    part_of(c, &sl, &m, &l);
+    if (l > 0.f) mloc = fmaxf(mloc, m);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
@@ -1109,19 +1164,15 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_rows_kernel(DecodeArgs
   float lsum = 0.f;
   int nvsum = 0;
   for (int64_t c0 = ca; c0 <= cb; c0 += 32) {
-    const int64_t c = c0 + lane;
-    int64_t sl = -1;
+    int64_t sl = sl0;
+    float m = m0, l = l0;
+    if (c0 != ca) part_of(c0 + lane, &sl, &m, &l);
     float w = 0.f;
-    if (c <= cb && cta_begin(c + 1, T, G) > cta_begin(c, T, G)) {
-      sl = part_slot(c, P, T, G);
-      const int64_t o = (sl * H + h) * 2;
-      const float lc = __ldcg(a.ml_part + o + 1);
-      if (lc > 0.f) {
-        w = exp2f(__ldcg(a.ml_part + o) - mstar);
-        lsum += lc * w;
-      }
-      if (h == 0) nvsum += __ldcg(a.nv_part + sl);
+    if (l > 0.f) {
+      w = exp2f(m - mstar);
+      lsum += l * w;
     }
+    if (h == 0 && sl >= 0) nvsum += __ldcg(a.nv_part + sl);
     const int n = int(cb - c0 + 1 < 32 ? cb - c0 + 1 : 32);
     for (int j = 0; j < n; j += 4) {  // four parts' loads in flight at once
       float wj[4];
