@@ -412,11 +412,12 @@ def main():
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": ncu_traffic(w.name),
                      "peak_source": peak_src,
-                     "kernel": f"smla decode, {args.kernel} kernel (one launch per step)",
+                     "kernel": (f"one smla_decode call ({args.kernel} decode kernel"
+                                + (" + merge kernel" if prob.plan.merge_kernel else "") + "), CUDA events"),
                      "algorithmic_bytes_per_launch": bytes_step},
         "e2e": {"value": weak_scaling_rows_per_s(world, w.n_q, steps, e2e_ms), "unit": "rows/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": steps,
+        "gpu_launches": steps * (2 if prob.plan.merge_kernel else 1),
         "clocks": clk.summary(),
         "cpu_baseline": cpu,
         "also": extra,

@@ -21,7 +21,7 @@ with no blocking, fusion or reordering beyond what the definition states:
   subnormals at exponent 0, no infinities, S.1111.111 is NaN, max 448.  The
   448 and 57344 constants of the [P1] writer rule are this format's.
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent (c-numbers as in the design notes):
 
 * c1  positions >= len and entries < 0 are masked, with or without has_invalid.
 * c2  an entry >= n_kv_rows is masked like -1 (the pages leave it undefined).
