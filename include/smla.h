@@ -112,8 +112,8 @@ typedef struct smla_decode_params {
   /* Planning hints; results never depend on them.  max_row_len: an upper
    * bound of the rows' slice lengths known on the host (e.g. top-k); <= 0 means
    * unknown (n_indices / n_q is used).  has_invalid: rows may end in -1
-   * padding; each row is then trimmed after its last entry >= 0 ([P1]
-   * "Tiles", has_invalid). */
+   * padding ([P1] "Tiles", has_invalid); masked entries are skipped either
+   * way, so this only informs the plan. */
   int32_t max_row_len;
   int32_t has_invalid;
   float sm_scale;
@@ -150,7 +150,7 @@ typedef struct smla_decode_params {
  * first and last tile) gets one partial per CTA, stored in workspace slot
  * 2 c + (P_r < b_c ? 0 : 1), and is merged from those slots ([P2]
  * stage_combine) by a second, small kernel launched right after
- * (merge_kernel = 1 whenever grid > 1; its CTA (r, h) merges head h of row r).
+ * (merge_kernel = 1 whenever grid > 1; a warp merges one head of a row).
  * CUDA-core kernel: one CTA per (row, chunk); chunk c of a row covers slice
  * positions [c chunk_len, (c + 1) chunk_len), the last chunk everything after;
  * partial slot r * num_splits + c; the last chunk to finish merges.
