@@ -181,7 +181,7 @@ int smla_plan(const smla_decode_params* params, int32_t num_sms, smla_plan_info*
  *   row_tile int64 [n_q + 1]     tensor-core kernel: P_r of every row, then T
  *   o_part   f32 [S][H][512]     unnormalised partial sum_t 2^(x_t - m) v_t of a row part
  *   ml_part f32 [S][H][2]        (m, l) of x_t = s_t * log2(e): m is the part's reference
- *                                maximum (its max, or at most 8 below it), l = sum_t 2^(x_t - m);
+ *                                maximum (its max, or at most 24 below it), l = sum_t 2^(x_t - m);
  *                                m = -inf, l = 0 for a part without keys
  *   nv_part int32 [S]            contributing keys of the part
  * The ticket counters must be zero when a call starts (e.g. allocate the

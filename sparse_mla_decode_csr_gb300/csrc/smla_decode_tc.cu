@@ -34,7 +34,8 @@
 //   QK  S^T[64 keys, HP heads] = K_tile[64 x 576] . Q^T       (M=64, N=HP, K=576)
 //   softmax on S^T in log2 units with a lazily moved per-head reference max:
 //       p = 2^(x - m_ref), x = s * sm_scale * log2 e; m_ref is raised (and O
-//       rescaled in TMEM) only when a score exceeds m_ref + 8, so p <= 256;
+//       rescaled in TMEM) only when a score exceeds m_ref + 24, so p <= 2^24
+//       (exact in bf16's range; f32 sums stay far from overflow);
 //       p is written as bf16 P^T
 //   PV  O^T[128 d, HP] += V^T[128 d, 64 keys] . P^T[64 keys, HP], four 128-dim
 //       M tiles; V^T is the same shared-memory key tile read MN-major.
@@ -101,7 +102,7 @@ constexpr int kQkWarpB = 13;   // QK K-steps [18, 36) -> S accumulator 1
 constexpr int kPvWarp = 14;    // PV
 constexpr int kRopeWarp = 15;  // rope copier
 constexpr int kQkSteps = kQK / 16;
-constexpr float kRescaleMargin = 8.f;            // p <= 2^8 before a max update
+constexpr float kRescaleMargin = 24.f;           // p <= 2^24 before a max update
 constexpr float kInitMax = -1.0e30f;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
 
@@ -521,52 +522,77 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
       need = ms->flag[wg][s][0] | ms->flag[wg][s][1] | ms->flag[wg][s][2] | ms->flag[wg][s][3];
       SMLA_TR(15, i);
       if (need) {
-        // exact tile max of this warpgroup's heads, then move the references
-        // (a row part starts from scratch: its old reference is -inf)
+        // exact tile max of this warpgroup's heads (a butterfly reduce-scatter:
+        // lane L ends with head L's max over the warp's keys), then lane h of the
+        // warpgroup's first warp moves head h's reference and publishes its
+        // factor; a row part starts from scratch (its old reference is -inf)
+        {
+          float v[HH];
 #pragma unroll
-        for (int h = 0; h < HH; ++h) {
-          float t = x[h];
+          for (int h = 0; h < HH; ++h) v[h] = x[h];
 #pragma unroll
-          for (int o = 1; o < 32; o <<= 1) t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, o));
-          if (lane == 0) ms->red[wg][qd][h] = t;
+          for (int hs = HH / 2; hs >= 1; hs >>= 1) {
+            const bool up = (lane & hs) != 0;
+#pragma unroll
+            for (int j = 0; j < hs; ++j) {
+              const float send = up ? v[j] : v[j + hs];
+              const float keep = up ? v[j + hs] : v[j];
+              v[j] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, hs));
+            }
+          }
+          float t = v[0];
+          if (HH < 32) t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, HH));
+          if (lane < HH) ms->red[wg][qd][lane] = t;
         }
         named_barrier(1 + wg, 128);
-#pragma unroll
-        for (int h = 0; h < HH; ++h) {
+        SMLA_TR(26, i);
+        if (qd == 0 && lane < HH) {
+          const int h = lane;
           const float tm = fmaxf(fmaxf(ms->red[wg][0][h], ms->red[wg][1][h]),
                                  fmaxf(ms->red[wg][2][h], ms->red[wg][3][h]));
           const float old = first ? kInitMax : mr[h];
-          const float al = ex2(old - fmaxf(old, tm));
-          lpart[h] *= al;
-          if (tid == wg * 128) ms->alpha[wg][h] = al;
+          const float nm = fmaxf(old, tm);
+          ms->alpha[wg][h] = ex2(old - nm);
+          mr[h] = nm;
         }
-        named_barrier(1 + wg, 128);  // everyone has read the old references
-        if (tid == wg * 128) {
-          for (int h = 0; h < HH; ++h) {
-            const float tm = fmaxf(fmaxf(ms->red[wg][0][h], ms->red[wg][1][h]),
-                                   fmaxf(ms->red[wg][2][h], ms->red[wg][3][h]));
-            const float old = first ? kInitMax : mr[h];
-            mr[h] = fmaxf(old, tm);
-          }
-        }
-        named_barrier(1 + wg, 128);  // the new references are visible
+        named_barrier(1 + wg, 128);  // the new references and factors are visible
+#pragma unroll
+        for (int h = 0; h < HH; ++h) lpart[h] *= ms->alpha[wg][h];
+        SMLA_TR(27, i);
         if (!first) {
           // O^T columns of this warpgroup's heads, all four 128-dim tiles:
           // wait for PV(i-1), then scale in place.
           wait_bar_warp(pv_done + ((i - 1) & 1), ((i - 1) >> 1) & 1, ms, a);
           tc_fence_after();
+          SMLA_TR(28, i);
+          // 8-head chunks whose factors are all 1 keep their columns as they are
+          uint32_t todo = 0;
+#pragma unroll
+          for (int cc = 0; cc < HH / 8; ++cc) {
+            bool one = true;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) one &= ms->alpha[wg][8 * cc + k] == 1.f;
+            todo |= one ? 0u : (1u << cc);
+          }
+          constexpr int kCb = HH / 8 < 2 ? HH / 8 : 2;  // 8-column chunks per load batch
 #pragma unroll 1
-          for (int mt = 0; mt < 4; ++mt) {
+          for (int mt = 0; mt < 4 && todo != 0; ++mt) {
             const uint32_t taddr = tmem + (uint32_t(32 * qd) << 16) + Lay::o_col(ob, mt) + uint32_t(wg * HH);
 #pragma unroll
-            for (int cc = 0; cc < HH / 8; ++cc) {
-              uint32_t v[8];
-              tmem_ld8(taddr + 8 * cc, v);
+            for (int c0 = 0; c0 < HH / 8; c0 += kCb) {
+              if (!(todo & (((1u << kCb) - 1) << c0))) continue;
+              // kCb chunks: all loads, one wait, scale, all stores
+              uint32_t v[8 * kCb];
+#pragma unroll
+              for (int u = 0; u < kCb; ++u) tmem_ld8(taddr + 8 * (c0 + u), *reinterpret_cast<uint32_t(*)[8]>(&v[8 * u]));
               tmem_wait_ld();
 #pragma unroll
-              for (int k = 0; k < 8; ++k)
-                v[k] = __float_as_uint(__uint_as_float(v[k]) * ms->alpha[wg][8 * cc + k]);
-              tmem_st8(taddr + 8 * cc, v);
+              for (int u = 0; u < kCb; ++u) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                  v[8 * u + k] = __float_as_uint(__uint_as_float(v[8 * u + k]) * ms->alpha[wg][8 * (c0 + u) + k]);
+                tmem_st8(taddr + 8 * (c0 + u), *reinterpret_cast<const uint32_t(*)[8]>(&v[8 * u]));
+              }
             }
           }
           tmem_wait_st();
