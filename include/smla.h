@@ -141,16 +141,18 @@ typedef struct smla_decode_params {
 /* How a decode call with given params is laid out on the GPU.
  *
  * Tensor-core kernel (the default): a persistent, balanced schedule.  Each row
- * r is cut into T_r = max(1, ceil(len_r / 64)) tiles of 64 slice positions;
- * the rows' tiles are concatenated in row order into one tile space of
- * T = sum_r T_r tiles, starting row r at tile P_r = sum_{r' < r} T_r'.  CTA c of
- * G = grid takes the tiles [b_c, e_c) with b_c = floor(c T / G), and streams
- * through them across row boundaries.  A row lying wholly inside one CTA's
- * range is finished there; a row shared by CTAs c_a..c_b (the CTAs holding its
- * first and last tile) gets one partial per CTA, stored in workspace slot
- * 2 c + (P_r < b_c ? 0 : 1), and is merged from those slots ([P2]
- * stage_combine) by a second, small kernel launched right after
- * (merge_kernel = 1 whenever grid > 1; a warp merges one head of a row).
+ * r is cut into T_r = max(1, ceil(len_r / 64)) tiles of 64 slice positions
+ * and takes 2 + T_r slots of a schedule space (2 slots stand for the cost of
+ * starting a row: its epilogue and q staging), rows in order, so row r's
+ * tiles are slots [R_r, R_r + T_r) with R_r = 2 + sum_{r' < r} (2 + T_r').  CTA
+ * c of G = grid takes the slots [b_c, e_c) with b_c = floor(c W / G), W the
+ * slot total, and streams through the tiles in its range across row
+ * boundaries.  A row lying wholly inside one CTA's range is finished there; a
+ * row shared by CTAs c_a..c_b (the CTAs holding its first and last tile) gets
+ * one partial per CTA, stored in workspace slot 2 c + (R_r < b_c ? 0 : 1), and
+ * is merged from those slots ([P2] stage_combine) by a second, small kernel
+ * launched right after (merge_kernel = 1 whenever grid > 1; a warp merges one
+ * head of a row).
  * CUDA-core kernel: one CTA per (row, chunk); chunk c of a row covers slice
  * positions [c chunk_len, (c + 1) chunk_len), the last chunk everything after;
  * partial slot r * num_splits + c; the last chunk to finish merges.
@@ -178,7 +180,7 @@ int smla_plan(const smla_decode_params* params, int32_t num_sms, smla_plan_info*
  *
  * Layout (each part 256-byte aligned), S = plan.partial_slots:
  *   ticket   int32 [n_q]         per-row arrival counters (CUDA-core kernel)
- *   row_tile int64 [n_q + 1]     tensor-core kernel: P_r of every row, then T
+ *   row_tile int64 [n_q + 1]     tensor-core kernel: first slot of every row, then W
  *   o_part   f32 [S][H][512]     unnormalised partial sum_t 2^(x_t - m) v_t of a row part
  *   ml_part f32 [S][H][2]        (m, l) of x_t = s_t * log2(e): m is the part's reference
  *                                maximum (its max, or at most 24 below it), l = sum_t 2^(x_t - m);

@@ -113,8 +113,9 @@ struct Misc {
   int32_t abort;
   int32_t is_last;
   int32_t first_row;      // schedule: first row of this CTA's range
-  int64_t first_tile;     // schedule: that row's first tile
-  int64_t total_tiles;    // schedule: T
+  int64_t first_tile;     // schedule: that row's first slot
+  int64_t total_tiles;    // schedule: W, the slot total
+  int32_t n_tiles;        // schedule: this CTA's (real) tiles
   int32_t flag[2][2][4];  // [warpgroup][stage][quarter] rescale votes
   uint8_t valid[kStages][kTileK];
   float mref[64];         // per-head reference maxima (log2 units)
@@ -249,34 +250,37 @@ struct Cursor {
   int32_t ntiles;   // its tile count T_row
   int32_t ta, tb;   // this CTA's tiles of the row: [ta, tb)
   int32_t t;        // current tile of the row
-  int64_t P;        // the row's first tile in the tile space
+  int64_t P;        // the slot of the row's first tile (after its start slots)
   int64_t beg;      // offset of the row's slice in indices[]
-  int64_t e;        // end of this CTA's range
+  int64_t e;        // end of this CTA's slot range
   bool live;
 
   __device__ __forceinline__ void load_row(const DecodeArgs& a) {
     len = row_len(a, row);
     ntiles = tiles_of_len(len);
     beg = __ldg(a.indptr + row);
-    tb = int32_t((e - P) < int64_t(ntiles) ? (e - P) : int64_t(ntiles));
+    const int64_t n = e - P;
+    tb = int32_t(n < 0 ? 0 : (n < int64_t(ntiles) ? n : int64_t(ntiles)));
+    if (tb <= 0) live = false;  // the range ends before this row's first tile
   }
+  // r0: the row whose slots hold b; P0: its first slot.
   __device__ __forceinline__ void init(const DecodeArgs& a, int32_t r0, int64_t P0, int64_t b, int64_t e_) {
     row = r0;
-    P = P0;
+    P = P0 + kRowStartSlots;
     e = e_;
     live = b < e_ && r0 < a.n_q;
     ta = tb = t = 0;
     if (!live) return;
     load_row(a);
-    ta = int32_t(b - P);
+    ta = int32_t(b > P ? b - P : 0);
     t = ta;
   }
   __device__ __forceinline__ void advance(const DecodeArgs& a) {
     if (!live) return;
     if (++t < tb) return;
-    P += ntiles;
+    P += ntiles + kRowStartSlots;
     ++row;
-    if (P >= e || row >= a.n_q) {
+    if (P - kRowStartSlots >= e || row >= a.n_q) {
       live = false;
       return;
     }
@@ -363,6 +367,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
     ms->is_last = 0;
     ms->first_row = a.n_q;
     ms->first_tile = 0;
+    ms->n_tiles = 0;
     fence_mbar_init();
   }
   if (warp == kQkWarpA) {
@@ -377,7 +382,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
     const int per = (n + kThreadsTC - 1) / kThreadsTC;
     const int lo = min(tid * per, n), hi = min(lo + per, n);
     int64_t local = 0;
-    for (int r = lo; r < hi; ++r) local += tiles_of_len(row_len(a, r));
+    for (int r = lo; r < hi; ++r) local += kRowStartSlots + tiles_of_len(row_len(a, r));
     // exclusive scan of the 512 partial sums: within each warp, then over the
     // 16 warp totals
     int64_t x = local;
@@ -401,18 +406,26 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
     }
     __syncthreads();
     const int64_t Tt = ms->total_tiles;
-    const int64_t b = cta_begin(c_id, Tt, G);
-    int64_t P = scan[32 + warp] + x - local;  // tiles before this thread's rows
+    const int64_t b = cta_begin(c_id, Tt, G), e = cta_begin(c_id + 1, Tt, G);
+    int64_t P = scan[32 + warp] + x - local;  // slots before this thread's rows
+    int32_t mine = 0;                         // tiles of these rows in [b, e)
     for (int r = lo; r < hi; ++r) {
       const int32_t nt_r = tiles_of_len(row_len(a, r));
-      if (P <= b && b < P + nt_r) {
+      const int64_t w = kRowStartSlots + nt_r;
+      if (P <= b && b < P + w) {
         ms->first_row = r;
         ms->first_tile = P;
       }
+      const int64_t t0 = P + kRowStartSlots;
+      const int64_t lo_t = b > t0 ? b : t0, hi_t = e < t0 + nt_r ? e : t0 + nt_r;
+      if (hi_t > lo_t) mine += int32_t(hi_t - lo_t);
       if (c_id == 0 && a.row_tile) a.row_tile[r] = P;  // for the merge kernel
-      P += nt_r;
+      P += w;
     }
     if (c_id == 0 && tid == 0 && a.row_tile) a.row_tile[n] = Tt;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+    if (lane == 0 && mine != 0) atomicAdd(&ms->n_tiles, mine);
   }
   tc_fence_before();
   __syncthreads();
@@ -420,7 +433,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
   SMLA_TR(1, 0);  // schedule known
   const int64_t T = ms->total_tiles;
   const int64_t cb = cta_begin(c_id, T, G), ce = cta_begin(c_id + 1, T, G);
-  const int32_t n_tiles = int32_t(ce - cb);  // this CTA's tiles
+  const int32_t n_tiles = ms->n_tiles;  // this CTA's tiles
   const int32_t row0 = ms->first_row;
   const int64_t P0 = ms->first_tile;
   const uint32_t tmem = ms->tmem_base;
@@ -1154,7 +1167,8 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_rows_kernel(DecodeArgs
   const int H = a.heads;
   if (pair >= int64_t(a.n_q) * H) return;
   const int row = int(pair / H), h = int(pair % H);
-  const int64_t P = __ldcg(a.row_tile + row), T = __ldcg(a.row_tile + a.n_q), G = a.grid;
+  const int64_t P = __ldcg(a.row_tile + row) + kRowStartSlots;  // the row's first tile slot
+  const int64_t T = __ldcg(a.row_tile + a.n_q), G = a.grid;
   const int32_t nt = int32_t(__ldcg(a.row_tile + row + 1) - P);
   const int64_t ca = cta_of_tile(P, T, G), cb = cta_of_tile(P + nt - 1, T, G);
   if (ca == cb) return;  // finished whole by one CTA

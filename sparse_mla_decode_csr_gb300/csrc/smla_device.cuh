@@ -157,6 +157,10 @@ namespace smla {
 // ---- the tensor-core kernel's balanced schedule (see smla_plan in smla.h) ----
 
 constexpr int kSchedTile = 64;
+// Schedule slots charged for starting a row (its epilogue and q staging cost
+// about two tiles of pipeline time): row r occupies kRowStartSlots virtual
+// slots and then its T_r tiles in the slot space the CTAs split evenly.
+constexpr int kRowStartSlots = 2;
 
 // Slice length of row r: max(indptr[r+1] - indptr[r], 0), capped by lens.
 __device__ __forceinline__ int32_t row_len(const DecodeArgs& a, int32_t r) {

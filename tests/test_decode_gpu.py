@@ -220,23 +220,24 @@ def test_split_partials_match_oracle_cuda_core():
             _check_part(o[sl], ml[sl], nv[sl], _oracle_part(c, r, lo, max(lo, hi)), f"row {r} chunk {ch}")
 
 
-def tc_schedule(lens, G):
+def tc_schedule(lens, G, start_slots=2):
     """The tensor-core kernel's row parts, restated from smla.h: rows cut into
-    64-key tiles, concatenated; CTA c takes tiles [c T / G, (c+1) T / G); a part
-    of a shared row lands in slot 2 c + (P_r < b_c ? 0 : 1).  Returns
-    {row: [(cta, slot, first position, end position), ...]}."""
+    64-key tiles; row r takes start_slots schedule slots and then its tiles, in
+    row order; CTA c takes slots [c W / G, (c+1) W / G); a part of a shared row
+    lands in slot 2 c + (R_r < b_c ? 0 : 1), R_r the slot of the row's first
+    tile.  Returns {row: [(cta, slot, first position, end position), ...]}."""
     tiles = [max(1, -(-L // 64)) for L in lens]
-    starts = np.concatenate([[0], np.cumsum(tiles)]).astype(np.int64)
-    T = int(starts[-1])
-    b = [c * T // G for c in range(G + 1)]
+    starts = np.concatenate([[0], np.cumsum([start_slots + n for n in tiles])]).astype(np.int64)
+    W = int(starts[-1])
+    b = [c * W // G for c in range(G + 1)]
     parts = {}
     for r, L in enumerate(lens):
-        P, nt = int(starts[r]), tiles[r]
+        R, nt = int(starts[r]) + start_slots, tiles[r]
         for c in range(G):
-            lo_t, hi_t = max(b[c], P), min(b[c + 1], P + nt)
+            lo_t, hi_t = max(b[c], R), min(b[c + 1], R + nt)
             if lo_t < hi_t:
-                slot = 2 * c + (0 if P < b[c] else 1)
-                parts.setdefault(r, []).append((c, slot, (lo_t - P) * 64, min((hi_t - P) * 64, L)))
+                slot = 2 * c + (0 if R < b[c] else 1)
+                parts.setdefault(r, []).append((c, slot, (lo_t - R) * 64, min((hi_t - R) * 64, L)))
     return parts
 
 
