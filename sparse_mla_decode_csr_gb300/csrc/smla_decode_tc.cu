@@ -298,17 +298,6 @@ struct Cursor {
   }
 };
 
-// CTAs (with non-empty ranges) holding tiles of the row whose tiles are
-// [P, P + nt): their count, and the range [c_a, c_b] to scan.
-__device__ __forceinline__ int32_t row_parts(int64_t P, int32_t nt, int64_t T, int64_t G, int64_t* ca,
-                                             int64_t* cb) {
-  *ca = cta_of_tile(P, T, G);
-  *cb = cta_of_tile(P + nt - 1, T, G);
-  int32_t n = 0;
-  for (int64_t c = *ca; c <= *cb; ++c) n += cta_begin(c + 1, T, G) > cta_begin(c, T, G);
-  return n;
-}
-
 template <int HP>
 __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) {
   using Lay = TcLayout<HP>;
@@ -382,6 +371,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
     const int per = (n + kThreadsTC - 1) / kThreadsTC;
     const int lo = min(tid * per, n), hi = min(lo + per, n);
     int64_t local = 0;
+#pragma unroll 1  // rolled (run once; small code)
     for (int r = lo; r < hi; ++r) local += kRowStartSlots + tiles_of_len(row_len(a, r));
     // exclusive scan of the 512 partial sums: within each warp, then over the
     // 16 warp totals
@@ -409,6 +399,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
     const int64_t b = cta_begin(c_id, Tt, G), e = cta_begin(c_id + 1, Tt, G);
     int64_t P = scan[32 + warp] + x - local;  // slots before this thread's rows
     int32_t mine = 0;                         // tiles of these rows in [b, e)
+#pragma unroll 1
     for (int r = lo; r < hi; ++r) {
       const int32_t nt_r = tiles_of_len(row_len(a, r));
       const int64_t w = kRowStartSlots + nt_r;
@@ -710,13 +701,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
 #pragma unroll 1
         for (int mt = wg; mt < 4; mt += Lay::SWG) {
           const int dg = latent_dim_of(mt * 128 + qd * 32 + lane);
+          constexpr int kOc = HP / 8 < 2 ? HP / 8 : 2;  // 8-column chunks per TMEM wait
 #pragma unroll 1
-          for (int cc = 0; cc < HP / 8; ++cc) {
-            uint32_t v[8];
-            tmem_ld8(tmem + (uint32_t(32 * qd) << 16) + Lay::o_col(ob, mt) + uint32_t(8 * cc), v);
+          for (int cc = 0; cc < HP / 8; cc += kOc) {
+            uint32_t v[8 * kOc];
+#pragma unroll
+            for (int u = 0; u < kOc; ++u)
+              tmem_ld8(tmem + (uint32_t(32 * qd) << 16) + Lay::o_col(ob, mt) + uint32_t(8 * (cc + u)),
+                       *reinterpret_cast<uint32_t(*)[8]>(&v[8 * u]));
             tmem_wait_ld();
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
+            for (int k = 0; k < 8 * kOc; ++k) {
               const int h = 8 * cc + k;
               if (h >= H) break;
               const float o = __uint_as_float(v[k]);
@@ -754,12 +749,21 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
         tc_fence_after();
         const uint32_t tile = tiles_u32 + s * kTileBytes;
         const uint32_t d = tmem + Lay::s_col(s, half);
-#pragma unroll
+        // K step k reads bytes [32 (k % 4), +32) of every 128-byte row of
+        // 64-dim chunk k / 4: the descriptors' start addresses (16-byte units)
+        // step by 2, and to the next chunk after every fourth step.  Rolled:
+        // the issue rate bounds this loop, and small code keeps the
+        // instruction caches free for the other roles.
+        const uint64_t a0 = smem_desc(tile, 16, 1024, kSw128), b0 = smem_desc(q_u32, 16, 1024, kSw128);
+        uint32_t alo = uint32_t(a0) + uint32_t((k0 >> 2) * (kChunkBytes >> 4) + (k0 & 3) * 2);
+        uint32_t blo = uint32_t(b0) + uint32_t((k0 >> 2) * (HP * 128 >> 4) + (k0 & 3) * 2);
+        const uint32_t ahi = uint32_t(a0 >> 32), bhi = uint32_t(b0 >> 32);
+#pragma unroll 1
         for (int k = k0; k < k1; ++k) {
-          const int ch = k >> 2, kk = k & 3;
-          const uint64_t ad = smem_desc(tile + ch * kChunkBytes + kk * 32, 16, 1024, kSw128);
-          const uint64_t bd = smem_desc(q_u32 + ch * (HP * 128) + kk * 32, 16, 1024, kSw128);
-          mma_f16_ss(d, ad, bd, Lay::idesc_qk, k > k0 ? 1u : 0u);
+          mma_f16_ss_w(d, alo, ahi, blo, bhi, Lay::idesc_qk, k > k0 ? 1u : 0u);
+          const bool next_chunk = (k & 3) == 3;
+          alo += next_chunk ? uint32_t((kChunkBytes >> 4) - 6) : 2u;
+          blo += next_chunk ? uint32_t((HP * 128 >> 4) - 6) : 2u;
         }
         mma_commit(s_full + s);
         SMLA_TR(22, i);
@@ -789,15 +793,23 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
         tc_fence_after();
         const uint32_t tile = tiles_u32 + s * kTileBytes;
         const uint32_t pst = p_u32 + (Lay::p_stages == 2 ? s : 0) * Lay::p_bytes;
-        // k-major order: consecutive MMAs go to different O tiles
-#pragma unroll
+        // k-major order: consecutive MMAs go to different O tiles.  O tile mt
+        // reads 64-dim chunks 2 mt and 2 mt + 1; K step k (16 keys) starts
+        // 2048 bytes into them and 16 P^T rows down (k rolled, as in the QK
+        // issue).
+        const uint64_t a0 = smem_desc(tile, kChunkBytes, 1024, kSw128);
+        const uint64_t b0 = smem_desc(pst, 8 * Lay::p_row, 8 * Lay::p_row, Lay::p_swz);
+        uint32_t alo = uint32_t(a0), blo = uint32_t(b0);
+        const uint32_t ahi = uint32_t(a0 >> 32), bhi = uint32_t(b0 >> 32);
+#pragma unroll 1
         for (int k = 0; k < kTileK / 16; ++k) {
+          const uint32_t acc = (first && k == 0) ? 0u : 1u;
 #pragma unroll
-          for (int mt = 0; mt < 4; ++mt) {
-            const uint64_t ad = smem_desc(tile + (2 * mt) * kChunkBytes + k * 2048, kChunkBytes, 1024, kSw128);
-            const uint64_t bd = smem_desc(pst + k * 16 * Lay::p_row, 8 * Lay::p_row, 8 * Lay::p_row, Lay::p_swz);
-            mma_f16_ss(tmem + Lay::o_col(ob, mt), ad, bd, Lay::idesc_pv, (first && k == 0) ? 0u : 1u);
-          }
+          for (int mt = 0; mt < 4; ++mt)
+            mma_f16_ss_w(tmem + Lay::o_col(ob, mt), alo + uint32_t(mt * (2 * kChunkBytes >> 4)), ahi, blo, bhi,
+                         Lay::idesc_pv, acc);
+          alo += 2048 >> 4;
+          blo += 16 * Lay::p_row >> 4;
         }
         mma_commit(kv_empty + s);
         mma_commit(pv_done + s);
