@@ -166,7 +166,8 @@ class Problem:
         self.sink = W.sinks(w, dev)
         self.out = torch.empty(w.n_q, w.heads, 512, dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty(w.n_q, w.heads, dtype=torch.float32, device=dev)
-        self.plan = smla.smla_plan(w.n_q, w.heads, w.max_row_len, self.indices.numel(), 0)
+        self.plan = smla.smla_plan(w.n_q, w.heads, w.max_row_len, self.indices.numel(), 0,
+                                   has_invalid=w.has_invalid)
         # a workspace of this problem's own (zeroed): its ticket counters stay valid
         nbytes = int(self.plan.workspace_bytes)
         self.ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev) if nbytes else None
@@ -208,6 +209,19 @@ def l2_flusher(dev):
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     buf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
     return lambda: buf.fill_(1)
+
+
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal
+
+
+def scale_histogram(kv: torch.Tensor) -> dict:
+    """log2 of the records' block scales (bytes [512, 528) as f32): how many
+    blocks have each power of two."""
+    sc = kv[:, 512:528].contiguous().view(torch.float32).flatten()
+    e = torch.log2(sc).round().to(torch.int64)
+    lo = int(e.min().item())
+    counts = torch.bincount(e - lo)
+    return {str(lo + i): int(c) for i, c in enumerate(counts.tolist()) if c}
 
 
 def time_device(prob: Problem, steps: int, warmup: int, flush, dist_ok: bool):
@@ -372,6 +386,9 @@ def main():
     total_ms = reduce_max(sum(times), dev)
     e2e_ms, h2d, d2h = time_e2e(prob, args.steps, flush)
     e2e_ms = reduce_max(e2e_ms, dev)
+    # the same steps without the L2 flush (records gathered by several rows,
+    # and with caches under the L2's size the whole cache, stay in L2)
+    warm_ms = statistics.mean(time_device(prob, max(10, args.steps // 2), args.warmup, lambda: None, False))
 
     extra = {}
     for name in [x for x in args.also.split(",") if x and x != args.workload]:
@@ -384,6 +401,8 @@ def main():
         extra[wx.name] = {"rows_per_s": wx.n_q / (mean_ms * 1e-3), "ms_per_step": mean_ms,
                           "gathered_kv_gbs": gbs, "hbm_frac": gbs / peak,
                           "num_splits": px.plan.num_splits, "grid": px.plan.grid}
+        if wx.latent != "normal":
+            extra[wx.name]["log2_scale_histogram"] = scale_histogram(px.kv)
         del px
         torch.cuda.empty_cache()
 
@@ -413,11 +432,15 @@ def main():
                      "frac": achieved / peak, "traffic": ncu_traffic(w.name),
                      "peak_source": peak_src,
                      "kernel": (f"one smla_decode call ({args.kernel} decode kernel"
-                                + (" + merge kernel" if prob.plan.merge_kernel else "") + "), CUDA events"),
-                     "algorithmic_bytes_per_launch": bytes_step},
+                                + (" + merge kernel" if prob.plan.merge_kernel else "")
+                                + (" + row-trim pass" if prob.plan.trim_kernel else "") + "), CUDA events"),
+                     "algorithmic_bytes_per_launch": bytes_step,
+                     "frac_of_nominal": achieved / NOMINAL_HBM_GBS, "nominal_gbs": NOMINAL_HBM_GBS},
+        "warm_l2": {"ms_per_step": warm_ms, "gathered_kv_gbs": bytes_step / (warm_ms * 1e-3) / 1e9,
+                    "note": "no L2 flush between steps; not an HBM figure"},
         "e2e": {"value": weak_scaling_rows_per_s(world, w.n_q, steps, e2e_ms), "unit": "rows/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": steps * (2 if prob.plan.merge_kernel else 1),
+        "gpu_launches": steps * (1 + int(prob.plan.merge_kernel) + int(prob.plan.trim_kernel)),
         "clocks": clk.summary(),
         "cpu_baseline": cpu,
         "also": extra,

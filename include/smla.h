@@ -112,8 +112,10 @@ typedef struct smla_decode_params {
   /* Planning hints; results never depend on them.  max_row_len: an upper
    * bound of the rows' slice lengths known on the host (e.g. top-k); <= 0 means
    * unknown (n_indices / n_q is used).  has_invalid: rows may end in -1
-   * padding ([P1] "Tiles", has_invalid); masked entries are skipped either
-   * way, so this only informs the plan. */
+   * padding ([P1] "Tiles", has_invalid).  Masked entries contribute nothing
+   * either way; with has_invalid the tensor-core plan first trims each row to
+   * its last entry >= 0 (a pass with a warp per row, plan.trim_kernel = 1) so
+   * that the decode skips tiles of padding. */
   int32_t max_row_len;
   int32_t has_invalid;
   float sm_scale;
@@ -157,9 +159,14 @@ typedef struct smla_decode_params {
  * positions [c chunk_len, (c + 1) chunk_len), the last chunk everything after;
  * partial slot r * num_splits + c; the last chunk to finish merges.
  *
+ * Tensor-core kernel with has_invalid: a pass before the decode (warp per
+ * row, 512 slice positions per step from the end) writes each row's length
+ * trimmed to its last entry >= 0 into the workspace, and the decode schedules
+ * those lengths (trim_kernel = 1).
+ *
  * Fields: kernel (SMLA_KERNEL_*), grid (CTAs of the decode launch), tile_len
  * (keys per tile), num_splits and chunk_len (CUDA-core kernel only),
- * partial_slots, merge_kernel, workspace_bytes.  num_sms > 0 makes the plan
+ * partial_slots, merge_kernel, trim_kernel, workspace_bytes.  num_sms > 0 makes the plan
  * pure host arithmetic (no CUDA call); num_sms = 0 asks the current device. */
 typedef struct smla_plan_info {
   int32_t kernel;
@@ -169,7 +176,7 @@ typedef struct smla_plan_info {
   int32_t chunk_len;
   int32_t partial_slots;
   int32_t merge_kernel;
-  int32_t pad;
+  int32_t trim_kernel;
   int64_t workspace_bytes;
 } smla_plan_info;
 
@@ -186,6 +193,7 @@ int smla_plan(const smla_decode_params* params, int32_t num_sms, smla_plan_info*
  *                                maximum (its max, or at most 24 below it), l = sum_t 2^(x_t - m);
  *                                m = -inf, l = 0 for a part without keys
  *   nv_part int32 [S]            contributing keys of the part
+ *   lens    int32 [n_q]          trimmed row lengths (only when plan.trim_kernel)
  * The ticket counters must be zero when a call starts (e.g. allocate the
  * workspace zeroed); every completed call returns them to zero.  A call with
  * other sizes may have written partials over that region, so re-zero bytes
@@ -194,8 +202,9 @@ int smla_plan(const smla_decode_params* params, int32_t num_sms, smla_plan_info*
  * (same stream); a call that reports SMLA_STATUS_TIMEOUT leaves it undefined. */
 size_t smla_decode_workspace_size(const smla_decode_params* params);
 
-/* Sparse MLA decode (the definition above): one kernel launch (two when the
- * plan has merge_kernel = 1).  Each CTA gathers its tiles' records,
+/* Sparse MLA decode (the definition above): one decode launch, preceded by
+ * the row-trim pass when plan.trim_kernel = 1 and followed by the merge kernel
+ * when plan.merge_kernel = 1.  Each CTA gathers its tiles' records,
  * dequantises them to bf16 (exact), runs QK over 576 dims and PV over 512 dims
  * on the tcgen05 tensor cores with an online softmax in between, and writes
  * out / lse of its whole rows and partials of shared rows (see smla_plan).

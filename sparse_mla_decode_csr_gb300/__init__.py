@@ -75,7 +75,7 @@ class PlanInfo(ctypes.Structure):
         ("chunk_len", ctypes.c_int32),
         ("partial_slots", ctypes.c_int32),
         ("merge_kernel", ctypes.c_int32),
-        ("pad", ctypes.c_int32),
+        ("trim_kernel", ctypes.c_int32),
         ("workspace_bytes", ctypes.c_int64),
     ]
 
@@ -128,18 +128,19 @@ def _stream(stream) -> Optional[int]:
 
 
 def _plan_params(n_q, num_heads, max_row_len=0, n_indices=0, num_splits=0,
-                 kernel=KERNEL_TENSOR_CORE) -> DecodeParams:
+                 kernel=KERNEL_TENSOR_CORE, has_invalid=False) -> DecodeParams:
     p = DecodeParams()
     p.n_q, p.num_heads, p.max_row_len, p.n_indices = int(n_q), int(num_heads), int(max_row_len), int(n_indices)
-    p.num_splits, p.kernel = int(num_splits), int(kernel)
+    p.num_splits, p.kernel, p.has_invalid = int(num_splits), int(kernel), int(bool(has_invalid))
     return p
 
 
 def smla_plan(n_q: int, num_heads: int, max_row_len: int = 0, n_indices: int = 0,
-              num_splits: int = 0, num_sms: int = 0, kernel: int = KERNEL_TENSOR_CORE) -> PlanInfo:
+              num_splits: int = 0, num_sms: int = 0, kernel: int = KERNEL_TENSOR_CORE,
+              has_invalid: bool = False) -> PlanInfo:
     """The launch plan of a decode call (pure host arithmetic when num_sms > 0)."""
     info = PlanInfo()
-    p = _plan_params(n_q, num_heads, max_row_len, n_indices, num_splits, kernel)
+    p = _plan_params(n_q, num_heads, max_row_len, n_indices, num_splits, kernel, has_invalid)
     rc = lib.smla_plan(ctypes.byref(p), int(num_sms), ctypes.byref(info))
     if rc != 0:
         raise SmlaError(rc, "smla_plan")
@@ -148,8 +149,8 @@ def smla_plan(n_q: int, num_heads: int, max_row_len: int = 0, n_indices: int = 0
 
 def smla_decode_workspace_size(n_q: int, num_heads: int, max_row_len: int = 0,
                                n_indices: int = 0, num_splits: int = 0,
-                               kernel: int = KERNEL_TENSOR_CORE) -> int:
-    p = _plan_params(n_q, num_heads, max_row_len, n_indices, num_splits, kernel)
+                               kernel: int = KERNEL_TENSOR_CORE, has_invalid: bool = False) -> int:
+    p = _plan_params(n_q, num_heads, max_row_len, n_indices, num_splits, kernel, has_invalid)
     return int(lib.smla_decode_workspace_size(ctypes.byref(p)))
 
 
@@ -220,7 +221,7 @@ def smla_decode(q: torch.Tensor, kv_cache: torch.Tensor, n_kv_rows: int, indices
         if rc != 0:
             raise SmlaError(rc, "smla_plan")
         ws = workspace(int(plan.workspace_bytes), q.device,
-                       (n_q, heads, plan.kernel, plan.grid, plan.num_splits, plan.chunk_len))
+                       (n_q, heads, plan.kernel, plan.grid, plan.num_splits, plan.chunk_len, plan.trim_kernel))
     rc = lib.smla_decode(ctypes.byref(p), _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream))
     if rc != 0:
         raise SmlaError(rc, "smla_decode")

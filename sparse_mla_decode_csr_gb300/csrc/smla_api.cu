@@ -44,9 +44,10 @@ double split_cost(int64_t n_q, int heads, int64_t tiles, int s, int num_sms) {
 
 }  // namespace
 
-WorkspaceLayout workspace_layout(int32_t n_q, int32_t heads, int32_t slots) {
+WorkspaceLayout workspace_layout(int32_t n_q, int32_t heads, int32_t slots, bool trim_lens) {
   WorkspaceLayout w{};
-  if (slots <= 0) return w;
+  w.lens_off = -1;
+  if (slots <= 0 && !trim_lens) return w;
   int64_t off = 0;
   w.ticket_off = off;
   off = align256(off + int64_t(n_q) * 4);
@@ -58,6 +59,10 @@ WorkspaceLayout workspace_layout(int32_t n_q, int32_t heads, int32_t slots) {
   off = align256(off + int64_t(slots) * heads * 2 * 4);
   w.nv_off = off;
   off = align256(off + int64_t(slots) * 4);
+  if (trim_lens) {  // trimmed row lengths (has_invalid pre-pass), after everything else
+    w.lens_off = off;
+    off = align256(off + int64_t(n_q) * 4);
+  }
   w.total = off;
   return w;
 }
@@ -120,7 +125,10 @@ int smla_plan(const smla_decode_params* p, int32_t num_sms, smla_plan_info* plan
     plan->partial_slots = 2 * plan->grid;
     // rows shared between CTAs are merged by a second, parallel kernel
     plan->merge_kernel = (n_q > 0 && plan->grid > 1) ? 1 : 0;
-    plan->workspace_bytes = n_q > 0 ? workspace_layout(n_q, num_heads, plan->partial_slots).total : 0;
+    // rows that may end in -1 padding are trimmed first by a row-per-warp pass
+    plan->trim_kernel = (n_q > 0 && p->has_invalid) ? 1 : 0;
+    plan->workspace_bytes =
+        n_q > 0 ? workspace_layout(n_q, num_heads, plan->partial_slots, plan->trim_kernel != 0).total : 0;
     return SMLA_OK;
   }
   int s = 1;
@@ -143,7 +151,8 @@ int smla_plan(const smla_decode_params* p, int32_t num_sms, smla_plan_info* plan
   plan->grid = int32_t(int64_t(n_q) * s);
   plan->partial_slots = s > 1 ? n_q * s : 0;
   plan->merge_kernel = 0;
-  plan->workspace_bytes = workspace_layout(n_q, num_heads, plan->partial_slots).total;
+  plan->trim_kernel = 0;
+  plan->workspace_bytes = workspace_layout(n_q, num_heads, plan->partial_slots, false).total;
   return SMLA_OK;
 }
 
@@ -190,7 +199,7 @@ int smla_decode(const smla_decode_params* params, void* workspace, size_t worksp
   L.p = *params;
   rc = smla_plan(params, 0, &L.plan);
   if (rc != SMLA_OK) return rc;
-  L.ws = workspace_layout(params->n_q, params->num_heads, L.plan.partial_slots);
+  L.ws = workspace_layout(params->n_q, params->num_heads, L.plan.partial_slots, L.plan.trim_kernel != 0);
   if (L.ws.total > 0 && (workspace == nullptr || int64_t(workspace_bytes) < L.ws.total))
     return SMLA_ERR_WORKSPACE;
   if (L.ws.total > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return SMLA_ERR_ALIGN;

@@ -19,10 +19,10 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 // Workspace offsets of one plan (see smla_decode_workspace_size in smla.h).
 struct WorkspaceLayout {
-  int64_t ticket_off, rowtile_off, o_off, ml_off, nv_off, total;
+  int64_t ticket_off, rowtile_off, o_off, ml_off, nv_off, lens_off, total;
 };
 
-WorkspaceLayout workspace_layout(int32_t n_q, int32_t heads, int32_t slots);
+WorkspaceLayout workspace_layout(int32_t n_q, int32_t heads, int32_t slots, bool trim_lens);
 
 // Everything a decode kernel needs, resolved on the host.
 struct DecodeLaunch {

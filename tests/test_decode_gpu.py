@@ -321,3 +321,30 @@ def test_single_key_rows_return_every_e4m3_code_exactly(heads, kernel):
     assert st == 0 and (nv.cpu().numpy() == 1).all()
     assert np.array_equal(got, np.broadcast_to(want[:, None, :], got.shape)), \
         f"max |diff| {np.abs(got - want[:, None, :]).max()}"
+
+
+@pytest.mark.parametrize("splits", [0, 3])
+def test_has_invalid_trims_padding_without_changing_results(splits):
+    """Rows of a fixed stride whose tails are -1 padding: with has_invalid the
+    tensor-core plan trims each row to its last entry >= 0 before the decode.
+    Rows: a valid prefix, all padding, a prefix whose last entry >= 0 is out of
+    range (kept by the trim, masked and flagged by the decode), a single key at
+    position 0, no padding at all (several trim steps of 512 positions), and a
+    prefix longer than the caller's lens cap."""
+    stride, keep = 1300, [700, 0, 5, 1, 1300, 640]
+    c = small_case(len(keep), 16, 1500, [stride] * len(keep), seed=77, invalid=0.1, sink=True)
+    ind = c["indices"].view(len(keep), stride).clone()
+    for r, k in enumerate(keep):
+        ind[r, k:] = -1
+    ind[2, 4] = 1500 + 5
+    ind[3, 0] = 17
+    c["indices"] = ind.flatten().contiguous()
+    lens = torch.tensor([stride] * 5 + [300], dtype=torch.int32)
+    plan = smla.smla_plan(len(keep), 16, stride, c["indices"].numel(), splits, has_invalid=True)
+    assert plan.trim_kernel == 1
+    out_t, lse_t, st_t = run_small(c, lens=lens, has_invalid=True, num_splits=splits, max_row_len=stride,
+                                   what="trimmed")
+    out_f, lse_f, st_f = run_small(c, lens=lens, has_invalid=False, num_splits=splits, max_row_len=stride,
+                                   what="untrimmed")
+    assert st_t & smla.STATUS_INDEX_OOB and st_f & smla.STATUS_INDEX_OOB
+    assert torch.isinf(lse_t[1]).all() and torch.count_nonzero(out_t[1].float()) == 0

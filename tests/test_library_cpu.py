@@ -123,3 +123,13 @@ def test_pack_rejects_bad_arguments_on_host():
     assert f(0x1004, 512, 0x1000, 64, 4, 0x2000, None) == -4
     assert f(0x1000, 512, 0x1000, 64, -1, 0x2000, None) == -2
     assert f(0x1000, 512, 0x1000, 64, 0, 0x2000, None) == 0
+
+
+def test_plan_trims_rows_only_for_the_tensor_core_kernel_with_has_invalid():
+    base = smla.smla_plan(256, 16, 2048, 256 * 2048, 0, 152)
+    trim = smla.smla_plan(256, 16, 2048, 256 * 2048, 0, 152, has_invalid=True)
+    cc = smla.smla_plan(256, 16, 2048, 256 * 2048, 0, 152, kernel=smla.KERNEL_CUDA_CORE, has_invalid=True)
+    assert base.trim_kernel == 0 and trim.trim_kernel == 1 and cc.trim_kernel == 0
+    # the trimmed lengths take one more int32 per row at the end of the workspace
+    assert trim.workspace_bytes >= base.workspace_bytes + 4 * 256
+    assert trim.grid == base.grid and trim.partial_slots == base.partial_slots
