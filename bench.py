@@ -224,6 +224,37 @@ def scale_histogram(kv: torch.Tensor) -> dict:
     return {str(lo + i): int(c) for i, c in enumerate(counts.tolist()) if c}
 
 
+def time_writer(dev, n: int = 1 << 20, reps: int = 10) -> dict:
+    """The record writer (smla_pack_records) on n records of bf16 latent and
+    rope already in HBM: 1152 B read and 656 B written per record, L2 flushed
+    before each call."""
+    import sparse_mla_decode_csr_gb300 as smla
+
+    g = torch.Generator(device=dev)
+    g.manual_seed(0x5EED)
+    lat = torch.randn(n, 512, generator=g, device=dev).to(torch.bfloat16)
+    rope = torch.randn(n, 64, generator=g, device=dev).to(torch.bfloat16)
+    kv = torch.empty(n, 656, dtype=torch.uint8, device=dev)
+    flush = l2_flusher(dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        smla.smla_pack_records(lat, rope, kv, stream)
+    ms = []
+    for _ in range(reps):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        smla.smla_pack_records(lat, rope, kv, stream)
+        b.record(stream)
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    t = statistics.mean(ms)
+    gbs = n * (1152 + 656) / (t * 1e-3) / 1e9
+    peak, _ = measured_peaks()
+    return {"records": n, "ms_per_call": t, "gbs": gbs, "hbm_frac": gbs / peak,
+            "bytes_per_record": 1152 + 656}
+
+
 def time_device(prob: Problem, steps: int, warmup: int, flush, dist_ok: bool):
     stream = torch.cuda.current_stream(prob.dev)
     for _ in range(warmup):
@@ -391,6 +422,7 @@ def main():
     warm_ms = statistics.mean(time_device(prob, max(10, args.steps // 2), args.warmup, lambda: None, False))
 
     extra = {}
+    writer = time_writer(dev) if rank == 0 else None
     for name in [x for x in args.also.split(",") if x and x != args.workload]:
         wx = W.WORKLOADS[name]
         px = Problem(wx, dev, args.kernel)
@@ -444,6 +476,7 @@ def main():
         "clocks": clk.summary(),
         "cpu_baseline": cpu,
         "also": extra,
+        "writer": writer,
     }
     print(json.dumps(line), flush=True)
     if dist_ok:

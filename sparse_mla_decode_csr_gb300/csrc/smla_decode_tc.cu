@@ -1275,40 +1275,51 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_rows_kernel(DecodeArgs
   dst[1] = hi;
 }
 
-// Row trimming ([P1] "Tiles", has_invalid: rows may end in -1 padding): warp
-// per row finds the last slice position holding an entry >= 0 (scanning from
-// the end, 512 positions per step, all loads in flight) and writes that
-// position + 1 as the row's length for the decode launch.  Every position cut
-// off is masked, so the results are unchanged; the decode only skips tiles
-// that hold no key.
+// Row trimming ([P1] "Tiles", has_invalid: rows may end in -1 padding): a CTA
+// of kTrimWarps warps per row finds the last slice position holding an entry
+// >= 0 and writes that position + 1 as the row's length for the decode
+// launch.  The slice is cut into chunks of 512 positions; warp w takes chunks
+// last - w, last - w - kTrimWarps, ... (16 loads per lane in flight per chunk)
+// and stops at its first chunk with such an entry; the row's answer is the
+// largest over the warps.  Every position cut off is masked, so the results
+// are unchanged; the decode only skips tiles that hold no key.
 constexpr int kTrimWarps = 4;
 constexpr int kTrimUnroll = 16;
+constexpr int kTrimChunk = 32 * kTrimUnroll;
 
 __global__ void __launch_bounds__(32 * kTrimWarps) trim_rows_kernel(DecodeArgs a, int32_t* lens_out) {
-  const int lane = threadIdx.x & 31;
-  const int row = int(blockIdx.x) * kTrimWarps + int(threadIdx.x >> 5);
-  if (row >= a.n_q) return;
+  __shared__ int32_t best_w[kTrimWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int row = int(blockIdx.x);
   const int32_t len = row_len(a, row);
   const int64_t beg = __ldg(a.indptr + row);
-  int32_t keep = 0;
+  const int32_t n_chunks = (len + kTrimChunk - 1) / kTrimChunk;
+  int32_t found = 0;
 #pragma unroll 1
-  for (int32_t hi = len; hi > 0; hi -= 32 * kTrimUnroll) {
+  for (int32_t ch = n_chunks - 1 - warp; ch >= 0; ch -= kTrimWarps) {
     int32_t best = 0;
 #pragma unroll
     for (int u = 0; u < kTrimUnroll; ++u) {
-      const int32_t pos = hi - 1 - lane - 32 * u;
+      const int32_t pos = ch * kTrimChunk + 32 * u + lane;
       const int64_t off = beg + pos;
-      const int32_t v = (pos >= 0 && off >= 0 && off < a.n_indices) ? __ldg(a.indices + off) : -1;
-      if (v >= 0 && pos + 1 > best) best = pos + 1;
+      const int32_t v = (pos < len && off >= 0 && off < a.n_indices) ? __ldg(a.indices + off) : -1;
+      if (v >= 0) best = pos + 1;  // positions grow with u
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) best = max(best, __shfl_xor_sync(0xffffffffu, best, o));
     if (best > 0) {
-      keep = best;
+      found = best;
       break;
     }
   }
-  if (lane == 0) lens_out[row] = keep;
+  if (lane == 0) best_w[warp] = found;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int32_t keep = 0;
+#pragma unroll
+    for (int w = 0; w < kTrimWarps; ++w) keep = max(keep, best_w[w]);
+    lens_out[row] = keep;
+  }
 }
 
 template <int HP>
@@ -1319,8 +1330,7 @@ cudaError_t launch_tc_hp(const DecodeLaunch& L) {
   DecodeArgs args = make_decode_args(L);
   if (L.plan.trim_kernel && L.ws.lens_off >= 0) {
     int32_t* lens_trim = reinterpret_cast<int32_t*>(static_cast<char*>(L.workspace) + L.ws.lens_off);
-    trim_rows_kernel<<<unsigned((L.p.n_q + kTrimWarps - 1) / kTrimWarps), 32 * kTrimWarps, 0, L.stream>>>(args,
-                                                                                                    lens_trim);
+    trim_rows_kernel<<<unsigned(L.p.n_q), 32 * kTrimWarps, 0, L.stream>>>(args, lens_trim);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     args.lens = lens_trim;  // the caller's lens already capped these
