@@ -1165,18 +1165,27 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
   }
 }
 
-// Merge kernel: warp (row, head) merges the head's partials of a row that was
-// shared between CTAs of the decode launch ([P2] stage_combine: max of the
-// parts' maxima, rescaled sums, sink in the denominator); rows finished whole
-// there are skipped.  The decode launch's CTA 0 left every row's first tile
-// and the tile total in the workspace.  Lane L owns latent dims
-// [16 L, 16 L + 16); four parts' loads are in flight at a time.
+// Merge kernel: merges each head's partials of a row that was shared between
+// CTAs of the decode launch ([P2] stage_combine: max of the parts' maxima,
+// rescaled sums, sink in the denominator); rows finished whole there are
+// skipped.  The decode launch's CTA 0 left every row's first slot and the
+// slot total in the workspace.  kSplit = 1: a warp per (row, head), four per
+// CTA.  kSplit = 4 (rows shared by many CTAs): a CTA per (row, head) whose
+// warp w takes parts ca + w, ca + w + 4, ..., the warps' sums meeting in
+// shared memory.  Lane L owns latent dims [16 L, 16 L + 16); four parts'
+// loads are in flight per warp.
 constexpr int kMergeWarps = 4;
+constexpr int kMergeBatch = 4;
 
+template <int kSplit>
 __global__ void __launch_bounds__(32 * kMergeWarps) merge_rows_kernel(DecodeArgs a) {
+  __shared__ float red_m[kSplit], red_l[kSplit];
+  __shared__ int32_t red_nv[kSplit];
+  __shared__ float red_acc[kSplit][16][33];  // [warp][value][lane], padded
   const int lane = threadIdx.x & 31;
-  const int64_t pair = int64_t(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
+  const int w = kSplit == 1 ? 0 : int(threadIdx.x >> 5);  // this warp's place among the pair's warps
   const int H = a.heads;
+  const int64_t pair = kSplit == 1 ? int64_t(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5) : int64_t(blockIdx.x);
   if (pair >= int64_t(a.n_q) * H) return;
   const int row = int(pair / H), h = int(pair % H);
   const int64_t P = __ldcg(a.row_tile + row) + kRowStartSlots;  // the row's first tile slot
@@ -1184,7 +1193,6 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_rows_kernel(DecodeArgs
   const int32_t nt = int32_t(__ldcg(a.row_tile + row + 1) - P);
   const int64_t ca = cta_of_tile(P, T, G), cb = cta_of_tile(P + nt - 1, T, G);
   if (ca == cb) return;  // finished whole by one CTA
-  // Lane j holds part ca + j + 32 k of round k: its slot and (m, l), read once.
   auto part_of = [&](int64_t c, int64_t* sl, float* m, float* l) {
     *sl = -1;
     *m = -INFINITY;
@@ -1195,43 +1203,57 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_rows_kernel(DecodeArgs
     *m = ml.x;
     *l = ml.y;
   };
-  // pass 1: the largest part maximum (the first round's parts stay in registers)
+  // this warp's parts: c = ca + w + kSplit i; lane j holds part i = 32 k + j
+  // of round k (its slot and (m, l), read once for the first round)
+  const int64_t first = ca + w;
+  const int64_t n_mine = first <= cb ? (cb - first) / kSplit + 1 : 0;
   int64_t sl0;
   float m0, l0;
-  part_of(ca + lane, &sl0, &m0, &l0);
+  part_of(first + int64_t(kSplit) * lane, &sl0, &m0, &l0);
+  // pass 1: the largest part maximum
   float mloc = l0 > 0.f ? m0 : -INFINITY;
-  for (int64_t c = ca + 32 + lane; c <= cb; c += 32) {
+#pragma unroll 1
+  for (int64_t i = 32 + lane; i < n_mine; i += 32) {
     int64_t sl;
     float m, l;
-    part_of(c, &sl, &m, &l);
+    part_of(first + kSplit * i, &sl, &m, &l);
     if (l > 0.f) mloc = fmaxf(mloc, m);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
-  const float mstar = mloc;
-  // pass 2: weights, their sum and the merged numerator (32 parts per round)
+  float mstar = mloc;
+  if (kSplit > 1) {
+    if (lane == 0) red_m[w] = mloc;
+    __syncthreads();
+    mstar = red_m[0];
+#pragma unroll
+    for (int k = 1; k < kSplit; ++k) mstar = fmaxf(mstar, red_m[k]);
+  }
+  // pass 2: weights, their sum and this warp's share of the merged numerator
   float acc[16];
 #pragma unroll
   for (int q = 0; q < 16; ++q) acc[q] = 0.f;
   float lsum = 0.f;
   int nvsum = 0;
-  for (int64_t c0 = ca; c0 <= cb; c0 += 32) {
+#pragma unroll 1
+  for (int64_t i0 = 0; i0 < n_mine; i0 += 32) {
     int64_t sl = sl0;
     float m = m0, l = l0;
-    if (c0 != ca) part_of(c0 + lane, &sl, &m, &l);
-    float w = 0.f;
+    if (i0 != 0) part_of(first + kSplit * (i0 + lane), &sl, &m, &l);
+    float wt = 0.f;
     if (l > 0.f) {
-      w = exp2f(m - mstar);
-      lsum += l * w;
+      wt = exp2f(m - mstar);
+      lsum += l * wt;
     }
     if (h == 0 && sl >= 0) nvsum += __ldcg(a.nv_part + sl);
-    const int n = int(cb - c0 + 1 < 32 ? cb - c0 + 1 : 32);
-    for (int j = 0; j < n; j += 4) {  // four parts' loads in flight at once
-      float wj[4];
-      float4 v[4][4];
+    const int n = int(n_mine - i0 < 32 ? n_mine - i0 : 32);
+#pragma unroll 1
+    for (int j = 0; j < n; j += kMergeBatch) {  // kMergeBatch parts' loads in flight at once
+      float wj[kMergeBatch];
+      float4 v[kMergeBatch][4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        wj[u] = __shfl_sync(0xffffffffu, w, (j + u) & 31);
+      for (int u = 0; u < kMergeBatch; ++u) {
+        wj[u] = __shfl_sync(0xffffffffu, wt, (j + u) & 31);
         const int64_t slj = __shfl_sync(0xffffffffu, sl, (j + u) & 31);
         if (j + u >= n) wj[u] = 0.f;
         const float4* src = reinterpret_cast<const float4*>(a.o_part + (slj * H + h) * kLatent + 16 * lane);
@@ -1239,7 +1261,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_rows_kernel(DecodeArgs
         for (int q = 0; q < 4; ++q) v[u][q] = wj[u] != 0.f ? __ldcg(src + q) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kMergeBatch; ++u) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           acc[4 * q] = fmaf(wj[u], v[u][q].x, acc[4 * q]);
@@ -1254,6 +1276,23 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_rows_kernel(DecodeArgs
   for (int o = 16; o > 0; o >>= 1) {
     lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
     nvsum += __shfl_xor_sync(0xffffffffu, nvsum, o);
+  }
+  if (kSplit > 1) {
+    if (lane == 0) {
+      red_l[w] = lsum;
+      red_nv[w] = nvsum;
+    }
+#pragma unroll
+    for (int q = 0; q < 16; ++q) red_acc[w][q][lane] = acc[q];
+    __syncthreads();
+    if (w != 0) return;
+#pragma unroll
+    for (int k = 1; k < kSplit; ++k) {
+      lsum += red_l[k];
+      nvsum += red_nv[k];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) acc[q] += red_acc[k][q][lane];
+    }
   }
   float fac = 0.f, lse = 0.f;
   finish_head(mstar, lsum, a.sink, h, &fac, &lse);
@@ -1339,7 +1378,12 @@ cudaError_t launch_tc_hp(const DecodeLaunch& L) {
   e = cudaGetLastError();
   if (e != cudaSuccess || !L.plan.merge_kernel) return e;
   const int64_t pairs = int64_t(L.p.n_q) * L.p.num_heads;
-  merge_rows_kernel<<<unsigned((pairs + kMergeWarps - 1) / kMergeWarps), 32 * kMergeWarps, 0, L.stream>>>(args);
+  // rows shared by many CTAs (few rows over the grid) split each head's parts
+  // over a CTA's four warps
+  if (int64_t(L.plan.grid) > 8 * int64_t(L.p.n_q))
+    merge_rows_kernel<kMergeWarps><<<unsigned(pairs), 32 * kMergeWarps, 0, L.stream>>>(args);
+  else
+    merge_rows_kernel<1><<<unsigned((pairs + kMergeWarps - 1) / kMergeWarps), 32 * kMergeWarps, 0, L.stream>>>(args);
   return cudaGetLastError();
 }
 
