@@ -12,10 +12,11 @@
 //   warps 0-3 (and 4-7 at 64 heads)  softmax: warpgroup g owns head columns
 //               [g*HH, (g+1)*HH) (HH = all heads up to 32, 32 at 64 heads); they
 //               also stage q, move the reference maxima (rescaling O in TMEM),
-//               and run each row part's epilogue and merge
+//               and run each row part's epilogue (partials of shared rows)
 //   warps 12-14 MMA issuers, one thread each on three different SM
 //               sub-partitions (a single thread issues a tcgen05.mma only every
-//               ~55 cycles): 12 and 13 issue the two halves of QK's K = 576
+//               ~50 cycles; QK on one thread instead of two makes a decode step
+//               ~10% slower): 12 and 13 issue the two halves of QK's K = 576
 //               into two S accumulators, 14 issues PV; warp 12 owns TMEM
 //   warps 4-11 (8-11 at 64 heads)  latent converters: gather the 512 E4M3
 //               bytes and the four scales of each tile's records (64-bit
