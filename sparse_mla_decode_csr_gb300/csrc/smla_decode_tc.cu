@@ -475,9 +475,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
       const uint32_t ph = (i >> 1) & 1;
       const bool first = c.first(), last = c.last();
       const int ob = Lay::n_ob == 2 ? (seg & 1) : 0;
-      if (first) stage_q(c.row);  // every QK that read the previous q has completed
+      if (i == 0) stage_q(c.row);  // later rows' q is staged once the previous part's P is out
       if (last && i + 1 < n_tiles) {
-        // the next row's q is staged at its first tile: bring it into L2 now
+        // the next row's q is staged after this tile's P: bring it into L2 now
         const char* qn = reinterpret_cast<const char*>(a.q + int64_t(c.row + 1) * a.q_stride_row);
         for (int k = tid; k < H * (kQK * 2 / 128); k += kSoftmaxThreads) {
           const int h = k / (kQK * 2 / 128), line = k % (kQK * 2 / 128);
@@ -635,6 +635,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full + s);
       SMLA_TR(12, i);
+      // The next row's q, before this part's epilogue, so that its QKs can
+      // start meanwhile: every QK that read this row's q completed before S
+      // was read above.
+      if (last && i + 1 < n_tiles) stage_q(c.row + 1);
 
       if (last) {
         // ---------- epilogue of this row part ----------
