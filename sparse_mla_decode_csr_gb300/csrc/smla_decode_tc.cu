@@ -1175,15 +1175,18 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
 // rescaled sums, sink in the denominator); rows finished whole there are
 // skipped.  The decode launch's CTA 0 left every row's first slot and the
 // slot total in the workspace.  kSplit = 1: a warp per (row, head), four per
-// CTA.  kSplit = 4 (rows shared by many CTAs): a CTA per (row, head) whose
-// warp w takes parts ca + w, ca + w + 4, ..., the warps' sums meeting in
-// shared memory.  Lane L owns latent dims [16 L, 16 L + 16); four parts'
-// loads are in flight per warp.
-constexpr int kMergeWarps = 4;
+// CTA.  kSplit = 8 (rows shared by many CTAs): a CTA of eight warps per
+// (row, head), warp w taking parts ca + w, ca + w + 8, ..., the warps'
+// results meeting in shared memory.  One pass: a part's slot comes from the
+// schedule, so its (m, l) and its O rows (lane L: latent dims [16 L, 16 L +
+// 16)) are loaded together, four parts at a time, and the warp keeps a running
+// maximum, rescaling its sums when it moves.
+constexpr int kMergeWarps = 4;   // warps per CTA with kSplit = 1
+constexpr int kMergeSplit = 8;   // warps per (row, head) for rows with many parts
 constexpr int kMergeBatch = 4;
 
 template <int kSplit>
-__global__ void __launch_bounds__(32 * kMergeWarps) merge_rows_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(32 * (kSplit == 1 ? kMergeWarps : kSplit)) merge_rows_kernel(DecodeArgs a) {
   __shared__ float red_m[kSplit], red_l[kSplit];
   __shared__ int32_t red_nv[kSplit];
   __shared__ float red_acc[kSplit][16][33];  // [warp][value][lane], padded
@@ -1198,92 +1201,68 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_rows_kernel(DecodeArgs
   const int32_t nt = int32_t(__ldcg(a.row_tile + row + 1) - P);
   const int64_t ca = cta_of_tile(P, T, G), cb = cta_of_tile(P + nt - 1, T, G);
   if (ca == cb) return;  // finished whole by one CTA
-  auto part_of = [&](int64_t c, int64_t* sl, float* m, float* l) {
-    *sl = -1;
-    *m = -INFINITY;
-    *l = 0.f;
-    if (c > cb || cta_begin(c + 1, T, G) == cta_begin(c, T, G)) return;  // past the end / CTA without tiles
-    *sl = part_slot(c, P, T, G);
-    const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.ml_part + (*sl * H + h) * 2));
-    *m = ml.x;
-    *l = ml.y;
-  };
-  // this warp's parts: c = ca + w + kSplit i; lane j holds part i = 32 k + j
-  // of round k (its slot and (m, l), read once for the first round)
+  // this warp's parts: c = ca + w + kSplit i
   const int64_t first = ca + w;
   const int64_t n_mine = first <= cb ? (cb - first) / kSplit + 1 : 0;
-  int64_t sl0;
-  float m0, l0;
-  part_of(first + int64_t(kSplit) * lane, &sl0, &m0, &l0);
-  // pass 1: the largest part maximum
-  float mloc = l0 > 0.f ? m0 : -INFINITY;
-#pragma unroll 1
-  for (int64_t i = 32 + lane; i < n_mine; i += 32) {
-    int64_t sl;
-    float m, l;
-    part_of(first + kSplit * i, &sl, &m, &l);
-    if (l > 0.f) mloc = fmaxf(mloc, m);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
-  float mstar = mloc;
-  if (kSplit > 1) {
-    if (lane == 0) red_m[w] = mloc;
-    __syncthreads();
-    mstar = red_m[0];
-#pragma unroll
-    for (int k = 1; k < kSplit; ++k) mstar = fmaxf(mstar, red_m[k]);
-  }
-  // pass 2: weights, their sum and this warp's share of the merged numerator
+  float mrun = -INFINITY, lsum = 0.f;  // running maximum and the sum against it
+  int nvsum = 0;
   float acc[16];
 #pragma unroll
   for (int q = 0; q < 16; ++q) acc[q] = 0.f;
-  float lsum = 0.f;
-  int nvsum = 0;
 #pragma unroll 1
   for (int64_t i0 = 0; i0 < n_mine; i0 += 32) {
-    int64_t sl = sl0;
-    float m = m0, l = l0;
-    if (i0 != 0) part_of(first + kSplit * (i0 + lane), &sl, &m, &l);
-    float wt = 0.f;
-    if (l > 0.f) {
-      wt = exp2f(m - mstar);
-      lsum += l * wt;
+    // lane j: part i0 + j's slot (from the schedule) and its (m, l)
+    const int64_t c = first + kSplit * (i0 + lane);
+    int64_t sl = -1;
+    float2 ml = make_float2(-INFINITY, 0.f);
+    if (c <= cb && cta_begin(c + 1, T, G) > cta_begin(c, T, G)) {  // a CTA with tiles
+      sl = part_slot(c, P, T, G);
+      ml = __ldcg(reinterpret_cast<const float2*>(a.ml_part + (sl * H + h) * 2));
     }
     if (h == 0 && sl >= 0) nvsum += __ldcg(a.nv_part + sl);
     const int n = int(n_mine - i0 < 32 ? n_mine - i0 : 32);
 #pragma unroll 1
-    for (int j = 0; j < n; j += kMergeBatch) {  // kMergeBatch parts' loads in flight at once
-      float wj[kMergeBatch];
+    for (int j = 0; j < n; j += kMergeBatch) {
       float4 v[kMergeBatch][4];
+      int64_t slj[kMergeBatch];
 #pragma unroll
-      for (int u = 0; u < kMergeBatch; ++u) {
-        wj[u] = __shfl_sync(0xffffffffu, wt, (j + u) & 31);
-        const int64_t slj = __shfl_sync(0xffffffffu, sl, (j + u) & 31);
-        if (j + u >= n) wj[u] = 0.f;
-        const float4* src = reinterpret_cast<const float4*>(a.o_part + (slj * H + h) * kLatent + 16 * lane);
+      for (int u = 0; u < kMergeBatch; ++u) {  // O rows first: their addresses need only the slot
+        slj[u] = __shfl_sync(0xffffffffu, sl, (j + u) & 31);
+        if (j + u >= n) slj[u] = -1;
+        const float4* src = reinterpret_cast<const float4*>(a.o_part + (slj[u] * H + h) * kLatent + 16 * lane);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) v[u][q] = wj[u] != 0.f ? __ldcg(src + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q = 0; q < 4; ++q) v[u][q] = slj[u] >= 0 ? __ldcg(src + q) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int u = 0; u < kMergeBatch; ++u) {
+        const float m = __shfl_sync(0xffffffffu, ml.x, (j + u) & 31);
+        const float l = __shfl_sync(0xffffffffu, ml.y, (j + u) & 31);
+        if (slj[u] < 0 || !(l > 0.f)) continue;  // uniform over the warp
+        if (m > mrun) {  // the running maximum moves: rescale what was summed
+          const float f = exp2f(mrun - m);
+          lsum *= f;
+#pragma unroll
+          for (int q = 0; q < 16; ++q) acc[q] *= f;
+          mrun = m;
+        }
+        const float wt = exp2f(m - mrun);
+        lsum = fmaf(l, wt, lsum);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          acc[4 * q] = fmaf(wj[u], v[u][q].x, acc[4 * q]);
-          acc[4 * q + 1] = fmaf(wj[u], v[u][q].y, acc[4 * q + 1]);
-          acc[4 * q + 2] = fmaf(wj[u], v[u][q].z, acc[4 * q + 2]);
-          acc[4 * q + 3] = fmaf(wj[u], v[u][q].w, acc[4 * q + 3]);
+          acc[4 * q] = fmaf(wt, v[u][q].x, acc[4 * q]);
+          acc[4 * q + 1] = fmaf(wt, v[u][q].y, acc[4 * q + 1]);
+          acc[4 * q + 2] = fmaf(wt, v[u][q].z, acc[4 * q + 2]);
+          acc[4 * q + 3] = fmaf(wt, v[u][q].w, acc[4 * q + 3]);
         }
       }
     }
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
-    nvsum += __shfl_xor_sync(0xffffffffu, nvsum, o);
-  }
+  for (int o = 16; o > 0; o >>= 1) nvsum += __shfl_xor_sync(0xffffffffu, nvsum, o);
+  float mstar = mrun;
   if (kSplit > 1) {
     if (lane == 0) {
+      red_m[w] = mrun;
       red_l[w] = lsum;
       red_nv[w] = nvsum;
     }
@@ -1291,12 +1270,20 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_rows_kernel(DecodeArgs
     for (int q = 0; q < 16; ++q) red_acc[w][q][lane] = acc[q];
     __syncthreads();
     if (w != 0) return;
+    mstar = red_m[0];
 #pragma unroll
-    for (int k = 1; k < kSplit; ++k) {
-      lsum += red_l[k];
+    for (int k = 1; k < kSplit; ++k) mstar = fmaxf(mstar, red_m[k]);
+    lsum = 0.f;
+    nvsum = 0;
+#pragma unroll
+    for (int q = 0; q < 16; ++q) acc[q] = 0.f;
+#pragma unroll 1
+    for (int k = 0; k < kSplit; ++k) {
+      const float f = red_l[k] > 0.f ? exp2f(red_m[k] - mstar) : 0.f;
+      lsum = fmaf(red_l[k], f, lsum);
       nvsum += red_nv[k];
 #pragma unroll
-      for (int q = 0; q < 16; ++q) acc[q] += red_acc[k][q][lane];
+      for (int q = 0; q < 16; ++q) acc[q] = fmaf(f, red_acc[k][q][lane], acc[q]);
     }
   }
   float fac = 0.f, lse = 0.f;
@@ -1384,9 +1371,9 @@ cudaError_t launch_tc_hp(const DecodeLaunch& L) {
   if (e != cudaSuccess || !L.plan.merge_kernel) return e;
   const int64_t pairs = int64_t(L.p.n_q) * L.p.num_heads;
   // rows shared by many CTAs (few rows over the grid) split each head's parts
-  // over a CTA's four warps
+  // over a CTA's eight warps
   if (int64_t(L.plan.grid) > 8 * int64_t(L.p.n_q))
-    merge_rows_kernel<kMergeWarps><<<unsigned(pairs), 32 * kMergeWarps, 0, L.stream>>>(args);
+    merge_rows_kernel<kMergeSplit><<<unsigned(pairs), 32 * kMergeSplit, 0, L.stream>>>(args);
   else
     merge_rows_kernel<1><<<unsigned((pairs + kMergeWarps - 1) / kMergeWarps), 32 * kMergeWarps, 0, L.stream>>>(args);
   return cudaGetLastError();
