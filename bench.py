@@ -466,7 +466,8 @@ def main():
         cpu = cpu_baseline(w, args.cpu_seconds)
     line = {
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": steps,
-        "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": mean_ms, "ms_per_step_median": statistics.median(times),
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "n_q": w.n_q, "heads": w.heads, "topk": w.topk,
                    "n_kv_rows": w.n_kv_rows, "rows_per_gpu": w.n_q, "l2": "flushed between steps",
