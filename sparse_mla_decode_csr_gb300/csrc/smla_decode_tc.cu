@@ -1179,14 +1179,16 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
 // (row, head), warp w taking parts ca + w, ca + w + 8, ..., the warps'
 // results meeting in shared memory.  One pass: a part's slot comes from the
 // schedule, so its (m, l) and its O rows (lane L: latent dims [16 L, 16 L +
-// 16)) are loaded together, four parts at a time, and the warp keeps a running
-// maximum, rescaling its sums when it moves.
+// 16)) are loaded together, two parts at a time with kSplit = 1 (fewer
+// registers, more CTAs per SM: rows of a few parts are latency bound) and four
+// with kSplit = 8, and the warp keeps a running maximum, rescaling its sums
+// when it moves.
 constexpr int kMergeWarps = 4;   // warps per CTA with kSplit = 1
 constexpr int kMergeSplit = 8;   // warps per (row, head) for rows with many parts
-constexpr int kMergeBatch = 4;
 
 template <int kSplit>
 __global__ void __launch_bounds__(32 * (kSplit == 1 ? kMergeWarps : kSplit)) merge_rows_kernel(DecodeArgs a) {
+  constexpr int kMergeBatch = kSplit == 1 ? 2 : 4;  // parts' loads in flight per warp
   __shared__ float red_m[kSplit], red_l[kSplit];
   __shared__ int32_t red_nv[kSplit];
   __shared__ float red_acc[kSplit][16][33];  // [warp][value][lane], padded
