@@ -18,6 +18,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -69,11 +70,19 @@ def measured_peaks():
 
 
 def source_digest() -> str:
+    """Digest of the kernel sources' code: comments and runs of white space
+    are left out, so that a recorded ncu traffic figure stays tied to the code
+    it was measured on, not to its comments."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sparse_mla_decode_csr_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        if not name.endswith((".cu", ".cuh", ".h")):
+            continue
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(name.encode() + re.sub(r"\s+", " ", text).strip().encode())
     return h.hexdigest()[:16]
 
 

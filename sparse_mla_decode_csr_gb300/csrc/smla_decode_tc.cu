@@ -2,11 +2,13 @@
 // persistent and balanced.
 //
 // Schedule (documented with smla_plan in smla.h): every row is cut into 64-key
-// tiles, the rows' tiles are concatenated into one tile space, and CTA c of the
-// grid streams through the tiles [floor(c T / G), floor((c+1) T / G)) across
-// row boundaries.  A row wholly inside one CTA's range is finished there; a
-// shared row gets one (O, m, l) partial per CTA and is merged by the merge
-// kernel below.
+// tiles and takes two slots for the cost of starting it followed by its tiles;
+// the rows' slots form one space of W slots, and CTA c of the grid takes the
+// slots [floor(c W / G), floor((c+1) W / G)), streaming through the tiles in
+// its range across row boundaries.  A row wholly inside one CTA's range is
+// finished there; a shared row gets one (O, m, l) partial per CTA and is
+// merged by the merge kernel below.  With has_invalid, trim_rows_kernel first
+// cuts each row at its last entry >= 0.
 //
 // Warp roles (16 warps):
 //   warps 0-3 (and 4-7 at 64 heads)  softmax: warpgroup g owns head columns
@@ -24,8 +26,8 @@
 //               write the 64 x 512 bf16 latent of the key tile in the
 //               128-byte-swizzled K-major layout.  Up to 32 heads the latent
 //               bytes travel by cp.async into a per-warp shared-memory ring
-//               about a tile and a half ahead of the conversion; at 64 heads
-//               (no shared memory left) into registers one batch ahead
+//               about a tile ahead of the conversion; at 64 heads (no
+//               shared memory left) into registers one batch ahead
 //   warp 15     rope copier: the records' 128-byte bf16 rope goes straight into
 //               the key tile by cp.async (completion tracked by the tile's
 //               mbarrier), zeros for masked keys; it also writes the keys'
