@@ -119,7 +119,6 @@ struct Misc {
   int64_t first_tile;     // schedule: that row's first slot
   int64_t total_tiles;    // schedule: W, the slot total
   int32_t n_tiles;        // schedule: this CTA's (real) tiles
-  int32_t flag[2][2][4];  // [warpgroup][stage][quarter] rescale votes
   uint8_t valid[kStages][kTileK];
   float mref[64];         // per-head reference maxima (log2 units)
   float alpha[2][32];
@@ -523,10 +522,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
         x[h] = valid ? x[h] * a.sm_scale_log2 : -INFINITY;
         need |= x[h] > mr[h] + kRescaleMargin;
       }
-      need = __any_sync(0xffffffffu, need);
-      if (lane == 0) ms->flag[wg][s][qd] = need;
-      named_barrier(1 + wg, 128);
-      need = ms->flag[wg][s][0] | ms->flag[wg][s][1] | ms->flag[wg][s][2] | ms->flag[wg][s][3];
+      need = named_barrier_or(1 + wg, 128, need);  // any thread of the warpgroup
       SMLA_TR(15, i);
       if (need) {
         // exact tile max of this warpgroup's heads (a butterfly reduce-scatter:
