@@ -209,8 +209,13 @@ size_t smla_decode_workspace_size(const smla_decode_params* params);
  * on the tcgen05 tensor cores with an online softmax in between, and writes
  * out / lse of its whole rows and partials of shared rows (see smla_plan).
  * `workspace` may be NULL only when smla_decode_workspace_size() returns 0.
- * Accuracy: q, k and v enter the products exactly; p is rounded to bf16, sums
- * are f32, out is rounded to bf16 (round to nearest even). */
+ * Accuracy: q, k and v enter the products exactly when every block scale is a
+ * positive normal power of two up to 2^7 (all scales smla_pack_records
+ * writes); a block with any other f32 scale (zero, negative, not a power of
+ * two, above 2^7) has each latent value e4m3 * scale formed in f32 and
+ * rounded once to bf16 (exact where that product is a bf16), on a slower
+ * path.  p is rounded to bf16, sums are f32, out is rounded to bf16 (round to
+ * nearest even). */
 int smla_decode(const smla_decode_params* params, void* workspace, size_t workspace_bytes,
                 void* stream);
 

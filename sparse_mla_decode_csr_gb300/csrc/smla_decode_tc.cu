@@ -207,10 +207,10 @@ __device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity, Mi
 // float-format conversions, which run at a fraction of the ALU rate).  A byte
 // s.eeee.mmm put into bf16 bits as s | eeee.mmm << 4 is the bf16 of value
 // e4m3 * 2^-120 (E4M3 subnormals land on bf16 subnormals).  One exact multiply
-// by scale * 2^120 finishes it when that is a bf16, i.e. scale <= 2^7 (the
-// record writer's scales for |latent| <= 57344); otherwise two, by 2^120 and
-// then by the scale.  Codes 0x7F / 0xFF (E4M3 NaN, never written by the
-// writer) decode as finite values.
+// by scale * 2^120 finishes it when the scale is a normal power of two up to
+// 2^7 (the record writer's scales for |latent| <= 57344: plain_scale);
+// other scales go through dequant16_any.  Codes 0x7F / 0xFF (E4M3 NaN, never
+// written by the writer) decode as finite values.
 //
 // Each 32-bit word [b0 b1 b2 b3] yields the pairs (b0, b2) and (b1, b3): five
 // integer operations per four values.  So the lane's dims come out in the
@@ -229,6 +229,32 @@ __device__ __forceinline__ void dequant16(uint4 v, uint32_t m1, uint32_t (&o)[8]
     const uint32_t d = ((w[j] >> 4) & 0x07F007F0u) | (w[j] & 0x80008000u);         // b1, b3
     o[2 * j] = bf16x2_mul(e, m1);
     o[2 * j + 1] = bf16x2_mul(d, m1);
+  }
+}
+
+// A scale word that dequant16 turns into an exact one-multiply factor: a
+// positive normal power of two no larger than 2^7.
+__device__ __forceinline__ bool plain_scale(uint32_t scw) {
+  return (scw & 0x807FFFFFu) == 0u && scw - 0x00800000u <= 0x43000000u - 0x00800000u;
+}
+
+// The general path, for any f32 scale (zero, above 2^7, not a power of two,
+// negative): each value e4m3 * scale is formed in f32 and rounded to bf16, so
+// it is exact whenever that product is a bf16 (zero and power-of-two scales in
+// range) and otherwise within one bf16 rounding (plus an f32 one).  The bytes
+// go to f32 by the same bit placement as in dequant16 (value e4m3 * 2^-120,
+// subnormals included), and the output pairs are ordered as there.
+__device__ __forceinline__ float e4m3_scaled(uint32_t b, float sc) {  // b: the code in bits 0-7
+  return __uint_as_float(((b & 0x7Fu) << 20) | ((b & 0x80u) << 24)) * 0x1p120f * sc;
+}
+
+__device__ __forceinline__ void dequant16_any(uint4 v, uint32_t scw, uint32_t (&o)[8]) {
+  const float sc = __uint_as_float(scw);
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    o[2 * j] = pack_bf16x2(e4m3_scaled(w[j], sc), e4m3_scaled(w[j] >> 16, sc));           // b0, b2
+    o[2 * j + 1] = pack_bf16x2(e4m3_scaled(w[j] >> 8, sc), e4m3_scaled(w[j] >> 24, sc));  // b1, b3
   }
 }
 
@@ -921,7 +947,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
       auto key_id = [&](int32_t raw) -> int32_t { return (raw < 0 || raw >= a.n_kv_rows) ? -1 : raw; };
       auto load_scales = [&](int32_t keys) -> uint32_t {
         const int32_t id = __shfl_sync(0xffffffffu, keys, lane >> 2);
-        return id >= 0 ? ldg_u32_now(kv_sc + int64_t(id) * kRecordBytes) : 0u;
+        return id >= 0 ? ldg_u32_now(kv_sc + int64_t(id) * kRecordBytes) : 0x3F800000u;  // masked: scale 1
       };
       Cursor cr;  // tile of the newest raw entries
       cr.init(a, row0, P0, cb, ce);
@@ -944,7 +970,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
       static_assert(kPerConv % G == 0, "groups within a tile");
       static_assert(RG >= 3, "at least two groups in flight");
       int t = 0;       // tile being converted (keys k0)
-      bool fast = false;  // this tile takes the fast path
+      bool fast = false;   // this tile takes the fast path
+      bool plain = false;  // every scale of this tile is plain (masked records count as plain);
+                           // otherwise the tile is converted again at its end
       // the warp's rows cw + kConvWarps kk all have r % 8 == cw % 8 (kConvWarps is 8)
       static_assert(kConvWarps == 8, "row swizzle constant per warp");
       const uint32_t x_row = uint32_t(cw & 7) << 4;
@@ -986,9 +1014,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
         }
         const int s = t & 1;
         if (k == 0) {
-          // per tile: every key valid and every scale <= 2^7 -> the fast path
-          const bool ok = (lane >= kPerConv || k0 >= 0) && sc_cur <= 0x43000000u;
-          fast = __all_sync(0xffffffffu, ok);
+          // per tile: every scale plain, and every key valid too -> the fast path
+          const bool pl = plain_scale(sc_cur);
+          plain = __all_sync(0xffffffffu, pl);
+          fast = __all_sync(0xffffffffu, pl && (lane >= kPerConv || k0 >= 0));
         }
         cp_async_wait_group<RG - 2>();  // this lane's 16 bytes of records j .. j+G-1 have landed
         uint8_t* tile_base = tiles + s * kTileBytes + c_off + uint32_t(cw) * 128u;  // row r = cw + kConvWarps kk
@@ -1017,14 +1046,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
             if (id >= 0) {  // uniform over the warp
               const uint4 v = ld_shared_v4(ring_lane + uint32_t((gslot * G + g) * kLatent));
               const uint32_t scw = __shfl_sync(0xffffffffu, sc_cur, 4 * (k + g) + (lane >> 3));
-              const uint32_t sb2 = __byte_perm(scw, 0u, 0x3232);
-              const bool big = scw > 0x43000000u;  // scale above 2^7 (or not positive)
-              dequant16(v, big ? 0x7B807B80u /* 2^120 */ : sb2 + 0x3C003C00u /* scale 2^120 */, o);
-              if (__any_sync(0xffffffffu, big)) {
-                const uint32_t m2 = big ? sb2 : 0x3F803F80u;
-#pragma unroll
-                for (int q = 0; q < 8; ++q) o[q] = bf16x2_mul(o[q], m2);
-              }
+              dequant16(v, __byte_perm(scw, 0u, 0x3232) + 0x3C003C00u /* scale 2^120, twice */, o);
             }
             uint8_t* rb = tile_base + uint32_t(kConvWarps * (k + g)) * 128u;
             *reinterpret_cast<uint4*>(rb + (slot_lo ^ x_row)) = make_uint4(o[0], o[1], o[2], o[3]);
@@ -1034,6 +1056,22 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
         issue(j + (RG - 1) * G);  // into the group slot read one step ago
         gslot = gslot + 1 == RG ? 0 : gslot + 1;
         if (k + G == kPerConv) {
+          if (!plain) {
+            // a scale that is not plain (never written by the record writer):
+            // the tile's valid records again, from global memory, by the
+            // general path, over the rows stored above (same lanes, same bytes)
+#pragma unroll 1
+            for (int kk = 0; kk < kPerConv; ++kk) {
+              const int32_t id = __shfl_sync(0xffffffffu, k0, kk);
+              if (id < 0) continue;  // uniform over the warp
+              uint32_t o[8];
+              dequant16_any(ldg_v4_now(kv_lat + int64_t(id) * kRecordBytes),
+                            __shfl_sync(0xffffffffu, sc_cur, 4 * kk + (lane >> 3)), o);
+              uint8_t* rb = tile_base + uint32_t(kConvWarps * kk) * 128u;
+              *reinterpret_cast<uint4*>(rb + (slot_lo ^ x_row)) = make_uint4(o[0], o[1], o[2], o[3]);
+              *reinterpret_cast<uint4*>(rb + (slot_hi ^ x_row)) = make_uint4(o[4], o[5], o[6], o[7]);
+            }
+          }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(kv_full + s);
@@ -1073,28 +1111,39 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
     auto load_scales = [&](Batch& B, int32_t keys, int sub) {
       B.keys = keys;
       const int32_t id = __shfl_sync(0xffffffffu, keys, (sub * kBatch + (lane >> 2)) & 31);
-      B.sc = 0u;
+      B.sc = 0x3F800000u;  // a masked record (zero latent) takes scale 1: the plain path
       if (id >= 0) B.sc = ldg_u32_now(kv_sc + int64_t(id) * kRecordBytes);
     };
     // Record k of a batch: dequantise and store row r = cw + kConvWarps kk of
-    // the tile (16-byte slots swizzled with r % 8).
-    auto convert_rec = [&](const Batch& B, int k, uint8_t* tile, int sub) {
-      const int kk = sub * kBatch + k;
-      const int r = cw + kConvWarps * kk;
-      const uint32_t scw = __shfl_sync(0xffffffffu, B.sc, 4 * k + (lane >> 3));  // scale of lane's block
-      const uint32_t sb2 = __byte_perm(scw, 0u, 0x3232);  // the scale's bf16 bits, twice
-      const bool big = scw > 0x43000000u;                 // scale above 2^7 (or not positive)
-      uint32_t o[8];
-      dequant16(B.lat[k], big ? 0x7B807B80u /* 2^120 */ : sb2 + 0x3C003C00u /* scale 2^120 */, o);
-      if (__any_sync(0xffffffffu, big)) {
-        const uint32_t m2 = big ? sb2 : 0x3F803F80u;  // then times the scale (1 where done)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) o[j] = bf16x2_mul(o[j], m2);
-      }
+    // the tile (16-byte slots swizzled with r % 8).  The one-multiply path,
+    // exact for plain scales; a batch holding any other scale is redone by
+    // convert_general after it.
+    auto store_rec = [&](uint8_t* tile, int k, int sub, const uint32_t (&o)[8]) {
+      const int r = cw + kConvWarps * (sub * kBatch + k);
       uint8_t* rb = tile + c_off + uint32_t(r) * 128u;
       const uint32_t x = uint32_t(r & 7) << 4;
       *reinterpret_cast<uint4*>(rb + (slot_lo ^ x)) = make_uint4(o[0], o[1], o[2], o[3]);
       *reinterpret_cast<uint4*>(rb + (slot_hi ^ x)) = make_uint4(o[4], o[5], o[6], o[7]);
+    };
+    auto convert_rec = [&](const Batch& B, int k, uint8_t* tile, int sub) {
+      const uint32_t scw = __shfl_sync(0xffffffffu, B.sc, 4 * k + (lane >> 3));  // scale of lane's block
+      uint32_t o[8];
+      dequant16(B.lat[k], __byte_perm(scw, 0u, 0x3232) + 0x3C003C00u /* scale 2^120, twice */, o);
+      store_rec(tile, k, sub, o);
+    };
+    // A batch with a scale that is not plain (never written by the record
+    // writer): every valid record again, by the general path, over the rows
+    // convert_rec stored (the same lanes store the same bytes, in order).
+    auto convert_general = [&](const Batch& B, uint8_t* tile, int sub) {
+#pragma unroll 1
+      for (int k = 0; k < kBatch; ++k) {
+        const int32_t id = __shfl_sync(0xffffffffu, B.keys, (sub * kBatch + k) & 31);
+        if (id < 0) continue;  // uniform over the warp: a masked record stays zero
+        uint32_t o[8];
+        dequant16_any(ldg_v4_now(kv_lat + int64_t(id) * kRecordBytes),
+                      __shfl_sync(0xffffffffu, B.sc, 4 * k + (lane >> 3)), o);
+        store_rec(tile, k, sub, o);
+      }
     };
     Cursor c3;  // the tile whose raw entries are loaded next
     c3.init(a, row0, P0, cb, ce);
@@ -1135,6 +1184,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
         convert_rec(cur, k, tile, sub);
         if (more) load_rec(nxt, k, nsub);
       }
+      if (!__all_sync(0xffffffffu, plain_scale(cur.sc))) convert_general(cur, tile, sub);
       if (more) next_load();
       if (sub == kSub - 1) {
         fence_proxy_async_smem();

@@ -57,7 +57,7 @@ def run_gpu(q, kv, n_kv_rows, indices, indptr, lens, sm_scale, sink, *, max_row_
 U32 = 2.0 ** -24  # unit roundoff of f32
 
 
-def allowance(q, rec, indices, indptr, lens, sm_scale, sink, n_kv_rows=None):
+def allowance(q, rec, indices, indptr, lens, sm_scale, sink, n_kv_rows=None, operand_rel=0.0):
     """Rounding allowance of an f32 evaluation of the method, per output element.
 
     Scores: an f32 dot product of 576 terms is within ds_t = 576 u sum_d |q_d k_td|
@@ -67,6 +67,10 @@ def allowance(q, rec, indices, indptr, lens, sm_scale, sink, n_kv_rows=None):
     rounded to bf16 add 2^-8 sum_t w_t |v_td|.  For N(0,1) data this is ~1e-3;
     it only matters where the problem is ill-conditioned (heavy-tailed keys,
     near-tied scores).  Uses the oracle's own row slicing and record reader.
+
+    operand_rel: relative rounding of k and v on their way into the products
+    (0 where they enter exactly); it adds operand_rel sum_d |q_d k_td| to each
+    score's error and operand_rel sum_t w_t |v_td| to each output.
     """
     q = np.asarray(q, dtype=np.float64)
     n_q, heads, _ = q.shape
@@ -80,7 +84,7 @@ def allowance(q, rec, indices, indptr, lens, sm_scale, sink, n_kv_rows=None):
             continue
         keys, values = oracle.row_keys(rec, ids)
         s = oracle.row_scores(q[r], keys, sm_scale)
-        ds = 2.0 * 576 * U32 * abs(sm_scale) * (np.abs(q[r]) @ np.abs(keys).T)
+        ds = (2.0 * 576 * U32 + operand_rel) * abs(sm_scale) * (np.abs(q[r]) @ np.abs(keys).T)
         m = s.max(axis=1, keepdims=True)
         e = np.exp(s - m)
         den = e.sum(axis=1, keepdims=True)
@@ -90,7 +94,7 @@ def allowance(q, rec, indices, indptr, lens, sm_scale, sink, n_kv_rows=None):
         av = np.abs(values)
         out = w @ values
         wd = w * ds
-        out_allow[r] = wd @ av + wd.sum(axis=1, keepdims=True) * np.abs(out) + 2.0 ** -8 * (w @ av)
+        out_allow[r] = wd @ av + wd.sum(axis=1, keepdims=True) * np.abs(out) + (2.0 ** -8 + operand_rel) * (w @ av)
         lse_allow[r] = ds.max(axis=1)
     return out_allow, lse_allow
 

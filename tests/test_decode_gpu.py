@@ -348,3 +348,78 @@ def test_has_invalid_trims_padding_without_changing_results(splits):
                                    what="untrimmed")
     assert st_t & smla.STATUS_INDEX_OOB and st_f & smla.STATUS_INDEX_OOB
     assert torch.isinf(lse_t[1]).all() and torch.count_nonzero(out_t[1].float()) == 0
+
+
+@pytest.mark.parametrize("heads", [16, 32, 64])
+def test_scales_outside_the_writer_format(heads, kernel):
+    """Block scales the record writer never writes (its scales are powers of
+    two from 2^-22 to 2^7): not powers of two, zero, negative, above 2^7, f32
+    subnormal.  The oracle takes the stored f32 scale as it is (reading c10);
+    the tensor-core path dequantises such blocks in f32 and rounds each value
+    once to bf16, so the tolerance gains a relative 2^-8 on k and v.  Rows
+    cover tiles of plain scales only (the fast path), of other scales only,
+    mixed, and mixed with -1 entries (the per-record path).  Then rows of one
+    key and no sink, whose output is that key's latent as the kernel
+    dequantised it: bf16_rn(f32(e4m3) * f32 scale) bit for bit (both kernels
+    form each value so; blocks with f32-subnormal products are left out of
+    this part)."""
+    rng = np.random.default_rng(7 + heads)
+    g = torch.Generator().manual_seed(heads)
+    n = 1024
+    lat = torch.randn(n, 512, generator=g).to(torch.bfloat16)
+    rope = torch.randn(n, 64, generator=g).to(torch.bfloat16)
+    rec = oracle.pack_records(bits(lat), bits(rope))
+    sc = rec[:, 512:528].copy().view("<f4").reshape(n, 4).astype(np.float64)
+    half = n // 2  # records [half, n) get new scales
+    kind = rng.integers(0, 6, size=(half, 4))
+    mant = rng.uniform(1.0, 2.0, size=(half, 4))
+    big = np.exp2(rng.integers(8, 10, size=(half, 4))) * mant
+    new = np.select([kind == 0, kind == 1, kind == 2, kind == 3, kind == 4],
+                    [sc[half:] * mant,   # not a power of two, the same magnitude
+                     0.0,                # zero: the block's latent is 0
+                     -sc[half:] * mant,  # negative
+                     big,                # above 2^7 (the codes below are made small)
+                     1e-40 * mant],      # f32 subnormal
+                    sc[half:])           # kind 5: the writer's own scale
+    rec[half:, 512:528] = new.astype("<f4").view(np.uint8).reshape(half, 16)
+    for i, b in zip(*np.nonzero(kind == 3)):  # E4M3 subnormal codes (|x| <= 7 * 2^-9), random signs
+        codes = rng.integers(0, 8, size=128) | (rng.integers(0, 2, size=128) << 7)
+        rec[half + i, 128 * b:128 * (b + 1)] = codes.astype(np.uint8)
+    assert (kind == 1).any() and (kind == 3).any() and (kind == 4).any()
+
+    def ids(lo, hi, m):
+        return rng.integers(lo, hi, size=m).astype(np.int32)
+
+    mixed = ids(0, n, 150)
+    mixed[rng.random(150) < 0.2] = -1
+    rows = [ids(0, half, 256), ids(half, n, 200), ids(0, n, 300), mixed, ids(half, n, 1)]
+    indices = torch.from_numpy(np.concatenate(rows))
+    indptr = torch.from_numpy(np.cumsum([0] + [len(r) for r in rows]).astype(np.int32))
+    q = torch.randn(len(rows), heads, 576, generator=g).to(torch.bfloat16)
+    sink = torch.randn(heads, generator=g)
+    kv = torch.from_numpy(rec).to(DEV)
+    out, lse, nv, st = run_gpu(q.to(DEV), kv, n, indices.to(DEV), indptr.to(DEV), None, 0.0625,
+                               sink.float().to(DEV), max_row_len=300, kernel=kernel)
+    args = (q.double().numpy(), rec, indices.numpy(), indptr.numpy(), None, 0.0625, sink.double().numpy())
+    ref_out, ref_lse, ref_nv = oracle.sparse_mla_decode(*args, n_kv_rows=n)
+    assert st == 0
+    assert np.array_equal(nv.cpu().numpy(), ref_nv)
+    compare(out, lse, ref_out, ref_lse, f"scales, {heads} heads",
+            allow=allowance(*args, n_kv_rows=n, operand_rel=2.0 ** -8))
+
+    # one key per row, no sink: out = the key's dequantised latent exactly
+    normal = np.nonzero((kind != 4).all(axis=1))[0] + half
+    one = np.concatenate([rng.choice(normal, 56, replace=False), rng.choice(half, 8, replace=False)])
+    one = torch.from_numpy(one.astype(np.int32))
+    ptr1 = torch.arange(len(one) + 1, dtype=torch.int32)
+    q1 = torch.randn(len(one), heads, 576, generator=g).to(torch.bfloat16)
+    out1, _, nv1, st1 = run_gpu(q1.to(DEV), kv, n, one.to(DEV), ptr1.to(DEV), None, 0.0625, None,
+                                max_row_len=1, kernel=kernel)
+    unit_scales = np.tile(np.ones(1, "<f4").view(np.uint8), (len(one), 4))
+    codes = np.concatenate([rec[one.numpy(), :512], unit_scales, rec[one.numpy(), 528:]], axis=1)
+    unit, _, _ = oracle.unpack_records(codes)  # the E4M3 values (scale 1), exact in f32
+    scale32 = rec[one.numpy(), 512:528].copy().view("<f4").reshape(-1, 4)
+    want = torch.from_numpy(unit.astype(np.float32) * np.repeat(scale32, 128, axis=1)).to(torch.bfloat16)
+    assert st1 == 0 and (nv1.cpu() == 1).all()
+    diff = out1.cpu().float() != want[:, None, :].float()  # values (a zero's sign aside)
+    assert not diff.any(), f"single keys, {heads} heads: {int(diff.sum())} values differ"
