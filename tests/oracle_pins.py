@@ -347,4 +347,31 @@ def pin_index_buffer_bounds(orc):
     assert np.array_equal(nv, [2, 0])
 
 
+
+def pin_foreign_scales(orc):
+    # reading c10: a block scale the writer never writes (not a power of two,
+    # negative, zero, large, f32 subnormal) is taken as stored.  One key per
+    # row, so out is that key's latent; hand values: E4M3 0x38 = 1, 0xB8 = -1,
+    # 0x01 = 2^-9 (smallest subnormal), 0x7E = 448.
+    scales = np.array([3.0, -0.5, 0.0, 1000.0], dtype="<f4")
+    codes = np.array([0x38, 0xB8, 0x01, 0x7E], dtype=np.uint8)
+    hand = np.array([1.0, -1.0, 2.0 ** -9, 448.0])
+    rec = np.zeros((2, 656), dtype=np.uint8)
+    for b in range(4):
+        rec[0, 128 * b:128 * (b + 1)] = np.roll(codes, b)[np.arange(128) % 4]
+    rec[0, 512:528] = scales.view(np.uint8)
+    rec[1] = rec[0]
+    rec[1, 512:528] = np.full(4, 1e-40, dtype="<f4").view(np.uint8)  # f32 subnormal
+    q = random_q(2, 2, seed=31)
+    out, _, nv = orc.sparse_mla_decode(q, rec, np.array([0, 1], np.int32), np.array([0, 1, 2], np.int32))
+    assert np.array_equal(nv, [1, 1])
+    want = np.zeros((2, 512))
+    for b in range(4):
+        vals = np.roll(hand, b)[np.arange(128) % 4]
+        want[0, 128 * b:128 * (b + 1)] = vals * float(scales[b])
+        want[1, 128 * b:128 * (b + 1)] = vals * float(np.float32(1e-40))
+    assert np.array_equal(out[:, 0], want) and np.array_equal(out[:, 1], want), "foreign scales: latent as stored"
+    _, v_ref = torch_decode_records(rec)
+    assert np.array_equal(out[:, 0], v_ref), "foreign scales: torch's dtype views agree"
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

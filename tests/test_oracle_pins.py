@@ -124,6 +124,17 @@ def _mut_scale_squared(mp):
     mp.setattr(orc, "row_scores", lambda q, k, s: real(q, k, s * s))
 
 
+
+def _mut_scale_exponent_only(mp):
+    real = orc.unpack_records
+
+    def unpack_records(rec):  # a reader that keeps only each scale's power of two
+        lat, rope, sc = real(rec)
+        p2 = np.where(sc > 0, np.exp2(np.floor(np.log2(np.where(sc > 0, sc, 1.0)))), 0.0)
+        blocks = lat.reshape(lat.shape[0], 4, 128) / np.where(sc != 0, sc, 1.0)[:, :, None]
+        return (blocks * p2[:, :, None]).reshape(lat.shape[0], 512), rope, p2
+    mp.setattr(orc, "unpack_records", unpack_records)
+
 MUTATIONS = [v for k, v in sorted(globals().items()) if k.startswith("_mut_")]
 
 
