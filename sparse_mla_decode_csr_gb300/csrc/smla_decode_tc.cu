@@ -22,7 +22,9 @@
 //               into two S accumulators, 14 issues PV; warp 12 owns TMEM
 //   warps 4-11 (8-11 at 64 heads)  latent converters: gather the 512 E4M3
 //               bytes and the four scales of each tile's records (64-bit
-//               addressing), dequantise E4M3 * pow2 scale -> bf16 exactly, and
+//               addressing), dequantise E4M3 * pow2 scale -> bf16 exactly
+//               (a tile or batch holding any other scale is converted again
+//               by a general pass: e4m3 * scale in f32, rounded to bf16), and
 //               write the 64 x 512 bf16 latent of the key tile in the
 //               128-byte-swizzled K-major layout.  Up to 32 heads the latent
 //               bytes travel by cp.async into a per-warp shared-memory ring
