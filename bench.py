@@ -1,10 +1,14 @@
 #!/usr/bin/env python3
 """Sparse MLA decode throughput on GB300: query-rows/s and gathered-KV GB/s.
 
-One step = one smla_decode call (one kernel launch: gather, QK, softmax, PV
-and, for split rows, the fused combine) over one batch of the workload, with
-the KV cache, queries and index stream resident in HBM.  L2 is flushed
-between timed steps.  Prints ONE JSON line (rank 0).
+One step = one smla_decode call over one batch of the workload: the decode
+kernel (gather, QK, softmax, PV, epilogue), the merge kernel when rows are
+shared between CTAs, and the row-trim pass before them when the workload has
+-1 padding (has_invalid); the KV cache, queries and index stream are resident
+in HBM.  L2 is flushed between timed steps (a 256 MB write, then a 256 MB
+read: the read leaves the L2 holding clean lines, so the flush's own
+write-back does not land inside the timed step).  Prints ONE JSON line
+(rank 0).
 
   python bench.py [--gpus N --steps K --warmup W] [--workload decode]
   python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
@@ -46,11 +50,13 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="smla", choices=["smla", "reference"])
     ap.add_argument("--workload", default="decode", choices=sorted(W.WORKLOADS))
-    ap.add_argument("--also", default="wide", help="comma list of extra workloads to time ('' for none)")
+    ap.add_argument("--also", default="wide,ragged,long",
+                    help="comma list of extra workloads to time ('' for none)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle CPU-baseline budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel", default="tc", choices=["tc", "simt"],
-                    help="tc: the tcgen05 kernel; simt: the CUDA-core cross-check kernel")
+    ap.add_argument("--kernel", default="tc", choices=["tc", "fp8", "bf16", "simt"],
+                    help="tc: the default tensor-core choice (native fp8 up to 16 heads, else bf16); "
+                         "fp8 / bf16: force one tcgen05 kernel; simt: the CUDA-core cross-check kernel")
     return ap.parse_args()
 
 
@@ -163,7 +169,8 @@ class Problem:
         self.smla = smla
         self.w = w
         self.dev = dev
-        self.kernel = smla.KERNEL_TENSOR_CORE if kernel == "tc" else smla.KERNEL_CUDA_CORE
+        self.kernel = {"tc": smla.KERNEL_TENSOR_CORE, "fp8": smla.KERNEL_TENSOR_CORE_FP8,
+                       "bf16": smla.KERNEL_TENSOR_CORE_BF16, "simt": smla.KERNEL_CUDA_CORE}[kernel]
         self.kv = torch.empty(w.n_kv_rows, 656, dtype=torch.uint8, device=dev)
         for s in range(W.n_slabs(w)):
             lat, rope = W.latent_slab(w, s, dev)
@@ -176,7 +183,7 @@ class Problem:
         self.out = torch.empty(w.n_q, w.heads, 512, dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty(w.n_q, w.heads, dtype=torch.float32, device=dev)
         self.plan = smla.smla_plan(w.n_q, w.heads, w.max_row_len, self.indices.numel(), 0,
-                                   has_invalid=w.has_invalid)
+                                   has_invalid=w.has_invalid, kernel=self.kernel)
         # a workspace of this problem's own (zeroed): its ticket counters stay valid
         nbytes = int(self.plan.workspace_bytes)
         self.ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev) if nbytes else None
@@ -215,12 +222,26 @@ def weak_scaling_rows_per_s(world: int, rows_per_rank: int, steps: int, max_tota
 
 
 def l2_flusher(dev):
+    """Evicts the workload from L2 between timed steps: writes a buffer of at
+    least twice the L2 size, then reads another of the same size, so that the
+    L2 is left holding clean lines.  A write-only flush leaves up to an L2 of
+    dirty lines whose write-back then lands inside the next timed step (8-12 us
+    per launch on a 688 MB gather, measured with a gather-only kernel)."""
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    buf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
-    return lambda: buf.fill_(1)
+    n = max(2 * l2, 256 << 20)
+    wbuf = torch.empty(n, dtype=torch.uint8, device=dev)
+    rbuf = torch.ones(n // 4, dtype=torch.float32, device=dev)
+    sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def flush():
+        wbuf.fill_(1)
+        torch.sum(rbuf, out=sink)
+
+    return flush
 
 
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal
+KERNEL_NAMES = {1: "CUDA-core", 2: "bf16 tcgen05", 3: "native-fp8 tcgen05"}
 
 
 def scale_histogram(kv: torch.Tensor) -> dict:
@@ -453,6 +474,11 @@ def main():
         gbs = px.bytes_per_step() / (mean_ms * 1e-3) / 1e9
         extra[wx.name] = {"rows_per_s": wx.n_q / (mean_ms * 1e-3), "ms_per_step": mean_ms,
                           "gathered_kv_gbs": gbs, "hbm_frac": gbs / peak,
+                          "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                                       "frac": gbs / peak, "traffic": ncu_traffic(wx.name),
+                                       "algorithmic_bytes_per_launch": px.bytes_per_step()},
+                          "kernel": KERNEL_NAMES[px.plan.kernel],
+                          "gpu_launches_per_step": 1 + int(px.plan.merge_kernel) + int(px.plan.trim_kernel),
                           "num_splits": px.plan.num_splits, "grid": px.plan.grid}
         if wx.latent != "normal":
             extra[wx.name]["log2_scale_histogram"] = scale_histogram(px.kv)
@@ -479,13 +505,14 @@ def main():
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "n_q": w.n_q, "heads": w.heads, "topk": w.topk,
-                   "n_kv_rows": w.n_kv_rows, "rows_per_gpu": w.n_q, "l2": "flushed between steps",
+                   "n_kv_rows": w.n_kv_rows, "rows_per_gpu": w.n_q,
+                   "l2": "flushed between steps (256 MB written, then 256 MB read)",
                    "num_splits": prob.plan.num_splits, "grid": prob.plan.grid},
         "gathered_kv_gbs": achieved * world,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": ncu_traffic(w.name),
                      "peak_source": peak_src,
-                     "kernel": (f"one smla_decode call ({args.kernel} decode kernel"
+                     "kernel": (f"one smla_decode call ({KERNEL_NAMES[prob.plan.kernel]} decode kernel"
                                 + (" + merge kernel" if prob.plan.merge_kernel else "")
                                 + (" + row-trim pass" if prob.plan.trim_kernel else "") + "), CUDA events"),
                      "algorithmic_bytes_per_launch": bytes_step,

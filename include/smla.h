@@ -58,6 +58,13 @@ typedef enum smla_status {
 /* Bits a decode call ORs into *status (when status != NULL). */
 #define SMLA_STATUS_INDEX_OOB 0x1   /* an index >= n_kv_rows was met and masked */
 #define SMLA_STATUS_TIMEOUT 0x2     /* an in-kernel pipeline wait gave up: results invalid */
+#define SMLA_STATUS_SMEM_LAYOUT 0x4 /* the kernel could not align its shared memory and
+                                       computed nothing: results invalid */
+#define SMLA_STATUS_FOREIGN_SCALE 0x8 /* native-fp8 kernel: a gathered record holds a block
+                                         scale that is neither zero nor a positive normal
+                                         power of two (smla_pack_records never writes one);
+                                         the rows holding it are not computed exactly: run
+                                         SMLA_KERNEL_TENSOR_CORE_BF16 on such caches */
 
 #define SMLA_MAX_SPLITS 64
 
@@ -131,19 +138,30 @@ typedef struct smla_decode_params {
    * CUDA-core kernel cuts every row into k chunks; the tensor-core kernel
    * spreads the tiles over n_q * k CTAs (about k parts per row). */
   int32_t num_splits;
-  /* Which kernel runs the call: SMLA_KERNEL_TENSOR_CORE (0, default) or
-   * SMLA_KERNEL_CUDA_CORE (1, an fp32 CUDA-core kernel kept as a cross-check).
-   * Both compute the same definition. */
+  /* Which kernel runs the call (all compute the same definition):
+   *   SMLA_KERNEL_TENSOR_CORE (0, default): the native-fp8 kernel for the head
+   *     counts it supports (1..16), else the bf16 tensor-core kernel;
+   *   SMLA_KERNEL_CUDA_CORE (1): an fp32 CUDA-core kernel kept as a cross-check;
+   *   SMLA_KERNEL_TENSOR_CORE_BF16 (2): tcgen05 kind::f16 on latents dequantised
+   *     to bf16 (exact for power-of-two scales up to 2^7, any scale accepted);
+   *   SMLA_KERNEL_TENSOR_CORE_FP8 (3): tcgen05 kind::mxf8f6f4 on the E4M3 bytes as
+   *     they are, the block scales as E8M0 scale factors (heads 1..16; a call
+   *     with more heads returns SMLA_ERR_SHAPE).  Needs writer-format scales:
+   *     zero or positive normal powers of two; others set
+   *     SMLA_STATUS_FOREIGN_SCALE. */
   int32_t kernel;
 } smla_decode_params;
 
 #define SMLA_KERNEL_TENSOR_CORE 0
 #define SMLA_KERNEL_CUDA_CORE 1
+#define SMLA_KERNEL_TENSOR_CORE_BF16 2
+#define SMLA_KERNEL_TENSOR_CORE_FP8 3
 
 /* How a decode call with given params is laid out on the GPU.
  *
- * Tensor-core kernel (the default): a persistent, balanced schedule.  Each row
- * r is cut into T_r = max(1, ceil(len_r / 64)) tiles of 64 slice positions
+ * Tensor-core kernels (bf16: tile_len 64; native fp8: tile_len 128): a
+ * persistent, balanced schedule.  Each row r is cut into
+ * T_r = max(1, ceil(len_r / tile_len)) tiles of tile_len slice positions
  * and takes 2 + T_r slots of a schedule space (2 slots stand for the cost of
  * starting a row: its epilogue and q staging), rows in order, so row r's
  * tiles are slots [R_r, R_r + T_r) with R_r = 2 + sum_{r' < r} (2 + T_r').  CTA
@@ -164,7 +182,7 @@ typedef struct smla_decode_params {
  * trimmed to its last entry >= 0 into the workspace, and the decode schedules
  * those lengths (trim_kernel = 1).
  *
- * Fields: kernel (SMLA_KERNEL_*), grid (CTAs of the decode launch), tile_len
+ * Fields: kernel (the SMLA_KERNEL_* that runs: 1, 2 or 3), grid (CTAs of the decode launch), tile_len
  * (keys per tile), num_splits and chunk_len (CUDA-core kernel only),
  * partial_slots, merge_kernel, trim_kernel, workspace_bytes.  num_sms > 0 makes the plan
  * pure host arithmetic (no CUDA call); num_sms = 0 asks the current device. */

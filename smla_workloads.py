@@ -81,11 +81,13 @@ def latent_slab(w: Workload, slab: int, device="cpu"):
         lat = torch.randn(rows, LATENT_DIM, generator=g, device=device) * w.latent_std
     elif w.latent == "student_t3":
         # Student-t with 3 degrees of freedom: z / sqrt(chi2_3 / 3), times 2^e with
-        # e ~ U{-8..12} per (row, 128-wide block), clipped to |x| <= 57344.
+        # e ~ U{-5..12} per (row, 128-wide block), clipped to |x| <= 57344: the
+        # writer's block scales then span 2^-12 .. 2^7, the range the wide
+        # workload is specified with (plain t3 blocks alone give 2^-6 .. 2^-3).
         z = torch.randn(rows, LATENT_DIM, generator=g, device=device)
         c = torch.randn(rows, LATENT_DIM, 3, generator=g, device=device).square().sum(-1)
         t = z * torch.sqrt(3.0 / c)
-        e = torch.randint(-8, 13, (rows, LATENT_DIM // 128), generator=g, device=device)
+        e = torch.randint(-5, 13, (rows, LATENT_DIM // 128), generator=g, device=device)
         t = t * torch.exp2(e.float()).repeat_interleave(128, dim=1)
         lat = t
     else:

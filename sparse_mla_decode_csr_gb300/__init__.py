@@ -26,8 +26,12 @@ MAX_HEADS = 64
 MAX_SPLITS = 64
 STATUS_INDEX_OOB = 0x1
 STATUS_TIMEOUT = 0x2
-KERNEL_TENSOR_CORE = 0
+STATUS_SMEM_LAYOUT = 0x4
+STATUS_FOREIGN_SCALE = 0x8
+KERNEL_TENSOR_CORE = 0       # default: native fp8 where supported, else bf16 tensor cores
 KERNEL_CUDA_CORE = 1
+KERNEL_TENSOR_CORE_BF16 = 2
+KERNEL_TENSOR_CORE_FP8 = 3
 NOALLOC_SCRATCH_BYTES = 64 << 20  # SMLA_NOALLOC_SCRATCH_BYTES
 SMLA_ERR_WORKSPACE = -5
 

@@ -67,6 +67,33 @@ WorkspaceLayout workspace_layout(int32_t n_q, int32_t heads, int32_t slots, bool
   return w;
 }
 
+int check_decode_params(const smla_decode_params* p) {
+  if (p == nullptr) return SMLA_ERR_NULL;
+  if (p->n_q < 0 || p->num_heads < 1 || p->num_heads > SMLA_MAX_HEADS) return SMLA_ERR_SHAPE;
+  if (p->n_kv_rows < 0 || p->n_kv_rows > (int64_t(1) << 31) || p->n_indices < 0) return SMLA_ERR_SHAPE;
+  if (p->num_splits < 0 || p->num_splits > SMLA_MAX_SPLITS) return SMLA_ERR_SPLITS;
+  if (p->kernel < SMLA_KERNEL_TENSOR_CORE || p->kernel > SMLA_KERNEL_TENSOR_CORE_FP8) return SMLA_ERR_SHAPE;
+  if (p->kernel == SMLA_KERNEL_TENSOR_CORE_FP8 && !fp8_kernel_supports(p->num_heads)) return SMLA_ERR_SHAPE;
+  if (p->n_q == 0) return SMLA_OK;
+  if (!p->q || !p->indptr || !p->out) return SMLA_ERR_NULL;
+  if (p->n_kv_rows > 0 && !p->kv_cache) return SMLA_ERR_NULL;
+  if (p->n_indices > 0 && !p->indices) return SMLA_ERR_NULL;
+  if (p->q_stride_head < SMLA_QK_DIM && p->num_heads > 1) return SMLA_ERR_STRIDE;
+  if (p->q_stride_row < int64_t(p->num_heads - 1) * p->q_stride_head + SMLA_QK_DIM && p->n_q > 1)
+    return SMLA_ERR_STRIDE;
+  if (p->out_stride_head < SMLA_LATENT_DIM && p->num_heads > 1) return SMLA_ERR_STRIDE;
+  if (p->out_stride_row < int64_t(p->num_heads - 1) * p->out_stride_head + SMLA_LATENT_DIM && p->n_q > 1)
+    return SMLA_ERR_STRIDE;
+  if (p->q_stride_row < 0 || p->q_stride_head < 0 || p->out_stride_row < 0 || p->out_stride_head < 0)
+    return SMLA_ERR_STRIDE;
+  if (!aligned16(p->q) || !aligned16(p->out) || (p->kv_cache && !aligned16(p->kv_cache)))
+    return SMLA_ERR_ALIGN;
+  if ((p->q_stride_row | p->q_stride_head | p->out_stride_row | p->out_stride_head) & 7)
+    return SMLA_ERR_ALIGN;
+  if (!std::isfinite(p->sm_scale)) return SMLA_ERR_SHAPE;
+  return SMLA_OK;
+}
+
 }  // namespace smla
 
 using namespace smla;
@@ -103,7 +130,8 @@ int smla_plan(const smla_decode_params* p, int32_t num_sms, smla_plan_info* plan
   const int32_t n_q = p->n_q, num_heads = p->num_heads, num_splits = p->num_splits;
   if (n_q < 0 || num_heads < 1 || num_heads > SMLA_MAX_HEADS || p->n_indices < 0) return SMLA_ERR_SHAPE;
   if (num_splits < 0 || num_splits > SMLA_MAX_SPLITS) return SMLA_ERR_SPLITS;
-  if (p->kernel != SMLA_KERNEL_TENSOR_CORE && p->kernel != SMLA_KERNEL_CUDA_CORE) return SMLA_ERR_SHAPE;
+  if (p->kernel < SMLA_KERNEL_TENSOR_CORE || p->kernel > SMLA_KERNEL_TENSOR_CORE_FP8) return SMLA_ERR_SHAPE;
+  if (p->kernel == SMLA_KERNEL_TENSOR_CORE_FP8 && !fp8_kernel_supports(num_heads)) return SMLA_ERR_SHAPE;
   if (num_sms <= 0) {
     int rc = current_sm_count(&num_sms);
     if (rc != SMLA_OK) return rc;
@@ -112,9 +140,13 @@ int smla_plan(const smla_decode_params* p, int32_t num_sms, smla_plan_info* plan
   if (row_len <= 0) row_len = n_q > 0 ? (p->n_indices + n_q - 1) / n_q : 0;
   const int64_t tiles = std::max<int64_t>(1, (row_len + kTile - 1) / kTile);
   *plan = smla_plan_info{};
-  plan->kernel = p->kernel;
-  plan->tile_len = kTile;
-  if (p->kernel == SMLA_KERNEL_TENSOR_CORE) {
+  // the default picks the native-fp8 kernel where it supports the head count
+  int32_t kernel = p->kernel;
+  if (kernel == SMLA_KERNEL_TENSOR_CORE)
+    kernel = fp8_kernel_supports(num_heads) ? SMLA_KERNEL_TENSOR_CORE_FP8 : SMLA_KERNEL_TENSOR_CORE_BF16;
+  plan->kernel = kernel;
+  plan->tile_len = kernel == SMLA_KERNEL_TENSOR_CORE_FP8 ? fp8_tile_len() : kTile;
+  if (kernel != SMLA_KERNEL_CUDA_CORE) {
     // persistent: one CTA per SM, tiles balanced over them; forcing k splits
     // spreads the tiles over n_q * k CTAs instead
     int64_t g = num_splits > 0 ? int64_t(n_q) * num_splits : num_sms;
@@ -162,35 +194,9 @@ size_t smla_decode_workspace_size(const smla_decode_params* params) {
   return size_t(plan.workspace_bytes);
 }
 
-static int check_params(const smla_decode_params* p) {
-  if (p == nullptr) return SMLA_ERR_NULL;
-  if (p->n_q < 0 || p->num_heads < 1 || p->num_heads > SMLA_MAX_HEADS) return SMLA_ERR_SHAPE;
-  if (p->n_kv_rows < 0 || p->n_kv_rows > (int64_t(1) << 31) || p->n_indices < 0) return SMLA_ERR_SHAPE;
-  if (p->num_splits < 0 || p->num_splits > SMLA_MAX_SPLITS) return SMLA_ERR_SPLITS;
-  if (p->kernel != SMLA_KERNEL_TENSOR_CORE && p->kernel != SMLA_KERNEL_CUDA_CORE) return SMLA_ERR_SHAPE;
-  if (p->n_q == 0) return SMLA_OK;
-  if (!p->q || !p->indptr || !p->out) return SMLA_ERR_NULL;
-  if (p->n_kv_rows > 0 && !p->kv_cache) return SMLA_ERR_NULL;
-  if (p->n_indices > 0 && !p->indices) return SMLA_ERR_NULL;
-  if (p->q_stride_head < SMLA_QK_DIM && p->num_heads > 1) return SMLA_ERR_STRIDE;
-  if (p->q_stride_row < int64_t(p->num_heads - 1) * p->q_stride_head + SMLA_QK_DIM && p->n_q > 1)
-    return SMLA_ERR_STRIDE;
-  if (p->out_stride_head < SMLA_LATENT_DIM && p->num_heads > 1) return SMLA_ERR_STRIDE;
-  if (p->out_stride_row < int64_t(p->num_heads - 1) * p->out_stride_head + SMLA_LATENT_DIM && p->n_q > 1)
-    return SMLA_ERR_STRIDE;
-  if (p->q_stride_row < 0 || p->q_stride_head < 0 || p->out_stride_row < 0 || p->out_stride_head < 0)
-    return SMLA_ERR_STRIDE;
-  if (!aligned16(p->q) || !aligned16(p->out) || (p->kv_cache && !aligned16(p->kv_cache)))
-    return SMLA_ERR_ALIGN;
-  if ((p->q_stride_row | p->q_stride_head | p->out_stride_row | p->out_stride_head) & 7)
-    return SMLA_ERR_ALIGN;
-  if (!std::isfinite(p->sm_scale)) return SMLA_ERR_SHAPE;
-  return SMLA_OK;
-}
-
 int smla_decode(const smla_decode_params* params, void* workspace, size_t workspace_bytes,
                 void* stream) {
-  int rc = check_params(params);
+  int rc = check_decode_params(params);
   if (rc != SMLA_OK) return rc;
   if (params->n_q == 0) return SMLA_OK;
   rc = smla_device_check();
@@ -205,7 +211,9 @@ int smla_decode(const smla_decode_params* params, void* workspace, size_t worksp
   if (L.ws.total > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return SMLA_ERR_ALIGN;
   L.workspace = workspace;
   L.stream = static_cast<cudaStream_t>(stream);
-  cudaError_t err = params->kernel == SMLA_KERNEL_CUDA_CORE ? launch_decode_simt(L) : launch_decode_tc(L);
+  cudaError_t err = L.plan.kernel == SMLA_KERNEL_CUDA_CORE ? launch_decode_simt(L)
+                    : L.plan.kernel == SMLA_KERNEL_TENSOR_CORE_FP8 ? launch_decode_fp8(L)
+                                                                   : launch_decode_tc(L);
   return err == cudaSuccess ? SMLA_OK : SMLA_ERR_LAUNCH;
 }
 

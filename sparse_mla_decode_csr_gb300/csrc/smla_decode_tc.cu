@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
 #endif
   if (Lay::slack == 0 && (smem_u32(smem_raw) & 1023u) != 0) {
     // no room to realign: refuse (uniformly, before any barrier or TMEM use)
-    if (tid == 0 && a.status) atomicOr(a.status, SMLA_STATUS_TIMEOUT);
+    if (tid == 0 && a.status) atomicOr(a.status, SMLA_STATUS_SMEM_LAYOUT);
     return;
   }
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1411,16 +1411,25 @@ cudaError_t launch_tc_hp(const DecodeLaunch& L) {
   cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<HP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   DecodeArgs args = make_decode_args(L);
-  if (L.plan.trim_kernel && L.ws.lens_off >= 0) {
-    int32_t* lens_trim = reinterpret_cast<int32_t*>(static_cast<char*>(L.workspace) + L.ws.lens_off);
-    trim_rows_kernel<<<unsigned(L.p.n_q), 32 * kTrimWarps, 0, L.stream>>>(args, lens_trim);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    args.lens = lens_trim;  // the caller's lens already capped these
-  }
+  e = launch_trim(L, args);
+  if (e != cudaSuccess) return e;
   decode_tc_kernel<HP><<<L.plan.grid, kThreadsTC, smem, L.stream>>>(args);
   e = cudaGetLastError();
   if (e != cudaSuccess || !L.plan.merge_kernel) return e;
+  return launch_merge(L, args);
+}
+
+}  // namespace
+
+cudaError_t launch_trim(const DecodeLaunch& L, DecodeArgs& args) {
+  if (!(L.plan.trim_kernel && L.ws.lens_off >= 0)) return cudaSuccess;
+  int32_t* lens_trim = reinterpret_cast<int32_t*>(static_cast<char*>(L.workspace) + L.ws.lens_off);
+  trim_rows_kernel<<<unsigned(L.p.n_q), 32 * kTrimWarps, 0, L.stream>>>(args, lens_trim);
+  args.lens = lens_trim;  // the caller's lens already capped these
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge(const DecodeLaunch& L, const DecodeArgs& args) {
   const int64_t pairs = int64_t(L.p.n_q) * L.p.num_heads;
   // rows shared by many CTAs (few rows over the grid) split each head's parts
   // over a CTA's eight warps
@@ -1430,8 +1439,6 @@ cudaError_t launch_tc_hp(const DecodeLaunch& L) {
     merge_rows_kernel<1><<<unsigned((pairs + kMergeWarps - 1) / kMergeWarps), 32 * kMergeWarps, 0, L.stream>>>(args);
   return cudaGetLastError();
 }
-
-}  // namespace
 
 cudaError_t launch_decode_tc(const DecodeLaunch& L) {
   if (L.plan.grid <= 0) return cudaSuccess;

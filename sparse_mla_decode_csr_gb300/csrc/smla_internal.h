@@ -33,9 +33,23 @@ struct DecodeLaunch {
   cudaStream_t stream;
 };
 
+// Host-side argument checks of smla_decode (SMLA_OK or a negative status);
+// nothing is enqueued.
+int check_decode_params(const smla_decode_params* p);
+
+struct DecodeArgs;
+
 // Kernel launchers (one per translation unit).  Return a cudaError_t.
 cudaError_t launch_decode_simt(const DecodeLaunch& L);
 cudaError_t launch_decode_tc(const DecodeLaunch& L);
+cudaError_t launch_decode_fp8(const DecodeLaunch& L);
+// The row-trim pass before a tensor-core decode (when plan.trim_kernel; it
+// points args.lens at the trimmed lengths) and the merge of shared rows after it.
+cudaError_t launch_trim(const DecodeLaunch& L, DecodeArgs& args);
+cudaError_t launch_merge(const DecodeLaunch& L, const DecodeArgs& args);
+// Heads and tile length of the native-fp8 kernel.
+bool fp8_kernel_supports(int num_heads);
+int fp8_tile_len();
 cudaError_t launch_pack(const void* latent, int64_t latent_stride, const void* rope,
                         int64_t rope_stride, int64_t n, void* kv_out, cudaStream_t stream);
 

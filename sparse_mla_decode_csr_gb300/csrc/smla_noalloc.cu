@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "smla.h"
+#include "smla_internal.h"
 
 namespace {
 
@@ -43,10 +44,14 @@ int scratch_on_current_device(void** address) {
 }  // namespace
 
 extern "C" int smla_decode_noalloc(const smla_decode_params* params, void* stream) {
-  if (params == nullptr) return SMLA_ERR_NULL;
-  if (params->n_q == 0) return smla_decode(params, nullptr, 0, stream);  // argument checks only
+  // every argument check runs before anything is enqueued (the ticket clear below included)
+  int rc = smla::check_decode_params(params);
+  if (rc != SMLA_OK) return rc;
+  if (params->n_q == 0) return SMLA_OK;
+  rc = smla_device_check();
+  if (rc != SMLA_OK) return rc;
   smla_plan_info plan{};
-  int rc = smla_plan(params, 0, &plan);
+  rc = smla_plan(params, 0, &plan);
   if (rc != SMLA_OK) return rc;
   if (plan.workspace_bytes < 0 || uint64_t(plan.workspace_bytes) > SMLA_NOALLOC_SCRATCH_BYTES)
     return SMLA_ERR_WORKSPACE;

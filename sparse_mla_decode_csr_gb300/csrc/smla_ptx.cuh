@@ -185,6 +185,28 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
                : "memory");
 }
 
+// 32 lanes x 1 / 16 / 32 consecutive 32-bit columns (same lane mapping as tmem_ld8).
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
 // ---- tcgen05.mma ------------------------------------------------------------------
 // D[tmem] (+)= A[smem desc] * B[smem desc], kind::f16 (bf16/f16 inputs, f32 accumulate).
 __device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
@@ -208,6 +230,21 @@ __device__ __forceinline__ void mma_f16_ss_w(uint32_t d_tmem, uint32_t a_lo, uin
       "setp.ne.b32 p, %6, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, p;\n\t}" ::"r"(d_tmem),
       "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D[tmem] (+)= (A[smem desc] x SFA) * (B[smem desc] x SFB), kind::mxf8f6f4 with
+// E8M0 scale factors per 32 elements of K (scale_vec::1X) read from TMEM at
+// sfa_tmem / sfb_tmem (the byte within each 32-bit column is chosen by the
+// scale-factor ids of the instruction descriptor).  f32 accumulate.
+__device__ __forceinline__ void mma_mxf8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
 }
 
@@ -237,6 +274,18 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, int a_mn, int b_
          | (uint32_t(b_mn) << 16)       // B major
          | (uint32_t(n >> 3) << 17)     // N / 8
          | (uint32_t(m >> 4) << 24);    // M / 16
+}
+
+// Instruction descriptor of kind::mxf8f6f4 with E4M3 A and B, f32 accumulate and
+// UE8M0 scale factors; a_sf / b_sf pick the byte of the scale-factor columns.
+__host__ __device__ constexpr uint32_t idesc_mxf8(int m, int n, int a_mn, int b_mn, int a_sf, int b_sf) {
+  return (uint32_t(b_sf) << 4)          // B scale-factor id
+         | (uint32_t(a_mn) << 15)       // A major (E4M3 A and B: format code 0)
+         | (uint32_t(b_mn) << 16)       // B major
+         | (uint32_t(n >> 3) << 17)     // N / 8
+         | (1u << 23)                   // scale factors are UE8M0
+         | (uint32_t(m >> 4) << 24)     // M / 16
+         | (uint32_t(a_sf) << 29);      // A scale-factor id
 }
 
 __device__ __forceinline__ float ex2(float x) {

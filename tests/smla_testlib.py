@@ -35,7 +35,9 @@ def build_cache(w: W.Workload, dev, gen_device="cuda") -> torch.Tensor:
     return kv
 
 
-KERNELS = {"tc": smla.KERNEL_TENSOR_CORE, "simt": smla.KERNEL_CUDA_CORE}
+KERNELS = {"tc": smla.KERNEL_TENSOR_CORE, "simt": smla.KERNEL_CUDA_CORE,
+           "bf16": smla.KERNEL_TENSOR_CORE_BF16, "fp8": smla.KERNEL_TENSOR_CORE_FP8}
+FP8_MAX_HEADS = 16
 
 
 def run_gpu(q, kv, n_kv_rows, indices, indptr, lens, sm_scale, sink, *, max_row_len=0,
@@ -99,18 +101,26 @@ def allowance(q, rec, indices, indptr, lens, sm_scale, sink, n_kv_rows=None, ope
     return out_allow, lse_allow
 
 
-def compare(out_gpu, lse_gpu, ref_out, ref_lse, what="", allow=None):
+def compare(out_gpu, lse_gpu, ref_out, ref_lse, what="", allow=None, stats=None):
     """Element-wise |gpu - ref| <= 2e-2 + 1e-2 |ref| (+ the f32 rounding
     allowance of ill-conditioned elements) for out and finite lse; the
     norm-relative error of each (row, head) output <= 1e-2 (+ the norm of the
-    allowance); -inf lse exactly where the oracle has it."""
+    allowance); -inf lse exactly where the oracle has it.
+
+    stats (a dict, optional) receives how many out elements pass only through
+    the allowance ("allowance_only") and the largest allowance ("max_allowance")."""
     a_out, a_lse = (0.0, 0.0) if allow is None else allow
     g = out_gpu.float().cpu().double().numpy()
     assert np.isfinite(g).all(), f"{what}: non-finite output"
-    excess = np.abs(g - ref_out) - (ATOL + RTOL * np.abs(ref_out) + a_out)
+    err = np.abs(g - ref_out)
+    bare = ATOL + RTOL * np.abs(ref_out)
+    excess = err - (bare + a_out)
     worst = np.unravel_index(np.argmax(excess), excess.shape)
-    assert excess.max() <= 0, (f"{what}: out off by {np.abs(g - ref_out)[worst]:.4g} at {worst} "
+    assert excess.max() <= 0, (f"{what}: out off by {err[worst]:.4g} at {worst} "
                                f"(ref {ref_out[worst]:.4g}, gpu {g[worst]:.4g})")
+    if stats is not None:
+        stats["allowance_only"] = int((err > bare).sum())
+        stats["max_allowance"] = float(np.max(a_out)) if np.size(a_out) else 0.0
     num = np.linalg.norm(g - ref_out, axis=-1)
     den = np.linalg.norm(ref_out, axis=-1)
     slack = np.linalg.norm(np.broadcast_to(a_out, ref_out.shape), axis=-1)

@@ -29,6 +29,14 @@ def test_library_exports_every_declared_symbol():
     assert set(smla.EXPORTED_SYMBOLS) <= set(names)
 
 
+def test_status_bits_are_distinct():
+    bits = [smla.STATUS_INDEX_OOB, smla.STATUS_TIMEOUT, smla.STATUS_SMEM_LAYOUT, smla.STATUS_FOREIGN_SCALE]
+    assert len(set(bits)) == len(bits) and all(b & (b - 1) == 0 for b in bits)
+    text = open(os.path.join(ROOT, "include", "smla.h")).read()
+    for name, v in [("INDEX_OOB", 1), ("TIMEOUT", 2), ("SMEM_LAYOUT", 4), ("FOREIGN_SCALE", 8)]:
+        assert re.search(rf"#define SMLA_STATUS_{name} 0x{v:x}\b", text), name
+
+
 def test_strerror_names_every_code():
     for code in range(0, -9, -1):
         assert smla.strerror(code) != "unknown status"
@@ -57,8 +65,10 @@ def test_plan_properties_cuda_core(n_q, heads, row_len):
     (4, 16, 128), (64, 16, 2048), (256, 16, 2048), (128, 64, 2048), (4, 64, 16384), (1, 1, 1)])
 def test_plan_properties_tensor_core(n_q, heads, row_len):
     p = smla.smla_plan(n_q, heads, row_len, n_q * row_len, 0, 152)
-    assert p.kernel == smla.KERNEL_TENSOR_CORE
-    assert p.grid == 152 and p.tile_len == 64  # persistent: one CTA per SM
+    # the default resolves to the native-fp8 kernel up to 16 heads, else bf16
+    fp8 = heads <= 16
+    assert p.kernel == (smla.KERNEL_TENSOR_CORE_FP8 if fp8 else smla.KERNEL_TENSOR_CORE_BF16)
+    assert p.grid == 152 and p.tile_len == (128 if fp8 else 64)  # persistent: one CTA per SM
     assert p.partial_slots == 2 * p.grid
     assert p.merge_kernel == (p.grid > 1)
     need = n_q * 4 + (n_q + 1) * 8 + p.partial_slots * heads * (512 + 2) * 4 + p.partial_slots * 4
@@ -82,6 +92,10 @@ def test_plan_splits_short_batches_and_respects_forcing():
         smla.smla_plan(-1, 16, 700, 2100, 0, 152)
     with pytest.raises(smla.SmlaError):
         smla.smla_plan(3, 16, 700, 2100, 0, 152, kernel=7)
+    with pytest.raises(smla.SmlaError):  # the native-fp8 kernel takes up to 16 heads
+        smla.smla_plan(3, 17, 700, 2100, 0, 152, kernel=smla.KERNEL_TENSOR_CORE_FP8)
+    for k in (smla.KERNEL_TENSOR_CORE_BF16, smla.KERNEL_TENSOR_CORE_FP8):
+        assert smla.smla_plan(3, 16, 700, 2100, 0, 152, kernel=k).kernel == k
 
 
 def _params(**kw):
@@ -103,11 +117,23 @@ def _params(**kw):
     (dict(n_kv_rows=(1 << 31) + 1), -2), (dict(sm_scale=float("nan")), -2),
     (dict(q_stride_head=100), -3), (dict(out_stride_row=512), -3),
     (dict(q=0x1008), -4), (dict(out_stride_head=516, out_stride_row=16 * 516), -4), (dict(kv_cache=0x2004), -4),
-    (dict(num_splits=65), -6), (dict(num_splits=-1), -6), (dict(kernel=2), -2),
+    (dict(num_splits=65), -6), (dict(num_splits=-1), -6), (dict(kernel=4), -2),
+    (dict(kernel=3, num_heads=17), -2),
 ])
 def test_decode_rejects_bad_arguments_on_host(kw, code):
     p = _params(**kw)
     rc = smla.lib.smla_decode(ctypes.byref(p), None, 0, None)
+    assert rc == code, (kw, rc, smla.strerror(rc))
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None, kernel=1, num_splits=3), -1), (dict(indptr=None, kernel=1, num_splits=3), -1),
+    (dict(q=0x1008, kernel=1, num_splits=3), -4), (dict(q_stride_head=100), -3), (dict(num_heads=65), -2)])
+def test_noalloc_rejects_bad_arguments_before_enqueueing(kw, code):
+    # the checks run before the call touches the device (no CUDA device here):
+    # the CUDA-core split plan's ticket clear is never enqueued for a bad call
+    p = _params(**kw)
+    rc = smla.lib.smla_decode_noalloc(ctypes.byref(p), None)
     assert rc == code, (kw, rc, smla.strerror(rc))
 
 
