@@ -235,7 +235,7 @@ def l2_flusher(dev):
 
     def flush():
         wbuf.fill_(1)
-        torch.sum(rbuf, out=sink)
+        torch.sum(rbuf, dim=0, out=sink)
 
     return flush
 

@@ -195,6 +195,7 @@ typedef struct smla_plan_info {
   int32_t partial_slots;
   int32_t merge_kernel;
   int32_t trim_kernel;
+  int32_t head_groups;
   int64_t workspace_bytes;
 } smla_plan_info;
 
@@ -204,7 +205,8 @@ int smla_plan(const smla_decode_params* params, int32_t num_sms, smla_plan_info*
  * (0 when none; also 0 for invalid params).
  *
  * Layout (each part 256-byte aligned), S = plan.partial_slots:
- *   ticket   int32 [n_q]         per-row arrival counters (CUDA-core kernel)
+ *   ticket   int32 [2 n_q]       per-row (and head group) arrival counters (CUDA-core and
+ *                                native-fp8 kernels)
  *   row_tile int64 [n_q + 1]     tensor-core kernel: first slot of every row, then W
  *   o_part   f32 [S][H][512]     unnormalised partial sum_t 2^(x_t - m) v_t of a row part
  *   ml_part f32 [S][H][2]        (m, l) of x_t = s_t * log2(e): m is the part's reference
@@ -215,7 +217,7 @@ int smla_plan(const smla_decode_params* params, int32_t num_sms, smla_plan_info*
  * The ticket counters must be zero when a call starts (e.g. allocate the
  * workspace zeroed); every completed call returns them to zero.  A call with
  * other sizes may have written partials over that region, so re-zero bytes
- * [0, 4 n_q) before reusing a workspace across calls of different n_q,
+ * [0, 8 n_q) before reusing a workspace across calls of different n_q,
  * num_heads, kernel or plan.  Calls that share a workspace must be ordered
  * (same stream); a call that reports SMLA_STATUS_TIMEOUT leaves it undefined. */
 size_t smla_decode_workspace_size(const smla_decode_params* params);
@@ -263,9 +265,10 @@ int smla_decode(const smla_decode_params* params, void* workspace, size_t worksp
  *   - Sharing: every call on a device uses the same array and leaves its last
  *     contents there.  Calls whose work may overlap on the GPU (different
  *     streams without an ordering event) race on it and give wrong results;
- *     order them.  With the CUDA-core kernel the call first clears the
- *     ticket counters (bytes [0, 4 n_q)) on `stream`; the tensor-core kernel
- *     writes every part of the array it reads and needs nothing cleared.
+ *     order them.  With the CUDA-core and native-fp8 kernels the call first
+ *     clears the ticket counters (bytes [0, 8 n_q)) on `stream`; the bf16
+ *     tensor-core kernel writes every part of the array it reads and needs
+ *     nothing cleared.
  * Errors as smla_decode, plus SMLA_ERR_DEVICE when the set-up fails. */
 int smla_decode_noalloc(const smla_decode_params* params, void* stream);
 
@@ -286,6 +289,20 @@ const char* smla_strerror(int status);
 
 /* SMLA_OK when the current CUDA device can run the kernels (sm_103). */
 int smla_device_check(void);
+
+/* Limit, in ns, of every in-kernel pipeline wait of the tensor-core kernels
+ * launched after this call on the current device (process-wide); 0 restores
+ * the default of 2 s.  A wait that runs out sets SMLA_STATUS_TIMEOUT: the CTA
+ * then skips its remaining waits, still issues its pending copies and MMAs,
+ * waits (2 s at most each) until they have completed, frees its tensor memory
+ * and exits, so that the CUDA context stays usable.  out, lse, n_valid and the
+ * workspace are then undefined (re-zero the ticket region before the next
+ * call).  stall_first_wait = 1 makes the first softmax wait of every CTA wait
+ * on a barrier that nothing signals, so that it runs out after the limit: a
+ * test of that path, with no fault and no hang; 0 for normal operation.
+ * Returns SMLA_ERR_DEVICE off sm_103, SMLA_ERR_LAUNCH when the values cannot
+ * be set. */
+int smla_set_wait_limit(uint64_t limit_ns, int stall_first_wait);
 
 #ifdef __cplusplus
 }

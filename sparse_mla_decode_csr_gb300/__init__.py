@@ -80,6 +80,7 @@ class PlanInfo(ctypes.Structure):
         ("partial_slots", ctypes.c_int32),
         ("merge_kernel", ctypes.c_int32),
         ("trim_kernel", ctypes.c_int32),
+        ("head_groups", ctypes.c_int32),
         ("workspace_bytes", ctypes.c_int64),
     ]
 
@@ -106,13 +107,15 @@ def _load():
     lib.smla_strerror.restype = ctypes.c_char_p
     lib.smla_device_check.argtypes = []
     lib.smla_device_check.restype = ctypes.c_int
+    lib.smla_set_wait_limit.argtypes = [ctypes.c_uint64, ctypes.c_int]
+    lib.smla_set_wait_limit.restype = ctypes.c_int
     return lib
 
 
 lib = _load()
 
 EXPORTED_SYMBOLS = ("smla_plan", "smla_decode_workspace_size", "smla_decode", "smla_decode_noalloc",
-                    "smla_pack_records", "smla_strerror", "smla_device_check")
+                    "smla_pack_records", "smla_strerror", "smla_device_check", "smla_set_wait_limit")
 
 
 def strerror(code: int) -> str:
@@ -179,7 +182,7 @@ def workspace(nbytes: int, device, layout=None) -> Optional[torch.Tensor]:
         ws = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=dev)
     elif layout != last:
         n_q = layout[0] if layout else ws.numel() // 4
-        ws[: min(ws.numel(), 4 * n_q + 256)].zero_()
+        ws[: min(ws.numel(), 8 * n_q + 256)].zero_()
     _WS[key] = (ws, layout)
     return ws
 
@@ -287,3 +290,11 @@ def smla_pack_records(latent: torch.Tensor, rope: torch.Tensor, kv_out: torch.Te
 
 def smla_device_check() -> int:
     return int(lib.smla_device_check())
+
+
+def smla_set_wait_limit(limit_ns: int, stall_first_wait: bool = False) -> None:
+    """Limit of every in-kernel pipeline wait (0: the 2 s default), and the
+    timeout-path test switch; see smla.h."""
+    rc = lib.smla_set_wait_limit(int(limit_ns), int(bool(stall_first_wait)))
+    if rc != 0:
+        raise SmlaError(rc, "smla_set_wait_limit")

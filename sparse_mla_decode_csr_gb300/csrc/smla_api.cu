@@ -50,7 +50,7 @@ WorkspaceLayout workspace_layout(int32_t n_q, int32_t heads, int32_t slots, bool
   if (slots <= 0 && !trim_lens) return w;
   int64_t off = 0;
   w.ticket_off = off;
-  off = align256(off + int64_t(n_q) * 4);
+  off = align256(off + int64_t(n_q) * 2 * 4);  // per row and head group
   w.rowtile_off = off;
   off = align256(off + (int64_t(n_q) + 1) * 8);
   w.o_off = off;
@@ -125,6 +125,15 @@ int smla_device_check(void) {
   return (major == 10 && minor == 3) ? SMLA_OK : SMLA_ERR_DEVICE;
 }
 
+int smla_set_wait_limit(uint64_t limit_ns, int stall_first_wait) {
+  const int rc = smla_device_check();
+  if (rc != SMLA_OK) return rc;
+  if (smla::fp8_set_wait_limit(limit_ns, stall_first_wait) != cudaSuccess ||
+      smla::tc_set_wait_limit(limit_ns, stall_first_wait) != cudaSuccess)
+    return SMLA_ERR_LAUNCH;
+  return SMLA_OK;
+}
+
 int smla_plan(const smla_decode_params* p, int32_t num_sms, smla_plan_info* plan) {
   if (plan == nullptr || p == nullptr) return SMLA_ERR_NULL;
   const int32_t n_q = p->n_q, num_heads = p->num_heads, num_splits = p->num_splits;
@@ -146,17 +155,28 @@ int smla_plan(const smla_decode_params* p, int32_t num_sms, smla_plan_info* plan
     kernel = fp8_kernel_supports(num_heads) ? SMLA_KERNEL_TENSOR_CORE_FP8 : SMLA_KERNEL_TENSOR_CORE_BF16;
   plan->kernel = kernel;
   plan->tile_len = kernel == SMLA_KERNEL_TENSOR_CORE_FP8 ? fp8_tile_len() : kTile;
+  plan->head_groups = 1;
   if (kernel != SMLA_KERNEL_CUDA_CORE) {
     // persistent: one CTA per SM, tiles balanced over them; forcing k splits
-    // spreads the tiles over n_q * k CTAs instead
-    int64_t g = num_splits > 0 ? int64_t(n_q) * num_splits : num_sms;
-    g = std::max<int64_t>(1, std::min<int64_t>(g, 65535));
+    // spreads the tiles over n_q * k CTAs instead.  The native-fp8 kernel
+    // takes up to 32 heads per CTA: above that two CTAs (head groups) share
+    // each schedule range, and the grid counts ranges
+    const int hg = kernel == SMLA_KERNEL_TENSOR_CORE_FP8 ? fp8_head_groups(num_heads) : 1;
+    plan->head_groups = hg;
+    int64_t g = num_splits > 0 ? int64_t(n_q) * num_splits : std::max(1, num_sms / hg);
+    g = std::max<int64_t>(1, std::min<int64_t>(g, 65535 / hg));
     plan->grid = n_q > 0 ? int32_t(g) : 0;
     plan->num_splits = 0;
     plan->chunk_len = 0;
     plan->partial_slots = 2 * plan->grid;
-    // rows shared between CTAs are merged by a second, parallel kernel
-    plan->merge_kernel = (n_q > 0 && plan->grid > 1) ? 1 : 0;
+    // rows shared between CTAs are merged by a second, parallel kernel; the
+    // native-fp8 kernel merges rows of up to kMaxInKernelParts parts itself,
+    // and needs the merge kernel only when rows of the top-k length would span
+    // more CTAs (about grid / n_q + 1 each); it then merges only those rows
+    if (kernel == SMLA_KERNEL_TENSOR_CORE_FP8)
+      plan->merge_kernel = (n_q > 0 && (int64_t(plan->grid) + n_q - 1) / n_q + 1 > kMaxInKernelParts) ? 1 : 0;
+    else
+      plan->merge_kernel = (n_q > 0 && plan->grid > 1) ? 1 : 0;
     // rows that may end in -1 padding are trimmed first by a row-per-warp pass
     plan->trim_kernel = (n_q > 0 && p->has_invalid) ? 1 : 0;
     plan->workspace_bytes =

@@ -21,16 +21,17 @@
 //        P' carries ~8 significant bits (as a bf16 P would) down to 2^-18 of
 //        the tile's largest term.  O = O_hi + O_lo.
 //
-// Warp roles (16 warps, 512 threads, one CTA per SM):
-//   0-3   softmax (warp q owns the keys of TMEM lane quarter q of S)
+// Warp roles (20 warps, 640 threads, one CTA per SM):
+//   0-3   softmax (warp q owns the keys of TMEM lane quarter q of S; all the
+//         CTA's heads, 16 at a time; per-head values live one per lane)
 //   4-7   aux: E8M0 scale factors of each landed tile into TMEM, q staging
 //         (hi/lo split and its scale factors) per row part, and each row
 //         part's epilogue (out / lse or a partial of a shared row)
-//   8     QK issuer (16 block-scaled K-steps and 4 bf16 rope K-steps, one
-//         accumulator), 9 PV issuer (dim blocks one after another: a thread
-//         issues one MMA every ~130 cycles into one accumulator and slower
-//         when consecutive MMAs alternate accumulators)
-//   10-15 loaders: keys lw, lw + 6, ... of every 128-key tile (64-bit record
+//   8-9   QK issuers (16 heads: the K-steps split over two accumulators so
+//         that two MMA chains are in flight; a thread issues one MMA every
+//         ~120 cycles, two threads one every ~60), 10-11 PV issuers (dim
+//         blocks 0-1 and 2-3)
+//   12-19 loaders: keys lw, lw + 8, ... of every 128-key tile (64-bit record
 //         addressing, masked keys zero-filled, out-of-range entries flagged)
 //
 // The schedule is that of the bf16 tensor-core kernel with 128-key tiles: rows
@@ -49,82 +50,149 @@
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
+#include <cstddef>
 #include <cstdint>
 
 #include "smla_device.cuh"
 #include "smla_internal.h"
 #include "smla_ptx.cuh"
 
+#ifdef SMLA_TRACE
+// Optional stage trace (compile with -DSMLA_TRACE): lane 0 of each warp writes
+// (%globaltimer ns | tag << 48 | tile << 56) into
+// g_smla_trace_fp8[(cta * 20 + warp) * 256 + k].  Off in normal builds.
+__device__ unsigned long long* g_smla_trace_fp8;
+extern "C" int smla_trace_fp8_set(void* buf) {
+  unsigned long long* p = static_cast<unsigned long long*>(buf);
+  return int(cudaMemcpyToSymbol(g_smla_trace_fp8, &p, sizeof(p)));
+}
+#define F8_TR(tag, tile)                                                                                  \
+  do {                                                                                                    \
+    if (tr_buf != nullptr && (threadIdx.x & 31) == 0 && tr_k < 256)                                       \
+      tr_buf[(size_t(blockIdx.x) * 20 + (threadIdx.x >> 5)) * 256 + tr_k] =                               \
+          (smla::ptx::globaltimer() & 0xFFFFFFFFFFFFull) | (uint64_t((tag) & 0xFF) << 48) |                \
+          (uint64_t((tile) & 0xFF) << 56);                                                                 \
+    ++tr_k;                                                                                               \
+  } while (0)
+#else
+#define F8_TR(tag, tile) ((void)0)
+#endif
+
 namespace smla {
+
+// Limit of every pipeline wait in ns (0: kWaitLimitNs), and whether the first
+// softmax wait of each CTA waits on a barrier nothing signals (so that it runs
+// out: a test of the timeout path); read at kernel start.
+__device__ uint64_t g_fp8_wait_ns;
+__device__ int32_t g_fp8_stall;
+
 namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 640;
 constexpr int kTK = 128;        // keys per tile (M of QK)
-constexpr int kHP = 16;         // padded heads
-constexpr int kN = 2 * kHP;     // N of QK and PV: hi columns, then lo columns
 constexpr int kStages = 2;
-constexpr int kSoftmaxWarps = 4;
+constexpr int kSoftmaxWarps = 4;   // one per TMEM lane quarter
 constexpr int kAuxWarp0 = 4;
-constexpr int kQkWarp0 = 8;
-constexpr int kPvWarp0 = 9;
-constexpr int kLoadWarp0 = 10;
-constexpr int kLoadWarps = 6;
-constexpr int kKeysPerLoader = (kTK + kLoadWarps - 1) / kLoadWarps;  // 22 (keys lw, lw + 6, ...)
+constexpr int kQkWarp0 = 8;        // QK issuers
+constexpr int kPvWarp0 = 10;       // two PV issuers (dim blocks 0-1 and 2-3)
+constexpr int kLoadWarp0 = 12;
+constexpr int kLoadWarps = 8;
+constexpr int kKeysPerLoader = kTK / kLoadWarps;  // 16 (keys lw, lw + 8, ...)
 constexpr int kRowStart = 2;                      // schedule slots charged for starting a row
 constexpr float kLazy = 16.f;                     // reference max moves when passed by > 2^16
 constexpr float kInitMax = -1.0e30f;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait (default) and per MMA drain
+constexpr int kMaxHP = 32;
 
-// ---- shared memory (bytes from a 1024-aligned base) ----
+// ---- shared memory of a stage (bytes from a 1024-aligned base) ----
 constexpr int kChunk = kTK * 128;                       // one 128-byte column block of a tile (16 KB)
-constexpr int kOffRope = 4 * kChunk;
+constexpr int kOffRope = 4 * kChunk;                    // rope rows; P' of the tile once QK is done
 constexpr int kOffSc = 5 * kChunk;                      // scales: kTK x 16 B
 constexpr int kOffIds = kOffSc + kTK * 16;              // record ids (or -1): kTK x 4 B
 constexpr int kStageBytes = (kOffIds + kTK * 4 + 1023) / 1024 * 1024;
-constexpr int kQLatChunk = kN * 128;                    // one K-chunk of [q_hi | q_lo] (4 KB)
-constexpr int kQOffRope = 4 * kQLatChunk;
-constexpr int kQBytes = (kQOffRope + kHP * 128 + 1023) / 1024 * 1024;
-constexpr int kOffQ = kStages * kStageBytes;
-constexpr int kPBlock = 32 * kN;                        // P' of one 32-key chunk and dim block (1 KB)
-constexpr int kOffP = kOffQ + 2 * kQBytes;
-constexpr int kOffBar = kOffP + 16 * kPBlock;
-constexpr int kNumBars = 32;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;
 
-// ---- TMEM columns ----
-constexpr uint32_t kColS = 0;      // S: [buffer] x kN
-constexpr uint32_t kColO = 128;    // O: [buffer][block] x kN
-constexpr uint32_t kColSfa = 384;  // record scale factors: [stage] x 16
-constexpr uint32_t kColSfq = 416;  // q scale factors: [q buffer] x 16
-constexpr uint32_t kColSfv = 448;  // V^T scale factors (all 1; 16 columns written, 4 read)
-constexpr uint32_t kColSfp = 464;  // P' scale factors (byte b: dim block b)
-constexpr uint32_t kTmemCols = 512;
-
-__host__ __device__ constexpr uint32_t s_col(int sb) { return kColS + uint32_t(sb) * kN; }
-__host__ __device__ constexpr uint32_t o_col(int ob, int b) { return kColO + uint32_t(4 * ob + b) * kN; }
+// Layout of the kernel for HP padded heads per CTA (16 or 32).
+//   S columns  [hi heads 0..HP-1 | lo heads 0..HP-1] (QK's N order: q rows the same)
+//   O columns  per 128-dim block: [hi g0 | lo g0 | hi g1 | lo g1], g = 16-head group
+//              (PV's N order: the P' rows the same), so that a 32-row group of
+//              P' scale factors holds one head group
+template <int HP>
+struct Cfg {
+  static constexpr int kN = 2 * HP;                     // N of QK and of PV
+  static constexpr int kPass = HP / 16;                 // 16-head groups
+  static constexpr int kQkSplit = HP == 16 ? 2 : 1;     // QK accumulators, one issuer each
+  static constexpr int kQkSteps0 = kQkSplit == 2 ? 6 : 16;  // latent K-steps of issuer 0 (it also issues the rope)
+  static constexpr int kNQ = HP == 16 ? 2 : 1;          // q buffers
+  static constexpr int kNO = HP == 16 ? 2 : 1;          // O buffers in TMEM
+  static constexpr int kQLatChunk = kN * 128;           // one K-chunk of [q_hi | q_lo]
+  static constexpr int kQOffRope = 4 * kQLatChunk;
+  static constexpr int kQBytes = (kQOffRope + HP * 128 + 1023) / 1024 * 1024;
+  static constexpr int kPBlock = 32 * kN;               // P' of one 32-key chunk and dim block
+  // P' of a tile: 16 blocks [chunk][dim block]; the first 16 KB sit in the
+  // stage's rope rows (free once the tile's QK is done), the rest (32 heads)
+  // in one extra buffer shared by both stages
+  static constexpr int kPInRope = kChunk / kPBlock;     // blocks in the rope rows (16 or 8)
+  static constexpr int kPExtra = 16 * kPBlock - kChunk; // 0 or 16 KB
+  static constexpr int kOffQ = kStages * kStageBytes;
+  static constexpr int kOffPx = kOffQ + kNQ * kQBytes;
+  static constexpr int kOffBar = kOffPx + kPExtra;
+  static constexpr int kOffMisc = kOffBar + 32 * 8;
+  static constexpr Swizzle kPSw = kN == 32 ? kSw32 : kSw64;
+  static constexpr uint32_t kPSwMask = kN / 16 - 1;
+  // TMEM columns
+  static constexpr uint32_t kColS = 0;                            // [buffer][accumulator] x kN
+  static constexpr uint32_t kColO = 2 * kQkSplit * kN;            // [buffer][block] x kN
+  static constexpr uint32_t kColSfa = kColO + kNO * 4 * kN;       // record scale factors [stage] x 16
+  static constexpr uint32_t kColSfq = kColSfa + 32;               // q scale factors [q buffer] x 16
+  static constexpr uint32_t kColSfv = kColSfq + 16 * kNQ;         // V^T scale factors (all 1)
+  static constexpr uint32_t kColSfp = kColSfv + 16;               // P' scale factors [stage] x 4: head group
+  // scale-factor addresses of an MMA start on a multiple of 4 columns (the
+  // 32x128b layout of a 128-row block spans 4 columns)
+  __host__ __device__ static constexpr uint32_t sfp_col(int s) { return kColSfp + 4u * uint32_t(s); }
+  static_assert(kColSfa % 16 == 0 && kColSfq % 16 == 0 && kColSfv % 16 == 0 && kColSfp % 4 == 0, "SF columns");
+  static_assert(kColSfp + 8 <= 512, "TMEM columns");
+  __host__ __device__ static constexpr uint32_t s_col(int sb, int acc = 0) {
+    return kColS + uint32_t(sb * kQkSplit + acc) * kN;
+  }
+  __host__ __device__ static constexpr uint32_t o_col(int ob, int b) { return kColO + uint32_t(4 * ob + b) * kN; }
+};
 
 struct Misc {
   uint32_t tmem_base;
   int32_t abort;
+  uint64_t wait_ns;  // limit of a pipeline wait
+  int32_t stall;     // first softmax wait on kStall (never signalled)
   int32_t first_row;
   int32_t n_tiles;
   int64_t first_tile;
   int64_t total_tiles;
   int64_t scan[64];
-  int32_t red_max_t[2][kHP][kSoftmaxWarps];  // tile maxima per head and warp (order-preserving ints)
-  int32_t red_sc[2][kSoftmaxWarps][4];     // largest biased exponent of each block's scale per warp
-  float red_l[kSoftmaxWarps][kHP];
-  int32_t red_nv[kSoftmaxWarps];
-  float part_m[2][kHP];                 // per O buffer: a finished row part's (m, l, count)
-  float part_l[2][kHP];
+  alignas(16) int32_t red_max_t[2][kMaxHP][4];  // tile maxima per head and lane quarter (order-preserving ints; read as one 16-byte word)
+  int32_t red_sc[2][4][4];          // largest biased exponent of each block's scale per lane quarter
+  float red_l[4][kMaxHP];
+  int32_t red_nv[4];
+  float part_m[2][kMaxHP];                      // per O buffer: a finished row part's (m, l, count)
+  float part_l[2][kMaxHP];
   int32_t part_nv[2];
-  uint8_t sfq[kN][16];                  // q scale-factor bytes of the part being staged
+  uint8_t sfq[2 * kMaxHP][16];                  // q scale-factor bytes of the part being staged
+  float fac[kMaxHP];                            // epilogue: output factors of a whole row's heads
+  int32_t n_merge;                              // rows this CTA completes and merges at its end
+  int32_t merge_row[2];
+  int32_t merge_nt[2];
+  int32_t merge_parts[2];
+  int64_t merge_P[2];
+  int64_t merge_ca[2];
+  int64_t merge_cz[2];
+  int64_t merge_slot[2][kMaxInKernelParts];
 };
-constexpr int kSmemUsed = kOffMisc + int(sizeof(Misc));
-constexpr int kSmemTotal = kSmemUsed + 1024;  // slack to align the base
-static_assert(kSmemTotal <= 232448, "shared memory over the per-block limit");
+// (the 16-byte reads of red_max_t rows and 4-byte reads of sfq rows need these)
+static_assert(offsetof(Misc, red_max_t) % 16 == 0 && offsetof(Misc, sfq) % 4 == 0, "Misc layout");
+static_assert(Cfg<16>::kOffMisc % 16 == 0 && Cfg<32>::kOffMisc % 16 == 0, "Misc alignment");
+template <int HP>
+constexpr int smem_total() { return Cfg<HP>::kOffMisc + int(sizeof(Misc)) + 1024; }  // + slack to align the base
+static_assert(smem_total<16>() <= 232448 && smem_total<32>() <= 232448, "shared memory over the per-block limit");
 
 enum Bar {
   kKvFull = 0,    // [2] loaders -> aux (tile landed)
@@ -138,7 +206,9 @@ enum Bar {
   kQEmpty = 14,   // [2] QK issuers -> aux
   kOFull = 16,    // [2] PV issuers -> aux (a part's O complete)
   kOEmpty = 18,   // [2] aux -> PV issuers and softmax (O buffer read out)
-  kEpiReady = 20  // [2] softmax -> aux (a part's m, l, count posted)
+  kEpiReady = 20, // [2] softmax -> aux (a part's m, l, count posted)
+  kDrain = 22,    // MMA issuers: every MMA they issued has completed
+  kStall = 23     // never signalled (timeout-path test)
 };
 
 __device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t chunk16) {
@@ -156,12 +226,61 @@ __device__ __forceinline__ float pow2f(int e) {  // 2^e for -126 <= e <= 127
   return __int_as_float((e + 127) << 23);
 }
 
-// hi = E4M3(x), lo = E4M3(x - hi) for a pair (round to nearest even, saturating)
+// hi = E4M3(y), lo = E4M3(y - hi) for an f16 pair (round to nearest even,
+// saturating); y - hi is exact in f16 (hi is within a factor 2 of y)
+__device__ __forceinline__ void split_h2(uint32_t y, uint16_t& hi, uint16_t& lo) {
+  __half2_raw yr;
+  yr.x = uint16_t(y & 0xFFFFu);
+  yr.y = uint16_t(y >> 16);
+  hi = __nv_cvt_halfraw2_to_fp8x2(yr, __NV_SATFINITE, __NV_E4M3);
+  const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3);
+  const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&yr), *reinterpret_cast<const __half2*>(&hr));
+  lo = __nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&r), __NV_SATFINITE, __NV_E4M3);
+}
+
+// Four E4M3 codes of non-negative values (bytes < 0x80) -> the codes of the
+// values times 2^-m (0 <= m <= 16): exponent fields lowered by m, and 0 for a
+// value whose exponent field is <= m (it would leave the normal range).
+__device__ __forceinline__ uint32_t lower_codes(uint32_t x, int m) {
+  if (m == 0) return x;
+  if (m >= 15) return 0u;                                     // exponent fields are at most 15
+  const uint32_t t = uint32_t(8 * (m + 1)) * 0x01010101u;     // byte >= 8 (m + 1) <=> exponent field > m
+  const uint32_t d = (x | 0x80808080u) - t;                   // bit 7 of a byte: byte >= t (no borrow)
+  const uint32_t keep = ((d & 0x80808080u) >> 7) * 0xFFu;
+  return (x & keep) - ((uint32_t(8 * m) * 0x01010101u) & keep);
+}
+
+// The same for an f32 pair (q staging: full f32 precision into the split)
 __device__ __forceinline__ void split_pair(float x0, float x1, uint16_t& hi, uint16_t& lo) {
   hi = __nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3);
   const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3);
   const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hr));
   lo = __nv_cvt_float2_to_fp8x2(make_float2(x0 - hf.x, x1 - hf.y), __NV_SATFINITE, __NV_E4M3);
+}
+
+// Sum over the 32 lanes of v[h] for 16 heads at once: each halving step keeps
+// half of the heads and adds the partner's copy of them, so that lane L ends
+// with the total of head (L >> 1) & 15 (16 shuffles instead of 80).
+__device__ __forceinline__ float sum16(const float (&v)[16], int lane) {
+  float w8[8], w4[4], w2[2];
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float keep = b4 ? v[8 + j] : v[j], give = b4 ? v[j] : v[8 + j];
+    w8[j] = keep + __shfl_xor_sync(0xffffffffu, give, 16);
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float keep = b3 ? w8[4 + j] : w8[j], give = b3 ? w8[j] : w8[4 + j];
+    w4[j] = keep + __shfl_xor_sync(0xffffffffu, give, 8);
+  }
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const float keep = b2 ? w4[2 + j] : w4[j], give = b2 ? w4[j] : w4[2 + j];
+    w2[j] = keep + __shfl_xor_sync(0xffffffffu, give, 4);
+  }
+  float w = (b1 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? w2[0] : w2[1], 2);
+  return w + __shfl_xor_sync(0xffffffffu, w, 1);
 }
 
 struct Cursor {
@@ -208,18 +327,23 @@ struct Cursor {
   __device__ __forceinline__ int32_t p1() const { return min(t * kTK + kTK, len); }
 };
 
-__device__ __forceinline__ void set_abort(Misc* ms, const DecodeArgs& a) {
-  if (atomicExch(&ms->abort, 1) == 0 && a.status) atomicOr(a.status, SMLA_STATUS_TIMEOUT);
+__device__ __forceinline__ void set_abort(Misc* ms, int32_t* status) {
+  if (atomicExch(&ms->abort, 1) == 0 && status) atomicOr(status, SMLA_STATUS_TIMEOUT);
 }
 
 // A bounded pipeline wait; after any timeout every later wait returns false
 // at once so that all roles reach the teardown.  Loops holding named barriers
 // keep iterating after a failed wait (same barrier sequence in every thread).
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Misc* ms, const DecodeArgs& a) {
+// The polling loop is out of line: one copy of it in the kernel's code.
+__device__ __noinline__ bool wait_bar_slow(uint64_t* bar, uint32_t parity, Misc* ms, int32_t* status) {
   if (*reinterpret_cast<volatile int32_t*>(&ms->abort)) return false;
-  if (mbar_wait(bar, parity, kWaitLimitNs)) return true;
-  set_abort(ms, a);
+  if (mbar_wait(bar, parity, ms->wait_ns)) return true;
+  set_abort(ms, status);
   return false;
+}
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Misc* ms, const DecodeArgs& a) {
+  if (mbar_try_wait(bar, parity) && !*reinterpret_cast<volatile int32_t*>(&ms->abort)) return true;
+  return wait_bar_slow(bar, parity, ms, a.status);
 }
 __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, Misc* ms, const DecodeArgs& a) {
   return __all_sync(0xffffffffu, wait_bar(bar, parity, ms, a));
@@ -230,38 +354,352 @@ __device__ __forceinline__ int64_t slot_of(int64_t c, int64_t P, int64_t T, int6
   return 2 * c + (P < cta_begin(c, T, G) ? 0 : 1);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(DecodeArgs a) {
+// What the aux warps' out-of-line steps need from the kernel.
+struct AuxCtx {
+  const DecodeArgs* a;
+  uint8_t* smem;
+  Misc* ms;
+  uint64_t* bars;
+  uint32_t tmem, lane_base;
+  int H, h0, Hl, hg, g, lane, ta;
+  int64_t c_id, G, T;
+};
+
+// q of a row -> [q_hi | q_lo] E4M3 (K-major, 128-byte swizzled) with an E8M0
+// factor per (head, 32 dims) that brings the block's largest |q| to
+// [2^7, 2^8); q_rope (bf16) copied as it is; then the factors into TMEM.
+// Run by the four aux warps (out of line: one copy of its code).
+template <int HP>
+__device__ __noinline__ void aux_stage_q(const AuxCtx& x, int row, int qb) {
+  const DecodeArgs& a = *x.a;
+  using C = Cfg<HP>;
+  constexpr int kN = C::kN;
+  uint8_t* smem = x.smem;
+  Misc* ms = x.ms;
+  uint64_t* bars = x.bars;
+  const uint32_t tmem = x.tmem, lane_base = x.lane_base;
+  const int H = x.H, h0 = x.h0, Hl = x.Hl, hg = x.hg, g = x.g, lane = x.lane, ta = x.ta;
+  const int64_t c_id = x.c_id, G = x.G, T = x.T;
+  (void)kN; (void)hg; (void)g; (void)c_id; (void)G; (void)T; (void)h0; (void)H;
+      uint8_t* qs = smem + C::kOffQ + qb * C::kQBytes;
+#pragma unroll 1
+    for (int blk = ta; blk < HP * 16; blk += 128) {
+      const int h = blk >> 4, kb = blk & 15;
+      uint32_t hw[8], lw[8];
+      int sfb = 127;
+      if (h < Hl) {
+        const uint4* src =
+            reinterpret_cast<const uint4*>(a.q + row * a.q_stride_row + (h0 + h) * a.q_stride_head + 32 * kb);
+        uint4 v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[k] = __ldg(src + k);
+        float f[32];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            f[8 * k + 2 * j] = __uint_as_float(w[j] << 16);
+            f[8 * k + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+          }
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) amax = fmaxf(amax, fabsf(f[k]));
+        int e = amax > 0.f ? int((__float_as_uint(amax) >> 23) & 0xFF) - 127 - 7 : 0;
+        e = max(min(e, 120), -120);
+        sfb = e + 127;
+        const float inv = pow2f(-e);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          uint16_t h2, l2;
+          split_pair(f[2 * k] * inv, f[2 * k + 1] * inv, h2, l2);
+          if (k & 1) {
+            hw[k >> 1] |= uint32_t(h2) << 16;
+            lw[k >> 1] |= uint32_t(l2) << 16;
+          } else {
+            hw[k >> 1] = h2;
+            lw[k >> 1] = l2;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) hw[k] = lw[k] = 0u;
+      }
+      const int kc = kb >> 2, c0 = 2 * (kb & 3);
+      uint8_t* base = qs + kc * C::kQLatChunk;
+      *reinterpret_cast<uint4*>(base + sw128(h, c0)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *reinterpret_cast<uint4*>(base + sw128(h, c0 + 1)) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+      *reinterpret_cast<uint4*>(base + sw128(HP + h, c0)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      *reinterpret_cast<uint4*>(base + sw128(HP + h, c0 + 1)) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+      ms->sfq[h][kb] = uint8_t(sfb);
+      ms->sfq[HP + h][kb] = uint8_t(sfb);
+    }
+#pragma unroll 1
+    for (int k = ta; k < HP * 8; k += 128) {  // rope: HP rows x 128 bytes, 16-byte chunks
+      const int h = k >> 3, c16 = k & 7;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (h < Hl)
+        v = __ldg(reinterpret_cast<const uint4*>(a.q + row * a.q_stride_row + (h0 + h) * a.q_stride_head +
+                                                 kLatent + 8 * c16));
+      *reinterpret_cast<uint4*>(qs + C::kQOffRope + sw128(h, c16)) = v;
+    }
+    named_barrier(2, 128);
+    {
+      // q factors: B row n = 32 j + lane in column 4 g + j of K-block group
+      // g, byte k = K-block 4 g + k; unused columns hold 1
+      uint32_t v[16];
+#pragma unroll
+      for (int gk = 0; gk < 4; ++gk)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          v[4 * gk + j] = j < kN / 32 ? *reinterpret_cast<const uint32_t*>(&ms->sfq[32 * j + lane][4 * gk])
+                                      : 0x7F7F7F7Fu;
+      tmem_st16(tmem + lane_base + C::kColSfq + 16 * qb, v);
+      tmem_wait_st();
+    }
+    named_barrier(2, 128);  // sfq is reused by the next staging
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars + kQFull + qb);
+  }
+
+// A row part's epilogue (aux warps): out and lse of a whole row, or the
+// part's partial (O, m, l, count) of a shared row and its ticket; the part
+// that completes a row queues the row for the merge at the CTA's end.
+template <int HP>
+__device__ __noinline__ void aux_epilogue(const AuxCtx& x, const Cursor& pc, int pi) {
+  using C = Cfg<HP>;
+  const DecodeArgs& a = *x.a;
+  Misc* ms = x.ms;
+  uint64_t* bars = x.bars;
+  const uint32_t tmem = x.tmem, lane_base = x.lane_base;
+  const int H = x.H, h0 = x.h0, Hl = x.Hl, lane = x.lane, ta = x.ta;
+  const int64_t T = x.T, G = x.G;
+  const int ob = pi % C::kNO;
+  const uint32_t ph = (pi / C::kNO) & 1;
+  wait_warp(bars + kEpiReady + ob, ph, ms, a);
+  wait_warp(bars + kOFull + ob, ph, ms, a);
+  tc_fence_after();
+  const int row = pc.row;
+  const bool whole = pc.whole();
+  const int64_t slot = whole ? 0 : slot_of(x.c_id, pc.P, T, G);
+  // head ta's output factor and LSE (whole rows), or its partial (m, l)
+  if (ta < Hl) {
+    const float m = ms->part_m[ob][ta], l = ms->part_l[ob][ta];
+    if (whole) {
+      float f, lse_h;
+      finish_head(m, l, a.sink, h0 + ta, &f, &lse_h);
+      ms->fac[ta] = f;
+      if (a.lse) a.lse[int64_t(row) * H + h0 + ta] = lse_h;
+    } else {
+      reinterpret_cast<float2*>(a.ml_part)[slot * H + h0 + ta] = make_float2(m, l);
+    }
+  }
+  if (ta == 0) {
+    if (whole) {
+      if (a.n_valid && x.g == 0) a.n_valid[row] = ms->part_nv[ob];
+    } else {
+      a.nv_part[slot] = ms->part_nv[ob];  // the same count from either head group
+    }
+  }
+  named_barrier(2, 128);  // the factors
+  // O^T rows of this thread: dim 128 b + ta of every block b; columns
+  // [hi g | lo g] per 16-head group g
+#pragma unroll 1
+  for (int k = 0; k < 4 * C::kPass; ++k) {
+    const int b = k / C::kPass, pass = k % C::kPass;
+    const int d = 128 * b + ta;
+    uint32_t v0[16], v1[16];
+    tmem_ld16(tmem + lane_base + C::o_col(ob, b) + 32 * pass, v0);       // hi
+    tmem_ld16(tmem + lane_base + C::o_col(ob, b) + 32 * pass + 16, v1);  // lo
+    tmem_wait_ld();
+    const int hn = min(16, Hl - 16 * pass);
+    if (whole) {
+      uint16_t* dst = a.out + int64_t(row) * a.out_stride_row + int64_t(h0 + 16 * pass) * a.out_stride_head + d;
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (j < hn)
+          dst[int64_t(j) * a.out_stride_head] = __bfloat16_as_ushort(
+              __float2bfloat16_rn((__uint_as_float(v0[j]) + __uint_as_float(v1[j])) * ms->fac[16 * pass + j]));
+    } else {
+      float* dst = a.o_part + (slot * H + h0 + 16 * pass) * kLatent + d;
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (j < hn) dst[int64_t(j) * kLatent] = __uint_as_float(v0[j]) + __uint_as_float(v1[j]);
+    }
+  }
+  if (!whole) __threadfence();  // the partial is visible device-wide before the ticket below
+  tc_fence_before();
+  named_barrier(2, 128);  // every aux thread read the part's (m, l) and O (and fenced its partial)
+  if (lane == 0) mbar_arrive(bars + kOEmpty + ob);
+  if (!whole && ta == 0) {
+    // the CTAs holding this row's tiles ([P2] stage_split parts); the one whose
+    // part arrives last merges the row (this head group) after its own work
+    const int64_t ca = cta_of_tile(pc.P, T, G), cz = cta_of_tile(pc.P + pc.ntiles - 1, T, G);
+    int32_t parts = 0;
+    for (int64_t cc = ca; cc <= cz; ++cc) parts += cta_begin(cc + 1, T, G) > cta_begin(cc, T, G);
+    if (parts <= kMaxInKernelParts || !a.merge_kernel) {
+      if (atomicAdd(a.ticket + int64_t(row) * x.hg + x.g, 1) == parts - 1) {
+        const int k = ms->n_merge++;
+        ms->merge_row[k] = row;
+        ms->merge_P[k] = pc.P;
+        ms->merge_nt[k] = pc.ntiles;
+        ms->merge_parts[k] = parts;
+      }
+    }
+  }
+}
+
+// [P2] stage_combine, with the sink, of the rows this CTA completed: every
+// part's (m, l) and O, out and lse of heads [h0, h0 + Hl), the key count, and
+// the row's ticket back to zero.  All threads of the CTA, after its own work.
+// Rows of up to kMaxInKernelParts parts load every part's values at once (all
+// in registers); longer rows (no merge kernel in the plan) go part by part.
+__device__ __noinline__ void end_merge(const DecodeArgs& a, Misc* ms, int tid, int h0, int Hl, int hg, int g,
+                                       int64_t T, int64_t G) {
+  const int H = a.heads;
+  const int n_merge = ms->n_merge;
+  __threadfence();  // the other parts' partials, published before their tickets
+  if (tid < n_merge) {
+    const int k = tid;
+    const int64_t P = ms->merge_P[k];
+    const int64_t ca = cta_of_tile(P, T, G), cz = cta_of_tile(P + ms->merge_nt[k] - 1, T, G);
+    int n = 0;
+    for (int64_t cc = ca; cc <= cz && n < kMaxInKernelParts; ++cc)
+      if (cta_begin(cc + 1, T, G) > cta_begin(cc, T, G)) ms->merge_slot[k][n++] = slot_of(cc, P, T, G);
+    ms->merge_ca[k] = ca;
+    ms->merge_cz[k] = cz;
+  }
+  __syncthreads();
+#pragma unroll 1
+  for (int k = 0; k < n_merge; ++k) {
+    const int row = ms->merge_row[k];
+    const int parts = ms->merge_parts[k];
+    const int64_t P = ms->merge_P[k];
+    const int64_t ca = ms->merge_ca[k], cz = ms->merge_cz[k];
+    // unit u: head h0 + u / 128 of this group, float4 column u % 128 of the 512 latent dims
+#pragma unroll 1
+    for (int u = tid; u < Hl * (kLatent / 4); u += kThreads) {
+      const int h = h0 + u / (kLatent / 4), f = u % (kLatent / 4);
+      float mrun = -INFINITY, lsum = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (parts <= kMaxInKernelParts) {
+        float2 ml[kMaxInKernelParts];
+        float4 o[kMaxInKernelParts];
+#pragma unroll
+        for (int j = 0; j < kMaxInKernelParts; ++j) {
+          ml[j] = make_float2(-INFINITY, 0.f);
+          o[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (j < parts) {
+            const int64_t sl = ms->merge_slot[k][j];
+            ml[j] = __ldcg(reinterpret_cast<const float2*>(a.ml_part) + sl * H + h);
+            o[j] = __ldcg(reinterpret_cast<const float4*>(a.o_part + (sl * H + h) * kLatent) + f);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < kMaxInKernelParts; ++j)
+          if (ml[j].y != 0.f) mrun = fmaxf(mrun, ml[j].x);  // parts without keys (l = 0) take no part
+#pragma unroll
+        for (int j = 0; j < kMaxInKernelParts; ++j) {
+          const float wt = ml[j].y != 0.f ? ex2(ml[j].x - mrun) : 0.f;  // a NaN m or l stays NaN
+          lsum = fmaf(ml[j].y, wt, lsum);
+          acc.x = fmaf(wt, o[j].x, acc.x); acc.y = fmaf(wt, o[j].y, acc.y);
+          acc.z = fmaf(wt, o[j].z, acc.z); acc.w = fmaf(wt, o[j].w, acc.w);
+        }
+      } else {
+#pragma unroll 1
+        for (int64_t cc = ca; cc <= cz; ++cc) {
+          if (!(cta_begin(cc + 1, T, G) > cta_begin(cc, T, G))) continue;
+          const int64_t sl = slot_of(cc, P, T, G);
+          const float2 mj = __ldcg(reinterpret_cast<const float2*>(a.ml_part) + sl * H + h);
+          const float4 oj = __ldcg(reinterpret_cast<const float4*>(a.o_part + (sl * H + h) * kLatent) + f);
+          if (mj.y == 0.f) continue;
+          if (mj.x > mrun) {  // the running maximum moves: rescale what was summed
+            const float r = ex2(mrun - mj.x);
+            lsum *= r;
+            acc.x *= r; acc.y *= r; acc.z *= r; acc.w *= r;
+            mrun = mj.x;
+          }
+          const float wt = ex2(mj.x - mrun);
+          lsum = fmaf(mj.y, wt, lsum);
+          acc.x = fmaf(wt, oj.x, acc.x); acc.y = fmaf(wt, oj.y, acc.y);
+          acc.z = fmaf(wt, oj.z, acc.z); acc.w = fmaf(wt, oj.w, acc.w);
+        }
+      }
+      float fac, lse_h;
+      finish_head(mrun, lsum, a.sink, h, &fac, &lse_h);
+      uint2 v;
+      v.x = pack_bf16x2(acc.x * fac, acc.y * fac);
+      v.y = pack_bf16x2(acc.z * fac, acc.w * fac);
+      *reinterpret_cast<uint2*>(a.out + int64_t(row) * a.out_stride_row + int64_t(h) * a.out_stride_head + 4 * f) = v;
+      if (f == 0 && a.lse) a.lse[int64_t(row) * H + h] = lse_h;
+    }
+    if (tid == 0) {
+      if (g == 0 && a.n_valid) {
+        int32_t nv = 0;
+        for (int64_t cc = ca; cc <= cz; ++cc)
+          if (cta_begin(cc + 1, T, G) > cta_begin(cc, T, G)) nv += __ldcg(a.nv_part + slot_of(cc, P, T, G));
+        a.n_valid[row] = nv;
+      }
+      a.ticket[int64_t(row) * hg + g] = 0;  // ready for the next call
+    }
+  }
+}
+
+template <int HP>
+__global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_constant__ DecodeArgs a) {
+  using C = Cfg<HP>;
+  constexpr int kN = C::kN;
   extern __shared__ uint8_t smem_raw[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+#ifdef SMLA_TRACE
+  unsigned long long* const tr_buf = g_smla_trace_fp8;
+  int tr_k = 0;
+#endif
+  F8_TR(1, 0);
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  Misc* ms = reinterpret_cast<Misc*>(smem + kOffMisc);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  Misc* ms = reinterpret_cast<Misc*>(smem + C::kOffMisc);
   const int H = a.heads;
-  const int64_t G = gridDim.x, c_id = blockIdx.x;
+  // head groups: CTAs 2 c and 2 c + 1 of a two-group launch take the same
+  // schedule range c, heads [0, HP) and [HP, 2 HP)
+  const int hg = a.head_groups;
+  const int g = int(blockIdx.x) % hg;
+  const int64_t G = gridDim.x / hg, c_id = blockIdx.x / hg;
+  const int h0 = g * HP;
+  const int Hl = min(HP, H - h0);  // heads of this group
 
   if (tid == 0) {
     for (int s = 0; s < 2; ++s) {
       mbar_init(bars + kKvFull + s, kLoadWarps);
-      mbar_init(bars + kKvEmpty + s, 1);
+      mbar_init(bars + kKvEmpty + s, 2);
       mbar_init(bars + kSfReady + s, 4);
-      mbar_init(bars + kSFull + s, 1);
+      mbar_init(bars + kSFull + s, Cfg<HP>::kQkSplit);
       mbar_init(bars + kSEmpty + s, kSoftmaxWarps);
       mbar_init(bars + kQFull + s, 4);
-      mbar_init(bars + kQEmpty + s, 1);
-      mbar_init(bars + kOFull + s, 1);
+      mbar_init(bars + kQEmpty + s, Cfg<HP>::kQkSplit);
+      mbar_init(bars + kOFull + s, 2);
       mbar_init(bars + kOEmpty + s, 4);
       mbar_init(bars + kEpiReady + s, kSoftmaxWarps);
     }
     mbar_init(bars + kPFull, kSoftmaxWarps);
-    mbar_init(bars + kPvDone, 1);
+    mbar_init(bars + kPvDone, 2);
+    mbar_init(bars + kDrain, Cfg<HP>::kQkSplit + 2);
+    mbar_init(bars + kStall, 1);
+    ms->stall = g_fp8_stall;
     ms->abort = 0;
+    const uint64_t w = g_fp8_wait_ns;
+    ms->wait_ns = w != 0 ? w : kWaitLimitNs;
     ms->first_row = a.n_q;
     ms->first_tile = 0;
     ms->n_tiles = 0;
+    ms->n_merge = 0;
     fence_mbar_init();
   }
   if (warp == kQkWarp0) {
-    tmem_alloc(&ms->tmem_base, kTmemCols);
+    tmem_alloc(&ms->tmem_base, 512);
     tmem_relinquish();
   }
 
@@ -308,10 +746,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(DecodeArgs a) {
       const int64_t t0 = P + kRowStart;
       const int64_t lo_t = b > t0 ? b : t0, hi_t = e < t0 + nt_r ? e : t0 + nt_r;
       if (hi_t > lo_t) mine += int32_t(hi_t - lo_t);
-      if (c_id == 0 && a.row_tile) a.row_tile[r] = P;
+      if (blockIdx.x == 0 && a.row_tile) a.row_tile[r] = P;
       P += w;
     }
-    if (c_id == 0 && tid == 0 && a.row_tile) a.row_tile[n] = Tt;
+    if (blockIdx.x == 0 && tid == 0 && a.row_tile) a.row_tile[n] = Tt;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
     if (lane == 0 && mine != 0) atomicAdd(&ms->n_tiles, mine);
@@ -326,18 +764,30 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(DecodeArgs a) {
   const int64_t P0 = ms->first_tile;
   const uint32_t tmem = ms->tmem_base;
   const uint32_t smem_base = smem_u32(smem);
+  F8_TR(2, 0);
+  // P' block (32-key chunk ch, dim block b) of the tile in stage s
+  auto p_block = [&](int s, int ch, int b) -> uint32_t {
+    const int k = 4 * ch + b;
+    return k < C::kPInRope ? uint32_t(s * kStageBytes + kOffRope + k * C::kPBlock)
+                           : uint32_t(C::kOffPx + (k - C::kPInRope) * C::kPBlock);
+  };
 
   if (warp < kSoftmaxWarps) {
     // =================== softmax ===================
-    const int q = warp;
-    const int t = 32 * q + lane;  // this thread's key row of the tile
+    const int q = warp;              // TMEM lane quarter: keys 32 q .. 32 q + 31 of a tile
+    const int t = 32 * q + lane;     // this thread's key row of the tile
+    const int hl = lane & 15;        // per-head values: lane hl (and hl + 16) holds head 16 pass + hl
     const uint32_t lane_base = uint32_t(32 * q) << 16;
-    float mref[kHP], lpart[kHP];
+    // the P' blocks of this warp's keys live in the shared extra buffer (32 heads, chunks 2, 3)
+    const bool p_shared = 4 * q >= C::kPInRope;
+    const int hs = (lane >> 1) & 15;  // head (of a pass) of this lane's sum of p (see sum16)
+    float mref[C::kPass];  // reference max of head 16 pass + hl
+    float lsum[C::kPass];  // sum of p of head 16 pass + hs over this warp's keys of the part
     int nv = 0;
 #pragma unroll
-    for (int h = 0; h < kHP; ++h) {
-      mref[h] = kInitMax;
-      lpart[h] = 0.f;
+    for (int p = 0; p < C::kPass; ++p) {
+      mref[p] = kInitMax;
+      lsum[p] = 0.f;
     }
     Cursor c;
     c.init(a, row0, P0, cb, ce);
@@ -346,183 +796,198 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(DecodeArgs a) {
       const int s = i & 1;
       const uint32_t ph = (i >> 1) & 1;
       const bool first = c.first(), last = c.last();
-      const int ob = pi & 1;
+      const int ob = pi % C::kNO;
       const uint8_t* st = smem + s * kStageBytes;
+      const int rb = i & 1;  // reduction buffer (a warp may run one tile ahead)
       if (first) {
 #pragma unroll
-        for (int h = 0; h < kHP; ++h) lpart[h] = 0.f;
+        for (int p = 0; p < C::kPass; ++p) lsum[p] = 0.f;
         nv = 0;
       }
+      if (i == 0 && ms->stall) wait_warp(bars + kStall, 0, ms, a);
       wait_warp(bars + kSFull + s, ph, ms, a);
-      tc_fence_after();
-      float x[kHP];
-      {
-        uint32_t r0[16], r1[16];
-        tmem_ld16(tmem + lane_base + s_col(s), r0);       // q_hi columns (+ rope)
-        tmem_ld16(tmem + lane_base + s_col(s) + 16, r1);  // q_lo columns
-        tmem_wait_ld();
-#pragma unroll
-        for (int h = 0; h < kHP; ++h) x[h] = __uint_as_float(r0[h]) + __uint_as_float(r1[h]);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bars + kSEmpty + s);
       wait_warp(bars + kKvFull + s, ph, ms, a);  // (already complete) orders the loaders' ids and scales
+      F8_TR(10, i);
+      tc_fence_after();
       const int32_t id = *reinterpret_cast<const int32_t*>(st + kOffIds + 4 * t);
       const bool valid = id >= 0;
       nv += valid;
-#pragma unroll
-      for (int h = 0; h < kHP; ++h) x[h] = valid ? x[h] * a.sm_scale_log2 : -INFINITY;
-      // tile maxima per head and the largest exponent of each block's scale
-      const int rb = i & 1;  // reduction buffer (a warp may run one tile ahead)
-#pragma unroll
-      for (int h = 0; h < kHP; ++h) {
-        const int32_t m = __reduce_max_sync(0xffffffffu, ord(x[h]));
-        if (lane == h) ms->red_max_t[rb][h][q] = m;
-      }
+      uint32_t sw[4];
       {
         const uint4 scw = *reinterpret_cast<const uint4*>(st + kOffSc + 16 * t);
-        const uint32_t sw[4] = {scw.x, scw.y, scw.z, scw.w};
+        sw[0] = scw.x; sw[1] = scw.y; sw[2] = scw.z; sw[3] = scw.w;
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
           const int32_t e = __reduce_max_sync(0xffffffffu, valid ? int32_t((sw[b] >> 23) & 0xFF) : 0);
           if (lane == b) ms->red_sc[rb][q][b] = e;
         }
       }
-      named_barrier(1, 32 * kSoftmaxWarps);
-      float tmax[kHP];  // the tile's maximum of each head (over all four warps)
-#pragma unroll
-      for (int h = 0; h < kHP; ++h) {
-        const int4 m4 = *reinterpret_cast<const int4*>(&ms->red_max_t[rb][h][0]);
-        tmax[h] = unord(max(max(m4.x, m4.y), max(m4.z, m4.w)));
-      }
       bool pv_waited = false;
-      if (first) {
+      int es[4];  // the tile's block-b scales < 2^es_b
 #pragma unroll
-        for (int h = 0; h < kHP; ++h) {
-          const float tm = tmax[h];
-          mref[h] = (tm > kInitMax || tm != tm) ? tm : kInitMax;  // a NaN score keeps the row NaN
-        }
-      } else {
-        bool need = false;
+      for (int pass = 0; pass < C::kPass; ++pass) {
+        // scores x = (S_hi + S_lo) sm_scale log2(e) of heads 16 pass .. + 15, -inf when masked
+        float x[16];
+        {
+          const float xs = a.sm_scale_log2;
 #pragma unroll
-        for (int h = 0; h < kHP; ++h) need |= tmax[h] > mref[h] + kLazy;
-        if (need) {  // uniform: every thread sees the same maxima
-          // O holds PV of this part's earlier tiles: wait until they completed
-          wait_warp(bars + kPvDone, (i - 1) & 1, ms, a);
-          pv_waited = true;
-          tc_fence_after();
-          float alpha[kHP];
+          for (int h = 0; h < 16; ++h) x[h] = 0.f;
 #pragma unroll
-          for (int h = 0; h < kHP; ++h) {
-            const float tm = tmax[h];
-            const float mn = tm > mref[h] + kLazy ? tm : mref[h];
-            alpha[h] = exp2f(mref[h] - mn);
-            mref[h] = mn;
-            lpart[h] *= alpha[h];
+          for (int k = 0; k < 2 * C::kQkSplit; ++k) {
+            // accumulator k / 2, q_hi columns (+ rope) then q_lo columns
+            uint32_t r[16];
+            tmem_ld16(tmem + lane_base + C::s_col(s, k >> 1) + (k & 1) * HP + 16 * pass, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int h = 0; h < 16; ++h) x[h] += __uint_as_float(r[h]);
           }
+#pragma unroll
+          for (int h = 0; h < 16; ++h) x[h] = valid ? x[h] * xs : -INFINITY;
+        }
+        if (pass == C::kPass - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bars + kSEmpty + s);  // S read
+        }
+#pragma unroll
+        for (int h = 0; h < 16; ++h) {
+          const int32_t m = __reduce_max_sync(0xffffffffu, ord(x[h]));
+          if (lane == h) ms->red_max_t[rb][16 * pass + h][q] = m;
+        }
+        named_barrier(1, 32 * kSoftmaxWarps);
+        if (pass == 0) F8_TR(11, i);
+        // the tile's maximum of head 16 pass + hl over the four lane quarters
+        float tm;
+        {
+          const uint4 m4 = ld_shared_v4(smem_u32(&ms->red_max_t[rb][16 * pass + hl][0]));
+          tm = unord(max(max(int32_t(m4.x), int32_t(m4.y)), max(int32_t(m4.z), int32_t(m4.w))));
+        }
+        float mr = mref[pass];
+        if (first) {
+          mr = (tm > kInitMax || tm != tm) ? tm : kInitMax;
+        } else if (__any_sync(0xffffffffu, tm > mr + kLazy)) {  // the same in all four warps
+          const float mn = tm > mr + kLazy ? tm : mr;
+          const float alpha = ex2(mr - mn);
+          mr = mn;
+          lsum[pass] *= __shfl_sync(0xffffffffu, alpha, hs);
+          float al[16];
+#pragma unroll
+          for (int h = 0; h < 16; ++h) al[h] = __shfl_sync(0xffffffffu, alpha, h);
+          // O holds PV of this part's earlier tiles: wait until they completed,
+          // then rescale this pass's heads (hi and lo columns) in this lane quarter
+          if (!pv_waited) {
+            wait_warp(bars + kPvDone, (i - 1) & 1, ms, a);
+            pv_waited = true;
+          }
+          tc_fence_after();
 #pragma unroll 1
-          for (int k = 0; k < 8; ++k) {  // 4 blocks x (hi, lo) column groups of 16
+          for (int k = 0; k < 8; ++k) {  // 4 blocks x (hi, lo)
+            const uint32_t ta = tmem + lane_base + C::o_col(ob, k >> 1) + uint32_t(32 * pass + 16 * (k & 1));
             uint32_t v[16];
-            const uint32_t ta = tmem + lane_base + o_col(ob, k >> 1) + 16 * (k & 1);
             tmem_ld16(ta, v);
             tmem_wait_ld();
 #pragma unroll
-            for (int h = 0; h < kHP; ++h) v[h] = __float_as_uint(__uint_as_float(v[h]) * alpha[h]);
+            for (int h = 0; h < 16; ++h) v[h] = __float_as_uint(__uint_as_float(v[h]) * al[h]);
             tmem_st16(ta, v);
           }
           tmem_wait_st();
         }
-      }
-      // p = 2^(x - mref); P'_b = p * scale_b in units of the E8M0 factor
-      // 2^E(h, b), E = e_h + es_b - 8, where pmax_h = 2^(tmax_h - mref_h) < 2^e_h
-      // and the tile's largest block-b scale < 2^es_b: P' / 2^E < 2^8 <= 448.
-      // e_h is kept >= -20 (a head whose tile terms all lie 2^20 below its
-      // reference keeps 2^-10 relative precision on them).  x becomes p 2^-e_h.
-      int e_mine = 0;  // e_h of this lane's head (lane mod kHP), for the scale factors
+        mref[pass] = mr;
+        if (pass == 0) {
+          // the shared extra P' buffer was last read by PV(i - 1)
+          if (p_shared && i > 0 && !pv_waited) {
+            wait_warp(bars + kPvDone, (i - 1) & 1, ms, a);
+            pv_waited = true;
+          }
 #pragma unroll
-      for (int h = 0; h < kHP; ++h) {
-        const float p = exp2f(x[h] - mref[h]);  // x = -inf (masked) gives 0
-        lpart[h] += p;
-        const float pmax = exp2f(tmax[h] - mref[h]);
-        int e = int((__float_as_uint(pmax) >> 23) & 0xFF) - 126;
-        e = max(min(e, 17), -20);
-        x[h] = p * pow2f(-e);
-        if ((lane & (kHP - 1)) == h) e_mine = e;
-      }
-      if (i > 0 && !pv_waited) wait_warp(bars + kPvDone, (i - 1) & 1, ms, a);  // P' buffer free
-      uint32_t sf_word = 0;
-      {
-        const int chunk = q;  // this warp's 32 keys
-        uint32_t off0 = uint32_t(lane) * kN, off1 = off0 + 16;
-        off0 ^= ((off0 >> 7) & 1u) << 4;
-        off1 ^= ((off1 >> 7) & 1u) << 4;
+          for (int b = 0; b < 4; ++b) {
+            const int32_t e = max(max(ms->red_sc[rb][0][b], ms->red_sc[rb][1][b]),
+                                  max(ms->red_sc[rb][2][b], ms->red_sc[rb][3][b]));
+            es[b] = max(e, 1) - 126;
+          }
+        }
+        // p = 2^(x - mref).  P'_b = p * scale_b in units of the E8M0 factor
+        // 2^E(h, b), E = e_h - 7 + (the tile's largest block-b scale exponent),
+        // where pmax_h = 2^(tmax_h - mref_h) < 2^e_h: P'_b < 2^7.  It is formed
+        // as p'' = p 2^(7 - e_h) split once into E4M3 hi + lo codes, then, per
+        // block, the codes' exponent fields lowered by the key's distance m_b
+        // to the tile's largest block-b scale (exact for the writer's power-of-
+        // two scales; a value leaving E4M3's normal range becomes 0).  e_h is
+        // kept in [-20, 17] (a head whose tile terms all lie 2^20 below its
+        // reference keeps 2^-10 relative precision on them).
+        const int e_h = max(min(int((__float_as_uint(ex2(tm - mr)) >> 23) & 0xFF) - 126, 17), -20);
+        const float inv_h = pow2f(7 - e_h);
+#pragma unroll
+        for (int h = 0; h < 16; ++h) x[h] = ex2(x[h] - __shfl_sync(0xffffffffu, mr, h));  // x = -inf (masked) gives 0
+        lsum[pass] += sum16(x, lane);
+        uint32_t hw0[4], lw0[4];  // codes of heads 4k .. 4k + 3
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          uint16_t h0_, l0_, h1_, l1_;
+          const __half2 y0 = __floats2half2_rn(x[4 * k] * __shfl_sync(0xffffffffu, inv_h, 4 * k),
+                                               x[4 * k + 1] * __shfl_sync(0xffffffffu, inv_h, 4 * k + 1));
+          const __half2 y1 = __floats2half2_rn(x[4 * k + 2] * __shfl_sync(0xffffffffu, inv_h, 4 * k + 2),
+                                               x[4 * k + 3] * __shfl_sync(0xffffffffu, inv_h, 4 * k + 3));
+          split_h2(*reinterpret_cast<const uint32_t*>(&y0), h0_, l0_);
+          split_h2(*reinterpret_cast<const uint32_t*>(&y1), h1_, l1_);
+          hw0[k] = uint32_t(h0_) | (uint32_t(h1_) << 16);
+          lw0[k] = uint32_t(l0_) | (uint32_t(l1_) << 16);
+        }
 #pragma unroll 1
         for (int b = 0; b < 4; ++b) {
-          int32_t esb = ms->red_sc[rb][0][b];
-#pragma unroll
-          for (int w = 1; w < kSoftmaxWarps; ++w) esb = max(esb, ms->red_sc[rb][w][b]);
-          const int es = max(esb, 1) - 126;  // the tile's block-b scales < 2^es
-          sf_word |= uint32_t(min(max(e_mine + es - 8 + 127, 1), 254)) << (8 * b);
-          const uint32_t scale_b = *reinterpret_cast<const uint32_t*>(st + kOffSc + 16 * t + 4 * b);
-          const float sn = __uint_as_float(scale_b) * pow2f(min(max(8 - es, -126), 127));  // scale_b 2^(8 - es)
+          // (selects, not indexing: a rolled loop would put sw and es in local memory)
+          const uint32_t swb = b == 0 ? sw[0] : b == 1 ? sw[1] : b == 2 ? sw[2] : sw[3];
+          const int esb = b == 0 ? es[0] : b == 1 ? es[1] : b == 2 ? es[2] : es[3];
+          const int bexp = int((swb >> 23) & 0xFF);  // a zero (or f32-subnormal) scale gives 0
+          const int m = bexp == 0 ? 16 : min(max(esb + 126 - bexp, 0), 16);
           uint32_t hw[4], lw[4];
 #pragma unroll
-          for (int k = 0; k < kHP / 2; ++k) {
-            uint16_t h2, l2;
-            split_pair(x[2 * k] * sn, x[2 * k + 1] * sn, h2, l2);
-            if (k & 1) {
-              hw[k >> 1] |= uint32_t(h2) << 16;
-              lw[k >> 1] |= uint32_t(l2) << 16;
-            } else {
-              hw[k >> 1] = h2;
-              lw[k >> 1] = l2;
-            }
+          for (int k = 0; k < 4; ++k) {
+            hw[k] = lower_codes(hw0[k], m);
+            lw[k] = lower_codes(lw0[k], m);
           }
-          uint8_t* blk = smem + kOffP + (4 * chunk + b) * kPBlock;
+          // MN-major P' row of this key: [hi g0 | lo g0 | hi g1 | lo g1], 16 bytes each
+          uint8_t* blk = smem + p_block(s, q, b);
+          uint32_t off0 = uint32_t(lane) * kN + uint32_t(32 * pass), off1 = off0 + 16;
+          off0 ^= ((off0 >> 7) & C::kPSwMask) << 4;
+          off1 ^= ((off1 >> 7) & C::kPSwMask) << 4;
           *reinterpret_cast<uint4*>(blk + off0) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
           *reinterpret_cast<uint4*>(blk + off1) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
+        // P' scale factors of this tile's stage: row group g of B holds head
+        // group g (hi rows then lo rows), byte b the factor of dim block b;
+        // the same in every TMEM lane quarter (each warp writes its own)
+        uint32_t word = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) word |= uint32_t(min(max(e_h + es[b] - 8 + 127, 1), 254)) << (8 * b);
+        tmem_st1(tmem + lane_base + C::sfp_col(s) + uint32_t(pass), word);
       }
-      // P' scale factors: B row n (hi head n, lo head n - HP) of every dim block
-      // b in byte b, the same in every TMEM lane quarter
-      tmem_st1(tmem + lane_base + kColSfp, sf_word);
       tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bars + kPFull);
+      F8_TR(12, i);
       if (last) {
         // the part's l and count over its keys, for the aux warps' epilogue
 #pragma unroll
-        for (int h = 0; h < kHP; ++h) {
-          float v = lpart[h];
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-          if (lane == h) ms->red_l[q][h] = v;
-        }
+        for (int pass = 0; pass < C::kPass; ++pass)
+          if ((lane & 1) == 0) ms->red_l[q][16 * pass + hs] = lsum[pass];
         const int32_t nvw = __reduce_add_sync(0xffffffffu, nv);
         if (lane == 0) ms->red_nv[q] = nvw;
-        // the slot (m, l) of this O buffer was read by the epilogue two parts ago
-        wait_warp(bars + kOEmpty + ob, ((pi >> 1) & 1) ^ 1, ms, a);
+        // the (m, l) slot of this O buffer was read by the epilogue kNO parts ago
+        wait_warp(bars + kOEmpty + ob, ((pi / C::kNO) & 1) ^ 1, ms, a);
         named_barrier(1, 32 * kSoftmaxWarps);
         if (q == 0) {
-          if (lane < kHP) {
-            float l = 0.f;
 #pragma unroll
-            for (int w = 0; w < kSoftmaxWarps; ++w) l += ms->red_l[w][lane];
-            float m = mref[0];
-#pragma unroll
-            for (int k = 1; k < kHP; ++k) m = (k == lane) ? mref[k] : m;
-            ms->part_m[ob][lane] = m;
-            ms->part_l[ob][lane] = l;
+          for (int pass = 0; pass < C::kPass; ++pass) {
+            if (lane < 16) {
+              const int h = 16 * pass + lane;
+              ms->part_m[ob][h] = mref[pass];
+              ms->part_l[ob][h] = ms->red_l[0][h] + ms->red_l[1][h] + ms->red_l[2][h] + ms->red_l[3][h];
+            }
           }
-          if (lane == 0) {
-            int32_t n = 0;
-#pragma unroll
-            for (int w = 0; w < kSoftmaxWarps; ++w) n += ms->red_nv[w];
-            ms->part_nv[ob] = n;
-          }
+          if (lane == 0) ms->part_nv[ob] = ms->red_nv[0] + ms->red_nv[1] + ms->red_nv[2] + ms->red_nv[3];
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bars + kEpiReady + ob);
@@ -534,161 +999,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(DecodeArgs a) {
     const int q = warp - kAuxWarp0;  // TMEM lane quarter
     const int ta = 32 * q + lane;    // 0..127
     const uint32_t lane_base = uint32_t(32 * q) << 16;
+    const AuxCtx actx{&a, smem, ms, bars, tmem, lane_base, H, h0, Hl, hg, g, lane, ta, c_id, G, T};
     // V^T scale factors: 1 (E8M0 127) for every dim row and key block
     {
       uint32_t v[16];
 #pragma unroll
       for (int k = 0; k < 16; ++k) v[k] = 0x7F7F7F7Fu;
-      tmem_st16(tmem + lane_base + kColSfv, v);
+      tmem_st16(tmem + lane_base + C::kColSfv, v);
       tmem_wait_st();
     }
     // q of a row -> [q_hi | q_lo] E4M3 (K-major, 128-byte swizzled) with an
     // E8M0 factor per (head, 32 dims) that brings the block's largest |q| to
     // [2^7, 2^8); q_rope (bf16) copied as it is; then the factors into TMEM.
-    auto stage_q = [&](int row, int qb) {
-      uint8_t* qs = smem + kOffQ + qb * kQBytes;
-#pragma unroll 1
-      for (int blk = ta; blk < kHP * 16; blk += 128) {
-        const int h = blk >> 4, kb = blk & 15;
-        uint32_t hw[8], lw[8];
-        int sfb = 127;
-        if (h < H) {
-          const uint4* src = reinterpret_cast<const uint4*>(a.q + row * a.q_stride_row + h * a.q_stride_head + 32 * kb);
-          uint4 v[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) v[k] = __ldg(src + k);
-          float f[32];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              f[8 * k + 2 * j] = __uint_as_float(w[j] << 16);
-              f[8 * k + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-            }
-          }
-          float amax = 0.f;
-#pragma unroll
-          for (int k = 0; k < 32; ++k) amax = fmaxf(amax, fabsf(f[k]));
-          int e = amax > 0.f ? int((__float_as_uint(amax) >> 23) & 0xFF) - 127 - 7 : 0;
-          e = max(min(e, 120), -120);
-          sfb = e + 127;
-          const float inv = pow2f(-e);
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            uint16_t h2, l2;
-            split_pair(f[2 * k] * inv, f[2 * k + 1] * inv, h2, l2);
-            if (k & 1) {
-              hw[k >> 1] |= uint32_t(h2) << 16;
-              lw[k >> 1] |= uint32_t(l2) << 16;
-            } else {
-              hw[k >> 1] = h2;
-              lw[k >> 1] = l2;
-            }
-          }
-        } else {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) hw[k] = lw[k] = 0u;
-        }
-        const int kc = kb >> 2, c0 = 2 * (kb & 3);
-        uint8_t* base = qs + kc * kQLatChunk;
-        *reinterpret_cast<uint4*>(base + sw128(h, c0)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-        *reinterpret_cast<uint4*>(base + sw128(h, c0 + 1)) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
-        *reinterpret_cast<uint4*>(base + sw128(kHP + h, c0)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-        *reinterpret_cast<uint4*>(base + sw128(kHP + h, c0 + 1)) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
-        ms->sfq[h][kb] = uint8_t(sfb);
-        ms->sfq[kHP + h][kb] = uint8_t(sfb);
-      }
-      {  // rope: kHP rows x 128 bytes, one 16-byte chunk per thread
-        const int h = ta >> 3, c16 = ta & 7;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (h < H)
-          v = __ldg(reinterpret_cast<const uint4*>(a.q + row * a.q_stride_row + h * a.q_stride_head + kLatent + 8 * c16));
-        *reinterpret_cast<uint4*>(qs + kQOffRope + sw128(h, c16)) = v;
-      }
-      named_barrier(2, 128);
-      {
-        // q factors: row n = lane (row group 0), K-block group g in column 4 g,
-        // byte k = K-block 4 g + k; the other columns of each group unused
-        uint32_t v[16];
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          v[4 * g] = *reinterpret_cast<const uint32_t*>(&ms->sfq[lane][4 * g]);
-          v[4 * g + 1] = v[4 * g + 2] = v[4 * g + 3] = 0x7F7F7F7Fu;
-        }
-        tmem_st16(tmem + lane_base + kColSfq + 16 * qb, v);
-        tmem_wait_st();
-      }
-      named_barrier(2, 128);  // sfq is reused by the next staging
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bars + kQFull + qb);
-    };
-    auto epilogue = [&](const Cursor& pc, int pi) {
-      const int ob = pi & 1;
-      const uint32_t ph = (pi >> 1) & 1;
-      wait_warp(bars + kEpiReady + ob, ph, ms, a);
-      wait_warp(bars + kOFull + ob, ph, ms, a);
-      tc_fence_after();
-      const int row = pc.row;
-      const bool whole = pc.whole();
-      int64_t slot = 0;
-      if (!whole) slot = slot_of(c_id, pc.P, T, G);
-      float fac[kHP];
-#pragma unroll
-      for (int h = 0; h < kHP; ++h) {
-        float lse_h;
-        if (whole) finish_head(ms->part_m[ob][h], ms->part_l[ob][h], a.sink, h < H ? h : 0, &fac[h], &lse_h);
-        else fac[h] = 1.f;
-      }
-#pragma unroll 1
-      for (int b = 0; b < 4; ++b) {
-        uint32_t v0[16], v1[16];
-        tmem_ld16(tmem + lane_base + o_col(ob, b), v0);
-        tmem_ld16(tmem + lane_base + o_col(ob, b) + 16, v1);
-        tmem_wait_ld();
-        const int d = 128 * b + ta;
-        if (whole) {
-          uint16_t* dst = a.out + int64_t(row) * a.out_stride_row + d;
-#pragma unroll
-          for (int h = 0; h < kHP; ++h) {
-            if (h < H) {
-              const float o = (__uint_as_float(v0[h]) + __uint_as_float(v1[h])) * fac[h];
-              dst[int64_t(h) * a.out_stride_head] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
-            }
-          }
-        } else {
-          float* dst = a.o_part + (slot * H) * kLatent + d;
-#pragma unroll
-          for (int h = 0; h < kHP; ++h)
-            if (h < H) dst[int64_t(h) * kLatent] = __uint_as_float(v0[h]) + __uint_as_float(v1[h]);
-        }
-      }
-      if (ta < H) {
-        const float m = ms->part_m[ob][ta], l = ms->part_l[ob][ta];
-        if (whole) {
-          float f, lse_h;
-          finish_head(m, l, a.sink, ta, &f, &lse_h);
-          if (a.lse) a.lse[int64_t(row) * H + ta] = lse_h;
-        } else {
-          reinterpret_cast<float2*>(a.ml_part)[slot * H + ta] = make_float2(m, l);
-        }
-      }
-      if (ta == 0) {
-        if (whole) {
-          if (a.n_valid) a.n_valid[row] = ms->part_nv[ob];
-        } else {
-          a.nv_part[slot] = ms->part_nv[ob];
-        }
-      }
-      tc_fence_before();
-      named_barrier(2, 128);  // every aux thread read the part's (m, l) and O
-      if (lane == 0) mbar_arrive(bars + kOEmpty + ob);
-    };
     Cursor c;
     c.init(a, row0, P0, cb, ce);
-    if (n_tiles > 0) stage_q(c.row, 0);
+    if (n_tiles > 0) aux_stage_q<HP>(actx, c.row, 0);
     Cursor prev = c;
     int pi = 0;  // part of tile i
     for (int i = 0; i < n_tiles; ++i) {
@@ -698,6 +1023,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(DecodeArgs a) {
       // (1) the tile's record scale factors: row t = key, column 4 g + j holds
       // rows 32 j + lane, every byte the E8M0 of scale block g
       wait_warp(bars + kKvFull + s, ph, ms, a);
+      F8_TR(40, i);
       {
         uint32_t v[16];
         bool foreign = false;
@@ -706,29 +1032,32 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(DecodeArgs a) {
           const uint4 w4 = *reinterpret_cast<const uint4*>(st + kOffSc + 16 * (32 * j + lane));
           const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            const uint32_t e = (w[g] >> 23) & 0xFFu;
+          for (int gk = 0; gk < 4; ++gk) {
+            const uint32_t e = (w[gk] >> 23) & 0xFFu;
             // a positive normal power of two (any the writer makes) or zero
-            foreign |= !(w[g] == 0u || ((w[g] & 0x807FFFFFu) == 0u && e != 0u && e != 0xFFu));
-            v[4 * g + j] = e * 0x01010101u;
+            foreign |= !(w[gk] == 0u || ((w[gk] & 0x807FFFFFu) == 0u && e != 0u && e != 0xFFu));
+            v[4 * gk + j] = e * 0x01010101u;
           }
         }
-        tmem_st16(tmem + lane_base + kColSfa + 16 * s, v);
+        tmem_st16(tmem + lane_base + C::kColSfa + 16 * s, v);
         tmem_wait_st();
         if (__any_sync(0xffffffffu, foreign) && lane == 0 && a.status) atomicOr(a.status, SMLA_STATUS_FOREIGN_SCALE);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bars + kSfReady + s);
+      F8_TR(41, i);
       // (2) the previous part's epilogue, once this part has started
       if (i > 0 && c.first()) {
-        epilogue(prev, pi - 1);
+        aux_epilogue<HP>(actx, prev, pi - 1);
+        F8_TR(42, i);
       }
       // (3) the next part's q, as soon as its buffer is free
       if (c.last() && i + 1 < n_tiles) {
-        const int qb = (pi + 1) & 1;
-        wait_warp(bars + kQEmpty + qb, (((pi + 1) >> 1) & 1) ^ 1, ms, a);
-        stage_q(c.row + 1, qb);
+        const int qb = (pi + 1) % C::kNQ;
+        wait_warp(bars + kQEmpty + qb, (((pi + 1) / C::kNQ) & 1) ^ 1, ms, a);
+        aux_stage_q<HP>(actx, c.row + 1, qb);
+        F8_TR(43, i);
       }
       if (c.last()) {
         prev = c;
@@ -736,71 +1065,92 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(DecodeArgs a) {
       }
       c.advance(a);
     }
-    if (pi > 0) epilogue(prev, pi - 1);
+    if (pi > 0) aux_epilogue<HP>(actx, prev, pi - 1);
+    F8_TR(44, 0);
   } else if (warp < kPvWarp0) {
-    // =================== QK issuer ===================
-    Cursor c;
-    c.init(a, row0, P0, cb, ce);
-    int pi = 0;
-    for (int i = 0; i < n_tiles; ++i, c.advance(a)) {
-      const int s = i & 1;
-      const uint32_t ph = (i >> 1) & 1;
-      const int qb = pi & 1;
-      const bool first = c.first(), last = c.last();
-      wait_warp(bars + kSfReady + s, ph, ms, a);
-      wait_warp(bars + kSEmpty + s, ph ^ 1, ms, a);
-      if (first) wait_warp(bars + kQFull + qb, (pi >> 1) & 1, ms, a);
-      tc_fence_after();
+    // =================== QK issuers ===================
+    // 16 heads: warp kQkWarp0 issues latent K-steps 0-5 and the rope into
+    // accumulator 0, the next warp K-steps 6-15 into accumulator 1 (two
+    // MMA chains in flight); 32 heads: one warp, one accumulator
+    const int half = warp - kQkWarp0;
+    if (half < C::kQkSplit) {
+      Cursor c;
+      c.init(a, row0, P0, cb, ce);
+      int pi = 0;
+      const int kbeg = half == 0 ? 0 : C::kQkSteps0, kend = half == 0 ? C::kQkSteps0 : 16;
+      for (int i = 0; i < n_tiles; ++i, c.advance(a)) {
+        const int s = i & 1;
+        const uint32_t ph = (i >> 1) & 1;
+        const int qb = pi % C::kNQ;
+        const bool first = c.first(), last = c.last();
+        wait_warp(bars + kSfReady + s, ph, ms, a);
+        wait_warp(bars + kSEmpty + s, ph ^ 1, ms, a);
+        if (first) wait_warp(bars + kQFull + qb, (pi / C::kNQ) & 1, ms, a);
+        F8_TR(30, i);
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t st = smem_base + s * kStageBytes;
+          const uint32_t qs = smem_base + C::kOffQ + qb * C::kQBytes;
+          const uint32_t d = tmem + C::s_col(s, half);
+          // latent: K-steps of 32 E4M3 (K-chunk kc = 128 dims = scale block kc)
+#pragma unroll 1
+          for (int ks = kbeg; ks < kend; ++ks) {
+            const int kc = ks >> 2, sub = ks & 3;
+            const uint64_t ad = smem_desc(st + kc * kChunk + 32 * sub, 16, 1024, kSw128);
+            const uint64_t bd = smem_desc(qs + kc * C::kQLatChunk + 32 * sub, 16, 1024, kSw128);
+            mma_mxf8_ss(d, ad, bd, idesc_mxf8(128, kN, 0, 0, sub, sub), tmem + C::kColSfa + 16 * s + 4 * kc,
+                        tmem + C::kColSfq + 16 * qb + 4 * kc, ks > kbeg ? 1u : 0u);
+          }
+          if (half == 0) {
+            // rope: 4 K-steps of 16 bf16 into the q_hi columns
+#pragma unroll 1
+            for (int r = 0; r < 4; ++r) {
+              const uint64_t ad = smem_desc(st + kOffRope + 32 * r, 16, 1024, kSw128);
+              const uint64_t bd = smem_desc(qs + C::kQOffRope + 32 * r, 16, 1024, kSw128);
+              mma_f16_ss(d, ad, bd, idesc_bf16(128, HP, 0, 0), 1u);
+            }
+          }
+          mma_commit(bars + kSFull + s);
+          if (last) mma_commit(bars + kQEmpty + qb);
+        }
+        __syncwarp();
+        F8_TR(31, i);
+        if (last) ++pi;
+      }
+      // every MMA issued here has completed before TMEM is freed (also after a timeout)
       if (lane == 0) {
-        const uint32_t st = smem_base + s * kStageBytes;
-        const uint32_t qs = smem_base + kOffQ + qb * kQBytes;
-        const uint32_t d = tmem + s_col(s);
-        // latent: 16 K-steps of 32 E4M3 (K-chunk kc = 128 dims = scale block kc)
-#pragma unroll 1
-        for (int ks = 0; ks < 16; ++ks) {
-          const int kc = ks >> 2, sub = ks & 3;
-          const uint64_t ad = smem_desc(st + kc * kChunk + 32 * sub, 16, 1024, kSw128);
-          const uint64_t bd = smem_desc(qs + kc * kQLatChunk + 32 * sub, 16, 1024, kSw128);
-          mma_mxf8_ss(d, ad, bd, idesc_mxf8(128, kN, 0, 0, sub, sub), tmem + kColSfa + 16 * s + 4 * kc,
-                      tmem + kColSfq + 16 * qb + 4 * kc, ks > 0 ? 1u : 0u);
-        }
-        // rope: 4 K-steps of 16 bf16 into the q_hi columns
-#pragma unroll 1
-        for (int r = 0; r < 4; ++r) {
-          const uint64_t ad = smem_desc(st + kOffRope + 32 * r, 16, 1024, kSw128);
-          const uint64_t bd = smem_desc(qs + kQOffRope + 32 * r, 16, 1024, kSw128);
-          mma_f16_ss(d, ad, bd, idesc_bf16(128, kHP, 0, 0), 1u);
-        }
-        mma_commit(bars + kSFull + s);
-        if (last) mma_commit(bars + kQEmpty + qb);
+        mma_commit(bars + kDrain);
+        if (!mbar_wait(bars + kDrain, 0, kWaitLimitNs)) set_abort(ms, a.status);
       }
       __syncwarp();
-      if (last) ++pi;
     }
   } else if (warp < kLoadWarp0) {
-    // =================== PV issuer ===================
+    // =================== PV issuers: dim blocks 2 pair, 2 pair + 1 ===================
+    const int pair = warp - kPvWarp0;
     Cursor c;
     c.init(a, row0, P0, cb, ce);
     int pi = 0;
     for (int i = 0; i < n_tiles; ++i, c.advance(a)) {
       const int s = i & 1;
-      const int ob = pi & 1;
+      const int ob = pi % C::kNO;
       const bool first = c.first(), last = c.last();
       wait_warp(bars + kPFull, i & 1, ms, a);
-      if (first) wait_warp(bars + kOEmpty + ob, ((pi >> 1) & 1) ^ 1, ms, a);
+      if (first) wait_warp(bars + kOEmpty + ob, ((pi / C::kNO) & 1) ^ 1, ms, a);
+      F8_TR(60, i);
       tc_fence_after();
       if (lane == 0) {
         const uint32_t st = smem_base + s * kStageBytes;
         // block-major: consecutive MMAs accumulate into the same O block
 #pragma unroll 1
-        for (int b = 0; b < 4; ++b) {
+        for (int bb = 0; bb < 2; ++bb) {
+          const int b = 2 * pair + bb;
 #pragma unroll 1
           for (int ch = 0; ch < 4; ++ch) {
             // V^T: dims of block b (M, contiguous) x keys 32 ch .. (K, rows)
             const uint64_t ad = smem_desc(st + b * kChunk + ch * 4096, 16384, 1024, kSw128);
-            const uint64_t bd = smem_desc(smem_base + kOffP + (4 * ch + b) * kPBlock, 256, 256, kSw32);
-            mma_mxf8_ss(tmem + o_col(ob, b), ad, bd, idesc_mxf8(128, kN, 1, 1, 0, b), tmem + kColSfv, tmem + kColSfp,
-                        (first && ch == 0) ? 0u : 1u);
+            const uint64_t bd = smem_desc(smem_base + p_block(s, ch, b), 8 * kN, 8 * kN, C::kPSw);
+            mma_mxf8_ss(tmem + C::o_col(ob, b), ad, bd, idesc_mxf8(128, kN, 1, 1, 0, b), tmem + C::kColSfv,
+                        tmem + C::sfp_col(s), (first && ch == 0) ? 0u : 1u);
           }
         }
         mma_commit(bars + kPvDone);
@@ -808,103 +1158,122 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(DecodeArgs a) {
         if (last) mma_commit(bars + kOFull + ob);
       }
       __syncwarp();
+      F8_TR(61, i);
       if (last) ++pi;
     }
+    if (lane == 0) {
+      mma_commit(bars + kDrain);
+      if (!mbar_wait(bars + kDrain, 0, kWaitLimitNs)) set_abort(ms, a.status);
+    }
+    __syncwarp();
   } else {
     // =================== loaders ===================
     const int lw = warp - kLoadWarp0;
     const int kc = lane >> 3, c16 = lane & 7;
-    Cursor c;
-    c.init(a, row0, P0, cb, ce);
-    // raw entry of key (16 lw + lane) of the current tile, loaded a tile ahead
+    // raw entry of key lw + 8 lane (lanes 0-15) of a cursor's tile, or -1
     auto raw_of = [&](const Cursor& cu) -> int32_t {
-      const int32_t tk = lw + kLoadWarps * lane;  // key of this lane within the tile
-      if (!cu.live || lane >= kKeysPerLoader || tk >= kTK) return -1;
+      const int32_t tk = lw + kLoadWarps * lane;
+      if (!cu.live || lane >= kKeysPerLoader) return -1;
       const int32_t p = cu.p0() + tk;
       const int64_t off = cu.beg + p;
       if (p >= cu.p1() || off < 0 || off >= a.n_indices) return -1;
       return __ldg(a.indices + off);
     };
+    Cursor c;
+    c.init(a, row0, P0, cb, ce);
     int32_t raw = raw_of(c);
     bool oob = false;
     for (int i = 0; i < n_tiles; ++i) {
       const int s = i & 1;
       const uint32_t ph = (i >> 1) & 1;
-      Cursor nx = c;
-      nx.advance(a);
-      const int32_t raw_next = raw_of(nx);
-      if (!wait_warp(bars + kKvEmpty + s, ph ^ 1, ms, a)) {
-        c = nx;
-        raw = raw_next;
-        continue;
-      }
-      int32_t id = raw;
-      if (id >= a.n_kv_rows) {
-        oob = true;
-        id = -1;
-      }
-      if (id < 0) id = -1;
-      uint8_t* st = smem + s * kStageBytes;
-      const uint32_t st32 = smem_base + s * kStageBytes;
-#pragma unroll 2
-      for (int j = 0; j < kKeysPerLoader; ++j) {
-        const int t = lw + kLoadWarps * j;
-        if (t >= kTK) break;
-        const int32_t idj = __shfl_sync(0xffffffffu, id, j);
-        if (idj >= 0) {
-          const uint8_t* rec = a.kv + int64_t(idj) * kRecordBytes;
-          cp_async16(st32 + kc * kChunk + sw128(t, c16), rec + 16 * lane);
-          if (lane < 8)
-            cp_async16(st32 + kOffRope + sw128(t, lane), rec + kRopeOffset + 16 * lane);
-          else if (lane == 8)
-            cp_async16(st32 + kOffSc + 16 * t, rec + kScaleOffset);
-        } else {
-          *reinterpret_cast<uint4*>(st + kc * kChunk + sw128(t, c16)) = make_uint4(0, 0, 0, 0);
-          if (lane < 8)
-            *reinterpret_cast<uint4*>(st + kOffRope + sw128(t, lane)) = make_uint4(0, 0, 0, 0);
-          else if (lane == 8)
-            *reinterpret_cast<uint4*>(st + kOffSc + 16 * t) =
-                make_uint4(0x3F800000u, 0x3F800000u, 0x3F800000u, 0x3F800000u);
+      if (wait_warp(bars + kKvEmpty + s, ph ^ 1, ms, a)) {
+        F8_TR(50, i);
+        int32_t id = raw;
+        if (id >= a.n_kv_rows) {
+          oob = true;
+          id = -1;
         }
+        if (id < 0) id = -1;
+        uint8_t* st = smem + s * kStageBytes;
+        const uint32_t st32 = smem_base + s * kStageBytes;
+#pragma unroll 4
+        for (int j = 0; j < kKeysPerLoader; ++j) {
+          const int t = lw + kLoadWarps * j;
+          const int32_t idj = __shfl_sync(0xffffffffu, id, j);
+          if (idj >= 0) {
+            const uint8_t* rec = a.kv + int64_t(idj) * kRecordBytes;
+            cp_async16(st32 + kc * kChunk + sw128(t, c16), rec + 16 * lane);
+            if (lane < 8)
+              cp_async16(st32 + kOffRope + sw128(t, lane), rec + kRopeOffset + 16 * lane);
+            else if (lane == 8)
+              cp_async16(st32 + kOffSc + 16 * t, rec + kScaleOffset);
+          } else {
+            *reinterpret_cast<uint4*>(st + kc * kChunk + sw128(t, c16)) = make_uint4(0, 0, 0, 0);
+            if (lane < 8)
+              *reinterpret_cast<uint4*>(st + kOffRope + sw128(t, lane)) = make_uint4(0, 0, 0, 0);
+            else if (lane == 8)
+              *reinterpret_cast<uint4*>(st + kOffSc + 16 * t) =
+                  make_uint4(0x3F800000u, 0x3F800000u, 0x3F800000u, 0x3F800000u);
+          }
+        }
+        if (lane < kKeysPerLoader) *reinterpret_cast<int32_t*>(st + kOffIds + 4 * (lw + kLoadWarps * lane)) = id;
+        fence_proxy_async_smem();
+        cp_async_mbar_arrive(bars + kKvFull + s);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars + kKvFull + s);
+        F8_TR(51, i);
       }
-      if (lane < kKeysPerLoader && lw + kLoadWarps * lane < kTK)
-        *reinterpret_cast<int32_t*>(st + kOffIds + 4 * (lw + kLoadWarps * lane)) = id;
-      fence_proxy_async_smem();
-      cp_async_mbar_arrive(bars + kKvFull + s);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bars + kKvFull + s);
-      c = nx;
-      raw = raw_next;
+      c.advance(a);
+      raw = raw_of(c);  // the next tile's entries, loaded while this one lands
     }
     if (__any_sync(0xffffffffu, oob) && lane == 0 && a.status) atomicOr(a.status, SMLA_STATUS_INDEX_OOB);
     cp_async_wait_all();
   }
 
+  F8_TR(3, 0);
   tc_fence_before();
   __syncthreads();
   if (warp == kQkWarp0) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, 512);
   }
+  // ---- rows completed here: [P2] stage_combine of their parts, with the sink
+  F8_TR(4, ms->n_merge);
+  if (ms->n_merge > 0) end_merge(a, ms, tid, h0, Hl, hg, g, T, G);
+  F8_TR(5, 0);
 }
 
 }  // namespace
 
-bool fp8_kernel_supports(int num_heads) { return num_heads >= 1 && num_heads <= kHP; }
+bool fp8_kernel_supports(int num_heads) { return num_heads >= 1 && num_heads <= 2 * kMaxHP; }
 
 int fp8_tile_len() { return kTK; }
 
-cudaError_t launch_decode_fp8(const DecodeLaunch& L) {
-  if (L.plan.grid <= 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(decode_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTotal);
+cudaError_t fp8_set_wait_limit(uint64_t ns, int stall) {
+  const int32_t st = stall ? 1 : 0;
+  const cudaError_t e = cudaMemcpyToSymbol(g_fp8_wait_ns, &ns, sizeof(ns));
+  return e != cudaSuccess ? e : cudaMemcpyToSymbol(g_fp8_stall, &st, sizeof(st));
+}
+
+int fp8_head_groups(int num_heads) { return num_heads > kMaxHP ? 2 : 1; }
+
+template <int HP>
+static cudaError_t launch_fp8_hp(const DecodeLaunch& L) {
+  constexpr int smem = smem_total<HP>();
+  cudaError_t e = cudaFuncSetAttribute(decode_fp8_kernel<HP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   DecodeArgs args = make_decode_args(L);
   e = launch_trim(L, args);
   if (e != cudaSuccess) return e;
-  decode_fp8_kernel<<<L.plan.grid, kThreads, kSmemTotal, L.stream>>>(args);
+  decode_fp8_kernel<HP><<<L.plan.grid * L.plan.head_groups, kThreads, smem, L.stream>>>(args);
   e = cudaGetLastError();
   if (e != cudaSuccess || !L.plan.merge_kernel) return e;
   return launch_merge(L, args);
+}
+
+cudaError_t launch_decode_fp8(const DecodeLaunch& L) {
+  if (L.plan.grid <= 0) return cudaSuccess;
+  return L.p.num_heads <= 16 ? launch_fp8_hp<16>(L) : launch_fp8_hp<32>(L);
 }
 
 }  // namespace smla

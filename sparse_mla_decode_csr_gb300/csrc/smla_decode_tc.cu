@@ -77,6 +77,13 @@ extern "C" int smla_trace_set(void* buf) {
 #endif
 
 namespace smla {
+
+// Limit of every pipeline wait in ns (0: kWaitLimitNs), and whether the first
+// softmax wait of each CTA waits on a barrier nothing signals (so that it runs
+// out: a test of the timeout path); read at kernel start.
+__device__ uint64_t g_tc_wait_ns;
+__device__ int32_t g_tc_stall;
+
 namespace {
 
 using namespace ptx;
@@ -109,13 +116,15 @@ constexpr int kRopeWarp = 15;  // rope copier
 constexpr int kQkSteps = kQK / 16;
 constexpr float kRescaleMargin = 24.f;           // p <= 2^24 before a max update
 constexpr float kInitMax = -1.0e30f;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait (default) and per MMA drain
 
 static_assert(kSchedTile == kTileK, "schedule and pipeline tiles must agree");
 
 struct Misc {
   uint32_t tmem_base;
   int32_t abort;
+  uint64_t wait_ns;       // limit of a pipeline wait
+  int32_t stall;          // first softmax wait on a barrier never signalled
   int32_t is_last;
   int32_t first_row;      // schedule: first row of this CTA's range
   int64_t first_tile;     // schedule: that row's first slot
@@ -149,7 +158,7 @@ struct TcLayout {
   static constexpr int off_q = kStages * kTileBytes;
   static constexpr int off_p = off_q + q_bytes;
   static constexpr int off_bar = off_p + p_stages * p_bytes;
-  static constexpr int off_misc = off_bar + 16 * 8;
+  static constexpr int off_misc = off_bar + 32 * 8;  // 17 barriers used
   // Up to 32 heads each converter warp also owns a ring of kRing raw-latent
   // slots (512 B) in shared memory, filled by cp.async kRing - 1 records ahead
   // of the conversion; at 64 heads there is no room and latents are gathered
@@ -194,7 +203,7 @@ __device__ __forceinline__ void set_abort(Misc* ms, const DecodeArgs& a) {
 // thread executes the same barrier sequence.
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, Misc* ms, const DecodeArgs& a) {
   if (*reinterpret_cast<volatile int32_t*>(&ms->abort)) return false;
-  if (mbar_wait(bar, parity, kWaitLimitNs)) return true;
+  if (mbar_wait(bar, parity, ms->wait_ns)) return true;
   set_abort(ms, a);
   return false;
 }
@@ -364,6 +373,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
   uint64_t* o_free = bars + 12;
   uint64_t* q_full = bars + 14;
   uint64_t* mma_drain = bars + 15;
+  uint64_t* stall_bar = bars + 16;  // never signalled (timeout-path test)
   Misc* ms = reinterpret_cast<Misc*>(smem + Lay::off_misc);
   const int H = a.heads;
   const int64_t G = gridDim.x;
@@ -382,7 +392,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
     }
     mbar_init(q_full, kSoftmaxWarps);
     mbar_init(mma_drain, 3);  // the three issuers
+    mbar_init(stall_bar, 1);
     ms->abort = 0;
+    const uint64_t w = g_tc_wait_ns;
+    ms->wait_ns = w != 0 ? w : kWaitLimitNs;
+    ms->stall = g_tc_stall;
     ms->is_last = 0;
     ms->first_row = a.n_q;
     ms->first_tile = 0;
@@ -519,6 +533,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) decode_tc_kernel(DecodeArgs a) 
         nv = 0;
       }
       SMLA_TR(10, i);
+      if (i == 0 && ms->stall) wait_bar_warp(stall_bar, 0, ms, a);
       wait_bar_warp(kv_full + s, ph, ms, a);
       wait_bar_warp(s_full + s, ph, ms, a);
       SMLA_TR(11, i);
@@ -1253,6 +1268,11 @@ __global__ void __launch_bounds__(32 * (kSplit == 1 ? kMergeWarps : kSplit)) mer
   const int32_t nt = int32_t(__ldcg(a.row_tile + row + 1) - P);
   const int64_t ca = cta_of_tile(P, T, G), cb = cta_of_tile(P + nt - 1, T, G);
   if (ca == cb) return;  // finished whole by one CTA
+  if (a.merge_min_parts > 2) {  // rows of fewer parts were merged by the decode kernel
+    int64_t parts = 0;
+    for (int64_t c = ca; c <= cb && parts < a.merge_min_parts; ++c) parts += cta_begin(c + 1, T, G) > cta_begin(c, T, G);
+    if (parts < a.merge_min_parts) return;
+  }
   // this warp's parts: c = ca + w + kSplit i
   const int64_t first = ca + w;
   const int64_t n_mine = first <= cb ? (cb - first) / kSplit + 1 : 0;
@@ -1438,6 +1458,12 @@ cudaError_t launch_merge(const DecodeLaunch& L, const DecodeArgs& args) {
   else
     merge_rows_kernel<1><<<unsigned((pairs + kMergeWarps - 1) / kMergeWarps), 32 * kMergeWarps, 0, L.stream>>>(args);
   return cudaGetLastError();
+}
+
+cudaError_t tc_set_wait_limit(uint64_t ns, int stall) {
+  const int32_t st = stall ? 1 : 0;
+  const cudaError_t e = cudaMemcpyToSymbol(g_tc_wait_ns, &ns, sizeof(ns));
+  return e != cudaSuccess ? e : cudaMemcpyToSymbol(g_tc_stall, &st, sizeof(st));
 }
 
 cudaError_t launch_decode_tc(const DecodeLaunch& L) {

@@ -32,6 +32,8 @@ struct DecodeArgs {
   float sm_scale_log2;  // sm_scale * log2(e): scores are kept in log2 units
   int32_t n_q, heads, splits, chunk_len, has_invalid;
   int32_t grid, merge_kernel;  // tensor-core schedule
+  int32_t merge_min_parts;     // the merge kernel leaves rows of fewer parts alone
+  int32_t head_groups;         // native-fp8 kernel: CTAs per schedule range (heads split)
   // split workspace
   int32_t* ticket;
   int64_t* row_tile;  // tensor-core schedule: first tile of each row, then T
@@ -67,6 +69,9 @@ inline DecodeArgs make_decode_args(const DecodeLaunch& L) {
   a.has_invalid = p.has_invalid;
   a.grid = L.plan.grid;
   a.merge_kernel = L.plan.merge_kernel;
+  // the native-fp8 kernel merges rows of up to kMaxInKernelParts parts itself
+  a.merge_min_parts = L.plan.kernel == SMLA_KERNEL_TENSOR_CORE_FP8 ? kMaxInKernelParts + 1 : 2;
+  a.head_groups = L.plan.head_groups > 0 ? L.plan.head_groups : 1;
   if (L.ws.total > 0) {
     char* ws = static_cast<char*>(L.workspace);
     a.ticket = reinterpret_cast<int32_t*>(ws + L.ws.ticket_off);
@@ -131,10 +136,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 //   out = acc * factor, factor = 2^(m - m_f) / (2^(s - m_f) + l 2^(m - m_f)),
 //   m_f = max(m, s), s = sink * log2(e)        (the K2-back combine's fold)
 //   lse = (m + log2 l) * ln 2                  (the gfx950 epilogue's LSE)
-// and factor = 0, lse = -inf when l == 0 (no key).
+// and factor = 0, lse = -inf when l == 0 (no key); a NaN l (a NaN score)
+// gives NaN for both.
 __device__ __forceinline__ void finish_head(float m, float l, const float* sink, int h,
                                             float* factor, float* lse) {
-  if (!(l > 0.f)) {
+  if (l == 0.f) {
     *factor = 0.f;
     *lse = -INFINITY;
     return;

@@ -16,6 +16,10 @@ constexpr int kScaleOffset = 512;
 constexpr int kRopeOffset = 528;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+// Rows shared by at most this many CTAs are merged inside the native-fp8
+// decode kernel (by the CTA whose part completes the row); rows of more parts
+// are left to the merge kernel when the plan launches it.
+constexpr int kMaxInKernelParts = 8;
 
 // Workspace offsets of one plan (see smla_decode_workspace_size in smla.h).
 struct WorkspaceLayout {
@@ -50,6 +54,11 @@ cudaError_t launch_merge(const DecodeLaunch& L, const DecodeArgs& args);
 // Heads and tile length of the native-fp8 kernel.
 bool fp8_kernel_supports(int num_heads);
 int fp8_tile_len();
+int fp8_head_groups(int num_heads);
+// Pipeline wait limits of the tensor-core kernels (0: their 2 s default) and
+// the timeout-path test switch (see smla_set_wait_limit).
+cudaError_t fp8_set_wait_limit(uint64_t ns, int stall);
+cudaError_t tc_set_wait_limit(uint64_t ns, int stall);
 cudaError_t launch_pack(const void* latent, int64_t latent_stride, const void* rope,
                         int64_t rope_stride, int64_t n, void* kv_out, cudaStream_t stream);
 

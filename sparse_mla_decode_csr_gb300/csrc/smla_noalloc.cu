@@ -58,9 +58,10 @@ extern "C" int smla_decode_noalloc(const smla_decode_params* params, void* strea
   void* scratch = nullptr;
   rc = scratch_on_current_device(&scratch);
   if (rc != SMLA_OK) return rc;
-  if (plan.kernel == SMLA_KERNEL_CUDA_CORE && plan.workspace_bytes > 0) {
+  if ((plan.kernel == SMLA_KERNEL_CUDA_CORE || plan.kernel == SMLA_KERNEL_TENSOR_CORE_FP8) &&
+      plan.workspace_bytes > 0) {
     // per-row ticket counters at the start of the workspace must start at zero
-    if (cudaMemsetAsync(scratch, 0, size_t(params->n_q) * sizeof(int32_t),
+    if (cudaMemsetAsync(scratch, 0, size_t(params->n_q) * 2 * sizeof(int32_t),
                         static_cast<cudaStream_t>(stream)) != cudaSuccess)
       return SMLA_ERR_LAUNCH;
   }

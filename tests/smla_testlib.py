@@ -37,7 +37,7 @@ def build_cache(w: W.Workload, dev, gen_device="cuda") -> torch.Tensor:
 
 KERNELS = {"tc": smla.KERNEL_TENSOR_CORE, "simt": smla.KERNEL_CUDA_CORE,
            "bf16": smla.KERNEL_TENSOR_CORE_BF16, "fp8": smla.KERNEL_TENSOR_CORE_FP8}
-FP8_MAX_HEADS = 16
+FP8_MAX_HEADS = 64
 
 
 def run_gpu(q, kv, n_kv_rows, indices, indptr, lens, sm_scale, sink, *, max_row_len=0,

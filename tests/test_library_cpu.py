@@ -65,17 +65,22 @@ def test_plan_properties_cuda_core(n_q, heads, row_len):
     (4, 16, 128), (64, 16, 2048), (256, 16, 2048), (128, 64, 2048), (4, 64, 16384), (1, 1, 1)])
 def test_plan_properties_tensor_core(n_q, heads, row_len):
     p = smla.smla_plan(n_q, heads, row_len, n_q * row_len, 0, 152)
-    # the default resolves to the native-fp8 kernel up to 16 heads, else bf16
-    fp8 = heads <= 16
-    assert p.kernel == (smla.KERNEL_TENSOR_CORE_FP8 if fp8 else smla.KERNEL_TENSOR_CORE_BF16)
-    assert p.grid == 152 and p.tile_len == (128 if fp8 else 64)  # persistent: one CTA per SM
+    # the default resolves to the native-fp8 kernel (up to 64 heads)
+    assert p.kernel == smla.KERNEL_TENSOR_CORE_FP8 and p.tile_len == 128
+    hg = 2 if heads > 32 else 1  # two CTAs (head groups of up to 32) share a schedule range above 32 heads
+    assert p.head_groups == hg and p.grid == 152 // hg  # persistent: one CTA per SM
     assert p.partial_slots == 2 * p.grid
-    assert p.merge_kernel == (p.grid > 1)
-    need = n_q * 4 + (n_q + 1) * 8 + p.partial_slots * heads * (512 + 2) * 4 + p.partial_slots * 4
+    # rows of at most 8 parts are merged inside the kernel; the merge kernel
+    # runs only when top-k rows would span more CTAs
+    assert p.merge_kernel == (-(-p.grid // n_q) + 1 > 8)
+    need = 8 * n_q + (n_q + 1) * 8 + p.partial_slots * heads * (512 + 2) * 4 + p.partial_slots * 4
     assert p.workspace_bytes >= need
     for k in (1, 3, 64):
         f = smla.smla_plan(n_q, heads, row_len, n_q * row_len, k, 152)
-        assert f.grid == min(n_q * k, 65535)
+        assert f.grid == min(n_q * k, 65535 // hg)
+    b = smla.smla_plan(n_q, heads, row_len, n_q * row_len, 0, 152, kernel=smla.KERNEL_TENSOR_CORE_BF16)
+    assert b.kernel == smla.KERNEL_TENSOR_CORE_BF16 and b.tile_len == 64 and b.grid == 152
+    assert b.head_groups == 1 and b.merge_kernel == 1 and b.partial_slots == 2 * b.grid
 
 
 def test_plan_splits_short_batches_and_respects_forcing():
@@ -92,8 +97,8 @@ def test_plan_splits_short_batches_and_respects_forcing():
         smla.smla_plan(-1, 16, 700, 2100, 0, 152)
     with pytest.raises(smla.SmlaError):
         smla.smla_plan(3, 16, 700, 2100, 0, 152, kernel=7)
-    with pytest.raises(smla.SmlaError):  # the native-fp8 kernel takes up to 16 heads
-        smla.smla_plan(3, 17, 700, 2100, 0, 152, kernel=smla.KERNEL_TENSOR_CORE_FP8)
+    with pytest.raises(smla.SmlaError):  # more than 64 heads
+        smla.smla_plan(3, 65, 700, 2100, 0, 152, kernel=smla.KERNEL_TENSOR_CORE_FP8)
     for k in (smla.KERNEL_TENSOR_CORE_BF16, smla.KERNEL_TENSOR_CORE_FP8):
         assert smla.smla_plan(3, 16, 700, 2100, 0, 152, kernel=k).kernel == k
 
@@ -118,7 +123,7 @@ def _params(**kw):
     (dict(q_stride_head=100), -3), (dict(out_stride_row=512), -3),
     (dict(q=0x1008), -4), (dict(out_stride_head=516, out_stride_row=16 * 516), -4), (dict(kv_cache=0x2004), -4),
     (dict(num_splits=65), -6), (dict(num_splits=-1), -6), (dict(kernel=4), -2),
-    (dict(kernel=3, num_heads=17), -2),
+    (dict(kernel=3, num_heads=65), -2),
 ])
 def test_decode_rejects_bad_arguments_on_host(kw, code):
     p = _params(**kw)
