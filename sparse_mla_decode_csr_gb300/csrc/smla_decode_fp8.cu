@@ -21,17 +21,17 @@
 //        P' carries ~8 significant bits (as a bf16 P would) down to 2^-18 of
 //        the tile's largest term.  O = O_hi + O_lo.
 //
-// Warp roles (20 warps, 640 threads, one CTA per SM):
+// Warp roles (16 warps, 512 threads, one CTA per SM):
 //   0-3   softmax (warp q owns the keys of TMEM lane quarter q of S; all the
-//         CTA's heads, 16 at a time; per-head values live one per lane)
-//   4-7   aux: E8M0 scale factors of each landed tile into TMEM, q staging
-//         (hi/lo split and its scale factors) per row part, and each row
-//         part's epilogue (out / lse or a partial of a shared row)
-//   8-9   QK issuers (16 heads: the K-steps split over two accumulators so
-//         that two MMA chains are in flight; a thread issues one MMA every
-//         ~120 cycles, two threads one every ~60), 10-11 PV issuers (dim
-//         blocks 0-1 and 2-3)
-//   12-19 loaders: keys lw, lw + 8, ... of every 128-key tile (64-bit record
+//         CTA's heads, 16 at a time; per-head values live one per lane);
+//         warps 0 and 1 then issue the tile's PV (dim blocks 0-1 and 2-3)
+//   4-7   aux: E8M0 scale factors of each landed tile into TMEM, then the
+//         tile's QK (16 heads: warps 4 and 5 each issue part of the K-steps
+//         into their own accumulator, two MMA chains in flight; a thread
+//         issues one MMA every ~120 cycles); q staging (hi/lo split and its
+//         scale factors) per row part, and each row part's epilogue (out /
+//         lse or a partial of a shared row)
+//   8-15  loaders: keys lw, lw + 8, ... of every 128-key tile (64-bit record
 //         addressing, masked keys zero-filled, out-of-range entries flagged)
 //
 // The schedule is that of the bf16 tensor-core kernel with 128-key tiles: rows
@@ -90,14 +90,12 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 640;
+constexpr int kThreads = 512;
 constexpr int kTK = 128;        // keys per tile (M of QK)
 constexpr int kStages = 2;
 constexpr int kSoftmaxWarps = 4;   // one per TMEM lane quarter
-constexpr int kAuxWarp0 = 4;
-constexpr int kQkWarp0 = 8;        // QK issuers
-constexpr int kPvWarp0 = 10;       // two PV issuers (dim blocks 0-1 and 2-3)
-constexpr int kLoadWarp0 = 12;
+constexpr int kAuxWarp0 = 4;        // aux warps; the first kQkSplit of them issue QK
+constexpr int kLoadWarp0 = 8;
 constexpr int kLoadWarps = 8;
 constexpr int kKeysPerLoader = kTK / kLoadWarps;  // 16 (keys lw, lw + 8, ...)
 constexpr int kRowStart = 2;                      // schedule slots charged for starting a row
@@ -197,13 +195,10 @@ static_assert(smem_total<16>() <= 232448 && smem_total<32>() <= 232448, "shared 
 enum Bar {
   kKvFull = 0,    // [2] loaders -> aux (tile landed)
   kKvEmpty = 2,   // [2] PV issuers -> loaders (tile consumed)
-  kSfReady = 4,   // [2] aux -> QK issuers (scale factors in TMEM)
   kSFull = 6,     // [2] QK issuers -> softmax
   kSEmpty = 8,    // [2] softmax -> QK issuers
-  kPFull = 10,    // softmax -> PV issuers (P' and its scale factors written)
   kPvDone = 11,   // PV issuers -> softmax (P' buffer free, O quiescent)
-  kQFull = 12,    // [2] aux -> QK issuers
-  kQEmpty = 14,   // [2] QK issuers -> aux
+  kQEmpty = 14,   // [2] QK issuers -> aux (a q buffer's last QK completed)
   kOFull = 16,    // [2] PV issuers -> aux (a part's O complete)
   kOEmpty = 18,   // [2] aux -> PV issuers and softmax (O buffer read out)
   kEpiReady = 20, // [2] softmax -> aux (a part's m, l, count posted)
@@ -458,11 +453,11 @@ __device__ __noinline__ void aux_stage_q(const AuxCtx& x, int row, int qb) {
       tmem_st16(tmem + lane_base + C::kColSfq + 16 * qb, v);
       tmem_wait_st();
     }
-    named_barrier(2, 128);  // sfq is reused by the next staging
+    // (sfq is reused by the next staging; the aux warps issue the QKs that
+    // read this q only after the barrier that follows the next tile's scale
+    // factors, so this fence orders the q writes before them)
     fence_proxy_async_smem();
     tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bars + kQFull + qb);
   }
 
 // A row part's epilogue (aux warps): out and lse of a whole row, or the
@@ -675,16 +670,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
     for (int s = 0; s < 2; ++s) {
       mbar_init(bars + kKvFull + s, kLoadWarps);
       mbar_init(bars + kKvEmpty + s, 2);
-      mbar_init(bars + kSfReady + s, 4);
       mbar_init(bars + kSFull + s, Cfg<HP>::kQkSplit);
       mbar_init(bars + kSEmpty + s, kSoftmaxWarps);
-      mbar_init(bars + kQFull + s, 4);
       mbar_init(bars + kQEmpty + s, Cfg<HP>::kQkSplit);
       mbar_init(bars + kOFull + s, 2);
       mbar_init(bars + kOEmpty + s, 4);
       mbar_init(bars + kEpiReady + s, kSoftmaxWarps);
     }
-    mbar_init(bars + kPFull, kSoftmaxWarps);
     mbar_init(bars + kPvDone, 2);
     mbar_init(bars + kDrain, Cfg<HP>::kQkSplit + 2);
     mbar_init(bars + kStall, 1);
@@ -698,7 +690,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
     ms->n_merge = 0;
     fence_mbar_init();
   }
-  if (warp == kQkWarp0) {
+  if (warp == kAuxWarp0) {
     tmem_alloc(&ms->tmem_base, 512);
     tmem_relinquish();
   }
@@ -915,11 +907,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
         // two scales; a value leaving E4M3's normal range becomes 0).  e_h is
         // kept in [-20, 17] (a head whose tile terms all lie 2^20 below its
         // reference keeps 2^-10 relative precision on them).
+        if (pass == 0) F8_TR(13, i);
         const int e_h = max(min(int((__float_as_uint(ex2(tm - mr)) >> 23) & 0xFF) - 126, 17), -20);
         const float inv_h = pow2f(7 - e_h);
 #pragma unroll
         for (int h = 0; h < 16; ++h) x[h] = ex2(x[h] - __shfl_sync(0xffffffffu, mr, h));  // x = -inf (masked) gives 0
         lsum[pass] += sum16(x, lane);
+        if (pass == 0) F8_TR(14, i);
         uint32_t hw0[4], lw0[4];  // codes of heads 4k .. 4k + 3
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -933,6 +927,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
           hw0[k] = uint32_t(h0_) | (uint32_t(h1_) << 16);
           lw0[k] = uint32_t(l0_) | (uint32_t(l1_) << 16);
         }
+        if (pass == 0) F8_TR(15, i);
 #pragma unroll 1
         for (int b = 0; b < 4; ++b) {
           // (selects, not indexing: a rolled loop would put sw and es in local memory)
@@ -957,17 +952,45 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
         // P' scale factors of this tile's stage: row group g of B holds head
         // group g (hi rows then lo rows), byte b the factor of dim block b;
         // the same in every TMEM lane quarter (each warp writes its own)
+        if (pass == 0) F8_TR(16, i);
         uint32_t word = 0;
 #pragma unroll
         for (int b = 0; b < 4; ++b) word |= uint32_t(min(max(e_h + es[b] - 8 + 127, 1), 254)) << (8 * b);
         tmem_st1(tmem + lane_base + C::sfp_col(s) + uint32_t(pass), word);
       }
       tmem_wait_st();
+      F8_TR(17, i);
       fence_proxy_async_smem();
       tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bars + kPFull);
+      named_barrier(1, 32 * kSoftmaxWarps);  // the tile's P' and its scale factors are written
       F8_TR(12, i);
+      if (q < 2) {
+        // PV of the tile: warp q issues dim blocks 2 q and 2 q + 1 (block-
+        // major: consecutive MMAs accumulate into the same O block)
+        if (first) wait_warp(bars + kOEmpty + ob, ((pi / C::kNO) & 1) ^ 1, ms, a);
+        tc_fence_after();
+        F8_TR(60, i);
+        if (lane == 0) {
+          const uint32_t st32 = smem_base + s * kStageBytes;
+#pragma unroll 1
+          for (int bb = 0; bb < 2; ++bb) {
+            const int b = 2 * q + bb;
+#pragma unroll 1
+            for (int ch = 0; ch < 4; ++ch) {
+              // V^T: dims of block b (M, contiguous) x keys 32 ch .. (K, rows)
+              const uint64_t ad = smem_desc(st32 + b * kChunk + ch * 4096, 16384, 1024, kSw128);
+              const uint64_t bd = smem_desc(smem_base + p_block(s, ch, b), 8 * kN, 8 * kN, C::kPSw);
+              mma_mxf8_ss(tmem + C::o_col(ob, b), ad, bd, idesc_mxf8(128, kN, 1, 1, 0, b), tmem + C::kColSfv,
+                          tmem + C::sfp_col(s), (first && ch == 0) ? 0u : 1u);
+            }
+          }
+          mma_commit(bars + kPvDone);
+          mma_commit(bars + kKvEmpty + s);
+          if (last) mma_commit(bars + kOFull + ob);
+        }
+        __syncwarp();
+        F8_TR(61, i);
+      }
       if (last) {
         // the part's l and count over its keys, for the aux warps' epilogue
 #pragma unroll
@@ -994,7 +1017,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
         ++pi;
       }
     }
-  } else if (warp < kQkWarp0) {
+    if (q < 2) {
+      // every MMA issued here has completed before TMEM is freed (also after a timeout)
+      if (lane == 0) {
+        mma_commit(bars + kDrain);
+        if (!mbar_wait(bars + kDrain, 0, kWaitLimitNs)) set_abort(ms, a.status);
+      }
+      __syncwarp();
+    }
+  } else if (warp < kLoadWarp0) {
     // =================== aux: scale factors, q staging, epilogues ===================
     const int q = warp - kAuxWarp0;  // TMEM lane quarter
     const int ta = 32 * q + lane;    // 0..127
@@ -1044,9 +1075,45 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
         if (__any_sync(0xffffffffu, foreign) && lane == 0 && a.status) atomicOr(a.status, SMLA_STATUS_FOREIGN_SCALE);
       }
       tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bars + kSfReady + s);
+      named_barrier(2, 128);  // every lane quarter's factors are in TMEM
       F8_TR(41, i);
+      if (q < C::kQkSplit) {
+        // QK of the tile.  16 heads: warp 0 of the aux warps issues latent
+        // K-steps 0-5 and the rope into accumulator 0, warp 1 K-steps 6-15
+        // into accumulator 1; 32 heads: warp 0 alone, one accumulator
+        const int qb = pi % C::kNQ;
+        const int kbeg = q == 0 ? 0 : C::kQkSteps0, kend = q == 0 ? C::kQkSteps0 : 16;
+        wait_warp(bars + kSEmpty + s, ph ^ 1, ms, a);
+        tc_fence_after();
+        F8_TR(30, i);
+        if (lane == 0) {
+          const uint32_t st32 = smem_base + s * kStageBytes;
+          const uint32_t qs = smem_base + C::kOffQ + qb * C::kQBytes;
+          const uint32_t d = tmem + C::s_col(s, q);
+          // latent: K-steps of 32 E4M3 (K-chunk kc = 128 dims = scale block kc)
+#pragma unroll 1
+          for (int ks = kbeg; ks < kend; ++ks) {
+            const int kc = ks >> 2, sub = ks & 3;
+            const uint64_t ad = smem_desc(st32 + kc * kChunk + 32 * sub, 16, 1024, kSw128);
+            const uint64_t bd = smem_desc(qs + kc * C::kQLatChunk + 32 * sub, 16, 1024, kSw128);
+            mma_mxf8_ss(d, ad, bd, idesc_mxf8(128, kN, 0, 0, sub, sub), tmem + C::kColSfa + 16 * s + 4 * kc,
+                        tmem + C::kColSfq + 16 * qb + 4 * kc, ks > kbeg ? 1u : 0u);
+          }
+          if (q == 0) {
+            // rope: 4 K-steps of 16 bf16 into the q_hi columns
+#pragma unroll 1
+            for (int r = 0; r < 4; ++r) {
+              const uint64_t ad = smem_desc(st32 + kOffRope + 32 * r, 16, 1024, kSw128);
+              const uint64_t bd = smem_desc(qs + C::kQOffRope + 32 * r, 16, 1024, kSw128);
+              mma_f16_ss(d, ad, bd, idesc_bf16(128, HP, 0, 0), 1u);
+            }
+          }
+          mma_commit(bars + kSFull + s);
+          if (c.last()) mma_commit(bars + kQEmpty + qb);
+        }
+        __syncwarp();
+        F8_TR(31, i);
+      }
       // (2) the previous part's epilogue, once this part has started
       if (i > 0 && c.first()) {
         aux_epilogue<HP>(actx, prev, pi - 1);
@@ -1067,105 +1134,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
     }
     if (pi > 0) aux_epilogue<HP>(actx, prev, pi - 1);
     F8_TR(44, 0);
-  } else if (warp < kPvWarp0) {
-    // =================== QK issuers ===================
-    // 16 heads: warp kQkWarp0 issues latent K-steps 0-5 and the rope into
-    // accumulator 0, the next warp K-steps 6-15 into accumulator 1 (two
-    // MMA chains in flight); 32 heads: one warp, one accumulator
-    const int half = warp - kQkWarp0;
-    if (half < C::kQkSplit) {
-      Cursor c;
-      c.init(a, row0, P0, cb, ce);
-      int pi = 0;
-      const int kbeg = half == 0 ? 0 : C::kQkSteps0, kend = half == 0 ? C::kQkSteps0 : 16;
-      for (int i = 0; i < n_tiles; ++i, c.advance(a)) {
-        const int s = i & 1;
-        const uint32_t ph = (i >> 1) & 1;
-        const int qb = pi % C::kNQ;
-        const bool first = c.first(), last = c.last();
-        wait_warp(bars + kSfReady + s, ph, ms, a);
-        wait_warp(bars + kSEmpty + s, ph ^ 1, ms, a);
-        if (first) wait_warp(bars + kQFull + qb, (pi / C::kNQ) & 1, ms, a);
-        F8_TR(30, i);
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t st = smem_base + s * kStageBytes;
-          const uint32_t qs = smem_base + C::kOffQ + qb * C::kQBytes;
-          const uint32_t d = tmem + C::s_col(s, half);
-          // latent: K-steps of 32 E4M3 (K-chunk kc = 128 dims = scale block kc)
-#pragma unroll 1
-          for (int ks = kbeg; ks < kend; ++ks) {
-            const int kc = ks >> 2, sub = ks & 3;
-            const uint64_t ad = smem_desc(st + kc * kChunk + 32 * sub, 16, 1024, kSw128);
-            const uint64_t bd = smem_desc(qs + kc * C::kQLatChunk + 32 * sub, 16, 1024, kSw128);
-            mma_mxf8_ss(d, ad, bd, idesc_mxf8(128, kN, 0, 0, sub, sub), tmem + C::kColSfa + 16 * s + 4 * kc,
-                        tmem + C::kColSfq + 16 * qb + 4 * kc, ks > kbeg ? 1u : 0u);
-          }
-          if (half == 0) {
-            // rope: 4 K-steps of 16 bf16 into the q_hi columns
-#pragma unroll 1
-            for (int r = 0; r < 4; ++r) {
-              const uint64_t ad = smem_desc(st + kOffRope + 32 * r, 16, 1024, kSw128);
-              const uint64_t bd = smem_desc(qs + C::kQOffRope + 32 * r, 16, 1024, kSw128);
-              mma_f16_ss(d, ad, bd, idesc_bf16(128, HP, 0, 0), 1u);
-            }
-          }
-          mma_commit(bars + kSFull + s);
-          if (last) mma_commit(bars + kQEmpty + qb);
-        }
-        __syncwarp();
-        F8_TR(31, i);
-        if (last) ++pi;
-      }
-      // every MMA issued here has completed before TMEM is freed (also after a timeout)
+    if (q < C::kQkSplit) {
       if (lane == 0) {
         mma_commit(bars + kDrain);
         if (!mbar_wait(bars + kDrain, 0, kWaitLimitNs)) set_abort(ms, a.status);
       }
       __syncwarp();
     }
-  } else if (warp < kLoadWarp0) {
-    // =================== PV issuers: dim blocks 2 pair, 2 pair + 1 ===================
-    const int pair = warp - kPvWarp0;
-    Cursor c;
-    c.init(a, row0, P0, cb, ce);
-    int pi = 0;
-    for (int i = 0; i < n_tiles; ++i, c.advance(a)) {
-      const int s = i & 1;
-      const int ob = pi % C::kNO;
-      const bool first = c.first(), last = c.last();
-      wait_warp(bars + kPFull, i & 1, ms, a);
-      if (first) wait_warp(bars + kOEmpty + ob, ((pi / C::kNO) & 1) ^ 1, ms, a);
-      F8_TR(60, i);
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t st = smem_base + s * kStageBytes;
-        // block-major: consecutive MMAs accumulate into the same O block
-#pragma unroll 1
-        for (int bb = 0; bb < 2; ++bb) {
-          const int b = 2 * pair + bb;
-#pragma unroll 1
-          for (int ch = 0; ch < 4; ++ch) {
-            // V^T: dims of block b (M, contiguous) x keys 32 ch .. (K, rows)
-            const uint64_t ad = smem_desc(st + b * kChunk + ch * 4096, 16384, 1024, kSw128);
-            const uint64_t bd = smem_desc(smem_base + p_block(s, ch, b), 8 * kN, 8 * kN, C::kPSw);
-            mma_mxf8_ss(tmem + C::o_col(ob, b), ad, bd, idesc_mxf8(128, kN, 1, 1, 0, b), tmem + C::kColSfv,
-                        tmem + C::sfp_col(s), (first && ch == 0) ? 0u : 1u);
-          }
-        }
-        mma_commit(bars + kPvDone);
-        mma_commit(bars + kKvEmpty + s);
-        if (last) mma_commit(bars + kOFull + ob);
-      }
-      __syncwarp();
-      F8_TR(61, i);
-      if (last) ++pi;
-    }
-    if (lane == 0) {
-      mma_commit(bars + kDrain);
-      if (!mbar_wait(bars + kDrain, 0, kWaitLimitNs)) set_abort(ms, a.status);
-    }
-    __syncwarp();
   } else {
     // =================== loaders ===================
     const int lw = warp - kLoadWarp0;
@@ -1233,7 +1208,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
   F8_TR(3, 0);
   tc_fence_before();
   __syncthreads();
-  if (warp == kQkWarp0) {
+  if (warp == kAuxWarp0) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
