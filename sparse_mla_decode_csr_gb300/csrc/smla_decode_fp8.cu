@@ -24,7 +24,7 @@
 // Warp roles (16 warps, 512 threads, one CTA per SM):
 //   0-3   softmax (warp q owns the keys of TMEM lane quarter q of S; all the
 //         CTA's heads, 16 at a time; per-head values live one per lane);
-//         warps 0 and 1 then issue the tile's PV (dim blocks 0-1 and 2-3)
+//         each then issues the tile's PV of one 128-dim block
 //   4-7   aux: E8M0 scale factors of each landed tile into TMEM, then the
 //         tile's QK (16 heads: warps 4 and 5 each issue part of the K-steps
 //         into their own accumulator, two MMA chains in flight; a thread
@@ -120,8 +120,12 @@ template <int HP>
 struct Cfg {
   static constexpr int kN = 2 * HP;                     // N of QK and of PV
   static constexpr int kPass = HP / 16;                 // 16-head groups
-  static constexpr int kQkSplit = HP == 16 ? 2 : 1;     // QK accumulators, one issuer each
-  static constexpr int kQkSteps0 = kQkSplit == 2 ? 6 : 16;  // latent K-steps of issuer 0 (it also issues the rope)
+  // QK: kQkSplit accumulators, one issuer each (16 heads: four issuers of 4
+  // latent K-steps and one rope K-step each, S single-buffered so that the
+  // TMEM columns fit; 32 heads: one issuer, S double-buffered)
+  static constexpr int kQkSplit = HP == 16 ? 4 : 1;
+  static constexpr int kSBuf = HP == 16 ? 1 : 2;
+  static constexpr int kLatSteps = 16 / kQkSplit;       // latent K-steps of an issuer
   static constexpr int kNQ = HP == 16 ? 2 : 1;          // q buffers
   static constexpr int kNO = HP == 16 ? 2 : 1;          // O buffers in TMEM
   static constexpr int kQLatChunk = kN * 128;           // one K-chunk of [q_hi | q_lo]
@@ -141,7 +145,7 @@ struct Cfg {
   static constexpr uint32_t kPSwMask = kN / 16 - 1;
   // TMEM columns
   static constexpr uint32_t kColS = 0;                            // [buffer][accumulator] x kN
-  static constexpr uint32_t kColO = 2 * kQkSplit * kN;            // [buffer][block] x kN
+  static constexpr uint32_t kColO = kSBuf * kQkSplit * kN;        // [buffer][block] x kN
   static constexpr uint32_t kColSfa = kColO + kNO * 4 * kN;       // record scale factors [stage] x 16
   static constexpr uint32_t kColSfq = kColSfa + 32;               // q scale factors [q buffer] x 16
   static constexpr uint32_t kColSfv = kColSfq + 16 * kNQ;         // V^T scale factors (all 1)
@@ -183,6 +187,9 @@ struct Misc {
   int64_t merge_P[2];
   int64_t merge_ca[2];
   int64_t merge_cz[2];
+#ifdef SMLA_TRACE
+  uint64_t merge_t[3];
+#endif
   int64_t merge_slot[2][kMaxInKernelParts];
 };
 // (the 16-byte reads of red_max_t rows and 4-byte reads of sfq rows need these)
@@ -550,47 +557,76 @@ __device__ __noinline__ void aux_epilogue(const AuxCtx& x, const Cursor& pc, int
 // [P2] stage_combine, with the sink, of the rows this CTA completed: every
 // part's (m, l) and O, out and lse of heads [h0, h0 + Hl), the key count, and
 // the row's ticket back to zero.  All threads of the CTA, after its own work.
-// Rows of up to kMaxInKernelParts parts load every part's values at once (all
-// in registers); longer rows (no merge kernel in the plan) go part by part.
+// Warp k finds row k's parts (lane j: CTA ca + j) and loads their key counts;
+// then each thread combines 16 dims of one head (one pass over the row at 16
+// heads), with every part's loads in flight at once for rows of up to
+// kMaxInKernelParts parts (longer rows, which only a plan without the merge
+// kernel leaves here, go part by part).  The key counts are summed last, so
+// that their loads overlap the rest.
 __device__ __noinline__ void end_merge(const DecodeArgs& a, Misc* ms, int tid, int h0, int Hl, int hg, int g,
                                        int64_t T, int64_t G) {
   const int H = a.heads;
   const int n_merge = ms->n_merge;
   __threadfence();  // the other parts' partials, published before their tickets
-  if (tid < n_merge) {
-    const int k = tid;
+  const int warp = tid >> 5, lane = tid & 31;
+  int32_t nv = 0;  // warp k < n_merge: key counts of row k's parts of this lane
+  if (warp < n_merge) {
+    const int k = warp;
     const int64_t P = ms->merge_P[k];
     const int64_t ca = cta_of_tile(P, T, G), cz = cta_of_tile(P + ms->merge_nt[k] - 1, T, G);
-    int n = 0;
-    for (int64_t cc = ca; cc <= cz && n < kMaxInKernelParts; ++cc)
-      if (cta_begin(cc + 1, T, G) > cta_begin(cc, T, G)) ms->merge_slot[k][n++] = slot_of(cc, P, T, G);
-    ms->merge_ca[k] = ca;
-    ms->merge_cz[k] = cz;
+    int32_t n = 0;
+    for (int64_t c0 = ca; c0 <= cz; c0 += 32) {
+      const int64_t cc = c0 + lane;
+      const bool in = cc <= cz && cta_begin(cc + 1, T, G) > cta_begin(cc, T, G);
+      int64_t sl = 0;
+      if (in) {
+        sl = slot_of(cc, P, T, G);
+        nv += __ldcg(a.nv_part + sl);
+      }
+      const uint32_t m = __ballot_sync(0xffffffffu, in);
+      const int j = n + __popc(m & ((1u << lane) - 1u));
+      if (in && j < kMaxInKernelParts) ms->merge_slot[k][j] = sl;
+      n += __popc(m);
+    }
+    if (lane == 0) {
+      ms->merge_ca[k] = ca;
+      ms->merge_cz[k] = cz;
+    }
   }
   __syncthreads();
+#ifdef SMLA_TRACE
+  if (tid == 0) ms->merge_t[0] = globaltimer();
+#endif
 #pragma unroll 1
   for (int k = 0; k < n_merge; ++k) {
     const int row = ms->merge_row[k];
     const int parts = ms->merge_parts[k];
     const int64_t P = ms->merge_P[k];
     const int64_t ca = ms->merge_ca[k], cz = ms->merge_cz[k];
-    // unit u: head h0 + u / 128 of this group, float4 column u % 128 of the 512 latent dims
+    int64_t sl[kMaxInKernelParts];
+#pragma unroll
+    for (int j = 0; j < kMaxInKernelParts; ++j) sl[j] = j < parts ? ms->merge_slot[k][j] : 0;
+    // unit u: head h0 + u / 32 of this group, dims 16 (u % 32) .. + 15
 #pragma unroll 1
-    for (int u = tid; u < Hl * (kLatent / 4); u += kThreads) {
-      const int h = h0 + u / (kLatent / 4), f = u % (kLatent / 4);
+    for (int u = tid; u < Hl * (kLatent / 16); u += kThreads) {
+      const int h = h0 + u / (kLatent / 16), f = u % (kLatent / 16);
       float mrun = -INFINITY, lsum = 0.f;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      float acc[16];
+#pragma unroll
+      for (int d = 0; d < 16; ++d) acc[d] = 0.f;
       if (parts <= kMaxInKernelParts) {
         float2 ml[kMaxInKernelParts];
-        float4 o[kMaxInKernelParts];
+        float4 o[kMaxInKernelParts][4];
 #pragma unroll
         for (int j = 0; j < kMaxInKernelParts; ++j) {
           ml[j] = make_float2(-INFINITY, 0.f);
-          o[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o[j][e] = make_float4(0.f, 0.f, 0.f, 0.f);
           if (j < parts) {
-            const int64_t sl = ms->merge_slot[k][j];
-            ml[j] = __ldcg(reinterpret_cast<const float2*>(a.ml_part) + sl * H + h);
-            o[j] = __ldcg(reinterpret_cast<const float4*>(a.o_part + (sl * H + h) * kLatent) + f);
+            const float4* src = reinterpret_cast<const float4*>(a.o_part + (sl[j] * H + h) * kLatent) + 4 * f;
+            ml[j] = __ldcg(reinterpret_cast<const float2*>(a.ml_part) + sl[j] * H + h);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[j][e] = __ldcg(src + e);
           }
         }
 #pragma unroll
@@ -600,44 +636,70 @@ __device__ __noinline__ void end_merge(const DecodeArgs& a, Misc* ms, int tid, i
         for (int j = 0; j < kMaxInKernelParts; ++j) {
           const float wt = ml[j].y != 0.f ? ex2(ml[j].x - mrun) : 0.f;  // a NaN m or l stays NaN
           lsum = fmaf(ml[j].y, wt, lsum);
-          acc.x = fmaf(wt, o[j].x, acc.x); acc.y = fmaf(wt, o[j].y, acc.y);
-          acc.z = fmaf(wt, o[j].z, acc.z); acc.w = fmaf(wt, o[j].w, acc.w);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            acc[4 * e] = fmaf(wt, o[j][e].x, acc[4 * e]);
+            acc[4 * e + 1] = fmaf(wt, o[j][e].y, acc[4 * e + 1]);
+            acc[4 * e + 2] = fmaf(wt, o[j][e].z, acc[4 * e + 2]);
+            acc[4 * e + 3] = fmaf(wt, o[j][e].w, acc[4 * e + 3]);
+          }
         }
       } else {
 #pragma unroll 1
         for (int64_t cc = ca; cc <= cz; ++cc) {
           if (!(cta_begin(cc + 1, T, G) > cta_begin(cc, T, G))) continue;
-          const int64_t sl = slot_of(cc, P, T, G);
-          const float2 mj = __ldcg(reinterpret_cast<const float2*>(a.ml_part) + sl * H + h);
-          const float4 oj = __ldcg(reinterpret_cast<const float4*>(a.o_part + (sl * H + h) * kLatent) + f);
+          const int64_t s1 = slot_of(cc, P, T, G);
+          const float4* src = reinterpret_cast<const float4*>(a.o_part + (s1 * H + h) * kLatent) + 4 * f;
+          const float2 mj = __ldcg(reinterpret_cast<const float2*>(a.ml_part) + s1 * H + h);
+          float4 oj[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) oj[e] = __ldcg(src + e);
           if (mj.y == 0.f) continue;
           if (mj.x > mrun) {  // the running maximum moves: rescale what was summed
             const float r = ex2(mrun - mj.x);
             lsum *= r;
-            acc.x *= r; acc.y *= r; acc.z *= r; acc.w *= r;
+#pragma unroll
+            for (int d = 0; d < 16; ++d) acc[d] *= r;
             mrun = mj.x;
           }
           const float wt = ex2(mj.x - mrun);
           lsum = fmaf(mj.y, wt, lsum);
-          acc.x = fmaf(wt, oj.x, acc.x); acc.y = fmaf(wt, oj.y, acc.y);
-          acc.z = fmaf(wt, oj.z, acc.z); acc.w = fmaf(wt, oj.w, acc.w);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            acc[4 * e] = fmaf(wt, oj[e].x, acc[4 * e]);
+            acc[4 * e + 1] = fmaf(wt, oj[e].y, acc[4 * e + 1]);
+            acc[4 * e + 2] = fmaf(wt, oj[e].z, acc[4 * e + 2]);
+            acc[4 * e + 3] = fmaf(wt, oj[e].w, acc[4 * e + 3]);
+          }
         }
       }
       float fac, lse_h;
       finish_head(mrun, lsum, a.sink, h, &fac, &lse_h);
-      uint2 v;
-      v.x = pack_bf16x2(acc.x * fac, acc.y * fac);
-      v.y = pack_bf16x2(acc.z * fac, acc.w * fac);
-      *reinterpret_cast<uint2*>(a.out + int64_t(row) * a.out_stride_row + int64_t(h) * a.out_stride_head + 4 * f) = v;
+      uint4 v0, v1;
+      v0.x = pack_bf16x2(acc[0] * fac, acc[1] * fac);
+      v0.y = pack_bf16x2(acc[2] * fac, acc[3] * fac);
+      v0.z = pack_bf16x2(acc[4] * fac, acc[5] * fac);
+      v0.w = pack_bf16x2(acc[6] * fac, acc[7] * fac);
+      v1.x = pack_bf16x2(acc[8] * fac, acc[9] * fac);
+      v1.y = pack_bf16x2(acc[10] * fac, acc[11] * fac);
+      v1.z = pack_bf16x2(acc[12] * fac, acc[13] * fac);
+      v1.w = pack_bf16x2(acc[14] * fac, acc[15] * fac);
+      uint4* dst = reinterpret_cast<uint4*>(a.out + int64_t(row) * a.out_stride_row + int64_t(h) * a.out_stride_head + 16 * f);
+      dst[0] = v0;
+      dst[1] = v1;
       if (f == 0 && a.lse) a.lse[int64_t(row) * H + h] = lse_h;
     }
-    if (tid == 0) {
-      if (g == 0 && a.n_valid) {
-        int32_t nv = 0;
-        for (int64_t cc = ca; cc <= cz; ++cc)
-          if (cta_begin(cc + 1, T, G) > cta_begin(cc, T, G)) nv += __ldcg(a.nv_part + slot_of(cc, P, T, G));
-        a.n_valid[row] = nv;
-      }
+#ifdef SMLA_TRACE
+    if (tid == 0) ms->merge_t[1 + k] = globaltimer();
+#endif
+  }
+  // key counts and tickets (warp k: row k)
+  if (warp < n_merge) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) nv += __shfl_xor_sync(0xffffffffu, nv, o);
+    if (lane == 0) {
+      const int row = ms->merge_row[warp];
+      if (g == 0 && a.n_valid) a.n_valid[row] = nv;
       a.ticket[int64_t(row) * hg + g] = 0;  // ready for the next call
     }
   }
@@ -669,16 +731,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
   if (tid == 0) {
     for (int s = 0; s < 2; ++s) {
       mbar_init(bars + kKvFull + s, kLoadWarps);
-      mbar_init(bars + kKvEmpty + s, 2);
-      mbar_init(bars + kSFull + s, Cfg<HP>::kQkSplit);
+      mbar_init(bars + kKvEmpty + s, kSoftmaxWarps);  // the four PV issuers
+      mbar_init(bars + kSFull + s, Cfg<HP>::kQkSplit);  // [S buffer] (one or two used)
       mbar_init(bars + kSEmpty + s, kSoftmaxWarps);
       mbar_init(bars + kQEmpty + s, Cfg<HP>::kQkSplit);
-      mbar_init(bars + kOFull + s, 2);
+      mbar_init(bars + kOFull + s, kSoftmaxWarps);
       mbar_init(bars + kOEmpty + s, 4);
       mbar_init(bars + kEpiReady + s, kSoftmaxWarps);
     }
-    mbar_init(bars + kPvDone, 2);
-    mbar_init(bars + kDrain, Cfg<HP>::kQkSplit + 2);
+    mbar_init(bars + kPvDone, kSoftmaxWarps);
+    mbar_init(bars + kDrain, Cfg<HP>::kQkSplit + kSoftmaxWarps);
     mbar_init(bars + kStall, 1);
     ms->stall = g_fp8_stall;
     ms->abort = 0;
@@ -797,7 +859,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
         nv = 0;
       }
       if (i == 0 && ms->stall) wait_warp(bars + kStall, 0, ms, a);
-      wait_warp(bars + kSFull + s, ph, ms, a);
+      const int sb = i % C::kSBuf;                  // S buffer
+      const uint32_t sph = (i / C::kSBuf) & 1;
+      wait_warp(bars + kSFull + sb, sph, ms, a);
       wait_warp(bars + kKvFull + s, ph, ms, a);  // (already complete) orders the loaders' ids and scales
       F8_TR(10, i);
       tc_fence_after();
@@ -824,11 +888,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
           const float xs = a.sm_scale_log2;
 #pragma unroll
           for (int h = 0; h < 16; ++h) x[h] = 0.f;
-#pragma unroll
+#pragma unroll 1
           for (int k = 0; k < 2 * C::kQkSplit; ++k) {
-            // accumulator k / 2, q_hi columns (+ rope) then q_lo columns
+            // accumulator k / 2: q_hi columns (+ rope), then q_lo columns
             uint32_t r[16];
-            tmem_ld16(tmem + lane_base + C::s_col(s, k >> 1) + (k & 1) * HP + 16 * pass, r);
+            tmem_ld16(tmem + lane_base + C::s_col(sb, k >> 1) + (k & 1) * HP + 16 * pass, r);
             tmem_wait_ld();
 #pragma unroll
             for (int h = 0; h < 16; ++h) x[h] += __uint_as_float(r[h]);
@@ -839,7 +903,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
         if (pass == C::kPass - 1) {
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(bars + kSEmpty + s);  // S read
+          if (lane == 0) mbar_arrive(bars + kSEmpty + sb);  // S read
         }
 #pragma unroll
         for (int h = 0; h < 16; ++h) {
@@ -862,9 +926,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
           const float alpha = ex2(mr - mn);
           mr = mn;
           lsum[pass] *= __shfl_sync(0xffffffffu, alpha, hs);
-          float al[16];
-#pragma unroll
-          for (int h = 0; h < 16; ++h) al[h] = __shfl_sync(0xffffffffu, alpha, h);
           // O holds PV of this part's earlier tiles: wait until they completed,
           // then rescale this pass's heads (hi and lo columns) in this lane quarter
           if (!pv_waited) {
@@ -879,7 +940,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
             tmem_ld16(ta, v);
             tmem_wait_ld();
 #pragma unroll
-            for (int h = 0; h < 16; ++h) v[h] = __float_as_uint(__uint_as_float(v[h]) * al[h]);
+            for (int h = 0; h < 16; ++h) v[h] = __float_as_uint(__uint_as_float(v[h]) * __shfl_sync(0xffffffffu, alpha, h));
             tmem_st16(ta, v);
           }
           tmem_wait_st();
@@ -964,25 +1025,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
       tc_fence_before();
       named_barrier(1, 32 * kSoftmaxWarps);  // the tile's P' and its scale factors are written
       F8_TR(12, i);
-      if (q < 2) {
-        // PV of the tile: warp q issues dim blocks 2 q and 2 q + 1 (block-
-        // major: consecutive MMAs accumulate into the same O block)
+      {
+        // PV of the tile: warp q issues dim block b = q (four MMA chains in
+        // flight, one per O block)
         if (first) wait_warp(bars + kOEmpty + ob, ((pi / C::kNO) & 1) ^ 1, ms, a);
         tc_fence_after();
         F8_TR(60, i);
         if (lane == 0) {
           const uint32_t st32 = smem_base + s * kStageBytes;
+          const int b = q;
 #pragma unroll 1
-          for (int bb = 0; bb < 2; ++bb) {
-            const int b = 2 * q + bb;
-#pragma unroll 1
-            for (int ch = 0; ch < 4; ++ch) {
-              // V^T: dims of block b (M, contiguous) x keys 32 ch .. (K, rows)
-              const uint64_t ad = smem_desc(st32 + b * kChunk + ch * 4096, 16384, 1024, kSw128);
-              const uint64_t bd = smem_desc(smem_base + p_block(s, ch, b), 8 * kN, 8 * kN, C::kPSw);
-              mma_mxf8_ss(tmem + C::o_col(ob, b), ad, bd, idesc_mxf8(128, kN, 1, 1, 0, b), tmem + C::kColSfv,
-                          tmem + C::sfp_col(s), (first && ch == 0) ? 0u : 1u);
-            }
+          for (int ch = 0; ch < 4; ++ch) {
+            // V^T: dims of block b (M, contiguous) x keys 32 ch .. (K, rows)
+            const uint64_t ad = smem_desc(st32 + b * kChunk + ch * 4096, 16384, 1024, kSw128);
+            const uint64_t bd = smem_desc(smem_base + p_block(s, ch, b), 8 * kN, 8 * kN, C::kPSw);
+            mma_mxf8_ss(tmem + C::o_col(ob, b), ad, bd, idesc_mxf8(128, kN, 1, 1, 0, b), tmem + C::kColSfv,
+                        tmem + C::sfp_col(s), (first && ch == 0) ? 0u : 1u);
           }
           mma_commit(bars + kPvDone);
           mma_commit(bars + kKvEmpty + s);
@@ -1017,7 +1075,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
         ++pi;
       }
     }
-    if (q < 2) {
+    {
       // every MMA issued here has completed before TMEM is freed (also after a timeout)
       if (lane == 0) {
         mma_commit(bars + kDrain);
@@ -1078,18 +1136,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
       named_barrier(2, 128);  // every lane quarter's factors are in TMEM
       F8_TR(41, i);
       if (q < C::kQkSplit) {
-        // QK of the tile.  16 heads: warp 0 of the aux warps issues latent
-        // K-steps 0-5 and the rope into accumulator 0, warp 1 K-steps 6-15
-        // into accumulator 1; 32 heads: warp 0 alone, one accumulator
+        // QK of the tile.  16 heads: aux warp q issues latent K-steps
+        // 4 q .. 4 q + 3 and rope K-step q into accumulator q; 32 heads: aux
+        // warp 0 alone, one accumulator
         const int qb = pi % C::kNQ;
-        const int kbeg = q == 0 ? 0 : C::kQkSteps0, kend = q == 0 ? C::kQkSteps0 : 16;
-        wait_warp(bars + kSEmpty + s, ph ^ 1, ms, a);
+        const int kbeg = q * C::kLatSteps, kend = kbeg + C::kLatSteps;
+        const int rbeg = C::kQkSplit == 4 ? q : (q == 0 ? 0 : 4), rend = C::kQkSplit == 4 ? q + 1 : 4;
+        const int sb = i % C::kSBuf;
+        const uint32_t sph = (i / C::kSBuf) & 1;
+        wait_warp(bars + kSEmpty + sb, sph ^ 1, ms, a);
         tc_fence_after();
         F8_TR(30, i);
         if (lane == 0) {
           const uint32_t st32 = smem_base + s * kStageBytes;
           const uint32_t qs = smem_base + C::kOffQ + qb * C::kQBytes;
-          const uint32_t d = tmem + C::s_col(s, q);
+          const uint32_t d = tmem + C::s_col(sb, q);
           // latent: K-steps of 32 E4M3 (K-chunk kc = 128 dims = scale block kc)
 #pragma unroll 1
           for (int ks = kbeg; ks < kend; ++ks) {
@@ -1099,16 +1160,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
             mma_mxf8_ss(d, ad, bd, idesc_mxf8(128, kN, 0, 0, sub, sub), tmem + C::kColSfa + 16 * s + 4 * kc,
                         tmem + C::kColSfq + 16 * qb + 4 * kc, ks > kbeg ? 1u : 0u);
           }
-          if (q == 0) {
-            // rope: 4 K-steps of 16 bf16 into the q_hi columns
+          {
+            // rope: K-steps of 16 bf16 into the q_hi columns
 #pragma unroll 1
-            for (int r = 0; r < 4; ++r) {
+            for (int r = rbeg; r < rend; ++r) {
               const uint64_t ad = smem_desc(st32 + kOffRope + 32 * r, 16, 1024, kSw128);
               const uint64_t bd = smem_desc(qs + C::kQOffRope + 32 * r, 16, 1024, kSw128);
               mma_f16_ss(d, ad, bd, idesc_bf16(128, HP, 0, 0), 1u);
             }
           }
-          mma_commit(bars + kSFull + s);
+          mma_commit(bars + kSFull + sb);
           if (c.last()) mma_commit(bars + kQEmpty + qb);
         }
         __syncwarp();
@@ -1216,6 +1277,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
   F8_TR(4, ms->n_merge);
   if (ms->n_merge > 0) end_merge(a, ms, tid, h0, Hl, hg, g, T, G);
   F8_TR(5, 0);
+#ifdef SMLA_TRACE
+  if (tid == 0 && tr_buf != nullptr && ms->n_merge > 0) {
+    for (int k = 0; k <= ms->n_merge; ++k)
+      tr_buf[(size_t(blockIdx.x) * 20 + 19) * 256 + k] = (ms->merge_t[k] & 0xFFFFFFFFFFFFull) | (uint64_t(70 + k) << 48);
+  }
+#endif
 }
 
 }  // namespace

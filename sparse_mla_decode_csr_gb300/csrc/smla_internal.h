@@ -19,7 +19,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 // Rows shared by at most this many CTAs are merged inside the native-fp8
 // decode kernel (by the CTA whose part completes the row); rows of more parts
 // are left to the merge kernel when the plan launches it.
-constexpr int kMaxInKernelParts = 8;
+constexpr int kMaxInKernelParts = 4;
 
 // Workspace offsets of one plan (see smla_decode_workspace_size in smla.h).
 struct WorkspaceLayout {

@@ -290,7 +290,7 @@ __host__ __device__ constexpr uint32_t idesc_mxf8(int m, int n, int a_mn, int b_
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
-  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));  // (results below 2^-126 flush to 0)
   return y;
 }
 
