@@ -121,10 +121,10 @@ struct Cfg {
   static constexpr int kN = 2 * HP;                     // N of QK and of PV
   static constexpr int kPass = HP / 16;                 // 16-head groups
   // QK: kQkSplit accumulators, one issuer each (16 heads: four issuers of 4
-  // latent K-steps and one rope K-step each, S single-buffered so that the
-  // TMEM columns fit; 32 heads: one issuer, S double-buffered)
-  static constexpr int kQkSplit = HP == 16 ? 4 : 1;
-  static constexpr int kSBuf = HP == 16 ? 1 : 2;
+  // latent K-steps and one rope K-step each; 32 heads: two issuers of 8 and
+  // 2); S single-buffered so that the TMEM columns fit
+  static constexpr int kQkSplit = HP == 16 ? 4 : 2;
+  static constexpr int kSBuf = 1;
   static constexpr int kLatSteps = 16 / kQkSplit;       // latent K-steps of an issuer
   static constexpr int kNQ = HP == 16 ? 2 : 1;          // q buffers
   static constexpr int kNO = HP == 16 ? 2 : 1;          // O buffers in TMEM
@@ -180,17 +180,22 @@ struct Misc {
   int32_t part_nv[2];
   uint8_t sfq[2 * kMaxHP][16];                  // q scale-factor bytes of the part being staged
   float fac[kMaxHP];                            // epilogue: output factors of a whole row's heads
+  int32_t last_row;                             // schedule: the row of this CTA's last slot
+  int64_t last_tile;                            //   and that row's first slot
+  // the CTAs sharing this CTA's first (x = 0) and last (x = 1) row: their
+  // number, the range [ca, cz] they lie in, and the slots of the first
+  // kMaxInKernelParts of them (found after the prologue, used by the merge)
+  int32_t mparts[2];
+  int64_t mP[2];                                // the row's first tile slot
+  int64_t mca[2];
+  int64_t mcz[2];
+  int64_t mslot[2][kMaxInKernelParts];
   int32_t n_merge;                              // rows this CTA completes and merges at its end
   int32_t merge_row[2];
-  int32_t merge_nt[2];
-  int32_t merge_parts[2];
-  int64_t merge_P[2];
-  int64_t merge_ca[2];
-  int64_t merge_cz[2];
+  int32_t merge_x[2];                           // which of the two rows above
 #ifdef SMLA_TRACE
   uint64_t merge_t[3];
 #endif
-  int64_t merge_slot[2][kMaxInKernelParts];
 };
 // (the 16-byte reads of red_max_t rows and 4-byte reads of sfq rows need these)
 static_assert(offsetof(Misc, red_max_t) % 16 == 0 && offsetof(Misc, sfq) % 4 == 0, "Misc layout");
@@ -210,7 +215,8 @@ enum Bar {
   kOEmpty = 18,   // [2] aux -> PV issuers and softmax (O buffer read out)
   kEpiReady = 20, // [2] softmax -> aux (a part's m, l, count posted)
   kDrain = 22,    // MMA issuers: every MMA they issued has completed
-  kStall = 23     // never signalled (timeout-path test)
+  kStall = 23,    // never signalled (timeout-path test)
+  kMerge = 24     // the end merge's bulk copies
 };
 
 __device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t chunk16) {
@@ -538,17 +544,16 @@ __device__ __noinline__ void aux_epilogue(const AuxCtx& x, const Cursor& pc, int
   if (lane == 0) mbar_arrive(bars + kOEmpty + ob);
   if (!whole && ta == 0) {
     // the CTAs holding this row's tiles ([P2] stage_split parts); the one whose
-    // part arrives last merges the row (this head group) after its own work
-    const int64_t ca = cta_of_tile(pc.P, T, G), cz = cta_of_tile(pc.P + pc.ntiles - 1, T, G);
-    int32_t parts = 0;
-    for (int64_t cc = ca; cc <= cz; ++cc) parts += cta_begin(cc + 1, T, G) > cta_begin(cc, T, G);
+    // part arrives last merges the row (this head group) after its own work.
+    // A shared row is this CTA's first or last one (xi = 0 or 1)
+    const int xi = pi == 0 ? 0 : 1;
+    const int32_t parts = ms->mparts[xi];
     if (parts <= kMaxInKernelParts || !a.merge_kernel) {
       if (atomicAdd(a.ticket + int64_t(row) * x.hg + x.g, 1) == parts - 1) {
+        __threadfence();  // (acquire: the other parts' partials are read after this)
         const int k = ms->n_merge++;
         ms->merge_row[k] = row;
-        ms->merge_P[k] = pc.P;
-        ms->merge_nt[k] = pc.ntiles;
-        ms->merge_parts[k] = parts;
+        ms->merge_x[k] = xi;
       }
     }
   }
@@ -556,95 +561,104 @@ __device__ __noinline__ void aux_epilogue(const AuxCtx& x, const Cursor& pc, int
 
 // [P2] stage_combine, with the sink, of the rows this CTA completed: every
 // part's (m, l) and O, out and lse of heads [h0, h0 + Hl), the key count, and
-// the row's ticket back to zero.  All threads of the CTA, after its own work.
-// Warp k finds row k's parts (lane j: CTA ca + j) and loads their key counts;
-// then each thread combines 16 dims of one head (one pass over the row at 16
-// heads), with every part's loads in flight at once for rows of up to
-// kMaxInKernelParts parts (longer rows, which only a plan without the merge
-// kernel leaves here, go part by part).  The key counts are summed last, so
-// that their loads overlap the rest.
-__device__ __noinline__ void end_merge(const DecodeArgs& a, Misc* ms, int tid, int h0, int Hl, int hg, int g,
-                                       int64_t T, int64_t G) {
+// the row's ticket back to zero.  All threads of the CTA, after its own work
+// (the stages' shared memory is free then).  The parts' slots were found
+// after the prologue.  For rows of up to kMaxInKernelParts parts, one thread
+// copies each part's O rows of 16 heads (32 KB) into shared memory with bulk
+// copies (a plain-load gather of the same bytes is limited by the SM's load
+// throughput), the threads load the (m, l) meanwhile, then each thread
+// combines 16 dims of one head.  Longer rows (only a plan without the merge
+// kernel leaves them here) go part by part with plain loads.  Warp k loads
+// row k's key counts first and sums them last.
+static_assert(16 * (kLatent / 16) <= kThreads, "one merge unit per thread");
+static_assert(kMaxInKernelParts * 16 * kLatent * 4 <= kStages * kStageBytes, "merge staging fits the stages");
+__device__ __noinline__ void end_merge(const DecodeArgs& a, uint8_t* smem, uint64_t* bar, Misc* ms, int tid,
+                                       int h0, int Hl, int hg, int g, int64_t T, int64_t G) {
   const int H = a.heads;
   const int n_merge = ms->n_merge;
-  __threadfence();  // the other parts' partials, published before their tickets
   const int warp = tid >> 5, lane = tid & 31;
   int32_t nv = 0;  // warp k < n_merge: key counts of row k's parts of this lane
   if (warp < n_merge) {
-    const int k = warp;
-    const int64_t P = ms->merge_P[k];
-    const int64_t ca = cta_of_tile(P, T, G), cz = cta_of_tile(P + ms->merge_nt[k] - 1, T, G);
-    int32_t n = 0;
-    for (int64_t c0 = ca; c0 <= cz; c0 += 32) {
-      const int64_t cc = c0 + lane;
-      const bool in = cc <= cz && cta_begin(cc + 1, T, G) > cta_begin(cc, T, G);
-      int64_t sl = 0;
-      if (in) {
-        sl = slot_of(cc, P, T, G);
-        nv += __ldcg(a.nv_part + sl);
-      }
-      const uint32_t m = __ballot_sync(0xffffffffu, in);
-      const int j = n + __popc(m & ((1u << lane) - 1u));
-      if (in && j < kMaxInKernelParts) ms->merge_slot[k][j] = sl;
-      n += __popc(m);
-    }
-    if (lane == 0) {
-      ms->merge_ca[k] = ca;
-      ms->merge_cz[k] = cz;
+    const int xi = ms->merge_x[warp];
+    const int parts = ms->mparts[xi];
+    if (parts <= kMaxInKernelParts) {
+      if (lane < parts) nv = __ldcg(a.nv_part + ms->mslot[xi][lane]);
+    } else {
+      const int64_t ca = ms->mca[xi], cz = ms->mcz[xi], P = ms->mP[xi];
+      for (int64_t cc = ca + lane; cc <= cz; cc += 32)
+        if (cta_begin(cc + 1, T, G) > cta_begin(cc, T, G)) nv += __ldcg(a.nv_part + slot_of(cc, P, T, G));
     }
   }
-  __syncthreads();
 #ifdef SMLA_TRACE
   if (tid == 0) ms->merge_t[0] = globaltimer();
 #endif
+  uint32_t uses = 0;  // completed phases of `bar`
+  bool ok = true;
 #pragma unroll 1
   for (int k = 0; k < n_merge; ++k) {
     const int row = ms->merge_row[k];
-    const int parts = ms->merge_parts[k];
-    const int64_t P = ms->merge_P[k];
-    const int64_t ca = ms->merge_ca[k], cz = ms->merge_cz[k];
+    const int xi = ms->merge_x[k];
+    const int parts = ms->mparts[xi];
+    const int64_t P = ms->mP[xi], ca = ms->mca[xi], cz = ms->mcz[xi];
     int64_t sl[kMaxInKernelParts];
 #pragma unroll
-    for (int j = 0; j < kMaxInKernelParts; ++j) sl[j] = j < parts ? ms->merge_slot[k][j] : 0;
-    // unit u: head h0 + u / 32 of this group, dims 16 (u % 32) .. + 15
+    for (int j = 0; j < kMaxInKernelParts; ++j) sl[j] = j < parts ? ms->mslot[xi][j] : 0;
 #pragma unroll 1
-    for (int u = tid; u < Hl * (kLatent / 16); u += kThreads) {
-      const int h = h0 + u / (kLatent / 16), f = u % (kLatent / 16);
+    for (int hc = 0; hc < Hl; hc += 16) {  // 16 heads at a time
+      const int nh = min(16, Hl - hc);
+      const bool staged = parts <= kMaxInKernelParts;
+      if (staged) {
+        __syncthreads();  // the buffer's previous contents were read
+        if (tid == 0) {
+          fence_proxy_async_global();  // (this CTA's own partial was written by plain stores)
+          mbar_arrive_expect_tx(bar, uint32_t(parts * nh * kLatent * 4));
+          for (int j = 0; j < parts; ++j)
+            bulk_g2s(smem_u32(smem + j * (16 * kLatent * 4)), a.o_part + (sl[j] * H + h0 + hc) * kLatent,
+                     uint32_t(nh * kLatent * 4), bar);
+        }
+      }
+      // unit u: head h0 + hc + u / 32, dims 16 (u % 32) .. + 15
+      const int u = tid;
+      const bool active = u < nh * (kLatent / 16);
+      const int hh = u / (kLatent / 16), f = u % (kLatent / 16);
+      const int h = h0 + hc + hh;
       float mrun = -INFINITY, lsum = 0.f;
       float acc[16];
 #pragma unroll
       for (int d = 0; d < 16; ++d) acc[d] = 0.f;
-      if (parts <= kMaxInKernelParts) {
+      if (staged) {
         float2 ml[kMaxInKernelParts];
-        float4 o[kMaxInKernelParts][4];
 #pragma unroll
         for (int j = 0; j < kMaxInKernelParts; ++j) {
           ml[j] = make_float2(-INFINITY, 0.f);
+          if (active && j < parts) ml[j] = __ldcg(reinterpret_cast<const float2*>(a.ml_part) + sl[j] * H + h);
+        }
+        if (!mbar_wait(bar, uses & 1, kWaitLimitNs)) {
+          set_abort(ms, a.status);
+          ok = false;
+        }
+        ++uses;
+        if (active && ok) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) o[j][e] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (j < parts) {
-            const float4* src = reinterpret_cast<const float4*>(a.o_part + (sl[j] * H + h) * kLatent) + 4 * f;
-            ml[j] = __ldcg(reinterpret_cast<const float2*>(a.ml_part) + sl[j] * H + h);
+          for (int j = 0; j < kMaxInKernelParts; ++j)
+            if (ml[j].y != 0.f) mrun = fmaxf(mrun, ml[j].x);  // parts without keys (l = 0) take no part
 #pragma unroll
-            for (int e = 0; e < 4; ++e) o[j][e] = __ldcg(src + e);
+          for (int j = 0; j < kMaxInKernelParts; ++j) {
+            if (j >= parts) continue;
+            const float wt = ml[j].y != 0.f ? ex2(ml[j].x - mrun) : 0.f;  // a NaN m or l stays NaN
+            lsum = fmaf(ml[j].y, wt, lsum);
+            const uint32_t src = smem_u32(smem + j * (16 * kLatent * 4) + (hh * kLatent + 16 * f) * 4);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const uint4 o4 = ld_shared_v4(src + 16 * e);
+              acc[4 * e] = fmaf(wt, __uint_as_float(o4.x), acc[4 * e]);
+              acc[4 * e + 1] = fmaf(wt, __uint_as_float(o4.y), acc[4 * e + 1]);
+              acc[4 * e + 2] = fmaf(wt, __uint_as_float(o4.z), acc[4 * e + 2]);
+              acc[4 * e + 3] = fmaf(wt, __uint_as_float(o4.w), acc[4 * e + 3]);
+            }
           }
         }
-#pragma unroll
-        for (int j = 0; j < kMaxInKernelParts; ++j)
-          if (ml[j].y != 0.f) mrun = fmaxf(mrun, ml[j].x);  // parts without keys (l = 0) take no part
-#pragma unroll
-        for (int j = 0; j < kMaxInKernelParts; ++j) {
-          const float wt = ml[j].y != 0.f ? ex2(ml[j].x - mrun) : 0.f;  // a NaN m or l stays NaN
-          lsum = fmaf(ml[j].y, wt, lsum);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            acc[4 * e] = fmaf(wt, o[j][e].x, acc[4 * e]);
-            acc[4 * e + 1] = fmaf(wt, o[j][e].y, acc[4 * e + 1]);
-            acc[4 * e + 2] = fmaf(wt, o[j][e].z, acc[4 * e + 2]);
-            acc[4 * e + 3] = fmaf(wt, o[j][e].w, acc[4 * e + 3]);
-          }
-        }
-      } else {
+      } else if (active) {
 #pragma unroll 1
         for (int64_t cc = ca; cc <= cz; ++cc) {
           if (!(cta_begin(cc + 1, T, G) > cta_begin(cc, T, G))) continue;
@@ -673,21 +687,23 @@ __device__ __noinline__ void end_merge(const DecodeArgs& a, Misc* ms, int tid, i
           }
         }
       }
-      float fac, lse_h;
-      finish_head(mrun, lsum, a.sink, h, &fac, &lse_h);
-      uint4 v0, v1;
-      v0.x = pack_bf16x2(acc[0] * fac, acc[1] * fac);
-      v0.y = pack_bf16x2(acc[2] * fac, acc[3] * fac);
-      v0.z = pack_bf16x2(acc[4] * fac, acc[5] * fac);
-      v0.w = pack_bf16x2(acc[6] * fac, acc[7] * fac);
-      v1.x = pack_bf16x2(acc[8] * fac, acc[9] * fac);
-      v1.y = pack_bf16x2(acc[10] * fac, acc[11] * fac);
-      v1.z = pack_bf16x2(acc[12] * fac, acc[13] * fac);
-      v1.w = pack_bf16x2(acc[14] * fac, acc[15] * fac);
-      uint4* dst = reinterpret_cast<uint4*>(a.out + int64_t(row) * a.out_stride_row + int64_t(h) * a.out_stride_head + 16 * f);
-      dst[0] = v0;
-      dst[1] = v1;
-      if (f == 0 && a.lse) a.lse[int64_t(row) * H + h] = lse_h;
+      if (active) {
+        float fac, lse_h;
+        finish_head(mrun, lsum, a.sink, h, &fac, &lse_h);
+        uint4 v0, v1;
+        v0.x = pack_bf16x2(acc[0] * fac, acc[1] * fac);
+        v0.y = pack_bf16x2(acc[2] * fac, acc[3] * fac);
+        v0.z = pack_bf16x2(acc[4] * fac, acc[5] * fac);
+        v0.w = pack_bf16x2(acc[6] * fac, acc[7] * fac);
+        v1.x = pack_bf16x2(acc[8] * fac, acc[9] * fac);
+        v1.y = pack_bf16x2(acc[10] * fac, acc[11] * fac);
+        v1.z = pack_bf16x2(acc[12] * fac, acc[13] * fac);
+        v1.w = pack_bf16x2(acc[14] * fac, acc[15] * fac);
+        uint4* dst = reinterpret_cast<uint4*>(a.out + int64_t(row) * a.out_stride_row + int64_t(h) * a.out_stride_head + 16 * f);
+        dst[0] = v0;
+        dst[1] = v1;
+        if (f == 0 && a.lse) a.lse[int64_t(row) * H + h] = lse_h;
+      }
     }
 #ifdef SMLA_TRACE
     if (tid == 0) ms->merge_t[1 + k] = globaltimer();
@@ -742,12 +758,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
     mbar_init(bars + kPvDone, kSoftmaxWarps);
     mbar_init(bars + kDrain, Cfg<HP>::kQkSplit + kSoftmaxWarps);
     mbar_init(bars + kStall, 1);
+    mbar_init(bars + kMerge, 1);
     ms->stall = g_fp8_stall;
     ms->abort = 0;
     const uint64_t w = g_fp8_wait_ns;
     ms->wait_ns = w != 0 ? w : kWaitLimitNs;
     ms->first_row = a.n_q;
     ms->first_tile = 0;
+    ms->last_row = a.n_q;
+    ms->last_tile = 0;
+    ms->mparts[0] = ms->mparts[1] = 0;
     ms->n_tiles = 0;
     ms->n_merge = 0;
     fence_mbar_init();
@@ -796,6 +816,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
       if (P <= b && b < P + w) {
         ms->first_row = r;
         ms->first_tile = P;
+      }
+      // the row of this CTA's last tile: e - 1 is one of its tile slots, or
+      // one of the next row's start slots right after them
+      if ((P + kRowStart <= e - 1 && e - 1 < P + w) || (P + w <= e - 1 && e - 1 < P + w + kRowStart && P + w - 1 >= b)) {
+        ms->last_row = r;
+        ms->last_tile = P;
       }
       const int64_t t0 = P + kRowStart;
       const int64_t lo_t = b > t0 ? b : t0, hi_t = e < t0 + nt_r ? e : t0 + nt_r;
@@ -1103,6 +1129,33 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
     Cursor c;
     c.init(a, row0, P0, cb, ce);
     if (n_tiles > 0) aux_stage_q<HP>(actx, c.row, 0);
+    if (q < 2 && n_tiles > 0) {
+      // the CTAs sharing this CTA's first (q = 0) and last (q = 1) row, for
+      // a merge at the end (lane j looks at CTA ca + j; no waits, while the
+      // first tile is still in flight)
+      const int32_t r = q == 0 ? row0 : ms->last_row;
+      if (r < a.n_q) {
+        const int64_t Pr = (q == 0 ? P0 : ms->last_tile) + kRowStart;
+        const int32_t nt = Cursor::tiles_of(row_len(a, r));
+        const int64_t ca = cta_of_tile(Pr, T, G), cz = cta_of_tile(Pr + nt - 1, T, G);
+        int32_t n = 0;
+        for (int64_t c0 = ca; c0 <= cz; c0 += 32) {
+          const int64_t cc = c0 + lane;
+          const bool in = cc <= cz && cta_begin(cc + 1, T, G) > cta_begin(cc, T, G);
+          const uint32_t m = __ballot_sync(0xffffffffu, in);
+          const int j = n + __popc(m & ((1u << lane) - 1u));
+          if (in && j < kMaxInKernelParts) ms->mslot[q][j] = slot_of(cc, Pr, T, G);
+          n += __popc(m);
+        }
+        if (lane == 0) {
+          ms->mparts[q] = n;
+          ms->mP[q] = Pr;
+          ms->mca[q] = ca;
+          ms->mcz[q] = cz;
+        }
+      }
+    }
+    named_barrier(2, 128);  // (the epilogues read the lists)
     Cursor prev = c;
     int pi = 0;  // part of tile i
     for (int i = 0; i < n_tiles; ++i) {
@@ -1136,12 +1189,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
       named_barrier(2, 128);  // every lane quarter's factors are in TMEM
       F8_TR(41, i);
       if (q < C::kQkSplit) {
-        // QK of the tile.  16 heads: aux warp q issues latent K-steps
-        // 4 q .. 4 q + 3 and rope K-step q into accumulator q; 32 heads: aux
-        // warp 0 alone, one accumulator
+        // QK of the tile: aux warp q issues latent K-steps kLatSteps q ..
+        // and its share of the rope K-steps into accumulator q
         const int qb = pi % C::kNQ;
         const int kbeg = q * C::kLatSteps, kend = kbeg + C::kLatSteps;
-        const int rbeg = C::kQkSplit == 4 ? q : (q == 0 ? 0 : 4), rend = C::kQkSplit == 4 ? q + 1 : 4;
+        const int rbeg = q * (4 / C::kQkSplit), rend = rbeg + 4 / C::kQkSplit;
         const int sb = i % C::kSBuf;
         const uint32_t sph = (i / C::kSBuf) & 1;
         wait_warp(bars + kSEmpty + sb, sph ^ 1, ms, a);
@@ -1275,7 +1327,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
   }
   // ---- rows completed here: [P2] stage_combine of their parts, with the sink
   F8_TR(4, ms->n_merge);
-  if (ms->n_merge > 0) end_merge(a, ms, tid, h0, Hl, hg, g, T, G);
+  if (ms->n_merge > 0) end_merge(a, smem, bars + kMerge, ms, tid, h0, Hl, hg, g, T, G);
   F8_TR(5, 0);
 #ifdef SMLA_TRACE
   if (tid == 0 && tr_buf != nullptr && ms->n_merge > 0) {
