@@ -170,9 +170,15 @@ typedef struct smla_decode_params {
  * boundaries.  A row lying wholly inside one CTA's range is finished there; a
  * row shared by CTAs c_a..c_b (the CTAs holding its first and last tile) gets
  * one partial per CTA, stored in workspace slot 2 c + (R_r < b_c ? 0 : 1), and
- * is merged from those slots ([P2] stage_combine) by a second, small kernel
- * launched right after (merge_kernel = 1 whenever grid > 1; a warp merges one
- * head of a row).
+ * is merged from those slots ([P2] stage_combine).  bf16 kernel: by a second,
+ * small kernel launched right after (merge_kernel = 1 whenever grid > 1; a
+ * warp merges one head of a row).  Native-fp8 kernel (with more than 32
+ * heads two CTAs, head groups of 32, share each slot range): a row of up to 4
+ * parts is merged inside the decode launch by the CTA whose part arrives last
+ * (per-row ticket); when the other parts had all arrived before that CTA's
+ * final part ended, it merges from its own O without writing that part's
+ * partial.  Rows of more parts, possible only when ceil(grid / n_q) + 1 > 4,
+ * are left to the merge kernel (merge_kernel = 1 then).
  * CUDA-core kernel: one CTA per (row, chunk); chunk c of a row covers slice
  * positions [c chunk_len, (c + 1) chunk_len), the last chunk everything after;
  * partial slot r * num_splits + c; the last chunk to finish merges.
@@ -210,7 +216,8 @@ int smla_plan(const smla_decode_params* params, int32_t num_sms, smla_plan_info*
  *   row_tile int64 [n_q + 1]     tensor-core kernel: first slot of every row, then W
  *   o_part   f32 [S][H][512]     unnormalised partial sum_t 2^(x_t - m) v_t of a row part
  *   ml_part f32 [S][H][2]        (m, l) of x_t = s_t * log2(e): m is the part's reference
- *                                maximum (its max, or at most 24 below it), l = sum_t 2^(x_t - m);
+ *                                maximum (its max, or at most 24 (bf16 kernel) or 16 (native
+ *                                fp8) below it), l = sum_t 2^(x_t - m);
  *                                m = -inf, l = 0 for a part without keys
  *   nv_part int32 [S]            contributing keys of the part
  *   lens    int32 [n_q]          trimmed row lengths (only when plan.trim_kernel)

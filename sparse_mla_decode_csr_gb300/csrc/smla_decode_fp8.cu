@@ -180,6 +180,11 @@ struct Misc {
   int32_t part_nv[2];
   uint8_t sfq[2 * kMaxHP][16];                  // q scale-factor bytes of the part being staged
   float fac[kMaxHP];                            // epilogue: output factors of a whole row's heads
+  int32_t fast;                                 // the final part completes its row (merged in the epilogue)
+  int32_t fast_s_others, fast_s_own;            //   stages holding the other parts' O and this part's
+  int32_t merge_uses;                           // completed phases of the merge barrier
+  float2 fml[kMaxInKernelParts][kMaxHP];        // final-part merge: the other parts' (m, l)
+  int32_t fnv[kMaxInKernelParts];               //   and key counts
   int32_t last_row;                             // schedule: the row of this CTA's last slot
   int64_t last_tile;                            //   and that row's first slot
   // the CTAs sharing this CTA's first (x = 0) and last (x = 1) row: their
@@ -194,7 +199,7 @@ struct Misc {
   int32_t merge_row[2];
   int32_t merge_x[2];                           // which of the two rows above
 #ifdef SMLA_TRACE
-  uint64_t merge_t[3];
+  uint64_t merge_t[8];
 #endif
 };
 // (the 16-byte reads of red_max_t rows and 4-byte reads of sfq rows need these)
@@ -473,11 +478,117 @@ __device__ __noinline__ void aux_stage_q(const AuxCtx& x, int row, int qb) {
     tc_fence_before();
   }
 
+// [P2] stage_combine of a shared row by the CTA that holds its last part to
+// finish, inside that part's epilogue (aux warps; the CTA's final part).  The
+// other parts had all arrived when this part's last tile began, so their O
+// rows were bulk-copied into the stage freed by the previous tile and their
+// (m, l) and counts loaded then (see the aux loop); this part's O goes from
+// TMEM to the other stage, and no partial of this part is written.  Then out,
+// lse, n_valid, and the ticket back to 0.
+template <int HP>
+__device__ __noinline__ void aux_merge_final(const AuxCtx& x, const Cursor& pc, int ob, int parts, int s_others,
+                                             int s_own) {
+  using C = Cfg<HP>;
+  const DecodeArgs& a = *x.a;
+  Misc* ms = x.ms;
+  uint8_t* smem = x.smem;
+  uint64_t* bars = x.bars;
+  const uint32_t tmem = x.tmem, lane_base = x.lane_base;
+  const int H = x.H, h0 = x.h0, Hl = x.Hl, lane = x.lane, ta = x.ta;
+  const int row = pc.row;
+  const int no = parts - 1;                      // the other parts
+  const int rows_bytes = Hl * kLatent * 4;       // one part's O rows
+  uint8_t* others = smem + s_others * kStageBytes;
+  float* ow = reinterpret_cast<float*>(smem + s_own * kStageBytes);  // this part's O [Hl][512]
+#ifdef SMLA_TRACE
+  if (ta == 0) ms->merge_t[5] = globaltimer();
+#endif
+  // this part's O^T rows: dim 128 b + ta of every block b, heads of pass
+#pragma unroll 1
+  for (int k = 0; k < 4 * C::kPass; ++k) {
+    const int b = k / C::kPass, pass = k % C::kPass;
+    uint32_t v0[16], v1[16];
+    tmem_ld16(tmem + lane_base + C::o_col(ob, b) + 32 * pass, v0);       // hi
+    tmem_ld16(tmem + lane_base + C::o_col(ob, b) + 32 * pass + 16, v1);  // lo
+    tmem_wait_ld();
+    const int hn = min(16, Hl - 16 * pass);
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (j < hn) ow[(16 * pass + j) * kLatent + 128 * b + ta] = __uint_as_float(v0[j]) + __uint_as_float(v1[j]);
+  }
+  tc_fence_before();
+  named_barrier(2, 128);  // own O, the others' (m, l) and counts in shared memory
+  if (lane == 0) mbar_arrive(bars + kOEmpty + ob);
+#ifdef SMLA_TRACE
+  if (ta == 0) ms->merge_t[6] = globaltimer();
+#endif
+  const bool ok = mbar_wait(bars + kMerge, 0, kWaitLimitNs);
+  if (!ok) set_abort(ms, a.status);
+#ifdef SMLA_TRACE
+  if (ta == 0) ms->merge_t[7] = globaltimer();
+#endif
+  // unit u: head u / 32 of the group, dims 4 c + 128 e (c = u % 32, e = 0..3):
+  // a warp reads consecutive 16-byte words
+#pragma unroll 1
+  for (int u = ta; u < Hl * 32; u += 128) {
+    const int hh = u / 32, c = u % 32;
+    const float m0 = ms->part_m[ob][hh], l0 = ms->part_l[ob][hh];
+    float mrun = l0 != 0.f ? m0 : -INFINITY;
+    for (int jj = 0; jj < no; ++jj) {
+      const float2 mj = ms->fml[jj][hh];
+      if (mj.y != 0.f) mrun = fmaxf(mrun, mj.x);
+    }
+    float acc[16];
+    const float w0 = l0 != 0.f ? ex2(m0 - mrun) : 0.f;  // a NaN m or l stays NaN
+    float lsum = l0 * w0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint4 v = ld_shared_v4(smem_u32(ow + hh * kLatent + 128 * e + 4 * c));
+      acc[4 * e] = w0 * __uint_as_float(v.x);
+      acc[4 * e + 1] = w0 * __uint_as_float(v.y);
+      acc[4 * e + 2] = w0 * __uint_as_float(v.z);
+      acc[4 * e + 3] = w0 * __uint_as_float(v.w);
+    }
+    for (int jj = 0; jj < no; ++jj) {
+      const float2 mj = ms->fml[jj][hh];
+      const float wt = mj.y != 0.f ? ex2(mj.x - mrun) : 0.f;
+      lsum = fmaf(mj.y, wt, lsum);
+      const float* src = reinterpret_cast<const float*>(others + jj * rows_bytes) + hh * kLatent + 4 * c;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint4 v = ld_shared_v4(smem_u32(src + 128 * e));
+        acc[4 * e] = fmaf(wt, __uint_as_float(v.x), acc[4 * e]);
+        acc[4 * e + 1] = fmaf(wt, __uint_as_float(v.y), acc[4 * e + 1]);
+        acc[4 * e + 2] = fmaf(wt, __uint_as_float(v.z), acc[4 * e + 2]);
+        acc[4 * e + 3] = fmaf(wt, __uint_as_float(v.w), acc[4 * e + 3]);
+      }
+    }
+    const int h = h0 + hh;
+    float fac, lse_h;
+    finish_head(mrun, lsum, a.sink, h, &fac, &lse_h);
+    uint16_t* dst = a.out + int64_t(row) * a.out_stride_row + int64_t(h) * a.out_stride_head + 4 * c;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      *reinterpret_cast<uint2*>(dst + 128 * e) =
+          make_uint2(pack_bf16x2(acc[4 * e] * fac, acc[4 * e + 1] * fac), pack_bf16x2(acc[4 * e + 2] * fac, acc[4 * e + 3] * fac));
+    if (c == 0 && a.lse) a.lse[int64_t(row) * H + h] = lse_h;
+  }
+  if (ta == 0) {
+    int32_t nv = ms->part_nv[ob];
+    for (int jj = 0; jj < no; ++jj) nv += ms->fnv[jj];
+    if (x.g == 0 && a.n_valid) a.n_valid[row] = nv;
+    a.ticket[int64_t(row) * x.hg + x.g] = 0;  // ready for the next call
+    ms->merge_uses = 1;
+  }
+}
+
 // A row part's epilogue (aux warps): out and lse of a whole row, or the
 // part's partial (O, m, l, count) of a shared row and its ticket; the part
-// that completes a row queues the row for the merge at the CTA's end.
+// that completes a row queues the row for the merge at the CTA's end.  The
+// CTA's final part of a shared row whose other parts have all finished
+// (their tickets are in, read before the waits) merges the row right here.
 template <int HP>
-__device__ __noinline__ void aux_epilogue(const AuxCtx& x, const Cursor& pc, int pi) {
+__device__ __noinline__ void aux_epilogue(const AuxCtx& x, const Cursor& pc, int pi, bool final_part) {
   using C = Cfg<HP>;
   const DecodeArgs& a = *x.a;
   Misc* ms = x.ms;
@@ -487,11 +598,17 @@ __device__ __noinline__ void aux_epilogue(const AuxCtx& x, const Cursor& pc, int
   const int64_t T = x.T, G = x.G;
   const int ob = pi % C::kNO;
   const uint32_t ph = (pi / C::kNO) & 1;
+  const int row = pc.row;
+  const bool whole = pc.whole();
+  const int xi = pi == 0 ? 0 : 1;  // a shared row is this CTA's first or last one
+  const int32_t parts = whole ? 1 : ms->mparts[xi];
   wait_warp(bars + kEpiReady + ob, ph, ms, a);
   wait_warp(bars + kOFull + ob, ph, ms, a);
   tc_fence_after();
-  const int row = pc.row;
-  const bool whole = pc.whole();
+  if (final_part && ms->fast) {  // (decided when the part's last tile began)
+    aux_merge_final<HP>(x, pc, ob, parts, ms->fast_s_others, ms->fast_s_own);
+    return;
+  }
   const int64_t slot = whole ? 0 : slot_of(x.c_id, pc.P, T, G);
   // head ta's output factor and LSE (whole rows), or its partial (m, l)
   if (ta < Hl) {
@@ -544,10 +661,7 @@ __device__ __noinline__ void aux_epilogue(const AuxCtx& x, const Cursor& pc, int
   if (lane == 0) mbar_arrive(bars + kOEmpty + ob);
   if (!whole && ta == 0) {
     // the CTAs holding this row's tiles ([P2] stage_split parts); the one whose
-    // part arrives last merges the row (this head group) after its own work.
-    // A shared row is this CTA's first or last one (xi = 0 or 1)
-    const int xi = pi == 0 ? 0 : 1;
-    const int32_t parts = ms->mparts[xi];
+    // part arrives last merges the row (this head group) after its own work
     if (parts <= kMaxInKernelParts || !a.merge_kernel) {
       if (atomicAdd(a.ticket + int64_t(row) * x.hg + x.g, 1) == parts - 1) {
         __threadfence();  // (acquire: the other parts' partials are read after this)
@@ -592,7 +706,7 @@ __device__ __noinline__ void end_merge(const DecodeArgs& a, uint8_t* smem, uint6
 #ifdef SMLA_TRACE
   if (tid == 0) ms->merge_t[0] = globaltimer();
 #endif
-  uint32_t uses = 0;  // completed phases of `bar`
+  uint32_t uses = ms->merge_uses;  // completed phases of `bar`
   bool ok = true;
 #pragma unroll 1
   for (int k = 0; k < n_merge; ++k) {
@@ -607,37 +721,45 @@ __device__ __noinline__ void end_merge(const DecodeArgs& a, uint8_t* smem, uint6
     for (int hc = 0; hc < Hl; hc += 16) {  // 16 heads at a time
       const int nh = min(16, Hl - hc);
       const bool staged = parts <= kMaxInKernelParts;
+      // unit u: head h0 + hc + u / 32, dims 16 (u % 32) .. + 15
+      const int u = tid;
+      const bool active = u < nh * (kLatent / 16);
+      const int hh = u / (kLatent / 16), f = u % (kLatent / 16);
+      const int h = h0 + hc + hh;
+      // the parts' (m, l) and the sink of this head, loaded before anything waits
+      float2 ml[kMaxInKernelParts];
+#pragma unroll
+      for (int j = 0; j < kMaxInKernelParts; ++j) {
+        ml[j] = make_float2(-INFINITY, 0.f);
+        if (staged && active && j < parts) ml[j] = __ldcg(reinterpret_cast<const float2*>(a.ml_part) + sl[j] * H + h);
+      }
+      const float sink_h = (active && a.sink) ? __ldg(a.sink + h) : 0.f;
       if (staged) {
-        __syncthreads();  // the buffer's previous contents were read
+        if (k + hc > 0) __syncthreads();  // the buffer's previous contents were read
         if (tid == 0) {
           fence_proxy_async_global();  // (this CTA's own partial was written by plain stores)
           mbar_arrive_expect_tx(bar, uint32_t(parts * nh * kLatent * 4));
           for (int j = 0; j < parts; ++j)
             bulk_g2s(smem_u32(smem + j * (16 * kLatent * 4)), a.o_part + (sl[j] * H + h0 + hc) * kLatent,
                      uint32_t(nh * kLatent * 4), bar);
+#ifdef SMLA_TRACE
+          if (k == 0 && hc == 0) ms->merge_t[3] = globaltimer();
+#endif
         }
       }
-      // unit u: head h0 + hc + u / 32, dims 16 (u % 32) .. + 15
-      const int u = tid;
-      const bool active = u < nh * (kLatent / 16);
-      const int hh = u / (kLatent / 16), f = u % (kLatent / 16);
-      const int h = h0 + hc + hh;
       float mrun = -INFINITY, lsum = 0.f;
       float acc[16];
 #pragma unroll
       for (int d = 0; d < 16; ++d) acc[d] = 0.f;
       if (staged) {
-        float2 ml[kMaxInKernelParts];
-#pragma unroll
-        for (int j = 0; j < kMaxInKernelParts; ++j) {
-          ml[j] = make_float2(-INFINITY, 0.f);
-          if (active && j < parts) ml[j] = __ldcg(reinterpret_cast<const float2*>(a.ml_part) + sl[j] * H + h);
-        }
         if (!mbar_wait(bar, uses & 1, kWaitLimitNs)) {
           set_abort(ms, a.status);
           ok = false;
         }
         ++uses;
+#ifdef SMLA_TRACE
+        if (tid == 0 && k == 0 && hc == 0) ms->merge_t[4] = globaltimer();
+#endif
         if (active && ok) {
 #pragma unroll
           for (int j = 0; j < kMaxInKernelParts; ++j)
@@ -689,7 +811,7 @@ __device__ __noinline__ void end_merge(const DecodeArgs& a, uint8_t* smem, uint6
       }
       if (active) {
         float fac, lse_h;
-        finish_head(mrun, lsum, a.sink, h, &fac, &lse_h);
+        finish_head_v(mrun, lsum, a.sink != nullptr, sink_h, &fac, &lse_h);
         uint4 v0, v1;
         v0.x = pack_bf16x2(acc[0] * fac, acc[1] * fac);
         v0.y = pack_bf16x2(acc[2] * fac, acc[3] * fac);
@@ -768,6 +890,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
     ms->last_row = a.n_q;
     ms->last_tile = 0;
     ms->mparts[0] = ms->mparts[1] = 0;
+    ms->merge_uses = 0;
+    ms->fast = 0;
     ms->n_tiles = 0;
     ms->n_merge = 0;
     fence_mbar_init();
@@ -992,10 +1116,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
         // block, the codes' exponent fields lowered by the key's distance m_b
         // to the tile's largest block-b scale (exact for the writer's power-of-
         // two scales; a value leaving E4M3's normal range becomes 0).  e_h is
-        // kept in [-20, 17] (a head whose tile terms all lie 2^20 below its
-        // reference keeps 2^-10 relative precision on them).
+        // kept in [-20, kLazy + 1] (a head whose tile terms all lie 2^20 below
+        // its reference keeps 2^-10 relative precision on them).
         if (pass == 0) F8_TR(13, i);
-        const int e_h = max(min(int((__float_as_uint(ex2(tm - mr)) >> 23) & 0xFF) - 126, 17), -20);
+        const int e_h = max(min(int((__float_as_uint(ex2(tm - mr)) >> 23) & 0xFF) - 126, int(kLazy) + 1), -20);
         const float inv_h = pow2f(7 - e_h);
 #pragma unroll
         for (int h = 0; h < 16; ++h) x[h] = ex2(x[h] - __shfl_sync(0xffffffffu, mr, h));  // x = -inf (masked) gives 0
@@ -1227,9 +1351,49 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
         __syncwarp();
         F8_TR(31, i);
       }
+      if (i == n_tiles - 1 && i > 0 && c.last() && !c.whole()) {
+        // The CTA's final part, shared with other CTAs, ends with this tile.
+        // If the other parts have all arrived (their tickets are in), this
+        // CTA completes the row: their O rows are copied now into the stage
+        // of the previous tile (free once that tile's PV has completed) and
+        // merged in this part's epilogue, without a partial of this part.
+        const int xi = pi == 0 ? 0 : 1;
+        const int parts = ms->mparts[xi];
+        const int rows_bytes = Hl * kLatent * 4;
+        if (parts >= 2 && parts <= kMaxInKernelParts && (parts - 1) * rows_bytes <= kStageBytes) {
+          if (ta == 0) ms->fast = ld_acquire_gpu(a.ticket + int64_t(c.row) * hg + g) == parts - 1;
+          named_barrier(2, 128);
+          if (ms->fast) {
+            const int sp = (i - 1) & 1;
+            wait_warp(bars + kKvEmpty + sp, ((i - 1) >> 1) & 1, ms, a);  // PV(i - 1) has completed
+            const int64_t own = slot_of(c_id, c.P, T, G);
+            int jj = 0;
+            if (ta == 0) {
+              fence_proxy_async_global();  // (the other parts' partials are read by the async proxy)
+              mbar_arrive_expect_tx(bars + kMerge, uint32_t((parts - 1) * rows_bytes));
+            }
+            for (int j = 0; j < parts; ++j) {
+              const int64_t sl = ms->mslot[xi][j];
+              if (sl == own || jj >= parts - 1) continue;
+              if (ta == 0)
+                bulk_g2s(smem_base + uint32_t(sp * kStageBytes + jj * rows_bytes), a.o_part + (sl * H + h0) * kLatent,
+                         uint32_t(rows_bytes), bars + kMerge);
+              if (ta < Hl) ms->fml[jj][ta] = __ldcg(reinterpret_cast<const float2*>(a.ml_part) + sl * H + h0 + ta);
+              if (ta == 32 * jj) ms->fnv[jj] = __ldcg(a.nv_part + sl);
+              ++jj;
+            }
+            if (ta == 0) {
+              ms->fast_s_others = sp;
+              ms->fast_s_own = i & 1;
+            }
+            F8_TR(45, i);
+          }
+          named_barrier(2, 128);
+        }
+      }
       // (2) the previous part's epilogue, once this part has started
       if (i > 0 && c.first()) {
-        aux_epilogue<HP>(actx, prev, pi - 1);
+        aux_epilogue<HP>(actx, prev, pi - 1, false);
         F8_TR(42, i);
       }
       // (3) the next part's q, as soon as its buffer is free
@@ -1245,7 +1409,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
       }
       c.advance(a);
     }
-    if (pi > 0) aux_epilogue<HP>(actx, prev, pi - 1);
+    if (pi > 0) aux_epilogue<HP>(actx, prev, pi - 1, true);
     F8_TR(44, 0);
     if (q < C::kQkSplit) {
       if (lane == 0) {
@@ -1333,6 +1497,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
   if (tid == 0 && tr_buf != nullptr && ms->n_merge > 0) {
     for (int k = 0; k <= ms->n_merge; ++k)
       tr_buf[(size_t(blockIdx.x) * 20 + 19) * 256 + k] = (ms->merge_t[k] & 0xFFFFFFFFFFFFull) | (uint64_t(70 + k) << 48);
+    tr_buf[(size_t(blockIdx.x) * 20 + 19) * 256 + 8] = (ms->merge_t[3] & 0xFFFFFFFFFFFFull) | (uint64_t(73) << 48);
+    tr_buf[(size_t(blockIdx.x) * 20 + 19) * 256 + 9] = (ms->merge_t[4] & 0xFFFFFFFFFFFFull) | (uint64_t(74) << 48);
+  }
+  if (tid == 0 && tr_buf != nullptr && ms->fast) {
+    for (int k = 5; k < 8; ++k)
+      tr_buf[(size_t(blockIdx.x) * 20 + 19) * 256 + 10 + k] = (ms->merge_t[k] & 0xFFFFFFFFFFFFull) | (uint64_t(70 + k) << 48);
   }
 #endif
 }

@@ -137,23 +137,29 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 //   m_f = max(m, s), s = sink * log2(e)        (the K2-back combine's fold)
 //   lse = (m + log2 l) * ln 2                  (the gfx950 epilogue's LSE)
 // and factor = 0, lse = -inf when l == 0 (no key); a NaN l (a NaN score)
-// gives NaN for both.
-__device__ __forceinline__ void finish_head(float m, float l, const float* sink, int h,
-                                            float* factor, float* lse) {
+// gives NaN for both.  finish_head_v takes the head's sink value already
+// loaded (has_sink: a sink is given).
+__device__ __forceinline__ void finish_head_v(float m, float l, bool has_sink, float sink_h, float* factor,
+                                              float* lse) {
   if (l == 0.f) {
     *factor = 0.f;
     *lse = -INFINITY;
     return;
   }
   *lse = (m + log2f(l)) * kLn2;
-  if (sink == nullptr) {
+  if (!has_sink) {
     *factor = 1.f / l;
     return;
   }
-  const float s = sink[h] * kLog2e;
+  const float s = sink_h * kLog2e;
   const float mf = fmaxf(m, s);
   const float wm = exp2f(m - mf);
   *factor = wm / (exp2f(s - mf) + l * wm);
+}
+
+__device__ __forceinline__ void finish_head(float m, float l, const float* sink, int h,
+                                            float* factor, float* lse) {
+  finish_head_v(m, l, sink != nullptr, sink != nullptr ? sink[h] : 0.f, factor, lse);
 }
 
 }  // namespace smla

@@ -97,6 +97,13 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst_smem, const void* src, uin
       : "memory");
 }
 
+// A 32-bit load with acquire semantics at GPU scope.
+__device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(__cvta_generic_to_global(p)) : "memory");
+  return v;
+}
+
 // Orders this thread's earlier generic-proxy accesses to global memory before
 // its later async-proxy (bulk copy) accesses.
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }

@@ -268,8 +268,17 @@ def test_tensor_core_schedule_partials_match_oracle(k, tk):
     shared = [r for r, pr in parts.items() if len(pr) > 1]
     assert shared, "the case must exercise shared rows"
     for r in shared:
+        # the native-fp8 kernel's CTA that finishes a shared row last, after the
+        # row's other parts, may merge it without writing its own partial (its
+        # slot then stays as the zeroed workspace had it); every other part is
+        # written and checked
+        skipped = 0
         for cta, slot, lo, hi in parts[r]:
+            if tk == "fp8" and not ml[slot].any() and not o[slot].any() and nv[slot] == 0:
+                skipped += 1
+                continue
             _check_part(o[slot], ml[slot], nv[slot], _oracle_part(c, r, lo, hi), f"row {r} cta {cta}")
+        assert skipped <= 1, f"row {r}: {skipped} parts left no partial"
 
 
 @pytest.mark.parametrize("name", ["tiny", "decode", "ragged", "wide", "long"])
