@@ -181,10 +181,14 @@ struct Misc {
   uint8_t sfq[2 * kMaxHP][16];                  // q scale-factor bytes of the part being staged
   float fac[kMaxHP];                            // epilogue: output factors of a whole row's heads
   int32_t fast;                                 // the final part completes its row (merged in the epilogue)
-  int32_t fast_s_others, fast_s_own;            //   stages holding the other parts' O and this part's
+  int32_t fast_s_own;                           //   the stage that takes this part's O
   int32_t merge_uses;                           // completed phases of the merge barrier
-  float2 fml[kMaxInKernelParts][kMaxHP];        // final-part merge: the other parts' (m, l)
-  int32_t fnv[kMaxInKernelParts];               //   and key counts
+  int32_t fnv[kMaxInKernelParts];               // final-part merge: the other parts' key counts
+  // parts staged in shared memory for a combine: part j's O rows of heads
+  // [cb_h, cb_h + cb_nh) at byte offset cb_row[j] (rows of 512 f32), its
+  // (m, l) per head at cb_ml[j]
+  uint32_t cb_row[kMaxInKernelParts];
+  float2 cb_ml[kMaxInKernelParts][kMaxHP];
   int32_t last_row;                             // schedule: the row of this CTA's last slot
   int64_t last_tile;                            //   and that row's first slot
   // the CTAs sharing this CTA's first (x = 0) and last (x = 1) row: their
@@ -200,6 +204,7 @@ struct Misc {
   int32_t merge_x[2];                           // which of the two rows above
 #ifdef SMLA_TRACE
   uint64_t merge_t[8];
+  uint64_t comb_t[8];
 #endif
 };
 // (the 16-byte reads of red_max_t rows and 4-byte reads of sfq rows need these)
@@ -362,9 +367,16 @@ __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, Misc* 
   return __all_sync(0xffffffffu, wait_bar(bar, parity, ms, a));
 }
 
+// The schedule's CTA boundaries (cta_begin / cta_of_tile of the shared
+// schedule) through one out-of-line 64-bit division: a copy of the division
+// routine at every call site would cost ~1 KB of instructions each.
+__device__ __noinline__ int64_t div64(int64_t n, int64_t d) { return n / d; }
+__device__ __forceinline__ int64_t cbeg(int64_t c, int64_t T, int64_t G) { return div64(c * T, G); }
+__device__ __forceinline__ int64_t cof(int64_t t, int64_t T, int64_t G) { return div64((t + 1) * G - 1, T); }
+
 // Slot of a shared row part (the partial layout of the merge kernel).
 __device__ __forceinline__ int64_t slot_of(int64_t c, int64_t P, int64_t T, int64_t G) {
-  return 2 * c + (P < cta_begin(c, T, G) ? 0 : 1);
+  return 2 * c + (P < cbeg(c, T, G) ? 0 : 1);
 }
 
 // What the aux warps' out-of-line steps need from the kernel.
@@ -387,14 +399,13 @@ __device__ __noinline__ void aux_stage_q(const AuxCtx& x, int row, int qb) {
   const DecodeArgs& a = *x.a;
   using C = Cfg<HP>;
   constexpr int kN = C::kN;
-  uint8_t* smem = x.smem;
   Misc* ms = x.ms;
-  uint64_t* bars = x.bars;
   const uint32_t tmem = x.tmem, lane_base = x.lane_base;
-  const int H = x.H, h0 = x.h0, Hl = x.Hl, hg = x.hg, g = x.g, lane = x.lane, ta = x.ta;
-  const int64_t c_id = x.c_id, G = x.G, T = x.T;
-  (void)kN; (void)hg; (void)g; (void)c_id; (void)G; (void)T; (void)h0; (void)H;
-      uint8_t* qs = smem + C::kOffQ + qb * C::kQBytes;
+  const int h0 = x.h0, Hl = x.Hl, lane = x.lane, ta = x.ta;
+  uint8_t* qs = x.smem + C::kOffQ + qb * C::kQBytes;
+  // (the arguments' fields in registers, not reloaded after every store)
+  const uint16_t* const q_rows = a.q + row * a.q_stride_row + h0 * a.q_stride_head;
+  const int64_t qsh = a.q_stride_head;
 #pragma unroll 1
     for (int blk = ta; blk < HP * 16; blk += 128) {
       const int h = blk >> 4, kb = blk & 15;
@@ -402,7 +413,7 @@ __device__ __noinline__ void aux_stage_q(const AuxCtx& x, int row, int qb) {
       int sfb = 127;
       if (h < Hl) {
         const uint4* src =
-            reinterpret_cast<const uint4*>(a.q + row * a.q_stride_row + (h0 + h) * a.q_stride_head + 32 * kb);
+            reinterpret_cast<const uint4*>(q_rows + h * qsh + 32 * kb);
         uint4 v[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) v[k] = __ldg(src + k);
@@ -453,7 +464,7 @@ __device__ __noinline__ void aux_stage_q(const AuxCtx& x, int row, int qb) {
       const int h = k >> 3, c16 = k & 7;
       uint4 v = make_uint4(0, 0, 0, 0);
       if (h < Hl)
-        v = __ldg(reinterpret_cast<const uint4*>(a.q + row * a.q_stride_row + (h0 + h) * a.q_stride_head +
+        v = __ldg(reinterpret_cast<const uint4*>(q_rows + h * qsh +
                                                  kLatent + 8 * c16));
       *reinterpret_cast<uint4*>(qs + C::kQOffRope + sw128(h, c16)) = v;
     }
@@ -478,32 +489,151 @@ __device__ __noinline__ void aux_stage_q(const AuxCtx& x, int row, int qb) {
     tc_fence_before();
   }
 
+// [P2] stage_combine, with the sink, of `parts` parts staged in shared memory
+// (cb_row, cb_ml): out and lse of heads [hb, hb + nh) of `row`.  Unit u: head
+// u / 32, dims 4 c + 128 e (c = u % 32, e = 0..3), so that a warp reads
+// consecutive 16-byte words; threads t, t + nthreads, ...
+__device__ __noinline__ void combine_staged(const DecodeArgs& a, const uint8_t* smem, const Misc* ms, int parts,
+                                            int row, int hb, int nh, int t, int nthreads) {
+  // (the arguments' fields in registers: read through the reference they would
+  // be reloaded from the parameter buffer after every store)
+  uint16_t* const out_row = a.out + int64_t(row) * a.out_stride_row;
+  const int64_t osh = a.out_stride_head;
+  float* const lse_row = a.lse ? a.lse + int64_t(row) * a.heads : nullptr;
+  const float* const sink = a.sink;
+#ifdef SMLA_TRACE
+  int it = 0;
+#endif
+#pragma unroll 1
+  for (int u = t; u < nh * 32; u += nthreads) {
+#ifdef SMLA_TRACE
+    if (t == 0 && it < 2) const_cast<Misc*>(ms)->comb_t[4 * it] = globaltimer();
+#endif
+    const int hh = u / 32, c = u % 32;
+    float mrun = -INFINITY;
+#pragma unroll 1
+    for (int j = 0; j < parts; ++j) {
+      const float2 mj = ms->cb_ml[j][hh];
+      if (mj.y != 0.f) mrun = fmaxf(mrun, mj.x);  // parts without keys (l = 0) take no part
+    }
+    float acc[16];
+#pragma unroll
+    for (int d = 0; d < 16; ++d) acc[d] = 0.f;
+    float lsum = 0.f;
+#pragma unroll 1
+    for (int j = 0; j < parts; ++j) {
+      const float2 mj = ms->cb_ml[j][hh];
+      const float wt = mj.y != 0.f ? ex2(mj.x - mrun) : 0.f;  // a NaN m or l stays NaN
+      lsum = fmaf(mj.y, wt, lsum);
+      const uint32_t src = smem_u32(smem + ms->cb_row[j]) + uint32_t((hh * kLatent + 4 * c) * 4);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint4 v = ld_shared_v4(src + 512 * e);
+        acc[4 * e] = fmaf(wt, __uint_as_float(v.x), acc[4 * e]);
+        acc[4 * e + 1] = fmaf(wt, __uint_as_float(v.y), acc[4 * e + 1]);
+        acc[4 * e + 2] = fmaf(wt, __uint_as_float(v.z), acc[4 * e + 2]);
+        acc[4 * e + 3] = fmaf(wt, __uint_as_float(v.w), acc[4 * e + 3]);
+      }
+    }
+    const int h = hb + hh;
+#ifdef SMLA_TRACE
+    if (t == 0 && it < 2) const_cast<Misc*>(ms)->comb_t[4 * it + 1] = globaltimer();
+#endif
+    float fac, lse_h;
+    finish_head(mrun, lsum, sink, h, &fac, &lse_h);
+#ifdef SMLA_TRACE
+    if (t == 0 && it < 2) const_cast<Misc*>(ms)->comb_t[4 * it + 2] = globaltimer();
+#endif
+    uint16_t* dst = out_row + int64_t(h) * osh + 4 * c;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      *reinterpret_cast<uint2*>(dst + 128 * e) = make_uint2(pack_bf16x2(acc[4 * e] * fac, acc[4 * e + 1] * fac),
+                                                            pack_bf16x2(acc[4 * e + 2] * fac, acc[4 * e + 3] * fac));
+    if (c == 0 && lse_row) lse_row[h] = lse_h;
+#ifdef SMLA_TRACE
+    if (t == 0 && it < 2) const_cast<Misc*>(ms)->comb_t[4 * it + 3] = globaltimer();
+    ++it;
+#endif
+  }
+}
+
+// The same for a row of more than kMaxInKernelParts parts (only a plan
+// without the merge kernel leaves one here): part by part from global
+// memory with a running maximum.
+__device__ __noinline__ void combine_global(const DecodeArgs& a, int row, int hb, int nh, int64_t P, int64_t ca,
+                                            int64_t cz, int64_t T, int64_t G, int t, int nthreads) {
+  const int H = a.heads;
+  const float* const o_part = a.o_part;
+  const float2* const ml_part = reinterpret_cast<const float2*>(a.ml_part);
+  uint16_t* const out_row = a.out + int64_t(row) * a.out_stride_row;
+  const int64_t osh = a.out_stride_head;
+  float* const lse_row = a.lse ? a.lse + int64_t(row) * H : nullptr;
+  const float* const sink = a.sink;
+#pragma unroll 1
+  for (int u = t; u < nh * 32; u += nthreads) {
+    const int hh = u / 32, c = u % 32, h = hb + hh;
+    float mrun = -INFINITY, lsum = 0.f;
+    float acc[16];
+#pragma unroll
+    for (int d = 0; d < 16; ++d) acc[d] = 0.f;
+#pragma unroll 1
+    for (int64_t cc = ca; cc <= cz; ++cc) {
+      if (!(cbeg(cc + 1, T, G) > cbeg(cc, T, G))) continue;
+      const int64_t sl = slot_of(cc, P, T, G);
+      const float2 mj = __ldcg(ml_part + sl * H + h);
+      if (mj.y == 0.f) continue;
+      if (mj.x > mrun) {  // the running maximum moves: rescale what was summed
+        const float r = ex2(mrun - mj.x);
+        lsum *= r;
+#pragma unroll
+        for (int d = 0; d < 16; ++d) acc[d] *= r;
+        mrun = mj.x;
+      }
+      const float wt = ex2(mj.x - mrun);
+      lsum = fmaf(mj.y, wt, lsum);
+      const float* src = o_part + (sl * H + h) * kLatent + 4 * c;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(src + 128 * e));
+        acc[4 * e] = fmaf(wt, v.x, acc[4 * e]);
+        acc[4 * e + 1] = fmaf(wt, v.y, acc[4 * e + 1]);
+        acc[4 * e + 2] = fmaf(wt, v.z, acc[4 * e + 2]);
+        acc[4 * e + 3] = fmaf(wt, v.w, acc[4 * e + 3]);
+      }
+    }
+    float fac, lse_h;
+    finish_head(mrun, lsum, sink, h, &fac, &lse_h);
+    uint16_t* dst = out_row + int64_t(h) * osh + 4 * c;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      *reinterpret_cast<uint2*>(dst + 128 * e) = make_uint2(pack_bf16x2(acc[4 * e] * fac, acc[4 * e + 1] * fac),
+                                                            pack_bf16x2(acc[4 * e + 2] * fac, acc[4 * e + 3] * fac));
+    if (c == 0 && lse_row) lse_row[h] = lse_h;
+  }
+}
+
 // [P2] stage_combine of a shared row by the CTA that holds its last part to
 // finish, inside that part's epilogue (aux warps; the CTA's final part).  The
 // other parts had all arrived when this part's last tile began, so their O
 // rows were bulk-copied into the stage freed by the previous tile and their
-// (m, l) and counts loaded then (see the aux loop); this part's O goes from
-// TMEM to the other stage, and no partial of this part is written.  Then out,
-// lse, n_valid, and the ticket back to 0.
+// (m, l) and counts loaded then (staging descriptors 1 .. parts - 1, see the
+// aux loop); this part's O goes from TMEM to the other stage (descriptor 0),
+// and no partial of this part is written.  Then out, lse, n_valid, and the
+// ticket back to 0.
 template <int HP>
-__device__ __noinline__ void aux_merge_final(const AuxCtx& x, const Cursor& pc, int ob, int parts, int s_others,
-                                             int s_own) {
+__device__ __noinline__ void aux_merge_final(const AuxCtx& x, const Cursor& pc, int ob, int parts, int s_own) {
   using C = Cfg<HP>;
   const DecodeArgs& a = *x.a;
   Misc* ms = x.ms;
   uint8_t* smem = x.smem;
   uint64_t* bars = x.bars;
   const uint32_t tmem = x.tmem, lane_base = x.lane_base;
-  const int H = x.H, h0 = x.h0, Hl = x.Hl, lane = x.lane, ta = x.ta;
-  const int row = pc.row;
-  const int no = parts - 1;                      // the other parts
-  const int rows_bytes = Hl * kLatent * 4;       // one part's O rows
-  uint8_t* others = smem + s_others * kStageBytes;
+  const int Hl = x.Hl, lane = x.lane, ta = x.ta;
   float* ow = reinterpret_cast<float*>(smem + s_own * kStageBytes);  // this part's O [Hl][512]
 #ifdef SMLA_TRACE
   if (ta == 0) ms->merge_t[5] = globaltimer();
 #endif
-  // this part's O^T rows: dim 128 b + ta of every block b, heads of pass
+  // this part's O^T rows: dim 128 b + ta of every block b
 #pragma unroll 1
   for (int k = 0; k < 4 * C::kPass; ++k) {
     const int b = k / C::kPass, pass = k % C::kPass;
@@ -516,68 +646,24 @@ __device__ __noinline__ void aux_merge_final(const AuxCtx& x, const Cursor& pc, 
     for (int j = 0; j < 16; ++j)
       if (j < hn) ow[(16 * pass + j) * kLatent + 128 * b + ta] = __uint_as_float(v0[j]) + __uint_as_float(v1[j]);
   }
+  if (ta < Hl) ms->cb_ml[0][ta] = make_float2(ms->part_m[ob][ta], ms->part_l[ob][ta]);
+  if (ta == 0) ms->cb_row[0] = uint32_t(s_own * kStageBytes);
   tc_fence_before();
-  named_barrier(2, 128);  // own O, the others' (m, l) and counts in shared memory
+  named_barrier(2, 128);  // own O, the (m, l) and counts in shared memory
   if (lane == 0) mbar_arrive(bars + kOEmpty + ob);
 #ifdef SMLA_TRACE
   if (ta == 0) ms->merge_t[6] = globaltimer();
 #endif
-  const bool ok = mbar_wait(bars + kMerge, 0, kWaitLimitNs);
-  if (!ok) set_abort(ms, a.status);
+  if (!mbar_wait(bars + kMerge, 0, kWaitLimitNs)) set_abort(ms, a.status);
 #ifdef SMLA_TRACE
   if (ta == 0) ms->merge_t[7] = globaltimer();
 #endif
-  // unit u: head u / 32 of the group, dims 4 c + 128 e (c = u % 32, e = 0..3):
-  // a warp reads consecutive 16-byte words
-#pragma unroll 1
-  for (int u = ta; u < Hl * 32; u += 128) {
-    const int hh = u / 32, c = u % 32;
-    const float m0 = ms->part_m[ob][hh], l0 = ms->part_l[ob][hh];
-    float mrun = l0 != 0.f ? m0 : -INFINITY;
-    for (int jj = 0; jj < no; ++jj) {
-      const float2 mj = ms->fml[jj][hh];
-      if (mj.y != 0.f) mrun = fmaxf(mrun, mj.x);
-    }
-    float acc[16];
-    const float w0 = l0 != 0.f ? ex2(m0 - mrun) : 0.f;  // a NaN m or l stays NaN
-    float lsum = l0 * w0;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint4 v = ld_shared_v4(smem_u32(ow + hh * kLatent + 128 * e + 4 * c));
-      acc[4 * e] = w0 * __uint_as_float(v.x);
-      acc[4 * e + 1] = w0 * __uint_as_float(v.y);
-      acc[4 * e + 2] = w0 * __uint_as_float(v.z);
-      acc[4 * e + 3] = w0 * __uint_as_float(v.w);
-    }
-    for (int jj = 0; jj < no; ++jj) {
-      const float2 mj = ms->fml[jj][hh];
-      const float wt = mj.y != 0.f ? ex2(mj.x - mrun) : 0.f;
-      lsum = fmaf(mj.y, wt, lsum);
-      const float* src = reinterpret_cast<const float*>(others + jj * rows_bytes) + hh * kLatent + 4 * c;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint4 v = ld_shared_v4(smem_u32(src + 128 * e));
-        acc[4 * e] = fmaf(wt, __uint_as_float(v.x), acc[4 * e]);
-        acc[4 * e + 1] = fmaf(wt, __uint_as_float(v.y), acc[4 * e + 1]);
-        acc[4 * e + 2] = fmaf(wt, __uint_as_float(v.z), acc[4 * e + 2]);
-        acc[4 * e + 3] = fmaf(wt, __uint_as_float(v.w), acc[4 * e + 3]);
-      }
-    }
-    const int h = h0 + hh;
-    float fac, lse_h;
-    finish_head(mrun, lsum, a.sink, h, &fac, &lse_h);
-    uint16_t* dst = a.out + int64_t(row) * a.out_stride_row + int64_t(h) * a.out_stride_head + 4 * c;
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      *reinterpret_cast<uint2*>(dst + 128 * e) =
-          make_uint2(pack_bf16x2(acc[4 * e] * fac, acc[4 * e + 1] * fac), pack_bf16x2(acc[4 * e + 2] * fac, acc[4 * e + 3] * fac));
-    if (c == 0 && a.lse) a.lse[int64_t(row) * H + h] = lse_h;
-  }
+  combine_staged(a, smem, ms, parts, pc.row, x.h0, Hl, ta, 128);
   if (ta == 0) {
     int32_t nv = ms->part_nv[ob];
-    for (int jj = 0; jj < no; ++jj) nv += ms->fnv[jj];
-    if (x.g == 0 && a.n_valid) a.n_valid[row] = nv;
-    a.ticket[int64_t(row) * x.hg + x.g] = 0;  // ready for the next call
+    for (int jj = 0; jj < parts - 1; ++jj) nv += ms->fnv[jj];
+    if (x.g == 0 && a.n_valid) a.n_valid[pc.row] = nv;
+    a.ticket[int64_t(pc.row) * x.hg + x.g] = 0;  // ready for the next call
     ms->merge_uses = 1;
   }
 }
@@ -606,7 +692,7 @@ __device__ __noinline__ void aux_epilogue(const AuxCtx& x, const Cursor& pc, int
   wait_warp(bars + kOFull + ob, ph, ms, a);
   tc_fence_after();
   if (final_part && ms->fast) {  // (decided when the part's last tile began)
-    aux_merge_final<HP>(x, pc, ob, parts, ms->fast_s_others, ms->fast_s_own);
+    aux_merge_final<HP>(x, pc, ob, parts, ms->fast_s_own);
     return;
   }
   const int64_t slot = whole ? 0 : slot_of(x.c_id, pc.P, T, G);
@@ -630,6 +716,11 @@ __device__ __noinline__ void aux_epilogue(const AuxCtx& x, const Cursor& pc, int
     }
   }
   named_barrier(2, 128);  // the factors
+  // (the arguments' fields in registers: read through the reference they would
+  // be reloaded from the parameter buffer after every store)
+  uint16_t* const out_rows = a.out + int64_t(row) * a.out_stride_row + int64_t(h0) * a.out_stride_head;
+  const int64_t osh = a.out_stride_head;
+  float* const o_rows = a.o_part + (slot * H + h0) * kLatent;
   // O^T rows of this thread: dim 128 b + ta of every block b; columns
   // [hi g | lo g] per 16-head group g
 #pragma unroll 1
@@ -642,14 +733,14 @@ __device__ __noinline__ void aux_epilogue(const AuxCtx& x, const Cursor& pc, int
     tmem_wait_ld();
     const int hn = min(16, Hl - 16 * pass);
     if (whole) {
-      uint16_t* dst = a.out + int64_t(row) * a.out_stride_row + int64_t(h0 + 16 * pass) * a.out_stride_head + d;
+      uint16_t* dst = out_rows + int64_t(16 * pass) * osh + d;
 #pragma unroll
       for (int j = 0; j < 16; ++j)
         if (j < hn)
-          dst[int64_t(j) * a.out_stride_head] = __bfloat16_as_ushort(
+          dst[int64_t(j) * osh] = __bfloat16_as_ushort(
               __float2bfloat16_rn((__uint_as_float(v0[j]) + __uint_as_float(v1[j])) * ms->fac[16 * pass + j]));
     } else {
-      float* dst = a.o_part + (slot * H + h0 + 16 * pass) * kLatent + d;
+      float* dst = o_rows + (16 * pass) * kLatent + d;
 #pragma unroll
       for (int j = 0; j < 16; ++j)
         if (j < hn) dst[int64_t(j) * kLatent] = __uint_as_float(v0[j]) + __uint_as_float(v1[j]);
@@ -673,18 +764,15 @@ __device__ __noinline__ void aux_epilogue(const AuxCtx& x, const Cursor& pc, int
   }
 }
 
-// [P2] stage_combine, with the sink, of the rows this CTA completed: every
-// part's (m, l) and O, out and lse of heads [h0, h0 + Hl), the key count, and
-// the row's ticket back to zero.  All threads of the CTA, after its own work
-// (the stages' shared memory is free then).  The parts' slots were found
-// after the prologue.  For rows of up to kMaxInKernelParts parts, one thread
-// copies each part's O rows of 16 heads (32 KB) into shared memory with bulk
-// copies (a plain-load gather of the same bytes is limited by the SM's load
-// throughput), the threads load the (m, l) meanwhile, then each thread
-// combines 16 dims of one head.  Longer rows (only a plan without the merge
-// kernel leaves them here) go part by part with plain loads.  Warp k loads
-// row k's key counts first and sums them last.
-static_assert(16 * (kLatent / 16) <= kThreads, "one merge unit per thread");
+// [P2] stage_combine, with the sink, of the rows this CTA completed through
+// its tickets: every part's (m, l) and O, out and lse of heads [h0, h0 + Hl),
+// the key count, and the row's ticket back to zero.  All threads of the CTA,
+// after its own work (the stages' shared memory is free then).  The parts'
+// slots were found after the prologue.  For rows of up to kMaxInKernelParts
+// parts, one thread bulk-copies each part's O rows of 16 heads (32 KB) into
+// shared memory (a plain-load gather of the same bytes is limited by the
+// SM's load throughput) while the threads load the (m, l); then the staged
+// combine.  Warp k loads row k's key counts first and sums them last.
 static_assert(kMaxInKernelParts * 16 * kLatent * 4 <= kStages * kStageBytes, "merge staging fits the stages");
 __device__ __noinline__ void end_merge(const DecodeArgs& a, uint8_t* smem, uint64_t* bar, Misc* ms, int tid,
                                        int h0, int Hl, int hg, int g, int64_t T, int64_t G) {
@@ -700,132 +788,46 @@ __device__ __noinline__ void end_merge(const DecodeArgs& a, uint8_t* smem, uint6
     } else {
       const int64_t ca = ms->mca[xi], cz = ms->mcz[xi], P = ms->mP[xi];
       for (int64_t cc = ca + lane; cc <= cz; cc += 32)
-        if (cta_begin(cc + 1, T, G) > cta_begin(cc, T, G)) nv += __ldcg(a.nv_part + slot_of(cc, P, T, G));
+        if (cbeg(cc + 1, T, G) > cbeg(cc, T, G)) nv += __ldcg(a.nv_part + slot_of(cc, P, T, G));
     }
   }
 #ifdef SMLA_TRACE
   if (tid == 0) ms->merge_t[0] = globaltimer();
 #endif
   uint32_t uses = ms->merge_uses;  // completed phases of `bar`
-  bool ok = true;
 #pragma unroll 1
   for (int k = 0; k < n_merge; ++k) {
     const int row = ms->merge_row[k];
     const int xi = ms->merge_x[k];
     const int parts = ms->mparts[xi];
-    const int64_t P = ms->mP[xi], ca = ms->mca[xi], cz = ms->mcz[xi];
-    int64_t sl[kMaxInKernelParts];
-#pragma unroll
-    for (int j = 0; j < kMaxInKernelParts; ++j) sl[j] = j < parts ? ms->mslot[xi][j] : 0;
+    if (parts > kMaxInKernelParts) {
+      combine_global(a, row, h0, Hl, ms->mP[xi], ms->mca[xi], ms->mcz[xi], T, G, tid, kThreads);
+      continue;
+    }
 #pragma unroll 1
     for (int hc = 0; hc < Hl; hc += 16) {  // 16 heads at a time
       const int nh = min(16, Hl - hc);
-      const bool staged = parts <= kMaxInKernelParts;
-      // unit u: head h0 + hc + u / 32, dims 16 (u % 32) .. + 15
-      const int u = tid;
-      const bool active = u < nh * (kLatent / 16);
-      const int hh = u / (kLatent / 16), f = u % (kLatent / 16);
-      const int h = h0 + hc + hh;
-      // the parts' (m, l) and the sink of this head, loaded before anything waits
-      float2 ml[kMaxInKernelParts];
-#pragma unroll
-      for (int j = 0; j < kMaxInKernelParts; ++j) {
-        ml[j] = make_float2(-INFINITY, 0.f);
-        if (staged && active && j < parts) ml[j] = __ldcg(reinterpret_cast<const float2*>(a.ml_part) + sl[j] * H + h);
+      __syncthreads();  // the staging buffer and descriptors are free
+      if (tid == 0) {
+        fence_proxy_async_global();  // (partials are read by the async proxy)
+        mbar_arrive_expect_tx(bar, uint32_t(parts * nh * kLatent * 4));
+        for (int j = 0; j < parts; ++j) {
+          ms->cb_row[j] = uint32_t(j * (16 * kLatent * 4));
+          bulk_g2s(smem_u32(smem + j * (16 * kLatent * 4)), a.o_part + (ms->mslot[xi][j] * H + h0 + hc) * kLatent,
+                   uint32_t(nh * kLatent * 4), bar);
+        }
       }
-      const float sink_h = (active && a.sink) ? __ldg(a.sink + h) : 0.f;
-      if (staged) {
-        if (k + hc > 0) __syncthreads();  // the buffer's previous contents were read
-        if (tid == 0) {
-          fence_proxy_async_global();  // (this CTA's own partial was written by plain stores)
-          mbar_arrive_expect_tx(bar, uint32_t(parts * nh * kLatent * 4));
-          for (int j = 0; j < parts; ++j)
-            bulk_g2s(smem_u32(smem + j * (16 * kLatent * 4)), a.o_part + (sl[j] * H + h0 + hc) * kLatent,
-                     uint32_t(nh * kLatent * 4), bar);
+      if (tid < parts * nh) {
+        const int j = tid / nh, hh = tid % nh;
+        ms->cb_ml[j][hh] = __ldcg(reinterpret_cast<const float2*>(a.ml_part) + ms->mslot[xi][j] * H + h0 + hc + hh);
+      }
+      __syncthreads();
+      if (!mbar_wait(bar, uses & 1, kWaitLimitNs)) set_abort(ms, a.status);
+      ++uses;
 #ifdef SMLA_TRACE
-          if (k == 0 && hc == 0) ms->merge_t[3] = globaltimer();
+      if (tid == 0 && k == 0 && hc == 0) ms->merge_t[4] = globaltimer();
 #endif
-        }
-      }
-      float mrun = -INFINITY, lsum = 0.f;
-      float acc[16];
-#pragma unroll
-      for (int d = 0; d < 16; ++d) acc[d] = 0.f;
-      if (staged) {
-        if (!mbar_wait(bar, uses & 1, kWaitLimitNs)) {
-          set_abort(ms, a.status);
-          ok = false;
-        }
-        ++uses;
-#ifdef SMLA_TRACE
-        if (tid == 0 && k == 0 && hc == 0) ms->merge_t[4] = globaltimer();
-#endif
-        if (active && ok) {
-#pragma unroll
-          for (int j = 0; j < kMaxInKernelParts; ++j)
-            if (ml[j].y != 0.f) mrun = fmaxf(mrun, ml[j].x);  // parts without keys (l = 0) take no part
-#pragma unroll
-          for (int j = 0; j < kMaxInKernelParts; ++j) {
-            if (j >= parts) continue;
-            const float wt = ml[j].y != 0.f ? ex2(ml[j].x - mrun) : 0.f;  // a NaN m or l stays NaN
-            lsum = fmaf(ml[j].y, wt, lsum);
-            const uint32_t src = smem_u32(smem + j * (16 * kLatent * 4) + (hh * kLatent + 16 * f) * 4);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const uint4 o4 = ld_shared_v4(src + 16 * e);
-              acc[4 * e] = fmaf(wt, __uint_as_float(o4.x), acc[4 * e]);
-              acc[4 * e + 1] = fmaf(wt, __uint_as_float(o4.y), acc[4 * e + 1]);
-              acc[4 * e + 2] = fmaf(wt, __uint_as_float(o4.z), acc[4 * e + 2]);
-              acc[4 * e + 3] = fmaf(wt, __uint_as_float(o4.w), acc[4 * e + 3]);
-            }
-          }
-        }
-      } else if (active) {
-#pragma unroll 1
-        for (int64_t cc = ca; cc <= cz; ++cc) {
-          if (!(cta_begin(cc + 1, T, G) > cta_begin(cc, T, G))) continue;
-          const int64_t s1 = slot_of(cc, P, T, G);
-          const float4* src = reinterpret_cast<const float4*>(a.o_part + (s1 * H + h) * kLatent) + 4 * f;
-          const float2 mj = __ldcg(reinterpret_cast<const float2*>(a.ml_part) + s1 * H + h);
-          float4 oj[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) oj[e] = __ldcg(src + e);
-          if (mj.y == 0.f) continue;
-          if (mj.x > mrun) {  // the running maximum moves: rescale what was summed
-            const float r = ex2(mrun - mj.x);
-            lsum *= r;
-#pragma unroll
-            for (int d = 0; d < 16; ++d) acc[d] *= r;
-            mrun = mj.x;
-          }
-          const float wt = ex2(mj.x - mrun);
-          lsum = fmaf(mj.y, wt, lsum);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            acc[4 * e] = fmaf(wt, oj[e].x, acc[4 * e]);
-            acc[4 * e + 1] = fmaf(wt, oj[e].y, acc[4 * e + 1]);
-            acc[4 * e + 2] = fmaf(wt, oj[e].z, acc[4 * e + 2]);
-            acc[4 * e + 3] = fmaf(wt, oj[e].w, acc[4 * e + 3]);
-          }
-        }
-      }
-      if (active) {
-        float fac, lse_h;
-        finish_head_v(mrun, lsum, a.sink != nullptr, sink_h, &fac, &lse_h);
-        uint4 v0, v1;
-        v0.x = pack_bf16x2(acc[0] * fac, acc[1] * fac);
-        v0.y = pack_bf16x2(acc[2] * fac, acc[3] * fac);
-        v0.z = pack_bf16x2(acc[4] * fac, acc[5] * fac);
-        v0.w = pack_bf16x2(acc[6] * fac, acc[7] * fac);
-        v1.x = pack_bf16x2(acc[8] * fac, acc[9] * fac);
-        v1.y = pack_bf16x2(acc[10] * fac, acc[11] * fac);
-        v1.z = pack_bf16x2(acc[12] * fac, acc[13] * fac);
-        v1.w = pack_bf16x2(acc[14] * fac, acc[15] * fac);
-        uint4* dst = reinterpret_cast<uint4*>(a.out + int64_t(row) * a.out_stride_row + int64_t(h) * a.out_stride_head + 16 * f);
-        dst[0] = v0;
-        dst[1] = v1;
-        if (f == 0 && a.lse) a.lse[int64_t(row) * H + h] = lse_h;
-      }
+      combine_staged(a, smem, ms, parts, row, h0 + hc, nh, tid, kThreads);
     }
 #ifdef SMLA_TRACE
     if (tid == 0) ms->merge_t[1 + k] = globaltimer();
@@ -930,7 +932,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
     }
     __syncthreads();
     const int64_t Tt = ms->total_tiles;
-    const int64_t b = cta_begin(c_id, Tt, G), e = cta_begin(c_id + 1, Tt, G);
+    const int64_t b = cbeg(c_id, Tt, G), e = cbeg(c_id + 1, Tt, G);
     int64_t P = ms->scan[32 + warp] + x - local;
     int32_t mine = 0;
 #pragma unroll 1
@@ -962,7 +964,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
   __syncthreads();
   tc_fence_after();
   const int64_t T = ms->total_tiles;
-  const int64_t cb = cta_begin(c_id, T, G), ce = cta_begin(c_id + 1, T, G);
+  const int64_t cb = cbeg(c_id, T, G), ce = cbeg(c_id + 1, T, G);
   const int32_t n_tiles = ms->n_tiles;
   const int32_t row0 = ms->first_row;
   const int64_t P0 = ms->first_tile;
@@ -1225,14 +1227,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
         ++pi;
       }
     }
-    {
-      // every MMA issued here has completed before TMEM is freed (also after a timeout)
-      if (lane == 0) {
-        mma_commit(bars + kDrain);
-        if (!mbar_wait(bars + kDrain, 0, kWaitLimitNs)) set_abort(ms, a.status);
-      }
-      __syncwarp();
-    }
+    // the drain barrier completes once every MMA issued here has (the warp
+    // that frees TMEM waits for it)
+    if (lane == 0) mma_commit(bars + kDrain);
+    __syncwarp();
   } else if (warp < kLoadWarp0) {
     // =================== aux: scale factors, q staging, epilogues ===================
     const int q = warp - kAuxWarp0;  // TMEM lane quarter
@@ -1261,11 +1259,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
       if (r < a.n_q) {
         const int64_t Pr = (q == 0 ? P0 : ms->last_tile) + kRowStart;
         const int32_t nt = Cursor::tiles_of(row_len(a, r));
-        const int64_t ca = cta_of_tile(Pr, T, G), cz = cta_of_tile(Pr + nt - 1, T, G);
+        const int64_t ca = cof(Pr, T, G), cz = cof(Pr + nt - 1, T, G);
         int32_t n = 0;
         for (int64_t c0 = ca; c0 <= cz; c0 += 32) {
           const int64_t cc = c0 + lane;
-          const bool in = cc <= cz && cta_begin(cc + 1, T, G) > cta_begin(cc, T, G);
+          const bool in = cc <= cz && cbeg(cc + 1, T, G) > cbeg(cc, T, G);
           const uint32_t m = __ballot_sync(0xffffffffu, in);
           const int j = n + __popc(m & ((1u << lane) - 1u));
           if (in && j < kMaxInKernelParts) ms->mslot[q][j] = slot_of(cc, Pr, T, G);
@@ -1375,17 +1373,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
             for (int j = 0; j < parts; ++j) {
               const int64_t sl = ms->mslot[xi][j];
               if (sl == own || jj >= parts - 1) continue;
-              if (ta == 0)
+              if (ta == 0) {
+                ms->cb_row[1 + jj] = uint32_t(sp * kStageBytes + jj * rows_bytes);
                 bulk_g2s(smem_base + uint32_t(sp * kStageBytes + jj * rows_bytes), a.o_part + (sl * H + h0) * kLatent,
                          uint32_t(rows_bytes), bars + kMerge);
-              if (ta < Hl) ms->fml[jj][ta] = __ldcg(reinterpret_cast<const float2*>(a.ml_part) + sl * H + h0 + ta);
+              }
+              if (ta < Hl) ms->cb_ml[1 + jj][ta] = __ldcg(reinterpret_cast<const float2*>(a.ml_part) + sl * H + h0 + ta);
               if (ta == 32 * jj) ms->fnv[jj] = __ldcg(a.nv_part + sl);
               ++jj;
             }
-            if (ta == 0) {
-              ms->fast_s_others = sp;
-              ms->fast_s_own = i & 1;
-            }
+            if (ta == 0) ms->fast_s_own = i & 1;
             F8_TR(45, i);
           }
           named_barrier(2, 128);
@@ -1411,13 +1408,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
     }
     if (pi > 0) aux_epilogue<HP>(actx, prev, pi - 1, true);
     F8_TR(44, 0);
-    if (q < C::kQkSplit) {
-      if (lane == 0) {
-        mma_commit(bars + kDrain);
-        if (!mbar_wait(bars + kDrain, 0, kWaitLimitNs)) set_abort(ms, a.status);
-      }
-      __syncwarp();
-    }
+    if (q < C::kQkSplit && lane == 0) mma_commit(bars + kDrain);
+    __syncwarp();
   } else {
     // =================== loaders ===================
     const int lw = warp - kLoadWarp0;
@@ -1486,6 +1478,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
   tc_fence_before();
   __syncthreads();
   if (warp == kAuxWarp0) {
+    // every MMA of the CTA has completed before TMEM is freed (also after a
+    // timeout: this wait has its own limit)
+    if (lane == 0 && !mbar_wait(bars + kDrain, 0, kWaitLimitNs)) set_abort(ms, a.status);
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -1503,6 +1499,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
   if (tid == 0 && tr_buf != nullptr && ms->fast) {
     for (int k = 5; k < 8; ++k)
       tr_buf[(size_t(blockIdx.x) * 20 + 19) * 256 + 10 + k] = (ms->merge_t[k] & 0xFFFFFFFFFFFFull) | (uint64_t(70 + k) << 48);
+    for (int k = 0; k < 8; ++k)
+      tr_buf[(size_t(blockIdx.x) * 20 + 19) * 256 + 20 + k] = (ms->comb_t[k] & 0xFFFFFFFFFFFFull) | (uint64_t(80 + k) << 48);
   }
 #endif
 }

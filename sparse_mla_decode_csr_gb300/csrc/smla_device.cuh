@@ -146,15 +146,18 @@ __device__ __forceinline__ void finish_head_v(float m, float l, bool has_sink, f
     *lse = -INFINITY;
     return;
   }
-  *lse = (m + log2f(l)) * kLn2;
+  // (hardware approximations, relative error ~2^-21: out is bf16 and the
+  // LSE is compared at 1e-2; the accurate library forms are long code paths
+  // run once per row at a kernel's end)
+  *lse = (m + __log2f(l)) * kLn2;
   if (!has_sink) {
-    *factor = 1.f / l;
+    *factor = __fdividef(1.f, l);
     return;
   }
   const float s = sink_h * kLog2e;
   const float mf = fmaxf(m, s);
   const float wm = exp2f(m - mf);
-  *factor = wm / (exp2f(s - mf) + l * wm);
+  *factor = __fdividef(wm, exp2f(s - mf) + l * wm);
 }
 
 __device__ __forceinline__ void finish_head(float m, float l, const float* sink, int h,
