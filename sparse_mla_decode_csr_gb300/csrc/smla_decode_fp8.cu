@@ -182,7 +182,6 @@ struct Misc {
   float fac[kMaxHP];                            // epilogue: output factors of a whole row's heads
   int32_t fast;                                 // the final part completes its row (merged in the epilogue)
   int32_t fast_s_own;                           //   the stage that takes this part's O
-  int32_t merge_uses;                           // completed phases of the merge barrier
   int32_t fnv[kMaxInKernelParts];               // final-part merge: the other parts' key counts
   // parts staged in shared memory for a combine: part j's O rows of heads
   // [cb_h, cb_h + cb_nh) at byte offset cb_row[j] (rows of 512 f32), its
@@ -202,9 +201,10 @@ struct Misc {
   int32_t n_merge;                              // rows this CTA completes and merges at its end
   int32_t merge_row[2];
   int32_t merge_x[2];                           // which of the two rows above
+  int32_t merge_kind[2];                        // 1: staged by the final part (see aux_stage_final)
+  int32_t merge_own_nv;                         //   and that part's key count
 #ifdef SMLA_TRACE
   uint64_t merge_t[8];
-  uint64_t comb_t[8];
 #endif
 };
 // (the 16-byte reads of red_max_t rows and 4-byte reads of sfq rows need these)
@@ -501,59 +501,54 @@ __device__ __noinline__ void combine_staged(const DecodeArgs& a, const uint8_t* 
   const int64_t osh = a.out_stride_head;
   float* const lse_row = a.lse ? a.lse + int64_t(row) * a.heads : nullptr;
   const float* const sink = a.sink;
-#ifdef SMLA_TRACE
-  int it = 0;
-#endif
 #pragma unroll 1
   for (int u = t; u < nh * 32; u += nthreads) {
-#ifdef SMLA_TRACE
-    if (t == 0 && it < 2) const_cast<Misc*>(ms)->comb_t[4 * it] = globaltimer();
-#endif
     const int hh = u / 32, c = u % 32;
-    float mrun = -INFINITY;
-#pragma unroll 1
-    for (int j = 0; j < parts; ++j) {
-      const float2 mj = ms->cb_ml[j][hh];
-      if (mj.y != 0.f) mrun = fmaxf(mrun, mj.x);  // parts without keys (l = 0) take no part
+    // every part's (m, l) and 16 values first (independent loads), then the sums
+    float2 ml[kMaxInKernelParts];
+    uint4 v[kMaxInKernelParts][4];
+#pragma unroll
+    for (int j = 0; j < kMaxInKernelParts; ++j) {
+      ml[j] = make_float2(-INFINITY, 0.f);
+      if (j < parts) {
+        ml[j] = ms->cb_ml[j][hh];
+        const uint4* src = reinterpret_cast<const uint4*>(smem + ms->cb_row[j]) + (hh * kLatent + 4 * c) / 4;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[j][e] = src[32 * e];  // dims 128 e + 4 c ..
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[j][e] = make_uint4(0, 0, 0, 0);
+      }
     }
+    float mrun = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kMaxInKernelParts; ++j)
+      if (ml[j].y != 0.f) mrun = fmaxf(mrun, ml[j].x);  // parts without keys (l = 0) take no part
     float acc[16];
 #pragma unroll
     for (int d = 0; d < 16; ++d) acc[d] = 0.f;
     float lsum = 0.f;
-#pragma unroll 1
-    for (int j = 0; j < parts; ++j) {
-      const float2 mj = ms->cb_ml[j][hh];
-      const float wt = mj.y != 0.f ? ex2(mj.x - mrun) : 0.f;  // a NaN m or l stays NaN
-      lsum = fmaf(mj.y, wt, lsum);
-      const uint32_t src = smem_u32(smem + ms->cb_row[j]) + uint32_t((hh * kLatent + 4 * c) * 4);
+#pragma unroll
+    for (int j = 0; j < kMaxInKernelParts; ++j) {
+      const float wt = ml[j].y != 0.f ? ex2(ml[j].x - mrun) : 0.f;  // a NaN m or l stays NaN
+      lsum = fmaf(ml[j].y, wt, lsum);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const uint4 v = ld_shared_v4(src + 512 * e);
-        acc[4 * e] = fmaf(wt, __uint_as_float(v.x), acc[4 * e]);
-        acc[4 * e + 1] = fmaf(wt, __uint_as_float(v.y), acc[4 * e + 1]);
-        acc[4 * e + 2] = fmaf(wt, __uint_as_float(v.z), acc[4 * e + 2]);
-        acc[4 * e + 3] = fmaf(wt, __uint_as_float(v.w), acc[4 * e + 3]);
+        acc[4 * e] = fmaf(wt, __uint_as_float(v[j][e].x), acc[4 * e]);
+        acc[4 * e + 1] = fmaf(wt, __uint_as_float(v[j][e].y), acc[4 * e + 1]);
+        acc[4 * e + 2] = fmaf(wt, __uint_as_float(v[j][e].z), acc[4 * e + 2]);
+        acc[4 * e + 3] = fmaf(wt, __uint_as_float(v[j][e].w), acc[4 * e + 3]);
       }
     }
     const int h = hb + hh;
-#ifdef SMLA_TRACE
-    if (t == 0 && it < 2) const_cast<Misc*>(ms)->comb_t[4 * it + 1] = globaltimer();
-#endif
     float fac, lse_h;
     finish_head(mrun, lsum, sink, h, &fac, &lse_h);
-#ifdef SMLA_TRACE
-    if (t == 0 && it < 2) const_cast<Misc*>(ms)->comb_t[4 * it + 2] = globaltimer();
-#endif
     uint16_t* dst = out_row + int64_t(h) * osh + 4 * c;
 #pragma unroll
     for (int e = 0; e < 4; ++e)
       *reinterpret_cast<uint2*>(dst + 128 * e) = make_uint2(pack_bf16x2(acc[4 * e] * fac, acc[4 * e + 1] * fac),
                                                             pack_bf16x2(acc[4 * e + 2] * fac, acc[4 * e + 3] * fac));
     if (c == 0 && lse_row) lse_row[h] = lse_h;
-#ifdef SMLA_TRACE
-    if (t == 0 && it < 2) const_cast<Misc*>(ms)->comb_t[4 * it + 3] = globaltimer();
-    ++it;
-#endif
   }
 }
 
@@ -612,27 +607,21 @@ __device__ __noinline__ void combine_global(const DecodeArgs& a, int row, int hb
   }
 }
 
-// [P2] stage_combine of a shared row by the CTA that holds its last part to
-// finish, inside that part's epilogue (aux warps; the CTA's final part).  The
-// other parts had all arrived when this part's last tile began, so their O
-// rows were bulk-copied into the stage freed by the previous tile and their
-// (m, l) and counts loaded then (staging descriptors 1 .. parts - 1, see the
-// aux loop); this part's O goes from TMEM to the other stage (descriptor 0),
-// and no partial of this part is written.  Then out, lse, n_valid, and the
-// ticket back to 0.
+// The CTA's final part completes a shared row whose other parts had all
+// arrived when its last tile began: their O rows were then bulk-copied into
+// the stage freed by the previous tile and their (m, l) and counts loaded
+// (staging descriptors 1 .. parts - 1, see the aux loop).  Here (aux warps)
+// this part's O goes from TMEM to the other stage (descriptor 0) with its
+// (m, l), no partial of this part is written, and the row is queued for the
+// CTA's end, where all threads combine it.
 template <int HP>
-__device__ __noinline__ void aux_merge_final(const AuxCtx& x, const Cursor& pc, int ob, int parts, int s_own) {
+__device__ __noinline__ void aux_stage_final(const AuxCtx& x, const Cursor& pc, int ob, int xi, int s_own) {
   using C = Cfg<HP>;
-  const DecodeArgs& a = *x.a;
   Misc* ms = x.ms;
-  uint8_t* smem = x.smem;
   uint64_t* bars = x.bars;
   const uint32_t tmem = x.tmem, lane_base = x.lane_base;
   const int Hl = x.Hl, lane = x.lane, ta = x.ta;
-  float* ow = reinterpret_cast<float*>(smem + s_own * kStageBytes);  // this part's O [Hl][512]
-#ifdef SMLA_TRACE
-  if (ta == 0) ms->merge_t[5] = globaltimer();
-#endif
+  float* ow = reinterpret_cast<float*>(x.smem + s_own * kStageBytes);  // this part's O [Hl][512]
   // this part's O^T rows: dim 128 b + ta of every block b
 #pragma unroll 1
   for (int k = 0; k < 4 * C::kPass; ++k) {
@@ -647,25 +636,17 @@ __device__ __noinline__ void aux_merge_final(const AuxCtx& x, const Cursor& pc, 
       if (j < hn) ow[(16 * pass + j) * kLatent + 128 * b + ta] = __uint_as_float(v0[j]) + __uint_as_float(v1[j]);
   }
   if (ta < Hl) ms->cb_ml[0][ta] = make_float2(ms->part_m[ob][ta], ms->part_l[ob][ta]);
-  if (ta == 0) ms->cb_row[0] = uint32_t(s_own * kStageBytes);
-  tc_fence_before();
-  named_barrier(2, 128);  // own O, the (m, l) and counts in shared memory
-  if (lane == 0) mbar_arrive(bars + kOEmpty + ob);
-#ifdef SMLA_TRACE
-  if (ta == 0) ms->merge_t[6] = globaltimer();
-#endif
-  if (!mbar_wait(bars + kMerge, 0, kWaitLimitNs)) set_abort(ms, a.status);
-#ifdef SMLA_TRACE
-  if (ta == 0) ms->merge_t[7] = globaltimer();
-#endif
-  combine_staged(a, smem, ms, parts, pc.row, x.h0, Hl, ta, 128);
   if (ta == 0) {
-    int32_t nv = ms->part_nv[ob];
-    for (int jj = 0; jj < parts - 1; ++jj) nv += ms->fnv[jj];
-    if (x.g == 0 && a.n_valid) a.n_valid[pc.row] = nv;
-    a.ticket[int64_t(pc.row) * x.hg + x.g] = 0;  // ready for the next call
-    ms->merge_uses = 1;
+    ms->cb_row[0] = uint32_t(s_own * kStageBytes);
+    const int k = ms->n_merge++;
+    ms->merge_row[k] = pc.row;
+    ms->merge_x[k] = xi;
+    ms->merge_kind[k] = 1;
+    ms->merge_own_nv = ms->part_nv[ob];
   }
+  tc_fence_before();
+  named_barrier(2, 128);  // every aux thread read its O and (m, l)
+  if (lane == 0) mbar_arrive(bars + kOEmpty + ob);
 }
 
 // A row part's epilogue (aux warps): out and lse of a whole row, or the
@@ -692,7 +673,7 @@ __device__ __noinline__ void aux_epilogue(const AuxCtx& x, const Cursor& pc, int
   wait_warp(bars + kOFull + ob, ph, ms, a);
   tc_fence_after();
   if (final_part && ms->fast) {  // (decided when the part's last tile began)
-    aux_merge_final<HP>(x, pc, ob, parts, ms->fast_s_own);
+    aux_stage_final<HP>(x, pc, ob, xi, ms->fast_s_own);
     return;
   }
   const int64_t slot = whole ? 0 : slot_of(x.c_id, pc.P, T, G);
@@ -759,6 +740,7 @@ __device__ __noinline__ void aux_epilogue(const AuxCtx& x, const Cursor& pc, int
         const int k = ms->n_merge++;
         ms->merge_row[k] = row;
         ms->merge_x[k] = xi;
+        ms->merge_kind[k] = 0;
       }
     }
   }
@@ -783,7 +765,10 @@ __device__ __noinline__ void end_merge(const DecodeArgs& a, uint8_t* smem, uint6
   if (warp < n_merge) {
     const int xi = ms->merge_x[warp];
     const int parts = ms->mparts[xi];
-    if (parts <= kMaxInKernelParts) {
+    if (ms->merge_kind[warp] == 1) {  // counts loaded when the row was staged
+      if (lane == 0) nv = ms->merge_own_nv;
+      if (lane >= 1 && lane < parts) nv = ms->fnv[lane - 1];
+    } else if (parts <= kMaxInKernelParts) {
       if (lane < parts) nv = __ldcg(a.nv_part + ms->mslot[xi][lane]);
     } else {
       const int64_t ca = ms->mca[xi], cz = ms->mcz[xi], P = ms->mP[xi];
@@ -794,9 +779,19 @@ __device__ __noinline__ void end_merge(const DecodeArgs& a, uint8_t* smem, uint6
 #ifdef SMLA_TRACE
   if (tid == 0) ms->merge_t[0] = globaltimer();
 #endif
-  uint32_t uses = ms->merge_uses;  // completed phases of `bar`
+  uint32_t uses = 0;  // completed phases of `bar`
+  // the row staged by the final part first (its bulk copies are the barrier's
+  // first phase, and the other merges reuse its shared memory)
 #pragma unroll 1
   for (int k = 0; k < n_merge; ++k) {
+    if (ms->merge_kind[k] != 1) continue;
+    if (!mbar_wait(bar, 0, kWaitLimitNs)) set_abort(ms, a.status);
+    uses = 1;
+    combine_staged(a, smem, ms, ms->mparts[ms->merge_x[k]], ms->merge_row[k], h0, Hl, tid, kThreads);
+  }
+#pragma unroll 1
+  for (int k = 0; k < n_merge; ++k) {
+    if (ms->merge_kind[k] == 1) continue;
     const int row = ms->merge_row[k];
     const int xi = ms->merge_x[k];
     const int parts = ms->mparts[xi];
@@ -892,7 +887,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
     ms->last_row = a.n_q;
     ms->last_tile = 0;
     ms->mparts[0] = ms->mparts[1] = 0;
-    ms->merge_uses = 0;
     ms->fast = 0;
     ms->n_tiles = 0;
     ms->n_merge = 0;
@@ -1085,6 +1079,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
             pv_waited = true;
           }
           tc_fence_after();
+          float al[16];
+#pragma unroll
+          for (int h = 0; h < 16; ++h) al[h] = __shfl_sync(0xffffffffu, alpha, h);
 #pragma unroll 1
           for (int k = 0; k < 8; ++k) {  // 4 blocks x (hi, lo)
             const uint32_t ta = tmem + lane_base + C::o_col(ob, k >> 1) + uint32_t(32 * pass + 16 * (k & 1));
@@ -1092,7 +1089,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
             tmem_ld16(ta, v);
             tmem_wait_ld();
 #pragma unroll
-            for (int h = 0; h < 16; ++h) v[h] = __float_as_uint(__uint_as_float(v[h]) * __shfl_sync(0xffffffffu, alpha, h));
+            for (int h = 0; h < 16; ++h) v[h] = __float_as_uint(__uint_as_float(v[h]) * al[h]);
             tmem_st16(ta, v);
           }
           tmem_wait_st();
@@ -1495,12 +1492,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
       tr_buf[(size_t(blockIdx.x) * 20 + 19) * 256 + k] = (ms->merge_t[k] & 0xFFFFFFFFFFFFull) | (uint64_t(70 + k) << 48);
     tr_buf[(size_t(blockIdx.x) * 20 + 19) * 256 + 8] = (ms->merge_t[3] & 0xFFFFFFFFFFFFull) | (uint64_t(73) << 48);
     tr_buf[(size_t(blockIdx.x) * 20 + 19) * 256 + 9] = (ms->merge_t[4] & 0xFFFFFFFFFFFFull) | (uint64_t(74) << 48);
-  }
-  if (tid == 0 && tr_buf != nullptr && ms->fast) {
-    for (int k = 5; k < 8; ++k)
-      tr_buf[(size_t(blockIdx.x) * 20 + 19) * 256 + 10 + k] = (ms->merge_t[k] & 0xFFFFFFFFFFFFull) | (uint64_t(70 + k) << 48);
-    for (int k = 0; k < 8; ++k)
-      tr_buf[(size_t(blockIdx.x) * 20 + 19) * 256 + 20 + k] = (ms->comb_t[k] & 0xFFFFFFFFFFFFull) | (uint64_t(80 + k) << 48);
   }
 #endif
 }
