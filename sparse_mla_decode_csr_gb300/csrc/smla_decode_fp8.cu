@@ -647,6 +647,9 @@ __device__ __noinline__ void aux_stage_final(const AuxCtx& x, const Cursor& pc, 
   tc_fence_before();
   named_barrier(2, 128);  // every aux thread read its O and (m, l)
   if (lane == 0) mbar_arrive(bars + kOEmpty + ob);
+#ifdef SMLA_TRACE
+  if (ta == 0) ms->merge_t[5] = globaltimer();
+#endif
 }
 
 // A row part's epilogue (aux warps): out and lse of a whole row, or the
@@ -672,6 +675,9 @@ __device__ __noinline__ void aux_epilogue(const AuxCtx& x, const Cursor& pc, int
   wait_warp(bars + kEpiReady + ob, ph, ms, a);
   wait_warp(bars + kOFull + ob, ph, ms, a);
   tc_fence_after();
+#ifdef SMLA_TRACE
+  if (final_part && ta == 0) ms->merge_t[4] = globaltimer();
+#endif
   if (final_part && ms->fast) {  // (decided when the part's last tile began)
     aux_stage_final<HP>(x, pc, ob, xi, ms->fast_s_own);
     return;
@@ -787,7 +793,13 @@ __device__ __noinline__ void end_merge(const DecodeArgs& a, uint8_t* smem, uint6
     if (ms->merge_kind[k] != 1) continue;
     if (!mbar_wait(bar, 0, kWaitLimitNs)) set_abort(ms, a.status);
     uses = 1;
+#ifdef SMLA_TRACE
+    if (tid == 0) ms->merge_t[1] = globaltimer();
+#endif
     combine_staged(a, smem, ms, ms->mparts[ms->merge_x[k]], ms->merge_row[k], h0, Hl, tid, kThreads);
+#ifdef SMLA_TRACE
+    if (tid == 0) ms->merge_t[2] = globaltimer();
+#endif
   }
 #pragma unroll 1
   for (int k = 0; k < n_merge; ++k) {
@@ -819,15 +831,12 @@ __device__ __noinline__ void end_merge(const DecodeArgs& a, uint8_t* smem, uint6
       __syncthreads();
       if (!mbar_wait(bar, uses & 1, kWaitLimitNs)) set_abort(ms, a.status);
       ++uses;
-#ifdef SMLA_TRACE
-      if (tid == 0 && k == 0 && hc == 0) ms->merge_t[4] = globaltimer();
-#endif
       combine_staged(a, smem, ms, parts, row, h0 + hc, nh, tid, kThreads);
     }
-#ifdef SMLA_TRACE
-    if (tid == 0) ms->merge_t[1 + k] = globaltimer();
-#endif
   }
+#ifdef SMLA_TRACE
+  if (tid == 0) ms->merge_t[3] = globaltimer();
+#endif
   // key counts and tickets (warp k: row k)
   if (warp < n_merge) {
 #pragma unroll
@@ -888,6 +897,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
     ms->last_tile = 0;
     ms->mparts[0] = ms->mparts[1] = 0;
     ms->fast = 0;
+#ifdef SMLA_TRACE
+    for (int k = 0; k < 8; ++k) ms->merge_t[k] = 0;
+#endif
     ms->n_tiles = 0;
     ms->n_merge = 0;
     fence_mbar_init();
@@ -1487,11 +1499,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
   if (ms->n_merge > 0) end_merge(a, smem, bars + kMerge, ms, tid, h0, Hl, hg, g, T, G);
   F8_TR(5, 0);
 #ifdef SMLA_TRACE
-  if (tid == 0 && tr_buf != nullptr && ms->n_merge > 0) {
-    for (int k = 0; k <= ms->n_merge; ++k)
+  if (tid == 0 && tr_buf != nullptr) {
+    for (int k = 0; k < 6; ++k)
       tr_buf[(size_t(blockIdx.x) * 20 + 19) * 256 + k] = (ms->merge_t[k] & 0xFFFFFFFFFFFFull) | (uint64_t(70 + k) << 48);
-    tr_buf[(size_t(blockIdx.x) * 20 + 19) * 256 + 8] = (ms->merge_t[3] & 0xFFFFFFFFFFFFull) | (uint64_t(73) << 48);
-    tr_buf[(size_t(blockIdx.x) * 20 + 19) * 256 + 9] = (ms->merge_t[4] & 0xFFFFFFFFFFFFull) | (uint64_t(74) << 48);
   }
 #endif
 }
