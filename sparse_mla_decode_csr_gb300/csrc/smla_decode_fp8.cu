@@ -201,8 +201,9 @@ struct Misc {
   int32_t n_merge;                              // rows this CTA completes and merges at its end
   int32_t merge_row[2];
   int32_t merge_x[2];                           // which of the two rows above
-  int32_t merge_kind[2];                        // 1: staged by the final part (see aux_stage_final)
-  int32_t merge_own_nv;                         //   and that part's key count
+  int32_t merge_kind[2];                        // 1, 2: staged by the final part (see aux_stage_final)
+  int32_t merge_own_nv;                         //   and that part's key count and slot
+  int64_t merge_own_slot;
 #ifdef SMLA_TRACE
   uint64_t merge_t[8];
 #endif
@@ -494,7 +495,7 @@ __device__ __noinline__ void aux_stage_q(const AuxCtx& x, int row, int qb) {
 // u / 32, dims 4 c + 128 e (c = u % 32, e = 0..3), so that a warp reads
 // consecutive 16-byte words; threads t, t + nthreads, ...
 __device__ __noinline__ void combine_staged(const DecodeArgs& a, const uint8_t* smem, const Misc* ms, int parts,
-                                            int row, int hb, int nh, int t, int nthreads) {
+                                            int row, int hb, int nh, int t, int nthreads, bool dry = false) {
   // (the arguments' fields in registers: read through the reference they would
   // be reloaded from the parameter buffer after every store)
   uint16_t* const out_row = a.out + int64_t(row) * a.out_stride_row;
@@ -543,6 +544,7 @@ __device__ __noinline__ void combine_staged(const DecodeArgs& a, const uint8_t* 
     const int h = hb + hh;
     float fac, lse_h;
     finish_head(mrun, lsum, sink, h, &fac, &lse_h);
+    if (dry) continue;  // (a run that only brings this code into the instruction caches)
     uint16_t* dst = out_row + int64_t(h) * osh + 4 * c;
 #pragma unroll
     for (int e = 0; e < 4; ++e)
@@ -615,7 +617,7 @@ __device__ __noinline__ void combine_global(const DecodeArgs& a, int row, int hb
 // (m, l), no partial of this part is written, and the row is queued for the
 // CTA's end, where all threads combine it.
 template <int HP>
-__device__ __noinline__ void aux_stage_final(const AuxCtx& x, const Cursor& pc, int ob, int xi, int s_own) {
+__device__ __noinline__ void aux_stage_final(const AuxCtx& x, const Cursor& pc, int ob, int xi, int s_own, int kind) {
   using C = Cfg<HP>;
   Misc* ms = x.ms;
   uint64_t* bars = x.bars;
@@ -641,8 +643,9 @@ __device__ __noinline__ void aux_stage_final(const AuxCtx& x, const Cursor& pc, 
     const int k = ms->n_merge++;
     ms->merge_row[k] = pc.row;
     ms->merge_x[k] = xi;
-    ms->merge_kind[k] = 1;
+    ms->merge_kind[k] = kind;
     ms->merge_own_nv = ms->part_nv[ob];
+    ms->merge_own_slot = slot_of(x.c_id, pc.P, x.T, x.G);
   }
   tc_fence_before();
   named_barrier(2, 128);  // every aux thread read its O and (m, l)
@@ -672,6 +675,15 @@ __device__ __noinline__ void aux_epilogue(const AuxCtx& x, const Cursor& pc, int
   const bool whole = pc.whole();
   const int xi = pi == 0 ? 0 : 1;  // a shared row is this CTA's first or last one
   const int32_t parts = whole ? 1 : ms->mparts[xi];
+  const int rows_bytes = Hl * kLatent * 4;
+  // The final part of a shared row whose other parts have arrived by now
+  // (tickets read before the waits) completes the row without a partial:
+  // the stages are free once its last PV has completed, so the other parts'
+  // O rows are bulk-copied into stage 0 and this part's O goes to stage 1.
+  const bool may_late = final_part && !whole && !ms->fast && parts >= 2 && parts <= kMaxInKernelParts &&
+                        (parts - 1) * rows_bytes <= kStageBytes;
+  int32_t tk = -1;
+  if (may_late && ta == 0) tk = ld_acquire_gpu(a.ticket + int64_t(row) * x.hg + x.g);
   wait_warp(bars + kEpiReady + ob, ph, ms, a);
   wait_warp(bars + kOFull + ob, ph, ms, a);
   tc_fence_after();
@@ -679,8 +691,32 @@ __device__ __noinline__ void aux_epilogue(const AuxCtx& x, const Cursor& pc, int
   if (final_part && ta == 0) ms->merge_t[4] = globaltimer();
 #endif
   if (final_part && ms->fast) {  // (decided when the part's last tile began)
-    aux_stage_final<HP>(x, pc, ob, xi, ms->fast_s_own);
+    aux_stage_final<HP>(x, pc, ob, xi, ms->fast_s_own, 1);
     return;
+  }
+  if (may_late) {
+    if (ta == 0) {
+      ms->fast = tk == parts - 1;
+      if (ms->fast) {
+        fence_proxy_async_global();  // (the other parts' partials are read by the async proxy)
+        mbar_arrive_expect_tx(bars + kMerge, uint32_t((parts - 1) * rows_bytes));
+        const int64_t own = slot_of(x.c_id, pc.P, T, G);
+        int jj = 0;
+        for (int j = 0; j < parts; ++j) {
+          const int64_t sl = ms->mslot[xi][j];
+          if (sl == own || jj >= parts - 1) continue;
+          ms->cb_row[1 + jj] = uint32_t(jj * rows_bytes);
+          bulk_g2s(smem_u32(x.smem + jj * rows_bytes), a.o_part + (sl * H + h0) * kLatent, uint32_t(rows_bytes),
+                   bars + kMerge);
+          ++jj;
+        }
+      }
+    }
+    named_barrier(2, 128);
+    if (ms->fast) {  // (the other parts' (m, l) and counts are loaded at the end merge)
+      aux_stage_final<HP>(x, pc, ob, xi, 1, 2);
+      return;
+    }
   }
   const int64_t slot = whole ? 0 : slot_of(x.c_id, pc.P, T, G);
   // head ta's output factor and LSE (whole rows), or its partial (m, l)
@@ -774,6 +810,9 @@ __device__ __noinline__ void end_merge(const DecodeArgs& a, uint8_t* smem, uint6
     if (ms->merge_kind[warp] == 1) {  // counts loaded when the row was staged
       if (lane == 0) nv = ms->merge_own_nv;
       if (lane >= 1 && lane < parts) nv = ms->fnv[lane - 1];
+    } else if (ms->merge_kind[warp] == 2) {  // this part's count, the others' from their slots
+      if (lane == 0) nv = ms->merge_own_nv;
+      if (lane < parts && ms->mslot[xi][lane] != ms->merge_own_slot) nv += __ldcg(a.nv_part + ms->mslot[xi][lane]);
     } else if (parts <= kMaxInKernelParts) {
       if (lane < parts) nv = __ldcg(a.nv_part + ms->mslot[xi][lane]);
     } else {
@@ -790,7 +829,21 @@ __device__ __noinline__ void end_merge(const DecodeArgs& a, uint8_t* smem, uint6
   // first phase, and the other merges reuse its shared memory)
 #pragma unroll 1
   for (int k = 0; k < n_merge; ++k) {
-    if (ms->merge_kind[k] != 1) continue;
+    if (ms->merge_kind[k] == 0) continue;
+    if (ms->merge_kind[k] == 2) {
+      // the other parts' (m, l), in the order of their bulk copies
+      const int xi = ms->merge_x[k], parts = ms->mparts[xi];
+      if (tid < Hl) {
+        int jj = 0;
+        for (int j = 0; j < parts; ++j) {
+          const int64_t sl = ms->mslot[xi][j];
+          if (sl == ms->merge_own_slot || jj >= parts - 1) continue;
+          ms->cb_ml[1 + jj][tid] = __ldcg(reinterpret_cast<const float2*>(a.ml_part) + sl * H + h0 + tid);
+          ++jj;
+        }
+      }
+      __syncthreads();
+    }
     if (!mbar_wait(bar, 0, kWaitLimitNs)) set_abort(ms, a.status);
     uses = 1;
 #ifdef SMLA_TRACE
@@ -803,7 +856,7 @@ __device__ __noinline__ void end_merge(const DecodeArgs& a, uint8_t* smem, uint6
   }
 #pragma unroll 1
   for (int k = 0; k < n_merge; ++k) {
-    if (ms->merge_kind[k] == 1) continue;
+    if (ms->merge_kind[k] != 0) continue;
     const int row = ms->merge_row[k];
     const int xi = ms->merge_x[k];
     const int parts = ms->mparts[xi];
@@ -897,6 +950,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
     ms->last_tile = 0;
     ms->mparts[0] = ms->mparts[1] = 0;
     ms->fast = 0;
+    for (int j = 0; j < kMaxInKernelParts; ++j) {
+      ms->cb_row[j] = 0;
+      for (int h = 0; h < kMaxHP; ++h) ms->cb_ml[j][h] = make_float2(0.f, 0.f);
+    }
 #ifdef SMLA_TRACE
     for (int k = 0; k < 8; ++k) ms->merge_t[k] = 0;
 #endif
@@ -1001,6 +1058,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
       mref[p] = kInitMax;
       lsum[p] = 0.f;
     }
+    // The end merge's combine runs once per launch, at its end, when every
+    // instruction fetch that misses waits behind the other CTAs' gathers: run
+    // it now without its stores (on zeroed staging descriptors) while the
+    // first tiles are in flight, so that its code is in the caches then
+    if (n_tiles > 0) combine_staged(a, smem, ms, kMaxInKernelParts, 0, 0, 4, t, 32 * kSoftmaxWarps, true);
     Cursor c;
     c.init(a, row0, P0, cb, ce);
     int pi = 0;  // row part index within this CTA
