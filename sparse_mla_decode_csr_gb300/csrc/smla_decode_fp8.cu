@@ -180,8 +180,9 @@ struct Misc {
   int32_t part_nv[2];
   uint8_t sfq[2 * kMaxHP][16];                  // q scale-factor bytes of the part being staged
   float fac[kMaxHP];                            // epilogue: output factors of a whole row's heads
-  int32_t fast;                                 // the final part completes its row (merged in the epilogue)
+  int32_t fast;                                 // the final part completes its row (decided at its last tile)
   int32_t fast_s_own;                           //   the stage that takes this part's O
+  int32_t late;                                 // the same, decided in the final part's epilogue
   int32_t fnv[kMaxInKernelParts];               // final-part merge: the other parts' key counts
   // parts staged in shared memory for a combine: part j's O rows of heads
   // [cb_h, cb_h + cb_nh) at byte offset cb_row[j] (rows of 512 f32), its
@@ -695,9 +696,11 @@ __device__ __noinline__ void aux_epilogue(const AuxCtx& x, const Cursor& pc, int
     return;
   }
   if (may_late) {
+    // (a field of its own: the aux warps leave their waits at different times,
+    // and ms->fast is read after them above)
     if (ta == 0) {
-      ms->fast = tk == parts - 1;
-      if (ms->fast) {
+      ms->late = tk == parts - 1;
+      if (ms->late) {
         fence_proxy_async_global();  // (the other parts' partials are read by the async proxy)
         mbar_arrive_expect_tx(bars + kMerge, uint32_t((parts - 1) * rows_bytes));
         const int64_t own = slot_of(x.c_id, pc.P, T, G);
@@ -713,7 +716,7 @@ __device__ __noinline__ void aux_epilogue(const AuxCtx& x, const Cursor& pc, int
       }
     }
     named_barrier(2, 128);
-    if (ms->fast) {  // (the other parts' (m, l) and counts are loaded at the end merge)
+    if (ms->late) {  // (the other parts' (m, l) and counts are loaded at the end merge)
       aux_stage_final<HP>(x, pc, ob, xi, 1, 2);
       return;
     }
@@ -950,6 +953,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
     ms->last_tile = 0;
     ms->mparts[0] = ms->mparts[1] = 0;
     ms->fast = 0;
+    ms->fast_s_own = 0;
+    ms->late = 0;
     for (int j = 0; j < kMaxInKernelParts; ++j) {
       ms->cb_row[j] = 0;
       for (int h = 0; h < kMaxHP; ++h) ms->cb_ml[j][h] = make_float2(0.f, 0.f);
@@ -1109,13 +1114,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
 #pragma unroll
           for (int h = 0; h < 16; ++h) x[h] = 0.f;
 #pragma unroll 1
-          for (int k = 0; k < 2 * C::kQkSplit; ++k) {
-            // accumulator k / 2: q_hi columns (+ rope), then q_lo columns
-            uint32_t r[16];
-            tmem_ld16(tmem + lane_base + C::s_col(sb, k >> 1) + (k & 1) * HP + 16 * pass, r);
+          for (int acc = 0; acc < C::kQkSplit; ++acc) {
+            // accumulator acc: q_hi columns (+ rope) and q_lo columns, one wait
+            uint32_t r0[16], r1[16];
+            tmem_ld16(tmem + lane_base + C::s_col(sb, acc) + 16 * pass, r0);
+            tmem_ld16(tmem + lane_base + C::s_col(sb, acc) + HP + 16 * pass, r1);
             tmem_wait_ld();
 #pragma unroll
-            for (int h = 0; h < 16; ++h) x[h] += __uint_as_float(r[h]);
+            for (int h = 0; h < 16; ++h) x[h] += __uint_as_float(r0[h]) + __uint_as_float(r1[h]);
           }
 #pragma unroll
           for (int h = 0; h < 16; ++h) x[h] = valid ? x[h] * xs : -INFINITY;

@@ -314,6 +314,40 @@ def test_workload_parity(name, kernel):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("name,tk", [("ragged", "fp8"), ("wide", "fp8"), ("ragged", "bf16")])
+def test_repeated_launches_keep_parity_and_clear_tickets(name, tk):
+    """The in-kernel merge of shared rows takes one of several routes (the
+    last-arriving part's merge, or the final part's merge decided at its last
+    tile or in its epilogue), chosen by the order in which the CTAs sharing a
+    row finish.  Many launches, with the L2 flushed between them so that the
+    orders vary, must each match the oracle, report a clean status and leave
+    every row ticket at zero for the next call."""
+    w = W.WORKLOADS[name]
+    kv = build_cache(w, DEV)
+    q = W.queries(w, DEV)
+    indices, indptr = W.index_stream(w, DEV)
+    sink = W.sinks(w, DEV)
+    rows = list(range(w.n_q))
+    rec, sub, ptr_sub, _ = oracle_subproblem(w, indices, indptr, rows, kv)
+    args = (q.double().cpu().numpy(), rec, sub, ptr_sub, None, w.sm_scale,
+            None if sink is None else sink.double().cpu().numpy())
+    ref_out, ref_lse, ref_nv = oracle.sparse_mla_decode(*args, n_kv_rows=len(rec))
+    allow = allowance(*args, n_kv_rows=len(rec))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=DEV)
+    for it in range(24):
+        flush.fill_(it & 0xFF)
+        out, lse, nv, st = run_gpu(q, kv, w.n_kv_rows, indices, indptr, None, w.sm_scale, sink,
+                                   max_row_len=w.max_row_len, has_invalid=w.has_invalid, kernel=tk)
+        assert st == 0, f"launch {it}: status {st}"
+        assert np.array_equal(nv.cpu().numpy(), ref_nv), f"launch {it}: contributing-key counts differ"
+        compare(out, lse, ref_out, ref_lse, f"{name} launch {it}", allow=allow)
+        ws, _ = smla._WS[(torch.device(DEV).type, torch.cuda.current_device())]
+        tickets = ws[:8 * w.n_q].view(torch.int32)
+        assert int(tickets.abs().sum().item()) == 0, f"launch {it}: row tickets left non-zero"
+    del kv, flush
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("heads", [16, 33])
 def test_single_key_rows_return_every_e4m3_code_exactly(heads, kernel):
     needs(kernel, heads)
