@@ -162,9 +162,11 @@ typedef struct smla_decode_params {
  * Tensor-core kernels (bf16: tile_len 64; native fp8: tile_len 128): a
  * persistent, balanced schedule.  Each row r is cut into
  * T_r = max(1, ceil(len_r / tile_len)) tiles of tile_len slice positions
- * and takes 2 + T_r slots of a schedule space (2 slots stand for the cost of
- * starting a row: its epilogue and q staging), rows in order, so row r's
- * tiles are slots [R_r, R_r + T_r) with R_r = 2 + sum_{r' < r} (2 + T_r').  CTA
+ * and takes s + T_r slots of a schedule space (s slots stand for the cost of
+ * starting a row: its epilogue and q staging; s = 2, except s = 1 for the
+ * native-fp8 kernel above 16 heads, whose tiles take longer), rows in order,
+ * so row r's tiles are slots [R_r, R_r + T_r) with
+ * R_r = s + sum_{r' < r} (s + T_r').  CTA
  * c of G = grid takes the slots [b_c, e_c) with b_c = floor(c W / G), W the
  * slot total, and streams through the tiles in its range across row
  * boundaries.  A row lying wholly inside one CTA's range is finished there; a

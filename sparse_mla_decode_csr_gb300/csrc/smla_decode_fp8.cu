@@ -98,7 +98,6 @@ constexpr int kAuxWarp0 = 4;        // aux warps; the first kQkSplit of them iss
 constexpr int kLoadWarp0 = 8;
 constexpr int kLoadWarps = 8;
 constexpr int kKeysPerLoader = kTK / kLoadWarps;  // 16 (keys lw, lw + 8, ...)
-constexpr int kRowStart = 2;                      // schedule slots charged for starting a row
 constexpr float kLazy = 16.f;                     // reference max moves when passed by > 2^16
 constexpr float kInitMax = -1.0e30f;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait (default) and per MMA drain
@@ -124,6 +123,10 @@ struct Cfg {
   // latent K-steps and one rope K-step each; 32 heads: two issuers of 8 and
   // 2); S single-buffered so that the TMEM columns fit
   static constexpr int kQkSplit = HP == 16 ? 4 : 2;
+  // schedule slots charged for starting a row (its q staging and epilogue):
+  // two 128-key tiles at 16 heads, one at 32, measured best on the
+  // workloads of each width (the 32-head tile is ~1.5x longer)
+  static constexpr int kRowStart = HP == 16 ? 2 : 1;
   static constexpr int kSBuf = 1;
   static constexpr int kLatSteps = 16 / kQkSplit;       // latent K-steps of an issuer
   static constexpr int kNQ = HP == 16 ? 2 : 1;          // q buffers
@@ -303,6 +306,7 @@ __device__ __forceinline__ float sum16(const float (&v)[16], int lane) {
   return w + __shfl_xor_sync(0xffffffffu, w, 1);
 }
 
+template <int kRowStart>
 struct Cursor {
   int32_t row, len, ntiles, ta, tb, t;
   int64_t P, beg, e;
@@ -618,7 +622,8 @@ __device__ __noinline__ void combine_global(const DecodeArgs& a, int row, int hb
 // (m, l), no partial of this part is written, and the row is queued for the
 // CTA's end, where all threads combine it.
 template <int HP>
-__device__ __noinline__ void aux_stage_final(const AuxCtx& x, const Cursor& pc, int ob, int xi, int s_own, int kind) {
+__device__ __noinline__ void aux_stage_final(const AuxCtx& x, const Cursor<Cfg<HP>::kRowStart>& pc, int ob, int xi,
+                                             int s_own, int kind) {
   using C = Cfg<HP>;
   Misc* ms = x.ms;
   uint64_t* bars = x.bars;
@@ -662,7 +667,7 @@ __device__ __noinline__ void aux_stage_final(const AuxCtx& x, const Cursor& pc, 
 // CTA's final part of a shared row whose other parts have all finished
 // (their tickets are in, read before the waits) merges the row right here.
 template <int HP>
-__device__ __noinline__ void aux_epilogue(const AuxCtx& x, const Cursor& pc, int pi, bool final_part) {
+__device__ __noinline__ void aux_epilogue(const AuxCtx& x, const Cursor<Cfg<HP>::kRowStart>& pc, int pi, bool final_part) {
   using C = Cfg<HP>;
   const DecodeArgs& a = *x.a;
   Misc* ms = x.ms;
@@ -908,6 +913,7 @@ __device__ __noinline__ void end_merge(const DecodeArgs& a, uint8_t* smem, uint6
 template <int HP>
 __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_constant__ DecodeArgs a) {
   using C = Cfg<HP>;
+  using Cur = Cursor<C::kRowStart>;
   constexpr int kN = C::kN;
   extern __shared__ uint8_t smem_raw[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -955,10 +961,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
     ms->fast = 0;
     ms->fast_s_own = 0;
     ms->late = 0;
-    for (int j = 0; j < kMaxInKernelParts; ++j) {
-      ms->cb_row[j] = 0;
-      for (int h = 0; h < kMaxHP; ++h) ms->cb_ml[j][h] = make_float2(0.f, 0.f);
-    }
 #ifdef SMLA_TRACE
     for (int k = 0; k < 8; ++k) ms->merge_t[k] = 0;
 #endif
@@ -970,6 +972,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
     tmem_alloc(&ms->tmem_base, 512);
     tmem_relinquish();
   }
+  // zeroed staging descriptors (read by the softmax warps' early combine run)
+  static_assert(kMaxInKernelParts * kMaxHP <= kThreads, "one descriptor entry per thread");
+  if (tid < kMaxInKernelParts * kMaxHP) ms->cb_ml[tid / kMaxHP][tid % kMaxHP] = make_float2(0.f, 0.f);
+  if (tid < kMaxInKernelParts) ms->cb_row[tid] = 0;
+  F8_TR(6, 0);
 
   // ---- schedule: slot counts of all rows, their prefix, this CTA's first row
   {
@@ -978,7 +985,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
     const int lo = min(tid * per, n), hi = min(lo + per, n);
     int64_t local = 0;
 #pragma unroll 1
-    for (int r = lo; r < hi; ++r) local += kRowStart + Cursor::tiles_of(row_len(a, r));
+    for (int r = lo; r < hi; ++r) local += C::kRowStart + Cur::tiles_of(row_len(a, r));
     int64_t x = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -987,6 +994,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
     }
     if (lane == 31) ms->scan[warp] = x;
     __syncthreads();
+    F8_TR(7, 0);
     if (warp == 0) {
       const int64_t v = lane < kThreads / 32 ? ms->scan[lane] : 0;
       int64_t t = v;
@@ -999,25 +1007,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
       if (lane == 31) ms->total_tiles = t;
     }
     __syncthreads();
+    F8_TR(8, 0);
     const int64_t Tt = ms->total_tiles;
     const int64_t b = cbeg(c_id, Tt, G), e = cbeg(c_id + 1, Tt, G);
     int64_t P = ms->scan[32 + warp] + x - local;
     int32_t mine = 0;
 #pragma unroll 1
     for (int r = lo; r < hi; ++r) {
-      const int32_t nt_r = Cursor::tiles_of(row_len(a, r));
-      const int64_t w = kRowStart + nt_r;
+      const int32_t nt_r = Cur::tiles_of(row_len(a, r));
+      const int64_t w = C::kRowStart + nt_r;
       if (P <= b && b < P + w) {
         ms->first_row = r;
         ms->first_tile = P;
       }
       // the row of this CTA's last tile: e - 1 is one of its tile slots, or
       // one of the next row's start slots right after them
-      if ((P + kRowStart <= e - 1 && e - 1 < P + w) || (P + w <= e - 1 && e - 1 < P + w + kRowStart && P + w - 1 >= b)) {
+      if ((P + C::kRowStart <= e - 1 && e - 1 < P + w) ||
+          (P + w <= e - 1 && e - 1 < P + w + C::kRowStart && P + w - 1 >= b)) {
         ms->last_row = r;
         ms->last_tile = P;
       }
-      const int64_t t0 = P + kRowStart;
+      const int64_t t0 = P + C::kRowStart;
       const int64_t lo_t = b > t0 ? b : t0, hi_t = e < t0 + nt_r ? e : t0 + nt_r;
       if (hi_t > lo_t) mine += int32_t(hi_t - lo_t);
       if (blockIdx.x == 0 && a.row_tile) a.row_tile[r] = P;
@@ -1027,6 +1037,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
     if (lane == 0 && mine != 0) atomicAdd(&ms->n_tiles, mine);
+    F8_TR(9, 0);
   }
   tc_fence_before();
   __syncthreads();
@@ -1068,7 +1079,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
     // it now without its stores (on zeroed staging descriptors) while the
     // first tiles are in flight, so that its code is in the caches then
     if (n_tiles > 0) combine_staged(a, smem, ms, kMaxInKernelParts, 0, 0, 4, t, 32 * kSoftmaxWarps, true);
-    Cursor c;
+    Cur c;
     c.init(a, row0, P0, cb, ce);
     int pi = 0;  // row part index within this CTA
     for (int i = 0; i < n_tiles; ++i, c.advance(a)) {
@@ -1325,7 +1336,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
     // q of a row -> [q_hi | q_lo] E4M3 (K-major, 128-byte swizzled) with an
     // E8M0 factor per (head, 32 dims) that brings the block's largest |q| to
     // [2^7, 2^8); q_rope (bf16) copied as it is; then the factors into TMEM.
-    Cursor c;
+    Cur c;
     c.init(a, row0, P0, cb, ce);
     if (n_tiles > 0) aux_stage_q<HP>(actx, c.row, 0);
     if (q < 2 && n_tiles > 0) {
@@ -1334,8 +1345,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
       // first tile is still in flight)
       const int32_t r = q == 0 ? row0 : ms->last_row;
       if (r < a.n_q) {
-        const int64_t Pr = (q == 0 ? P0 : ms->last_tile) + kRowStart;
-        const int32_t nt = Cursor::tiles_of(row_len(a, r));
+        const int64_t Pr = (q == 0 ? P0 : ms->last_tile) + C::kRowStart;
+        const int32_t nt = Cur::tiles_of(row_len(a, r));
         const int64_t ca = cof(Pr, T, G), cz = cof(Pr + nt - 1, T, G);
         int32_t n = 0;
         for (int64_t c0 = ca; c0 <= cz; c0 += 32) {
@@ -1355,7 +1366,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
       }
     }
     named_barrier(2, 128);  // (the epilogues read the lists)
-    Cursor prev = c;
+    Cur prev = c;
     int pi = 0;  // part of tile i
     for (int i = 0; i < n_tiles; ++i) {
       const int s = i & 1;
@@ -1391,8 +1402,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
         // QK of the tile: aux warp q issues latent K-steps kLatSteps q ..
         // and its share of the rope K-steps into accumulator q
         const int qb = pi % C::kNQ;
-        const int kbeg = q * C::kLatSteps, kend = kbeg + C::kLatSteps;
-        const int rbeg = q * (4 / C::kQkSplit), rend = rbeg + 4 / C::kQkSplit;
+        const int kbeg = q * C::kLatSteps;
+        const int rbeg = q * (4 / C::kQkSplit);
         const int sb = i % C::kSBuf;
         const uint32_t sph = (i / C::kSBuf) & 1;
         wait_warp(bars + kSEmpty + sb, sph ^ 1, ms, a);
@@ -1402,23 +1413,31 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
           const uint32_t st32 = smem_base + s * kStageBytes;
           const uint32_t qs = smem_base + C::kOffQ + qb * C::kQBytes;
           const uint32_t d = tmem + C::s_col(sb, q);
-          // latent: K-steps of 32 E4M3 (K-chunk kc = 128 dims = scale block kc)
+          // latent: K-steps of 32 E4M3 (K-chunk kc = 128 dims = scale block kc).
+          // The descriptors of this issuer's first K-step, stepped by constant
+          // offsets of their start-address field (shared addresses < 256 KB:
+          // the 14-bit field never carries)
+          const int kc0 = kbeg >> 2;
+          uint64_t ad = smem_desc(st32 + kc0 * kChunk, 16, 1024, kSw128);
+          uint64_t bd = smem_desc(qs + kc0 * C::kQLatChunk, 16, 1024, kSw128);
+          uint32_t sfa = tmem + C::kColSfa + 16 * s + 4 * kc0, sfb = tmem + C::kColSfq + 16 * qb + 4 * kc0;
 #pragma unroll 1
-          for (int ks = kbeg; ks < kend; ++ks) {
-            const int kc = ks >> 2, sub = ks & 3;
-            const uint64_t ad = smem_desc(st32 + kc * kChunk + 32 * sub, 16, 1024, kSw128);
-            const uint64_t bd = smem_desc(qs + kc * C::kQLatChunk + 32 * sub, 16, 1024, kSw128);
-            mma_mxf8_ss(d, ad, bd, idesc_mxf8(128, kN, 0, 0, sub, sub), tmem + C::kColSfa + 16 * s + 4 * kc,
-                        tmem + C::kColSfq + 16 * qb + 4 * kc, ks > kbeg ? 1u : 0u);
+          for (int j = 0; j < C::kLatSteps; ++j) {
+            const int sub = j & 3;
+            mma_mxf8_ss(d, ad, bd, idesc_mxf8(128, kN, 0, 0, sub, sub), sfa, sfb, j > 0 ? 1u : 0u);
+            const bool next_chunk = sub == 3;  // 32 bytes on, or the next 128-dim K-chunk
+            ad += next_chunk ? uint64_t((kChunk - 96) >> 4) : 2u;
+            bd += next_chunk ? uint64_t((C::kQLatChunk - 96) >> 4) : 2u;
+            sfa += next_chunk ? 4u : 0u;
+            sfb += next_chunk ? 4u : 0u;
           }
           {
             // rope: K-steps of 16 bf16 into the q_hi columns
-#pragma unroll 1
-            for (int r = rbeg; r < rend; ++r) {
-              const uint64_t ad = smem_desc(st32 + kOffRope + 32 * r, 16, 1024, kSw128);
-              const uint64_t bd = smem_desc(qs + C::kQOffRope + 32 * r, 16, 1024, kSw128);
-              mma_f16_ss(d, ad, bd, idesc_bf16(128, HP, 0, 0), 1u);
-            }
+            const uint64_t ar0 = smem_desc(st32 + kOffRope + 32 * rbeg, 16, 1024, kSw128);
+            const uint64_t br0 = smem_desc(qs + C::kQOffRope + 32 * rbeg, 16, 1024, kSw128);
+#pragma unroll
+            for (int r = 0; r < 4 / C::kQkSplit; ++r)
+              mma_f16_ss(d, ar0 + uint64_t(2 * r), br0 + uint64_t(2 * r), idesc_bf16(128, HP, 0, 0), 1u);
           }
           mma_commit(bars + kSFull + sb);
           if (c.last()) mma_commit(bars + kQEmpty + qb);
@@ -1492,7 +1511,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
     const int lw = warp - kLoadWarp0;
     const int kc = lane >> 3, c16 = lane & 7;
     // raw entry of key lw + 8 lane (lanes 0-15) of a cursor's tile, or -1
-    auto raw_of = [&](const Cursor& cu) -> int32_t {
+    auto raw_of = [&](const Cur& cu) -> int32_t {
       const int32_t tk = lw + kLoadWarps * lane;
       if (!cu.live || lane >= kKeysPerLoader) return -1;
       const int32_t p = cu.p0() + tk;
@@ -1500,9 +1519,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
       if (p >= cu.p1() || off < 0 || off >= a.n_indices) return -1;
       return __ldg(a.indices + off);
     };
-    Cursor c;
+    Cur c;
     c.init(a, row0, P0, cb, ce);
     int32_t raw = raw_of(c);
+    F8_TR(52, 0);
     bool oob = false;
     for (int i = 0; i < n_tiles; ++i) {
       const int s = i & 1;
@@ -1594,6 +1614,7 @@ static cudaError_t launch_fp8_hp(const DecodeLaunch& L) {
   cudaError_t e = cudaFuncSetAttribute(decode_fp8_kernel<HP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   DecodeArgs args = make_decode_args(L);
+  args.row_start_slots = Cfg<HP>::kRowStart;  // (read by the merge kernel)
   e = launch_trim(L, args);
   if (e != cudaSuccess) return e;
   decode_fp8_kernel<HP><<<L.plan.grid * L.plan.head_groups, kThreads, smem, L.stream>>>(args);

@@ -1263,7 +1263,7 @@ __global__ void __launch_bounds__(32 * (kSplit == 1 ? kMergeWarps : kSplit)) mer
   const int64_t pair = kSplit == 1 ? int64_t(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5) : int64_t(blockIdx.x);
   if (pair >= int64_t(a.n_q) * H) return;
   const int row = int(pair / H), h = int(pair % H);
-  const int64_t P = __ldcg(a.row_tile + row) + kRowStartSlots;  // the row's first tile slot
+  const int64_t P = __ldcg(a.row_tile + row) + a.row_start_slots;  // the row's first tile slot
   const int64_t T = __ldcg(a.row_tile + a.n_q), G = a.grid;
   const int32_t nt = int32_t(__ldcg(a.row_tile + row + 1) - P);
   const int64_t ca = cta_of_tile(P, T, G), cb = cta_of_tile(P + nt - 1, T, G);

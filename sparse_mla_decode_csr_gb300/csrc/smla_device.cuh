@@ -34,6 +34,7 @@ struct DecodeArgs {
   int32_t grid, merge_kernel;  // tensor-core schedule
   int32_t merge_min_parts;     // the merge kernel leaves rows of fewer parts alone
   int32_t head_groups;         // native-fp8 kernel: CTAs per schedule range (heads split)
+  int32_t row_start_slots;     // tensor-core schedule: slots charged for starting a row
   // split workspace
   int32_t* ticket;
   int64_t* row_tile;  // tensor-core schedule: first tile of each row, then T
@@ -41,6 +42,11 @@ struct DecodeArgs {
   float* ml_part;
   int32_t* nv_part;
 };
+
+// Schedule slots charged for starting a row (its epilogue and q staging cost
+// about two tiles of pipeline time): row r occupies kRowStartSlots virtual
+// slots and then its T_r tiles in the slot space the CTAs split evenly.
+constexpr int kRowStartSlots = 2;  // (the bf16 kernel's charge; see DecodeArgs::row_start_slots)
 
 inline DecodeArgs make_decode_args(const DecodeLaunch& L) {
   DecodeArgs a{};
@@ -72,6 +78,7 @@ inline DecodeArgs make_decode_args(const DecodeLaunch& L) {
   // the native-fp8 kernel merges rows of up to kMaxInKernelParts parts itself
   a.merge_min_parts = L.plan.kernel == SMLA_KERNEL_TENSOR_CORE_FP8 ? kMaxInKernelParts + 1 : 2;
   a.head_groups = L.plan.head_groups > 0 ? L.plan.head_groups : 1;
+  a.row_start_slots = kRowStartSlots;  // (the native-fp8 launcher sets its own)
   if (L.ws.total > 0) {
     char* ws = static_cast<char*>(L.workspace);
     a.ticket = reinterpret_cast<int32_t*>(ws + L.ws.ticket_off);
@@ -172,11 +179,6 @@ namespace smla {
 // ---- the tensor-core kernel's balanced schedule (see smla_plan in smla.h) ----
 
 constexpr int kSchedTile = 64;
-// Schedule slots charged for starting a row (its epilogue and q staging cost
-// about two tiles of pipeline time): row r occupies kRowStartSlots virtual
-// slots and then its T_r tiles in the slot space the CTAs split evenly.
-constexpr int kRowStartSlots = 2;
-
 // Slice length of row r: max(indptr[r+1] - indptr[r], 0), capped by lens.
 __device__ __forceinline__ int32_t row_len(const DecodeArgs& a, int32_t r) {
   int64_t len = int64_t(__ldg(a.indptr + r + 1)) - __ldg(a.indptr + r);
