@@ -1159,29 +1159,50 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
         if (first) {
           mr = (tm > kInitMax || tm != tm) ? tm : kInitMax;
         } else if (__any_sync(0xffffffffu, tm > mr + kLazy)) {  // the same in all four warps
+          // heads whose reference moves (lanes hl and hl + 16 hold the same head)
+          const uint32_t moved = __ballot_sync(0xffffffffu, tm > mr + kLazy) & 0xFFFFu;
           const float mn = tm > mr + kLazy ? tm : mr;
-          const float alpha = ex2(mr - mn);
+          const float alpha = ex2(mr - mn);  // exactly 1 for the heads that keep theirs
           mr = mn;
           lsum[pass] *= __shfl_sync(0xffffffffu, alpha, hs);
           // O holds PV of this part's earlier tiles: wait until they completed,
-          // then rescale this pass's heads (hi and lo columns) in this lane quarter
+          // then rescale the moved heads' hi and lo columns in this lane quarter
           if (!pv_waited) {
             wait_warp(bars + kPvDone, (i - 1) & 1, ms, a);
             pv_waited = true;
           }
           tc_fence_after();
-          float al[16];
+          const uint32_t ob_col = tmem + lane_base + C::o_col(ob, 0) + uint32_t(32 * pass);
+          if (__popc(moved) > 4) {  // many heads: 16 columns at a time
+            float al[16];
 #pragma unroll
-          for (int h = 0; h < 16; ++h) al[h] = __shfl_sync(0xffffffffu, alpha, h);
+            for (int h = 0; h < 16; ++h) al[h] = __shfl_sync(0xffffffffu, alpha, h);
 #pragma unroll 1
-          for (int k = 0; k < 8; ++k) {  // 4 blocks x (hi, lo)
-            const uint32_t ta = tmem + lane_base + C::o_col(ob, k >> 1) + uint32_t(32 * pass + 16 * (k & 1));
-            uint32_t v[16];
-            tmem_ld16(ta, v);
-            tmem_wait_ld();
+            for (int k = 0; k < 8; ++k) {  // 4 blocks x (hi, lo)
+              const uint32_t ta = ob_col + uint32_t(k >> 1) * kN + uint32_t(16 * (k & 1));
+              uint32_t v[16];
+              tmem_ld16(ta, v);
+              tmem_wait_ld();
 #pragma unroll
-            for (int h = 0; h < 16; ++h) v[h] = __float_as_uint(__uint_as_float(v[h]) * al[h]);
-            tmem_st16(ta, v);
+              for (int h = 0; h < 16; ++h) v[h] = __float_as_uint(__uint_as_float(v[h]) * al[h]);
+              tmem_st16(ta, v);
+            }
+          } else {  // a few heads (the usual case once a row's maxima settle): their 8 columns each
+            uint32_t mv = moved;
+#pragma unroll 1
+            while (mv != 0u) {
+              const int h = __ffs(mv) - 1;
+              mv &= mv - 1u;
+              const float al_h = __shfl_sync(0xffffffffu, alpha, h);
+              uint32_t v[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) tmem_ld1(ob_col + uint32_t(k >> 1) * kN + uint32_t(16 * (k & 1) + h), v[k]);
+              tmem_wait_ld();
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                tmem_st1(ob_col + uint32_t(k >> 1) * kN + uint32_t(16 * (k & 1) + h),
+                         __float_as_uint(__uint_as_float(v[k]) * al_h));
+            }
           }
           tmem_wait_st();
         }
