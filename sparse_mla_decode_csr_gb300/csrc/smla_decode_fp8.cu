@@ -127,6 +127,11 @@ struct Cfg {
   // two 128-key tiles at 16 heads, one at 32, measured best on the
   // workloads of each width (the 32-head tile is ~1.5x longer)
   static constexpr int kRowStart = HP == 16 ? 2 : 1;
+  // 32 heads: the aux warps take the softmax of heads 16..31 (the second
+  // 16-head pass) of every tile, the softmax warps heads 0..15
+  static constexpr bool kSplitPass = HP == 32;
+  static constexpr int kPassA = kSplitPass ? 1 : kPass;           // passes of the softmax warps
+  static constexpr int kSReaders = kSplitPass ? 8 : 4;            // warps reading a tile's S
   static constexpr int kSBuf = 1;
   static constexpr int kLatSteps = 16 / kQkSplit;       // latent K-steps of an issuer
   static constexpr int kNQ = HP == 16 ? 2 : 1;          // q buffers
@@ -175,7 +180,7 @@ struct Misc {
   int64_t total_tiles;
   int64_t scan[64];
   alignas(16) int32_t red_max_t[2][kMaxHP][4];  // tile maxima per head and lane quarter (order-preserving ints; read as one 16-byte word)
-  int32_t red_sc[2][4][4];          // largest biased exponent of each block's scale per lane quarter
+  int32_t red_sc[2][2][4][4];       // [group][buffer][lane quarter][block]: largest biased scale exponent
   float red_l[4][kMaxHP];
   int32_t red_nv[4];
   float part_m[2][kMaxHP];                      // per O buffer: a finished row part's (m, l, count)
@@ -231,7 +236,8 @@ enum Bar {
   kEpiReady = 20, // [2] softmax -> aux (a part's m, l, count posted)
   kDrain = 22,    // MMA issuers: every MMA they issued has completed
   kStall = 23,    // never signalled (timeout-path test)
-  kMerge = 24     // the end merge's bulk copies
+  kMerge = 24,    // the end merge's bulk copies
+  kPReady = 25    // [2] 32 heads: aux warps -> PV issuers (heads 16..31 of a tile's P' written)
 };
 
 __device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t chunk16) {
@@ -910,6 +916,244 @@ __device__ __noinline__ void end_merge(const DecodeArgs& a, uint8_t* smem, uint6
   }
 }
 
+// Shared-memory offset of the P' block (32-key chunk ch, dim block b) of the
+// tile in stage s: the first kPInRope blocks sit in the stage's rope rows,
+// the rest (32 heads) in the extra buffer both stages share.
+template <int HP>
+__device__ __forceinline__ uint32_t p_block_off(int s, int ch, int b) {
+  using C = Cfg<HP>;
+  const int k = 4 * ch + b;
+  return k < C::kPInRope ? uint32_t(s * kStageBytes + kOffRope + k * C::kPBlock)
+                         : uint32_t(C::kOffPx + (k - C::kPInRope) * C::kPBlock);
+}
+
+// This thread's key of the tile in stage st: whether it is valid, its four
+// block scales, and (into grp's buffer rb) the largest biased exponent of
+// each block's scale over the warp's valid keys.
+__device__ __forceinline__ bool tile_key(const uint8_t* st, int t, int lane, int q, int grp, int rb, Misc* ms,
+                                         uint32_t (&sw)[4]) {
+  const int32_t id = *reinterpret_cast<const int32_t*>(st + kOffIds + 4 * t);
+  const bool valid = id >= 0;
+  const uint4 scw = *reinterpret_cast<const uint4*>(st + kOffSc + 16 * t);
+  sw[0] = scw.x;
+  sw[1] = scw.y;
+  sw[2] = scw.z;
+  sw[3] = scw.w;
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const int32_t e = __reduce_max_sync(0xffffffffu, valid ? int32_t((sw[b] >> 23) & 0xFF) : 0);
+    if (lane == b) ms->red_sc[grp][rb][q][b] = e;
+  }
+  return valid;
+}
+
+// What one softmax pass of a tile needs (per thread; in registers).
+struct PassCtx {
+  const DecodeArgs* a;
+  uint8_t* smem;
+  Misc* ms;
+  uint64_t* bars;
+  uint32_t tmem, lane_base;
+  int q, lane, i, s, sb, rb, ob;
+  bool first, valid, p_shared;
+  uint32_t sw[4];             // the key's four block scales (f32 bits)
+  int grp;                    // 0: softmax warps, 1: aux warps (own scale-exponent buffer)
+  uint32_t bar_id;            // the group's named barrier (its four warps)
+  int first_pass, last_pass;  // the group's passes
+#ifdef SMLA_TRACE
+  unsigned long long* tr_buf;
+  int* tr_k;
+#endif
+};
+
+// One 16-head pass (heads 16 pass .. 16 pass + 15) of a tile's softmax for this
+// thread's key row: scores from S, the heads' tile maxima across the group's
+// four lane quarters, the lazy reference update (rescaling O in TMEM), p and
+// its sum, and the P' blocks and their scale factors for the PV.  Run by the
+// softmax warps (every pass at 16 heads, pass 0 at 32) and at 32 heads by the
+// aux warps (pass 1).
+template <int HP>
+__device__ __forceinline__ void softmax_pass(const PassCtx& z, const int pass, float& mref, float& lsum,
+                                             bool& pv_waited, int (&es)[4]) {
+  using C = Cfg<HP>;
+  constexpr int kN = C::kN;
+  const DecodeArgs& a = *z.a;
+  uint8_t* const smem = z.smem;
+  Misc* const ms = z.ms;
+  uint64_t* const bars = z.bars;
+  const uint32_t tmem = z.tmem, lane_base = z.lane_base;
+  const int q = z.q, lane = z.lane, i = z.i, s = z.s, sb = z.sb, rb = z.rb, ob = z.ob;
+  const bool first = z.first, valid = z.valid, p_shared = z.p_shared;
+  const int hl = lane & 15;         // per-head values: lane hl (and hl + 16) holds head 16 pass + hl
+  const int hs = (lane >> 1) & 15;  // head (of the pass) of this lane's sum of p (see sum16)
+  const uint32_t sw[4] = {z.sw[0], z.sw[1], z.sw[2], z.sw[3]};
+#ifdef SMLA_TRACE
+  unsigned long long* const tr_buf = z.tr_buf;
+  int& tr_k = *z.tr_k;
+#endif
+  // scores x = (S_hi + S_lo) sm_scale log2(e) of heads 16 pass .. + 15, -inf when masked
+  float x[16];
+  {
+    const float xs = a.sm_scale_log2;
+#pragma unroll
+    for (int h = 0; h < 16; ++h) x[h] = 0.f;
+#pragma unroll 1
+    for (int acc = 0; acc < C::kQkSplit; ++acc) {
+      // accumulator acc: q_hi columns (+ rope) and q_lo columns, one wait
+      uint32_t r0[16], r1[16];
+      tmem_ld16(tmem + lane_base + C::s_col(sb, acc) + 16 * pass, r0);
+      tmem_ld16(tmem + lane_base + C::s_col(sb, acc) + HP + 16 * pass, r1);
+      tmem_wait_ld();
+#pragma unroll
+      for (int h = 0; h < 16; ++h) x[h] += __uint_as_float(r0[h]) + __uint_as_float(r1[h]);
+    }
+#pragma unroll
+    for (int h = 0; h < 16; ++h) x[h] = valid ? x[h] * xs : -INFINITY;
+  }
+  if (pass == z.last_pass) {  // the group's last S columns of the tile
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars + kSEmpty + sb);  // S read
+  }
+#pragma unroll
+  for (int h = 0; h < 16; ++h) {
+    const int32_t m = __reduce_max_sync(0xffffffffu, ord(x[h]));
+    if (lane == h) ms->red_max_t[rb][16 * pass + h][q] = m;
+  }
+  named_barrier(z.bar_id, 128);
+  if (pass == z.first_pass) F8_TR(11, i);
+  // the tile's maximum of head 16 pass + hl over the four lane quarters
+  float tm;
+  {
+    const uint4 m4 = ld_shared_v4(smem_u32(&ms->red_max_t[rb][16 * pass + hl][0]));
+    tm = unord(max(max(int32_t(m4.x), int32_t(m4.y)), max(int32_t(m4.z), int32_t(m4.w))));
+  }
+  float mr = mref;
+  if (first) {
+    mr = (tm > kInitMax || tm != tm) ? tm : kInitMax;
+  } else if (__any_sync(0xffffffffu, tm > mr + kLazy)) {  // the same in all four warps
+    // heads whose reference moves (lanes hl and hl + 16 hold the same head)
+    const uint32_t moved = __ballot_sync(0xffffffffu, tm > mr + kLazy) & 0xFFFFu;
+    const float mn = tm > mr + kLazy ? tm : mr;
+    const float alpha = ex2(mr - mn);  // exactly 1 for the heads that keep theirs
+    mr = mn;
+    lsum *= __shfl_sync(0xffffffffu, alpha, hs);
+    // O holds PV of this part's earlier tiles: wait until they completed,
+    // then rescale the moved heads' hi and lo columns in this lane quarter
+    if (!pv_waited) {
+      wait_warp(bars + kPvDone, (i - 1) & 1, ms, a);
+      pv_waited = true;
+    }
+    tc_fence_after();
+    const uint32_t ob_col = tmem + lane_base + C::o_col(ob, 0) + uint32_t(32 * pass);
+    if (__popc(moved) > 4) {  // many heads: 16 columns at a time
+      float al[16];
+#pragma unroll
+      for (int h = 0; h < 16; ++h) al[h] = __shfl_sync(0xffffffffu, alpha, h);
+#pragma unroll 1
+      for (int k = 0; k < 8; ++k) {  // 4 blocks x (hi, lo)
+        const uint32_t ta = ob_col + uint32_t(k >> 1) * kN + uint32_t(16 * (k & 1));
+        uint32_t v[16];
+        tmem_ld16(ta, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int h = 0; h < 16; ++h) v[h] = __float_as_uint(__uint_as_float(v[h]) * al[h]);
+        tmem_st16(ta, v);
+      }
+    } else {  // a few heads (the usual case once a row's maxima settle): their 8 columns each
+      uint32_t mv = moved;
+#pragma unroll 1
+      while (mv != 0u) {
+        const int h = __ffs(mv) - 1;
+        mv &= mv - 1u;
+        const float al_h = __shfl_sync(0xffffffffu, alpha, h);
+        uint32_t v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) tmem_ld1(ob_col + uint32_t(k >> 1) * kN + uint32_t(16 * (k & 1) + h), v[k]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          tmem_st1(ob_col + uint32_t(k >> 1) * kN + uint32_t(16 * (k & 1) + h),
+                   __float_as_uint(__uint_as_float(v[k]) * al_h));
+      }
+    }
+    tmem_wait_st();
+  }
+  mref = mr;
+  if (pass == z.first_pass) {
+    // the shared extra P' buffer was last read by PV(i - 1)
+    if (p_shared && i > 0 && !pv_waited) {
+      wait_warp(bars + kPvDone, (i - 1) & 1, ms, a);
+      pv_waited = true;
+    }
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int32_t e = max(max(ms->red_sc[z.grp][rb][0][b], ms->red_sc[z.grp][rb][1][b]),
+                            max(ms->red_sc[z.grp][rb][2][b], ms->red_sc[z.grp][rb][3][b]));
+      es[b] = max(e, 1) - 126;
+    }
+  }
+  // p = 2^(x - mref).  P'_b = p * scale_b in units of the E8M0 factor
+  // 2^E(h, b), E = e_h - 7 + (the tile's largest block-b scale exponent),
+  // where pmax_h = 2^(tmax_h - mref_h) < 2^e_h: P'_b < 2^7.  It is formed
+  // as p'' = p 2^(7 - e_h) split once into E4M3 hi + lo codes, then, per
+  // block, the codes' exponent fields lowered by the key's distance m_b
+  // to the tile's largest block-b scale (exact for the writer's power-of-
+  // two scales; a value leaving E4M3's normal range becomes 0).  e_h is
+  // kept in [-20, kLazy + 1] (a head whose tile terms all lie 2^20 below
+  // its reference keeps 2^-10 relative precision on them).
+  if (pass == z.first_pass) F8_TR(13, i);
+  const int e_h = max(min(int((__float_as_uint(ex2(tm - mr)) >> 23) & 0xFF) - 126, int(kLazy) + 1), -20);
+  const float inv_h = pow2f(7 - e_h);
+#pragma unroll
+  for (int h = 0; h < 16; ++h) x[h] = ex2(x[h] - __shfl_sync(0xffffffffu, mr, h));  // x = -inf (masked) gives 0
+  lsum += sum16(x, lane);
+  if (pass == z.first_pass) F8_TR(14, i);
+  uint32_t hw0[4], lw0[4];  // codes of heads 4k .. 4k + 3
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint16_t h0_, l0_, h1_, l1_;
+    const __half2 y0 = __floats2half2_rn(x[4 * k] * __shfl_sync(0xffffffffu, inv_h, 4 * k),
+                                         x[4 * k + 1] * __shfl_sync(0xffffffffu, inv_h, 4 * k + 1));
+    const __half2 y1 = __floats2half2_rn(x[4 * k + 2] * __shfl_sync(0xffffffffu, inv_h, 4 * k + 2),
+                                         x[4 * k + 3] * __shfl_sync(0xffffffffu, inv_h, 4 * k + 3));
+    split_h2(*reinterpret_cast<const uint32_t*>(&y0), h0_, l0_);
+    split_h2(*reinterpret_cast<const uint32_t*>(&y1), h1_, l1_);
+    hw0[k] = uint32_t(h0_) | (uint32_t(h1_) << 16);
+    lw0[k] = uint32_t(l0_) | (uint32_t(l1_) << 16);
+  }
+  if (pass == z.first_pass) F8_TR(15, i);
+#pragma unroll 1
+  for (int b = 0; b < 4; ++b) {
+    // (selects, not indexing: a rolled loop would put sw and es in local memory)
+    const uint32_t swb = b == 0 ? sw[0] : b == 1 ? sw[1] : b == 2 ? sw[2] : sw[3];
+    const int esb = b == 0 ? es[0] : b == 1 ? es[1] : b == 2 ? es[2] : es[3];
+    const int bexp = int((swb >> 23) & 0xFF);  // a zero (or f32-subnormal) scale gives 0
+    const int m = bexp == 0 ? 16 : min(max(esb + 126 - bexp, 0), 16);
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      hw[k] = lower_codes(hw0[k], m);
+      lw[k] = lower_codes(lw0[k], m);
+    }
+    // MN-major P' row of this key: [hi g0 | lo g0 | hi g1 | lo g1], 16 bytes each
+    uint8_t* blk = smem + p_block_off<HP>(s, q, b);
+    uint32_t off0 = uint32_t(lane) * kN + uint32_t(32 * pass), off1 = off0 + 16;
+    off0 ^= ((off0 >> 7) & C::kPSwMask) << 4;
+    off1 ^= ((off1 >> 7) & C::kPSwMask) << 4;
+    *reinterpret_cast<uint4*>(blk + off0) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4*>(blk + off1) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  }
+  // P' scale factors of this tile's stage: row group g of B holds head
+  // group g (hi rows then lo rows), byte b the factor of dim block b;
+  // the same in every TMEM lane quarter (each warp writes its own)
+  if (pass == z.first_pass) F8_TR(16, i);
+  uint32_t word = 0;
+#pragma unroll
+  for (int b = 0; b < 4; ++b) word |= uint32_t(min(max(e_h + es[b] - 8 + 127, 1), 254)) << (8 * b);
+  tmem_st1(tmem + lane_base + C::sfp_col(s) + uint32_t(pass), word);
+}
+
 template <int HP>
 __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_constant__ DecodeArgs a) {
   using C = Cfg<HP>;
@@ -939,11 +1183,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
       mbar_init(bars + kKvFull + s, kLoadWarps);
       mbar_init(bars + kKvEmpty + s, kSoftmaxWarps);  // the four PV issuers
       mbar_init(bars + kSFull + s, Cfg<HP>::kQkSplit);  // [S buffer] (one or two used)
-      mbar_init(bars + kSEmpty + s, kSoftmaxWarps);
+      mbar_init(bars + kSEmpty + s, Cfg<HP>::kSReaders);
       mbar_init(bars + kQEmpty + s, Cfg<HP>::kQkSplit);
       mbar_init(bars + kOFull + s, kSoftmaxWarps);
       mbar_init(bars + kOEmpty + s, 4);
-      mbar_init(bars + kEpiReady + s, kSoftmaxWarps);
+      mbar_init(bars + kEpiReady + s, Cfg<HP>::kSReaders);
+      mbar_init(bars + kPReady + s, kSoftmaxWarps);
     }
     mbar_init(bars + kPvDone, kSoftmaxWarps);
     mbar_init(bars + kDrain, Cfg<HP>::kQkSplit + kSoftmaxWarps);
@@ -1050,23 +1295,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
   const uint32_t tmem = ms->tmem_base;
   const uint32_t smem_base = smem_u32(smem);
   F8_TR(2, 0);
-  // P' block (32-key chunk ch, dim block b) of the tile in stage s
-  auto p_block = [&](int s, int ch, int b) -> uint32_t {
-    const int k = 4 * ch + b;
-    return k < C::kPInRope ? uint32_t(s * kStageBytes + kOffRope + k * C::kPBlock)
-                           : uint32_t(C::kOffPx + (k - C::kPInRope) * C::kPBlock);
-  };
 
   if (warp < kSoftmaxWarps) {
     // =================== softmax ===================
     const int q = warp;              // TMEM lane quarter: keys 32 q .. 32 q + 31 of a tile
     const int t = 32 * q + lane;     // this thread's key row of the tile
-    const int hl = lane & 15;        // per-head values: lane hl (and hl + 16) holds head 16 pass + hl
     const uint32_t lane_base = uint32_t(32 * q) << 16;
     // the P' blocks of this warp's keys live in the shared extra buffer (32 heads, chunks 2, 3)
     const bool p_shared = 4 * q >= C::kPInRope;
     const int hs = (lane >> 1) & 15;  // head (of a pass) of this lane's sum of p (see sum16)
-    float mref[C::kPass];  // reference max of head 16 pass + hl
+    float mref[C::kPass];  // reference max of head 16 pass + (lane & 15)
     float lsum[C::kPass];  // sum of p of head 16 pass + hs over this warp's keys of the part
     int nv = 0;
 #pragma unroll
@@ -1101,190 +1339,43 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
       wait_warp(bars + kKvFull + s, ph, ms, a);  // (already complete) orders the loaders' ids and scales
       F8_TR(10, i);
       tc_fence_after();
-      const int32_t id = *reinterpret_cast<const int32_t*>(st + kOffIds + 4 * t);
-      const bool valid = id >= 0;
-      nv += valid;
-      uint32_t sw[4];
-      {
-        const uint4 scw = *reinterpret_cast<const uint4*>(st + kOffSc + 16 * t);
-        sw[0] = scw.x; sw[1] = scw.y; sw[2] = scw.z; sw[3] = scw.w;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          const int32_t e = __reduce_max_sync(0xffffffffu, valid ? int32_t((sw[b] >> 23) & 0xFF) : 0);
-          if (lane == b) ms->red_sc[rb][q][b] = e;
-        }
-      }
+      PassCtx z;
+      z.valid = tile_key(st, t, lane, q, 0, rb, ms, z.sw);
+      nv += z.valid;
+      z.a = &a;
+      z.smem = smem;
+      z.ms = ms;
+      z.bars = bars;
+      z.tmem = tmem;
+      z.lane_base = lane_base;
+      z.q = q;
+      z.lane = lane;
+      z.i = i;
+      z.s = s;
+      z.sb = sb;
+      z.rb = rb;
+      z.ob = ob;
+      z.first = first;
+      z.p_shared = p_shared;
+      z.grp = 0;
+      z.bar_id = 1;
+      z.first_pass = 0;
+      z.last_pass = C::kPassA - 1;
+#ifdef SMLA_TRACE
+      z.tr_buf = tr_buf;
+      z.tr_k = &tr_k;
+#endif
       bool pv_waited = false;
       int es[4];  // the tile's block-b scales < 2^es_b
 #pragma unroll
-      for (int pass = 0; pass < C::kPass; ++pass) {
-        // scores x = (S_hi + S_lo) sm_scale log2(e) of heads 16 pass .. + 15, -inf when masked
-        float x[16];
-        {
-          const float xs = a.sm_scale_log2;
-#pragma unroll
-          for (int h = 0; h < 16; ++h) x[h] = 0.f;
-#pragma unroll 1
-          for (int acc = 0; acc < C::kQkSplit; ++acc) {
-            // accumulator acc: q_hi columns (+ rope) and q_lo columns, one wait
-            uint32_t r0[16], r1[16];
-            tmem_ld16(tmem + lane_base + C::s_col(sb, acc) + 16 * pass, r0);
-            tmem_ld16(tmem + lane_base + C::s_col(sb, acc) + HP + 16 * pass, r1);
-            tmem_wait_ld();
-#pragma unroll
-            for (int h = 0; h < 16; ++h) x[h] += __uint_as_float(r0[h]) + __uint_as_float(r1[h]);
-          }
-#pragma unroll
-          for (int h = 0; h < 16; ++h) x[h] = valid ? x[h] * xs : -INFINITY;
-        }
-        if (pass == C::kPass - 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bars + kSEmpty + sb);  // S read
-        }
-#pragma unroll
-        for (int h = 0; h < 16; ++h) {
-          const int32_t m = __reduce_max_sync(0xffffffffu, ord(x[h]));
-          if (lane == h) ms->red_max_t[rb][16 * pass + h][q] = m;
-        }
-        named_barrier(1, 32 * kSoftmaxWarps);
-        if (pass == 0) F8_TR(11, i);
-        // the tile's maximum of head 16 pass + hl over the four lane quarters
-        float tm;
-        {
-          const uint4 m4 = ld_shared_v4(smem_u32(&ms->red_max_t[rb][16 * pass + hl][0]));
-          tm = unord(max(max(int32_t(m4.x), int32_t(m4.y)), max(int32_t(m4.z), int32_t(m4.w))));
-        }
-        float mr = mref[pass];
-        if (first) {
-          mr = (tm > kInitMax || tm != tm) ? tm : kInitMax;
-        } else if (__any_sync(0xffffffffu, tm > mr + kLazy)) {  // the same in all four warps
-          // heads whose reference moves (lanes hl and hl + 16 hold the same head)
-          const uint32_t moved = __ballot_sync(0xffffffffu, tm > mr + kLazy) & 0xFFFFu;
-          const float mn = tm > mr + kLazy ? tm : mr;
-          const float alpha = ex2(mr - mn);  // exactly 1 for the heads that keep theirs
-          mr = mn;
-          lsum[pass] *= __shfl_sync(0xffffffffu, alpha, hs);
-          // O holds PV of this part's earlier tiles: wait until they completed,
-          // then rescale the moved heads' hi and lo columns in this lane quarter
-          if (!pv_waited) {
-            wait_warp(bars + kPvDone, (i - 1) & 1, ms, a);
-            pv_waited = true;
-          }
-          tc_fence_after();
-          const uint32_t ob_col = tmem + lane_base + C::o_col(ob, 0) + uint32_t(32 * pass);
-          if (__popc(moved) > 4) {  // many heads: 16 columns at a time
-            float al[16];
-#pragma unroll
-            for (int h = 0; h < 16; ++h) al[h] = __shfl_sync(0xffffffffu, alpha, h);
-#pragma unroll 1
-            for (int k = 0; k < 8; ++k) {  // 4 blocks x (hi, lo)
-              const uint32_t ta = ob_col + uint32_t(k >> 1) * kN + uint32_t(16 * (k & 1));
-              uint32_t v[16];
-              tmem_ld16(ta, v);
-              tmem_wait_ld();
-#pragma unroll
-              for (int h = 0; h < 16; ++h) v[h] = __float_as_uint(__uint_as_float(v[h]) * al[h]);
-              tmem_st16(ta, v);
-            }
-          } else {  // a few heads (the usual case once a row's maxima settle): their 8 columns each
-            uint32_t mv = moved;
-#pragma unroll 1
-            while (mv != 0u) {
-              const int h = __ffs(mv) - 1;
-              mv &= mv - 1u;
-              const float al_h = __shfl_sync(0xffffffffu, alpha, h);
-              uint32_t v[8];
-#pragma unroll
-              for (int k = 0; k < 8; ++k) tmem_ld1(ob_col + uint32_t(k >> 1) * kN + uint32_t(16 * (k & 1) + h), v[k]);
-              tmem_wait_ld();
-#pragma unroll
-              for (int k = 0; k < 8; ++k)
-                tmem_st1(ob_col + uint32_t(k >> 1) * kN + uint32_t(16 * (k & 1) + h),
-                         __float_as_uint(__uint_as_float(v[k]) * al_h));
-            }
-          }
-          tmem_wait_st();
-        }
-        mref[pass] = mr;
-        if (pass == 0) {
-          // the shared extra P' buffer was last read by PV(i - 1)
-          if (p_shared && i > 0 && !pv_waited) {
-            wait_warp(bars + kPvDone, (i - 1) & 1, ms, a);
-            pv_waited = true;
-          }
-#pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            const int32_t e = max(max(ms->red_sc[rb][0][b], ms->red_sc[rb][1][b]),
-                                  max(ms->red_sc[rb][2][b], ms->red_sc[rb][3][b]));
-            es[b] = max(e, 1) - 126;
-          }
-        }
-        // p = 2^(x - mref).  P'_b = p * scale_b in units of the E8M0 factor
-        // 2^E(h, b), E = e_h - 7 + (the tile's largest block-b scale exponent),
-        // where pmax_h = 2^(tmax_h - mref_h) < 2^e_h: P'_b < 2^7.  It is formed
-        // as p'' = p 2^(7 - e_h) split once into E4M3 hi + lo codes, then, per
-        // block, the codes' exponent fields lowered by the key's distance m_b
-        // to the tile's largest block-b scale (exact for the writer's power-of-
-        // two scales; a value leaving E4M3's normal range becomes 0).  e_h is
-        // kept in [-20, kLazy + 1] (a head whose tile terms all lie 2^20 below
-        // its reference keeps 2^-10 relative precision on them).
-        if (pass == 0) F8_TR(13, i);
-        const int e_h = max(min(int((__float_as_uint(ex2(tm - mr)) >> 23) & 0xFF) - 126, int(kLazy) + 1), -20);
-        const float inv_h = pow2f(7 - e_h);
-#pragma unroll
-        for (int h = 0; h < 16; ++h) x[h] = ex2(x[h] - __shfl_sync(0xffffffffu, mr, h));  // x = -inf (masked) gives 0
-        lsum[pass] += sum16(x, lane);
-        if (pass == 0) F8_TR(14, i);
-        uint32_t hw0[4], lw0[4];  // codes of heads 4k .. 4k + 3
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          uint16_t h0_, l0_, h1_, l1_;
-          const __half2 y0 = __floats2half2_rn(x[4 * k] * __shfl_sync(0xffffffffu, inv_h, 4 * k),
-                                               x[4 * k + 1] * __shfl_sync(0xffffffffu, inv_h, 4 * k + 1));
-          const __half2 y1 = __floats2half2_rn(x[4 * k + 2] * __shfl_sync(0xffffffffu, inv_h, 4 * k + 2),
-                                               x[4 * k + 3] * __shfl_sync(0xffffffffu, inv_h, 4 * k + 3));
-          split_h2(*reinterpret_cast<const uint32_t*>(&y0), h0_, l0_);
-          split_h2(*reinterpret_cast<const uint32_t*>(&y1), h1_, l1_);
-          hw0[k] = uint32_t(h0_) | (uint32_t(h1_) << 16);
-          lw0[k] = uint32_t(l0_) | (uint32_t(l1_) << 16);
-        }
-        if (pass == 0) F8_TR(15, i);
-#pragma unroll 1
-        for (int b = 0; b < 4; ++b) {
-          // (selects, not indexing: a rolled loop would put sw and es in local memory)
-          const uint32_t swb = b == 0 ? sw[0] : b == 1 ? sw[1] : b == 2 ? sw[2] : sw[3];
-          const int esb = b == 0 ? es[0] : b == 1 ? es[1] : b == 2 ? es[2] : es[3];
-          const int bexp = int((swb >> 23) & 0xFF);  // a zero (or f32-subnormal) scale gives 0
-          const int m = bexp == 0 ? 16 : min(max(esb + 126 - bexp, 0), 16);
-          uint32_t hw[4], lw[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            hw[k] = lower_codes(hw0[k], m);
-            lw[k] = lower_codes(lw0[k], m);
-          }
-          // MN-major P' row of this key: [hi g0 | lo g0 | hi g1 | lo g1], 16 bytes each
-          uint8_t* blk = smem + p_block(s, q, b);
-          uint32_t off0 = uint32_t(lane) * kN + uint32_t(32 * pass), off1 = off0 + 16;
-          off0 ^= ((off0 >> 7) & C::kPSwMask) << 4;
-          off1 ^= ((off1 >> 7) & C::kPSwMask) << 4;
-          *reinterpret_cast<uint4*>(blk + off0) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-          *reinterpret_cast<uint4*>(blk + off1) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-        }
-        // P' scale factors of this tile's stage: row group g of B holds head
-        // group g (hi rows then lo rows), byte b the factor of dim block b;
-        // the same in every TMEM lane quarter (each warp writes its own)
-        if (pass == 0) F8_TR(16, i);
-        uint32_t word = 0;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) word |= uint32_t(min(max(e_h + es[b] - 8 + 127, 1), 254)) << (8 * b);
-        tmem_st1(tmem + lane_base + C::sfp_col(s) + uint32_t(pass), word);
-      }
+      for (int pass = 0; pass < C::kPassA; ++pass) softmax_pass<HP>(z, pass, mref[pass], lsum[pass], pv_waited, es);
       tmem_wait_st();
       F8_TR(17, i);
       fence_proxy_async_smem();
       tc_fence_before();
       named_barrier(1, 32 * kSoftmaxWarps);  // the tile's P' and its scale factors are written
+      // (32 heads: and the aux warps' heads 16..31)
+      if constexpr (C::kSplitPass) wait_warp(bars + kPReady + s, ph, ms, a);
       F8_TR(12, i);
       {
         // PV of the tile: warp q issues dim block b = q (four MMA chains in
@@ -1299,7 +1390,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
           for (int ch = 0; ch < 4; ++ch) {
             // V^T: dims of block b (M, contiguous) x keys 32 ch .. (K, rows)
             const uint64_t ad = smem_desc(st32 + b * kChunk + ch * 4096, 16384, 1024, kSw128);
-            const uint64_t bd = smem_desc(smem_base + p_block(s, ch, b), 8 * kN, 8 * kN, C::kPSw);
+            const uint64_t bd = smem_desc(smem_base + p_block_off<HP>(s, ch, b), 8 * kN, 8 * kN, C::kPSw);
             mma_mxf8_ss(tmem + C::o_col(ob, b), ad, bd, idesc_mxf8(128, kN, 1, 1, 0, b), tmem + C::kColSfv,
                         tmem + C::sfp_col(s), (first && ch == 0) ? 0u : 1u);
           }
@@ -1313,7 +1404,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
       if (last) {
         // the part's l and count over its keys, for the aux warps' epilogue
 #pragma unroll
-        for (int pass = 0; pass < C::kPass; ++pass)
+        for (int pass = 0; pass < C::kPassA; ++pass)
           if ((lane & 1) == 0) ms->red_l[q][16 * pass + hs] = lsum[pass];
         const int32_t nvw = __reduce_add_sync(0xffffffffu, nv);
         if (lane == 0) ms->red_nv[q] = nvw;
@@ -1322,7 +1413,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
         named_barrier(1, 32 * kSoftmaxWarps);
         if (q == 0) {
 #pragma unroll
-          for (int pass = 0; pass < C::kPass; ++pass) {
+          for (int pass = 0; pass < C::kPassA; ++pass) {
             if (lane < 16) {
               const int h = 16 * pass + lane;
               ms->part_m[ob][h] = mref[pass];
@@ -1346,6 +1437,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
     const int ta = 32 * q + lane;    // 0..127
     const uint32_t lane_base = uint32_t(32 * q) << 16;
     const AuxCtx actx{&a, smem, ms, bars, tmem, lane_base, H, h0, Hl, hg, g, lane, ta, c_id, G, T};
+    float mref_b = kInitMax;  // 32 heads: reference max of head 16 + (lane & 15)
+    float lsum_b = 0.f;       //   and the sum of p of head 16 + ((lane >> 1) & 15) over the part's keys
+    (void)mref_b;
+    (void)lsum_b;
     // V^T scale factors: 1 (E8M0 127) for every dim row and key block
     {
       uint32_t v[16];
@@ -1509,6 +1604,63 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
       if (i > 0 && c.first()) {
         aux_epilogue<HP>(actx, prev, pi - 1, false);
         F8_TR(42, i);
+      }
+      if constexpr (C::kSplitPass) {
+        // (2b) 32 heads: the softmax of heads 16..31 of the tile (the softmax
+        // warps take heads 0..15 at the same time)
+        const bool first = c.first(), last = c.last();
+        const int ob = pi % C::kNO;
+        const int rb = i & 1;
+        const int sb = i % C::kSBuf;
+        if (first) lsum_b = 0.f;
+        wait_warp(bars + kSFull + sb, (i / C::kSBuf) & 1, ms, a);
+        tc_fence_after();
+        PassCtx z;
+        z.valid = tile_key(st, ta, lane, q, 1, rb, ms, z.sw);
+        z.a = &a;
+        z.smem = smem;
+        z.ms = ms;
+        z.bars = bars;
+        z.tmem = tmem;
+        z.lane_base = lane_base;
+        z.q = q;
+        z.lane = lane;
+        z.i = i;
+        z.s = s;
+        z.sb = sb;
+        z.rb = rb;
+        z.ob = ob;
+        z.first = first;
+        z.p_shared = 4 * q >= C::kPInRope;
+        z.grp = 1;
+        z.bar_id = 2;
+        z.first_pass = 1;
+        z.last_pass = 1;
+#ifdef SMLA_TRACE
+        z.tr_buf = tr_buf;
+        z.tr_k = &tr_k;
+#endif
+        bool pv_waited = false;
+        int es[4];
+        softmax_pass<HP>(z, 1, mref_b, lsum_b, pv_waited, es);
+        tmem_wait_st();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars + kPReady + s);  // this warp's P' rows and factors are written
+        if (last) {
+          // the part's l of heads 16..31, and their (m, l) for the epilogue
+          if ((lane & 1) == 0) ms->red_l[q][16 + ((lane >> 1) & 15)] = lsum_b;
+          wait_warp(bars + kOEmpty + ob, ((pi / C::kNO) & 1) ^ 1, ms, a);
+          named_barrier(2, 128);
+          if (q == 0 && lane < 16) {
+            const int h = 16 + lane;
+            ms->part_m[ob][h] = mref_b;
+            ms->part_l[ob][h] = ms->red_l[0][h] + ms->red_l[1][h] + ms->red_l[2][h] + ms->red_l[3][h];
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bars + kEpiReady + ob);
+        }
       }
       // (3) the next part's q, as soon as its buffer is free
       if (c.last() && i + 1 < n_tiles) {
