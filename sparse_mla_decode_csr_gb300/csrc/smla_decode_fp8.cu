@@ -418,68 +418,86 @@ __device__ __noinline__ void aux_stage_q(const AuxCtx& x, int row, int qb) {
   // (the arguments' fields in registers, not reloaded after every store)
   const uint16_t* const q_rows = a.q + row * a.q_stride_row + h0 * a.q_stride_head;
   const int64_t qsh = a.q_stride_head;
+  // The q loads of the thread's next unit are issued before the current one
+  // is converted, and the rope loads first of all: one global round trip
+  // instead of one per unit (the staging sits between two QKs at 32 heads).
+  constexpr int kRopeUnits = (HP * 8 + 127) / 128;
+  uint4 rv[kRopeUnits];
+#pragma unroll
+  for (int r = 0; r < kRopeUnits; ++r) {
+    const int k = ta + 128 * r, h = k >> 3, c16 = k & 7;
+    rv[r] = make_uint4(0, 0, 0, 0);
+    if (k < HP * 8 && h < Hl) rv[r] = __ldg(reinterpret_cast<const uint4*>(q_rows + h * qsh + kLatent + 8 * c16));
+  }
+  auto load_unit = [&](int blk, uint4 (&v)[4]) {
+    const int h = blk >> 4, kb = blk & 15;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) v[k] = make_uint4(0, 0, 0, 0);
+    if (blk < HP * 16 && h < Hl) {
+      const uint4* src = reinterpret_cast<const uint4*>(q_rows + h * qsh + 32 * kb);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) v[k] = __ldg(src + k);
+    }
+  };
+  uint4 vn[4];
+  load_unit(ta, vn);
 #pragma unroll 1
-    for (int blk = ta; blk < HP * 16; blk += 128) {
-      const int h = blk >> 4, kb = blk & 15;
-      uint32_t hw[8], lw[8];
-      int sfb = 127;
-      if (h < Hl) {
-        const uint4* src =
-            reinterpret_cast<const uint4*>(q_rows + h * qsh + 32 * kb);
-        uint4 v[4];
+  for (int blk = ta; blk < HP * 16; blk += 128) {
+    const int h = blk >> 4, kb = blk & 15;
+    uint4 v[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) v[k] = __ldg(src + k);
-        float f[32];
+    for (int k = 0; k < 4; ++k) v[k] = vn[k];
+    load_unit(blk + 128, vn);
+    uint32_t hw[8], lw[8];
+    int sfb = 127;
+    if (h < Hl) {
+      float f[32];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            f[8 * k + 2 * j] = __uint_as_float(w[j] << 16);
-            f[8 * k + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-          }
+        for (int j = 0; j < 4; ++j) {
+          f[8 * k + 2 * j] = __uint_as_float(w[j] << 16);
+          f[8 * k + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
         }
-        float amax = 0.f;
-#pragma unroll
-        for (int k = 0; k < 32; ++k) amax = fmaxf(amax, fabsf(f[k]));
-        int e = amax > 0.f ? int((__float_as_uint(amax) >> 23) & 0xFF) - 127 - 7 : 0;
-        e = max(min(e, 120), -120);
-        sfb = e + 127;
-        const float inv = pow2f(-e);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          uint16_t h2, l2;
-          split_pair(f[2 * k] * inv, f[2 * k + 1] * inv, h2, l2);
-          if (k & 1) {
-            hw[k >> 1] |= uint32_t(h2) << 16;
-            lw[k >> 1] |= uint32_t(l2) << 16;
-          } else {
-            hw[k >> 1] = h2;
-            lw[k >> 1] = l2;
-          }
-        }
-      } else {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) hw[k] = lw[k] = 0u;
       }
-      const int kc = kb >> 2, c0 = 2 * (kb & 3);
-      uint8_t* base = qs + kc * C::kQLatChunk;
-      *reinterpret_cast<uint4*>(base + sw128(h, c0)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-      *reinterpret_cast<uint4*>(base + sw128(h, c0 + 1)) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
-      *reinterpret_cast<uint4*>(base + sw128(HP + h, c0)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-      *reinterpret_cast<uint4*>(base + sw128(HP + h, c0 + 1)) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
-      ms->sfq[h][kb] = uint8_t(sfb);
-      ms->sfq[HP + h][kb] = uint8_t(sfb);
+      float amax = 0.f;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) amax = fmaxf(amax, fabsf(f[k]));
+      int e = amax > 0.f ? int((__float_as_uint(amax) >> 23) & 0xFF) - 127 - 7 : 0;
+      e = max(min(e, 120), -120);
+      sfb = e + 127;
+      const float inv = pow2f(-e);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        uint16_t h2, l2;
+        split_pair(f[2 * k] * inv, f[2 * k + 1] * inv, h2, l2);
+        if (k & 1) {
+          hw[k >> 1] |= uint32_t(h2) << 16;
+          lw[k >> 1] |= uint32_t(l2) << 16;
+        } else {
+          hw[k >> 1] = h2;
+          lw[k >> 1] = l2;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) hw[k] = lw[k] = 0u;
     }
-#pragma unroll 1
-    for (int k = ta; k < HP * 8; k += 128) {  // rope: HP rows x 128 bytes, 16-byte chunks
-      const int h = k >> 3, c16 = k & 7;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (h < Hl)
-        v = __ldg(reinterpret_cast<const uint4*>(q_rows + h * qsh +
-                                                 kLatent + 8 * c16));
-      *reinterpret_cast<uint4*>(qs + C::kQOffRope + sw128(h, c16)) = v;
-    }
+    const int kc = kb >> 2, c0 = 2 * (kb & 3);
+    uint8_t* base = qs + kc * C::kQLatChunk;
+    *reinterpret_cast<uint4*>(base + sw128(h, c0)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4*>(base + sw128(h, c0 + 1)) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+    *reinterpret_cast<uint4*>(base + sw128(HP + h, c0)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    *reinterpret_cast<uint4*>(base + sw128(HP + h, c0 + 1)) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+    ms->sfq[h][kb] = uint8_t(sfb);
+    ms->sfq[HP + h][kb] = uint8_t(sfb);
+  }
+#pragma unroll
+  for (int r = 0; r < kRopeUnits; ++r) {  // rope: HP rows x 128 bytes, 16-byte chunks
+    const int k = ta + 128 * r, h = k >> 3, c16 = k & 7;
+    if (k < HP * 8) *reinterpret_cast<uint4*>(qs + C::kQOffRope + sw128(h, c16)) = rv[r];
+  }
     named_barrier(2, 128);
     {
       // q factors: B row n = 32 j + lane in column 4 g + j of K-block group
