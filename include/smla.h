@@ -162,15 +162,15 @@ typedef struct smla_decode_params {
  * Tensor-core kernels (bf16: tile_len 64; native fp8: tile_len 128): a
  * persistent, balanced schedule.  Each row r is cut into
  * T_r = max(1, ceil(len_r / tile_len)) tiles of tile_len slice positions
- * and takes s + T_r slots of a schedule space (s slots stand for the cost of
- * starting a row: its epilogue and q staging; s = 2, except s = 1 for the
- * native-fp8 kernel above 16 heads, whose tiles take longer), rows in order,
- * so row r's tiles are slots [R_r, R_r + T_r) with
- * R_r = s + sum_{r' < r} (s + T_r').  CTA
- * c of G = grid takes the slots [b_c, e_c) with b_c = floor(c W / G), W the
- * slot total, and streams through the tiles in its range across row
- * boundaries.  A row lying wholly inside one CTA's range is finished there; a
- * row shared by CTAs c_a..c_b (the CTAs holding its first and last tile) gets
+ * and takes s + k T_r slots of a schedule space, rows in order (s slots stand
+ * for the cost of starting a row: its epilogue and q staging; bf16 kernel:
+ * k = 1 slot per tile and s = 2; native-fp8 kernel: k = 2, s = 1, i.e. half
+ * a tile), so that tile t of row r starts at slot R_r + k t with
+ * R_r = s + sum_{r' < r} (s + k T_r').  CTA c of G = grid takes the slots
+ * [b_c, e_c) with b_c = floor(c W / G), W the slot total, and the tiles whose
+ * first slot lies there, and streams through them across row boundaries.
+ * A row lying wholly inside one CTA's range is finished there; a row shared
+ * by CTAs c_a..c_b (the CTAs holding its first and last tile) gets
  * one partial per CTA, stored in workspace slot 2 c + (R_r < b_c ? 0 : 1), and
  * is merged from those slots ([P2] stage_combine).  bf16 kernel: by a second,
  * small kernel launched right after (merge_kernel = 1 whenever grid > 1; a

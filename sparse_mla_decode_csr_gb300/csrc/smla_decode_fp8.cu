@@ -102,6 +102,10 @@ constexpr float kLazy = 16.f;                     // reference max moves when pa
 constexpr float kInitMax = -1.0e30f;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait (default) and per MMA drain
 constexpr int kMaxHP = 32;
+// schedule slots per 128-key tile: a tile belongs to the CTA whose slot range
+// holds its first slot, so that the CTAs' tile counts differ by at most one
+// even where row starts cost fractions of a tile
+constexpr int kTileSlots = 2;  // (a power of two: the merge kernel shifts by its log)
 
 // ---- shared memory of a stage (bytes from a 1024-aligned base) ----
 constexpr int kChunk = kTK * 128;                       // one 128-byte column block of a tile (16 KB)
@@ -124,9 +128,9 @@ struct Cfg {
   // 2); S single-buffered so that the TMEM columns fit
   static constexpr int kQkSplit = HP == 16 ? 4 : 2;
   // schedule slots charged for starting a row (its q staging and epilogue):
-  // two 128-key tiles at 16 heads, one at 32, measured best on the
-  // workloads of each width (the 32-head tile is ~1.5x longer)
-  static constexpr int kRowStart = HP == 16 ? 2 : 1;
+  // half a tile (kTileSlots = 2), measured best on decode (48.0 us against
+  // 49.9 at two tiles) with ragged, wide and long unchanged within noise
+  static constexpr int kRowStart = 1;
   // 32 heads: the aux warps take the softmax of heads 16..31 (the second
   // 16-head pass) of every tile, the softmax warps heads 0..15
   static constexpr bool kSplitPass = HP == 32;
@@ -206,6 +210,7 @@ struct Misc {
   int64_t mP[2];                                // the row's first tile slot
   int64_t mca[2];
   int64_t mcz[2];
+  int32_t mnt[2];                               // the row's tiles
   int64_t mslot[2][kMaxInKernelParts];
   int32_t n_merge;                              // rows this CTA completes and merges at its end
   int32_t merge_row[2];
@@ -322,8 +327,9 @@ struct Cursor {
     len = row_len(a, row);
     ntiles = tiles_of(len);
     beg = __ldg(a.indptr + row);
-    const int64_t n = e - P;
-    tb = int32_t(n < 0 ? 0 : (n < int64_t(ntiles) ? n : int64_t(ntiles)));
+    // the tiles whose first slot P + kTileSlots t lies before the range end
+    const int64_t n = e > P ? (e - P + kTileSlots - 1) / kTileSlots : 0;
+    tb = int32_t(n < int64_t(ntiles) ? n : int64_t(ntiles));
     if (tb <= 0) live = false;
   }
   __device__ __forceinline__ void init(const DecodeArgs& a, int32_t r0, int64_t P0, int64_t b, int64_t e_) {
@@ -334,15 +340,15 @@ struct Cursor {
     ta = tb = t = 0;
     if (!live) return;
     load_row(a);
-    ta = int32_t(b > P ? b - P : 0);
+    ta = int32_t(b > P ? (b - P + kTileSlots - 1) / kTileSlots : 0);  // the first tile whose first slot is >= b
     t = ta;
   }
   __device__ __forceinline__ void advance(const DecodeArgs& a) {
     if (!live) return;
     if (++t < tb) return;
-    P += ntiles + kRowStart;
+    P += int64_t(kTileSlots) * ntiles + kRowStart;
     ++row;
-    if (P - kRowStart >= e || row >= a.n_q) {
+    if (P >= e || row >= a.n_q) {
       live = false;
       return;
     }
@@ -385,6 +391,21 @@ __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, Misc* 
 __device__ __noinline__ int64_t div64(int64_t n, int64_t d) { return n / d; }
 __device__ __forceinline__ int64_t cbeg(int64_t c, int64_t T, int64_t G) { return div64(c * T, G); }
 __device__ __forceinline__ int64_t cof(int64_t t, int64_t T, int64_t G) { return div64((t + 1) * G - 1, T); }
+
+// The tiles [lo, hi) of a row (first tile slot F, nt tiles, tile t at slot
+// F + kTileSlots t) whose first slot lies in [b, e).
+__device__ __forceinline__ void tiles_in(int64_t F, int32_t nt, int64_t b, int64_t e, int32_t& lo, int32_t& hi) {
+  const int64_t l = b > F ? (b - F + kTileSlots - 1) / kTileSlots : 0;
+  const int64_t h = e > F ? (e - F + kTileSlots - 1) / kTileSlots : 0;
+  lo = int32_t(l < nt ? l : nt);
+  hi = int32_t(h < nt ? h : nt);
+}
+// Whether CTA c holds a tile of that row.
+__device__ __forceinline__ bool holds(int64_t c, int64_t F, int32_t nt, int64_t T, int64_t G) {
+  int32_t lo, hi;
+  tiles_in(F, nt, cbeg(c, T, G), cbeg(c + 1, T, G), lo, hi);
+  return hi > lo;
+}
 
 // Slot of a shared row part (the partial layout of the merge kernel).
 __device__ __forceinline__ int64_t slot_of(int64_t c, int64_t P, int64_t T, int64_t G) {
@@ -586,8 +607,8 @@ __device__ __noinline__ void combine_staged(const DecodeArgs& a, const uint8_t* 
 // The same for a row of more than kMaxInKernelParts parts (only a plan
 // without the merge kernel leaves one here): part by part from global
 // memory with a running maximum.
-__device__ __noinline__ void combine_global(const DecodeArgs& a, int row, int hb, int nh, int64_t P, int64_t ca,
-                                            int64_t cz, int64_t T, int64_t G, int t, int nthreads) {
+__device__ __noinline__ void combine_global(const DecodeArgs& a, int row, int hb, int nh, int64_t P, int32_t nt,
+                                            int64_t ca, int64_t cz, int64_t T, int64_t G, int t, int nthreads) {
   const int H = a.heads;
   const float* const o_part = a.o_part;
   const float2* const ml_part = reinterpret_cast<const float2*>(a.ml_part);
@@ -604,7 +625,7 @@ __device__ __noinline__ void combine_global(const DecodeArgs& a, int row, int hb
     for (int d = 0; d < 16; ++d) acc[d] = 0.f;
 #pragma unroll 1
     for (int64_t cc = ca; cc <= cz; ++cc) {
-      if (!(cbeg(cc + 1, T, G) > cbeg(cc, T, G))) continue;
+      if (!holds(cc, P, nt, T, G)) continue;
       const int64_t sl = slot_of(cc, P, T, G);
       const float2 mj = __ldcg(ml_part + sl * H + h);
       if (mj.y == 0.f) continue;
@@ -849,8 +870,9 @@ __device__ __noinline__ void end_merge(const DecodeArgs& a, uint8_t* smem, uint6
       if (lane < parts) nv = __ldcg(a.nv_part + ms->mslot[xi][lane]);
     } else {
       const int64_t ca = ms->mca[xi], cz = ms->mcz[xi], P = ms->mP[xi];
+      const int32_t nt = ms->mnt[xi];
       for (int64_t cc = ca + lane; cc <= cz; cc += 32)
-        if (cbeg(cc + 1, T, G) > cbeg(cc, T, G)) nv += __ldcg(a.nv_part + slot_of(cc, P, T, G));
+        if (holds(cc, P, nt, T, G)) nv += __ldcg(a.nv_part + slot_of(cc, P, T, G));
     }
   }
 #ifdef SMLA_TRACE
@@ -893,7 +915,7 @@ __device__ __noinline__ void end_merge(const DecodeArgs& a, uint8_t* smem, uint6
     const int xi = ms->merge_x[k];
     const int parts = ms->mparts[xi];
     if (parts > kMaxInKernelParts) {
-      combine_global(a, row, h0, Hl, ms->mP[xi], ms->mca[xi], ms->mcz[xi], T, G, tid, kThreads);
+      combine_global(a, row, h0, Hl, ms->mP[xi], ms->mnt[xi], ms->mca[xi], ms->mcz[xi], T, G, tid, kThreads);
       continue;
     }
 #pragma unroll 1
@@ -1248,7 +1270,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
     const int lo = min(tid * per, n), hi = min(lo + per, n);
     int64_t local = 0;
 #pragma unroll 1
-    for (int r = lo; r < hi; ++r) local += C::kRowStart + Cur::tiles_of(row_len(a, r));
+    for (int r = lo; r < hi; ++r) local += C::kRowStart + kTileSlots * Cur::tiles_of(row_len(a, r));
     int64_t x = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -1278,21 +1300,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
 #pragma unroll 1
     for (int r = lo; r < hi; ++r) {
       const int32_t nt_r = Cur::tiles_of(row_len(a, r));
-      const int64_t w = C::kRowStart + nt_r;
-      if (P <= b && b < P + w) {
+      const int64_t w = C::kRowStart + int64_t(kTileSlots) * nt_r;
+      const int64_t F = P + C::kRowStart;                   // the row's first tile slot
+      const int64_t L = F + int64_t(kTileSlots) * (nt_r - 1);  // and its last one
+      // the row of this CTA's first tile: the first row whose last tile is
+      // at or after b (the previous row's last tile slot is P - kTileSlots)
+      if (L >= b && P - kTileSlots < b) {
         ms->first_row = r;
         ms->first_tile = P;
       }
-      // the row of this CTA's last tile: e - 1 is one of its tile slots, or
-      // one of the next row's start slots right after them
-      if ((P + C::kRowStart <= e - 1 && e - 1 < P + w) ||
-          (P + w <= e - 1 && e - 1 < P + w + C::kRowStart && P + w - 1 >= b)) {
+      // the row of its last tile: the row whose first tile is before e and
+      // the next row's first tile not
+      if (F < e && P + w + C::kRowStart >= e) {
         ms->last_row = r;
         ms->last_tile = P;
       }
-      const int64_t t0 = P + C::kRowStart;
-      const int64_t lo_t = b > t0 ? b : t0, hi_t = e < t0 + nt_r ? e : t0 + nt_r;
-      if (hi_t > lo_t) mine += int32_t(hi_t - lo_t);
+      int32_t lo_t, hi_t;
+      tiles_in(F, nt_r, b, e, lo_t, hi_t);
+      if (hi_t > lo_t) mine += hi_t - lo_t;
       if (blockIdx.x == 0 && a.row_tile) a.row_tile[r] = P;
       P += w;
     }
@@ -1481,11 +1506,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
       if (r < a.n_q) {
         const int64_t Pr = (q == 0 ? P0 : ms->last_tile) + C::kRowStart;
         const int32_t nt = Cur::tiles_of(row_len(a, r));
-        const int64_t ca = cof(Pr, T, G), cz = cof(Pr + nt - 1, T, G);
+        const int64_t ca = cof(Pr, T, G), cz = cof(Pr + int64_t(kTileSlots) * (nt - 1), T, G);
         int32_t n = 0;
         for (int64_t c0 = ca; c0 <= cz; c0 += 32) {
           const int64_t cc = c0 + lane;
-          const bool in = cc <= cz && cbeg(cc + 1, T, G) > cbeg(cc, T, G);
+          const bool in = cc <= cz && holds(cc, Pr, nt, T, G);
           const uint32_t m = __ballot_sync(0xffffffffu, in);
           const int j = n + __popc(m & ((1u << lane) - 1u));
           if (in && j < kMaxInKernelParts) ms->mslot[q][j] = slot_of(cc, Pr, T, G);
@@ -1496,6 +1521,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
           ms->mP[q] = Pr;
           ms->mca[q] = ca;
           ms->mcz[q] = cz;
+          ms->mnt[q] = nt;
         }
       }
     }
@@ -1806,6 +1832,7 @@ static cudaError_t launch_fp8_hp(const DecodeLaunch& L) {
   if (e != cudaSuccess) return e;
   DecodeArgs args = make_decode_args(L);
   args.row_start_slots = Cfg<HP>::kRowStart;  // (read by the merge kernel)
+  args.tile_slots = kTileSlots;
   e = launch_trim(L, args);
   if (e != cudaSuccess) return e;
   decode_fp8_kernel<HP><<<L.plan.grid * L.plan.head_groups, kThreads, smem, L.stream>>>(args);

@@ -1265,12 +1265,13 @@ __global__ void __launch_bounds__(32 * (kSplit == 1 ? kMergeWarps : kSplit)) mer
   const int row = int(pair / H), h = int(pair % H);
   const int64_t P = __ldcg(a.row_tile + row) + a.row_start_slots;  // the row's first tile slot
   const int64_t T = __ldcg(a.row_tile + a.n_q), G = a.grid;
-  const int32_t nt = int32_t(__ldcg(a.row_tile + row + 1) - P);
-  const int64_t ca = cta_of_tile(P, T, G), cb = cta_of_tile(P + nt - 1, T, G);
+  const int64_t S = a.tile_slots;  // tile t of the row: first slot P + S t
+  const int32_t nt = int32_t((__ldcg(a.row_tile + row + 1) - P) >> (__ffsll(S) - 1));
+  const int64_t ca = cta_of_tile(P, T, G), cb = cta_of_tile(P + S * (nt - 1), T, G);
   if (ca == cb) return;  // finished whole by one CTA
   if (a.merge_min_parts > 2) {  // rows of fewer parts were merged by the decode kernel
     int64_t parts = 0;
-    for (int64_t c = ca; c <= cb && parts < a.merge_min_parts; ++c) parts += cta_begin(c + 1, T, G) > cta_begin(c, T, G);
+    for (int64_t c = ca; c <= cb && parts < a.merge_min_parts; ++c) parts += cta_holds_tile(c, P, nt, S, T, G);
     if (parts < a.merge_min_parts) return;
   }
   // this warp's parts: c = ca + w + kSplit i
@@ -1287,7 +1288,7 @@ __global__ void __launch_bounds__(32 * (kSplit == 1 ? kMergeWarps : kSplit)) mer
     const int64_t c = first + kSplit * (i0 + lane);
     int64_t sl = -1;
     float2 ml = make_float2(-INFINITY, 0.f);
-    if (c <= cb && cta_begin(c + 1, T, G) > cta_begin(c, T, G)) {  // a CTA with tiles
+    if (c <= cb && cta_holds_tile(c, P, nt, S, T, G)) {  // a CTA with tiles of the row
       sl = part_slot(c, P, T, G);
       ml = __ldcg(reinterpret_cast<const float2*>(a.ml_part + (sl * H + h) * 2));
     }

@@ -35,6 +35,7 @@ struct DecodeArgs {
   int32_t merge_min_parts;     // the merge kernel leaves rows of fewer parts alone
   int32_t head_groups;         // native-fp8 kernel: CTAs per schedule range (heads split)
   int32_t row_start_slots;     // tensor-core schedule: slots charged for starting a row
+  int32_t tile_slots;          //   and slots per tile (a tile belongs to the CTA holding its first slot)
   // split workspace
   int32_t* ticket;
   int64_t* row_tile;  // tensor-core schedule: first tile of each row, then T
@@ -79,6 +80,7 @@ inline DecodeArgs make_decode_args(const DecodeLaunch& L) {
   a.merge_min_parts = L.plan.kernel == SMLA_KERNEL_TENSOR_CORE_FP8 ? kMaxInKernelParts + 1 : 2;
   a.head_groups = L.plan.head_groups > 0 ? L.plan.head_groups : 1;
   a.row_start_slots = kRowStartSlots;  // (the native-fp8 launcher sets its own)
+  a.tile_slots = 1;
   if (L.ws.total > 0) {
     char* ws = static_cast<char*>(L.workspace);
     a.ticket = reinterpret_cast<int32_t*>(ws + L.ws.ticket_off);
@@ -202,6 +204,17 @@ __device__ __forceinline__ int64_t cta_begin(int64_t c, int64_t T, int64_t G) { 
 // The CTA whose range holds tile t: the largest c with floor(c T / G) <= t.
 __device__ __forceinline__ int64_t cta_of_tile(int64_t t, int64_t T, int64_t G) {
   return ((t + 1) * G - 1) / T;
+}
+
+// Whether CTA c holds a tile of a row whose nt tiles start at slots
+// F + S t (S a power of two): a tile belongs to the CTA whose range holds
+// its first slot.
+__device__ __forceinline__ bool cta_holds_tile(int64_t c, int64_t F, int32_t nt, int64_t S, int64_t T, int64_t G) {
+  const int64_t b = cta_begin(c, T, G), e = cta_begin(c + 1, T, G);
+  const int sh = __ffsll(S) - 1;  // (a shift, not a 64-bit division)
+  const int64_t lo = b > F ? (b - F + S - 1) >> sh : 0;
+  const int64_t hi = e > F ? (e - F + S - 1) >> sh : 0;
+  return (hi < nt ? hi : nt) > (lo < nt ? lo : nt);
 }
 
 // Partial slot of row part (CTA c, row starting at tile P).

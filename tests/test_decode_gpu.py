@@ -227,24 +227,27 @@ def test_split_partials_match_oracle_cuda_core():
             _check_part(o[sl], ml[sl], nv[sl], _oracle_part(c, r, lo, max(lo, hi)), f"row {r} chunk {ch}")
 
 
-def tc_schedule(lens, G, tile=64, start_slots=2):
+def tc_schedule(lens, G, tile=64, start_slots=2, tile_slots=1):
     """The tensor-core kernels' row parts, restated from smla.h: rows cut into
-    tile-key tiles; row r takes start_slots schedule slots and then its tiles,
-    in row order; CTA c takes slots [c W / G, (c+1) W / G); a part of a shared
-    row lands in slot 2 c + (R_r < b_c ? 0 : 1), R_r the slot of the row's
-    first tile.  Returns {row: [(cta, slot, first position, end position), ...]}."""
+    tile-key tiles; row r takes start_slots schedule slots and then tile_slots
+    slots per tile, in row order; CTA c takes slots [c W / G, (c+1) W / G) and
+    the tiles whose first slot lies there; a part of a shared row lands in
+    slot 2 c + (R_r < b_c ? 0 : 1), R_r the first slot of the row's first
+    tile.  Returns {row: [(cta, slot, first position, end position), ...]}."""
     tiles = [max(1, -(-L // tile)) for L in lens]
-    starts = np.concatenate([[0], np.cumsum([start_slots + n for n in tiles])]).astype(np.int64)
+    starts = np.concatenate([[0], np.cumsum([start_slots + tile_slots * n for n in tiles])]).astype(np.int64)
     W = int(starts[-1])
     b = [c * W // G for c in range(G + 1)]
     parts = {}
     for r, L in enumerate(lens):
         R, nt = int(starts[r]) + start_slots, tiles[r]
         for c in range(G):
-            lo_t, hi_t = max(b[c], R), min(b[c + 1], R + nt)
+            # the tiles t with R + tile_slots t in [b_c, b_c+1)
+            lo_t = min(nt, max(0, -(-(b[c] - R) // tile_slots)))
+            hi_t = min(nt, max(0, -(-(b[c + 1] - R) // tile_slots)))
             if lo_t < hi_t:
                 slot = 2 * c + (0 if R < b[c] else 1)
-                parts.setdefault(r, []).append((c, slot, (lo_t - R) * tile, min((hi_t - R) * tile, L)))
+                parts.setdefault(r, []).append((c, slot, lo_t * tile, min(hi_t * tile, L)))
     return parts
 
 
@@ -264,8 +267,10 @@ def test_tensor_core_schedule_partials_match_oracle(k, tk, heads):
     torch.cuda.synchronize()
     ticket, o, ml, nv = _read_workspace(ws, n_q, heads, plan.partial_slots)
     assert np.all(ticket == 0), "ticket counters must return to zero"
-    # slots charged per row start: 2, or 1 for the fp8 kernel above 16 heads
-    parts = tc_schedule(lens, plan.grid, tile=plan.tile_len, start_slots=1 if tk == "fp8" and heads > 16 else 2)
+    # the fp8 kernel counts half-tile slots (2 per tile) and charges a row
+    # start one of them; the bf16 kernel 1 slot per tile and 2 per row start
+    start, per_tile = (1, 2) if tk == "fp8" else (2, 1)
+    parts = tc_schedule(lens, plan.grid, tile=plan.tile_len, start_slots=start, tile_slots=per_tile)
     shared = [r for r, pr in parts.items() if len(pr) > 1]
     assert shared, "the case must exercise shared rows"
     for r in shared:
