@@ -242,6 +242,8 @@ def l2_flusher(dev):
 
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal
 KERNEL_NAMES = {1: "CUDA-core", 2: "bf16 tcgen05", 3: "native-fp8 tcgen05"}
+# the type each kernel multiplies in (all accumulate in f32)
+KERNEL_DTYPES = {1: "f32", 2: "bf16", 3: "e4m3"}
 
 
 def scale_histogram(kv: torch.Tensor) -> dict:
@@ -503,7 +505,7 @@ def main():
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": mean_ms, "ms_per_step_median": statistics.median(times),
         "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": KERNEL_DTYPES[prob.plan.kernel], "data": "synthetic",
         "config": {"workload": w.name, "n_q": w.n_q, "heads": w.heads, "topk": w.topk,
                    "n_kv_rows": w.n_kv_rows, "rows_per_gpu": w.n_q,
                    "l2": "flushed between steps (256 MB written, then 256 MB read)",
