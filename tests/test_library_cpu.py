@@ -62,7 +62,7 @@ def test_plan_properties_cuda_core(n_q, heads, row_len):
 
 
 @pytest.mark.parametrize("n_q,heads,row_len", [
-    (4, 16, 128), (64, 16, 2048), (256, 16, 2048), (128, 64, 2048), (4, 64, 16384), (1, 1, 1)])
+    (4, 16, 128), (32, 16, 2048), (64, 16, 2048), (256, 16, 2048), (128, 64, 2048), (4, 64, 16384), (1, 1, 1)])
 def test_plan_properties_tensor_core(n_q, heads, row_len):
     p = smla.smla_plan(n_q, heads, row_len, n_q * row_len, 0, 152)
     # the default resolves to the native-fp8 kernel (up to 64 heads)
@@ -70,9 +70,9 @@ def test_plan_properties_tensor_core(n_q, heads, row_len):
     hg = 2 if heads > 32 else 1  # two CTAs (head groups of up to 32) share a schedule range above 32 heads
     assert p.head_groups == hg and p.grid == 152 // hg  # persistent: one CTA per SM
     assert p.partial_slots == 2 * p.grid
-    # rows of at most 8 parts are merged inside the kernel; the merge kernel
+    # rows of at most 4 parts are merged inside the kernel; the merge kernel
     # runs only when top-k rows would span more CTAs
-    assert p.merge_kernel == (-(-p.grid // n_q) + 1 > 8)
+    assert p.merge_kernel == (-(-p.grid // n_q) + 1 > 4)
     need = 8 * n_q + (n_q + 1) * 8 + p.partial_slots * heads * (512 + 2) * 4 + p.partial_slots * 4
     assert p.workspace_bytes >= need
     for k in (1, 3, 64):
