@@ -242,7 +242,8 @@ enum Bar {
   kDrain = 22,    // MMA issuers: every MMA they issued has completed
   kStall = 23,    // never signalled (timeout-path test)
   kMerge = 24,    // the end merge's bulk copies
-  kPReady = 25    // [2] 32 heads: aux warps -> PV issuers (heads 16..31 of a tile's P' written)
+  kPReady = 25,   // [2] 32 heads: aux warps -> PV issuers (heads 16..31 of a tile's P' written)
+  kQReady = 27    // 32 heads: loader warps -> QK issuers (a new part's q staged)
 };
 
 __device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t chunk16) {
@@ -426,9 +427,13 @@ struct AuxCtx {
 // q of a row -> [q_hi | q_lo] E4M3 (K-major, 128-byte swizzled) with an E8M0
 // factor per (head, 32 dims) that brings the block's largest |q| to
 // [2^7, 2^8); q_rope (bf16) copied as it is; then the factors into TMEM.
-// Run by the four aux warps (out of line: one copy of its code).
+// Run by one warp group of nthreads threads (x.ta < nthreads; the aux warps,
+// or at 32 heads the loader warps at a row boundary) with its named barrier
+// bar_id; sf_writer: this warp writes the factors of its TMEM lane quarter.
+// Out of line: one copy of its code.
 template <int HP>
-__device__ __noinline__ void aux_stage_q(const AuxCtx& x, int row, int qb) {
+__device__ __noinline__ void aux_stage_q(const AuxCtx& x, int row, int qb, int nthreads, uint32_t bar_id,
+                                         bool sf_writer) {
   const DecodeArgs& a = *x.a;
   using C = Cfg<HP>;
   constexpr int kN = C::kN;
@@ -446,7 +451,7 @@ __device__ __noinline__ void aux_stage_q(const AuxCtx& x, int row, int qb) {
   uint4 rv[kRopeUnits];
 #pragma unroll
   for (int r = 0; r < kRopeUnits; ++r) {
-    const int k = ta + 128 * r, h = k >> 3, c16 = k & 7;
+    const int k = ta + nthreads * r, h = k >> 3, c16 = k & 7;
     rv[r] = make_uint4(0, 0, 0, 0);
     if (k < HP * 8 && h < Hl) rv[r] = __ldg(reinterpret_cast<const uint4*>(q_rows + h * qsh + kLatent + 8 * c16));
   }
@@ -463,12 +468,12 @@ __device__ __noinline__ void aux_stage_q(const AuxCtx& x, int row, int qb) {
   uint4 vn[4];
   load_unit(ta, vn);
 #pragma unroll 1
-  for (int blk = ta; blk < HP * 16; blk += 128) {
+  for (int blk = ta; blk < HP * 16; blk += nthreads) {
     const int h = blk >> 4, kb = blk & 15;
     uint4 v[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) v[k] = vn[k];
-    load_unit(blk + 128, vn);
+    load_unit(blk + nthreads, vn);
     uint32_t hw[8], lw[8];
     int sfb = 127;
     if (h < Hl) {
@@ -516,11 +521,11 @@ __device__ __noinline__ void aux_stage_q(const AuxCtx& x, int row, int qb) {
   }
 #pragma unroll
   for (int r = 0; r < kRopeUnits; ++r) {  // rope: HP rows x 128 bytes, 16-byte chunks
-    const int k = ta + 128 * r, h = k >> 3, c16 = k & 7;
+    const int k = ta + nthreads * r, h = k >> 3, c16 = k & 7;
     if (k < HP * 8) *reinterpret_cast<uint4*>(qs + C::kQOffRope + sw128(h, c16)) = rv[r];
   }
-    named_barrier(2, 128);
-    {
+    named_barrier(bar_id, nthreads);
+    if (sf_writer) {
       // q factors: B row n = 32 j + lane in column 4 g + j of K-block group
       // g, byte k = K-block 4 g + k; unused columns hold 1
       uint32_t v[16];
@@ -1229,6 +1234,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
       mbar_init(bars + kOEmpty + s, 4);
       mbar_init(bars + kEpiReady + s, Cfg<HP>::kSReaders);
       mbar_init(bars + kPReady + s, kSoftmaxWarps);
+      if (s == 0) mbar_init(bars + kQReady, kLoadWarps);
     }
     mbar_init(bars + kPvDone, kSoftmaxWarps);
     mbar_init(bars + kDrain, Cfg<HP>::kQkSplit + kSoftmaxWarps);
@@ -1497,7 +1503,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
     // [2^7, 2^8); q_rope (bf16) copied as it is; then the factors into TMEM.
     Cur c;
     c.init(a, row0, P0, cb, ce);
-    if (n_tiles > 0) aux_stage_q<HP>(actx, c.row, 0);
+    if (n_tiles > 0) aux_stage_q<HP>(actx, c.row, 0, 128, 2, true);
     if (q < 2 && n_tiles > 0) {
       // the CTAs sharing this CTA's first (q = 0) and last (q = 1) row, for
       // a merge at the end (lane j looks at CTA ca + j; no waits, while the
@@ -1567,6 +1573,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
         const int sb = i % C::kSBuf;
         const uint32_t sph = (i / C::kSBuf) & 1;
         wait_warp(bars + kSEmpty + sb, sph ^ 1, ms, a);
+        // 32 heads: a new part's q, staged by the loader warps
+        if (C::kSplitPass && i > 0 && c.first()) wait_warp(bars + kQReady, uint32_t((pi - 1) & 1), ms, a);
         tc_fence_after();
         F8_TR(30, i);
         if (lane == 0) {
@@ -1706,11 +1714,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
           if (lane == 0) mbar_arrive(bars + kEpiReady + ob);
         }
       }
-      // (3) the next part's q, as soon as its buffer is free
-      if (c.last() && i + 1 < n_tiles) {
+      // (3) the next part's q, as soon as its buffer is free (32 heads: the
+      // loader warps stage it, see there)
+      if (!C::kSplitPass && c.last() && i + 1 < n_tiles) {
         const int qb = (pi + 1) % C::kNQ;
         wait_warp(bars + kQEmpty + qb, (((pi + 1) / C::kNQ) & 1) ^ 1, ms, a);
-        aux_stage_q<HP>(actx, c.row + 1, qb);
+        aux_stage_q<HP>(actx, c.row + 1, qb, 128, 2, true);
         F8_TR(43, i);
       }
       if (c.last()) {
@@ -1741,6 +1750,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
     int32_t raw = raw_of(c);
     F8_TR(52, 0);
     bool oob = false;
+    int pl = 0;  // 32 heads: the part of tile i
+    (void)pl;
     for (int i = 0; i < n_tiles; ++i) {
       const int s = i & 1;
       const uint32_t ph = (i >> 1) & 1;
@@ -1780,6 +1791,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fp8_kernel(const __grid_co
         __syncwarp();
         if (lane == 0) mbar_arrive(bars + kKvFull + s);
         F8_TR(51, i);
+      }
+      if constexpr (C::kSplitPass) {
+        // 32 heads: a new part's q, staged here while the aux warps (which
+        // also run half of the softmax) finish the previous part's last tile;
+        // its buffer is free once that tile's QK has completed
+        if (i > 0 && c.first()) {
+          const int qb = pl % C::kNQ;
+          wait_warp(bars + kQEmpty + qb, ((pl / C::kNQ) & 1) ^ 1, ms, a);
+          const AuxCtx lx{&a, smem, ms, bars, tmem, uint32_t(32 * (lw & 3)) << 16, H, h0, Hl, hg, g, lane,
+                          tid - 32 * kLoadWarp0, c_id, G, T};
+          aux_stage_q<HP>(lx, c.row, qb, 32 * kLoadWarps, 3, lw < 4);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bars + kQReady);
+        }
+        if (c.last()) ++pl;
       }
       c.advance(a);
       raw = raw_of(c);  // the next tile's entries, loaded while this one lands
