@@ -827,10 +827,14 @@ __device__ __noinline__ void aux_epilogue(const AuxCtx& x, const Cursor<Cfg<HP>:
         if (j < hn) dst[int64_t(j) * kLatent] = __uint_as_float(v0[j]) + __uint_as_float(v1[j]);
     }
   }
-  if (!whole) __threadfence();  // the partial is visible device-wide before the ticket below
   tc_fence_before();
-  named_barrier(2, 128);  // every aux thread read the part's (m, l) and O (and fenced its partial)
+  named_barrier(2, 128);  // every aux thread read the part's (m, l) and O
+  // the O buffer is free for the next part's PV now, before the partial's fence
   if (lane == 0) mbar_arrive(bars + kOEmpty + ob);
+  if (!whole) {
+    __threadfence();        // the partial is visible device-wide before the ticket below
+    named_barrier(2, 128);  // (every aux thread's part of it)
+  }
   if (!whole && ta == 0) {
     // the CTAs holding this row's tiles ([P2] stage_split parts); the one whose
     // part arrives last merges the row (this head group) after its own work
