@@ -22,22 +22,25 @@
 //        the tile's largest term.  O = O_hi + O_lo.
 //
 // Warp roles (16 warps, 512 threads, one CTA per SM):
-//   0-3   softmax (warp q owns the keys of TMEM lane quarter q of S; all the
-//         CTA's heads, 16 at a time; per-head values live one per lane);
-//         each then issues the tile's PV of one 128-dim block
+//   0-3   softmax (warp q owns the keys of TMEM lane quarter q of S; heads
+//         16 at a time, per-head values one per lane; at 32 heads only heads
+//         0..15); each then issues the tile's PV of one 128-dim block
 //   4-7   aux: E8M0 scale factors of each landed tile into TMEM, then the
-//         tile's QK (16 heads: warps 4 and 5 each issue part of the K-steps
-//         into their own accumulator, two MMA chains in flight; a thread
-//         issues one MMA every ~120 cycles); q staging (hi/lo split and its
-//         scale factors) per row part, and each row part's epilogue (out /
-//         lse or a partial of a shared row)
+//         tile's QK (16 heads: all four warps issue part of the K-steps into
+//         their own accumulator; 32 heads: warps 4 and 5; a thread issues one
+//         MMA every ~120 cycles); at 32 heads also the softmax of heads
+//         16..31; each row part's epilogue (out / lse, or a partial of a
+//         shared row) and, at 16 heads, the next part's q staging
 //   8-15  loaders: keys lw, lw + 8, ... of every 128-key tile (64-bit record
-//         addressing, masked keys zero-filled, out-of-range entries flagged)
+//         addressing, masked keys zero-filled, out-of-range entries flagged);
+//         at 32 heads also a new part's q staging
 //
-// The schedule is that of the bf16 tensor-core kernel with 128-key tiles: rows
-// cut into tiles, two start slots per row, CTA c takes the slots
-// [floor(c W / G), floor((c+1) W / G)); rows shared between CTAs leave
-// partials merged by the merge kernel.
+// The schedule is that of the bf16 tensor-core kernel counted in half-tile
+// slots: a row takes one slot for its start and two per 128-key tile, CTA c
+// takes the slots [floor(c W / G), floor((c+1) W / G)) and the tiles whose
+// first slot lies there.  A row shared by up to four CTAs is merged inside
+// the launch by the CTA whose part arrives last (per-row tickets); longer
+// rows are left to the merge kernel.
 //
 // The maths is the sparse softmax attention of the gfx950 FlyDSL page (module
 // docstring: record layout, CSR tiles, masking; its latent QK runs as a scaled
@@ -538,9 +541,11 @@ __device__ __noinline__ void aux_stage_q(const AuxCtx& x, int row, int qb, int n
       tmem_st16(tmem + lane_base + C::kColSfq + 16 * qb, v);
       tmem_wait_st();
     }
-    // (sfq is reused by the next staging; the aux warps issue the QKs that
-    // read this q only after the barrier that follows the next tile's scale
-    // factors, so this fence orders the q writes before them)
+    // (sfq is reused by the next staging.  The QKs that read this q are
+    // issued after a barrier that follows these writes: the aux warps' named
+    // barrier after the next tile's scale factors, or at 32 heads the
+    // mbarrier the loader warps arrive on; this fence orders the q writes
+    // before them)
     fence_proxy_async_smem();
     tc_fence_before();
   }
