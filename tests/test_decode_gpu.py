@@ -14,7 +14,7 @@ import oracle
 import smla_workloads as W
 import sparse_mla_decode_csr_gb300 as smla
 from smla_testlib import (FP8_MAX_HEADS, KERNELS, allowance, bits, build_cache, compare, oracle_subproblem,
-                          pack_gpu, run_gpu)
+                          pack_gpu, run_gpu, tc_schedule)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -226,29 +226,6 @@ def test_split_partials_match_oracle_cuda_core():
             sl = r * splits + ch
             _check_part(o[sl], ml[sl], nv[sl], _oracle_part(c, r, lo, max(lo, hi)), f"row {r} chunk {ch}")
 
-
-def tc_schedule(lens, G, tile=64, start_slots=2, tile_slots=1):
-    """The tensor-core kernels' row parts, restated from smla.h: rows cut into
-    tile-key tiles; row r takes start_slots schedule slots and then tile_slots
-    slots per tile, in row order; CTA c takes slots [c W / G, (c+1) W / G) and
-    the tiles whose first slot lies there; a part of a shared row lands in
-    slot 2 c + (R_r < b_c ? 0 : 1), R_r the first slot of the row's first
-    tile.  Returns {row: [(cta, slot, first position, end position), ...]}."""
-    tiles = [max(1, -(-L // tile)) for L in lens]
-    starts = np.concatenate([[0], np.cumsum([start_slots + tile_slots * n for n in tiles])]).astype(np.int64)
-    W = int(starts[-1])
-    b = [c * W // G for c in range(G + 1)]
-    parts = {}
-    for r, L in enumerate(lens):
-        R, nt = int(starts[r]) + start_slots, tiles[r]
-        for c in range(G):
-            # the tiles t with R + tile_slots t in [b_c, b_c+1)
-            lo_t = min(nt, max(0, -(-(b[c] - R) // tile_slots)))
-            hi_t = min(nt, max(0, -(-(b[c + 1] - R) // tile_slots)))
-            if lo_t < hi_t:
-                slot = 2 * c + (0 if R < b[c] else 1)
-                parts.setdefault(r, []).append((c, slot, lo_t * tile, min(hi_t * tile, L)))
-    return parts
 
 
 @pytest.mark.parametrize("tk,heads", [("bf16", 16), ("fp8", 16), ("fp8", 32)])
