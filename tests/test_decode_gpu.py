@@ -501,18 +501,18 @@ def test_e4m3_nan_code_gives_nan_rows_like_the_oracle():
     compare(out[1:], lse[1:], ref_out[1:], ref_lse[1:], "rows without the NaN record")
 
 
-@pytest.mark.parametrize("tk", ["fp8", "bf16"])
-def test_wait_timeout_sets_status_and_leaves_the_context_usable(tk):
+@pytest.mark.parametrize("tk,heads", [("fp8", 16), ("bf16", 16), ("fp8", 32)])
+def test_wait_timeout_sets_status_and_leaves_the_context_usable(tk, heads):
     """Failure detection without a GPU fault: the first softmax wait of every
     CTA waits on a barrier that nothing signals, with a 1 ms limit; it runs
     out, the kernel reports SMLA_STATUS_TIMEOUT, drains its copies and MMAs
     and exits; later calls with the default limit run normally and give the
     same results."""
     lens = [700, 900, 300, 1000, 50, 600, 800, 1000]
-    c = small_case(len(lens), 16, 4000, lens, seed=91, sink=True)
+    c = small_case(len(lens), heads, 4000, lens, seed=91, sink=True)
     o_ref, l_ref, st_ref = run_small(c, max_row_len=1000, what="before", kernel=tk)
     assert st_ref & smla.STATUS_TIMEOUT == 0
-    n_q, heads = len(lens), 16
+    n_q = len(lens)
     ws = torch.zeros(smla.smla_decode_workspace_size(n_q, heads, max_row_len=1000,
                                                      n_indices=int(c["indices"].numel()),
                                                      kernel=KERNELS[tk]) + 256,
