@@ -133,6 +133,46 @@ def test_lens_and_bad_indptr(kernel):
     run_small(c, max_row_len=300, what="indptr tail", kernel=kernel)
 
 
+def test_tail_reads_stay_inside_slices_lens_and_the_index_buffer(kernel):
+    """Index canary: every index entry that no row may read (past a row's lens
+    cap, and past the end of the index buffer given to the call) names one of
+    a few poison records whose latent is ~5e4, so a single stray read would
+    dominate its row's output.  Rows end inside a tile (tail tiles) and the
+    last row's slice ends exactly at the end of the buffer; the buffer handed
+    over is a view whose following memory holds more poison entries."""
+    g = torch.Generator().manual_seed(123)
+    n_kv, n_poison, heads = 700, 8, 16
+    lat = torch.randn(n_kv, 512, generator=g).to(torch.bfloat16)
+    lat[:n_poison] = 5.0e4
+    rope = torch.randn(n_kv, 64, generator=g).to(torch.bfloat16)
+    slices, caps = [130, 300, 1, 257, 383], [130, 200, 1, 129, 383]  # slice lengths, lens caps
+    parts, ptr = [], [0]
+    for L, cap in zip(slices, caps):
+        ids = torch.randint(n_poison, n_kv, (L,), generator=g).to(torch.int32)
+        ids[cap:] = torch.randint(0, n_poison, (L - cap,), generator=g).to(torch.int32)  # past lens
+        parts.append(ids)
+        ptr.append(ptr[-1] + L)
+    live = torch.cat(parts)
+    guard = torch.randint(0, n_poison, (4096,), generator=g).to(torch.int32)  # past the buffer
+    backing = torch.cat([live, guard]).to(DEV)
+    indices_d = backing[:live.numel()]  # the call's buffer ends where the guard begins
+    indptr = torch.tensor(ptr, dtype=torch.int32)
+    lens = torch.tensor(caps, dtype=torch.int32)
+    q = torch.randn(len(slices), heads, 576, generator=g).to(torch.bfloat16)
+    rec = oracle.pack_records(bits(lat), bits(rope))
+    kv = pack_gpu(lat, rope, DEV)
+    assert np.array_equal(kv.cpu().numpy(), rec)
+    out, lse, nv, st = run_gpu(q.to(DEV), kv, n_kv, indices_d, indptr.to(DEV), lens.to(DEV), 0.0625, None,
+                               max_row_len=max(slices), kernel=kernel)
+    assert st == 0
+    args = (q.double().numpy(), rec, live.numpy(), indptr.numpy(), lens.numpy(), 0.0625, None)
+    ref_out, ref_lse, ref_nv = oracle.sparse_mla_decode(*args, n_kv_rows=n_kv)
+    assert np.array_equal(nv.cpu().numpy(), ref_nv) and list(ref_nv) == caps
+    compare(out, lse, ref_out, ref_lse, "index canary", allow=allowance(*args, n_kv_rows=n_kv))
+    # (a poison contribution would put |out| near 5e4; the live records' are O(1))
+    assert out.float().abs().max().item() < 100.0
+
+
 def test_duplicates_count_per_position(kernel):
     c = small_case(2, 16, 50, [300, 64], seed=51)
     run_small(c, max_row_len=300, what="duplicates", kernel=kernel)
